@@ -1,0 +1,20 @@
+"""CPU oracle for the routed-attention DiT block (test infrastructure only).
+
+This package is the slow, plain reference that the CUDA path is checked
+against.  Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg
+of ``bench.py`` may import it; the product library never calls it and has no
+CPU fallback.  It shares no code with the CUDA path: the only common module is
+``synthetic`` (seeded input draws).
+
+Arithmetic is float64 throughout, except where the method itself fixes a
+precision: the bf16 "mids" that the pages declare (modulated-norm output,
+projection outputs, head layout, attention output, residual stream) are
+rounded to bf16 exactly where the method stores bf16, and the top-k decision
+is taken on fp32 scores, the precision the FastH3 pages fix for routing.
+
+Parity status of each function is stated in its docstring; every function is
+pinned by a test in ``tests/test_oracle_pins.py`` except the composed block
+and denoiser, whose parity rests on the pinned parts (no weights, fixtures or
+worked examples exist on the pages).
+"""
+from .h3block import *  # noqa: F401,F403

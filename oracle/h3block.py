@@ -1,0 +1,478 @@
+"""Float64 CPU oracle of one routed-attention DiT block and the denoiser step.
+
+Test infrastructure only (see the package docstring): nothing in the product
+library imports or calls this module.
+
+Sources, cited by page title and section:
+
+* "TensorFold #949" = the page "ashhart/TensorFold pull request #949"
+  (MiniMax H3 / FastH3 denoiser on Metal): the "Precision" list, the
+  "What it adds" file list (block.zig, h3_routing.metal, h3_attention.metal),
+  the "Receipts" tile counts and the "Kernel contract" rules.
+* "h3.c README" = the page "Antirez/h3.c: MiniMax H3 inference engine for Mac
+  computers": the sampler/reuse paragraph, the layer-thinning paragraph, the
+  fused gated-AdaLN paragraph and the Q/K RMS + RoPE paragraph.
+* "H3-metal (zh)" = the page "H3-metal：Apple Silicon上的MiniMax-H3原生推理",
+  control table (whole-denoiser reuse row).
+
+Readings taken where the pages leave a step open are marked "Reading:".
+Array conventions: activations are [rows, features]; head-major tensors are
+[H, N, d]; linear weights are [out, in] and ``linear`` computes h @ W^T + b.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+from scipy.special import erf as _erf
+
+__all__ = [
+    "bf16", "f32", "rms_modulate", "linear", "gelu_erf", "head_rms_norm", "rope",
+    "video_tiles", "tile_means", "tile_scores", "topk_select", "topk_gap",
+    "topk_set_valid", "attend", "routed_attention", "pooled_branch", "gate_mix",
+    "attention_layer", "qkv_heads", "block_forward", "euler_update", "extrapolate",
+    "fresh_steps", "sigma_schedule", "denoise_forward", "thin_layers",
+]
+
+
+# ---------------------------------------------------------------------------
+# Storage roundings ("mids")
+# ---------------------------------------------------------------------------
+
+def bf16(a) -> np.ndarray:
+    """Round float64 values to the nearest bf16 (ties to even), returned as float64.
+
+    bf16 = 1 sign, 8 exponent, 7 mantissa bits (the storage type of weights and
+    activations, TensorFold #949 "Precision").  Done directly on the float64
+    bits: drop the low 45 mantissa bits with round-to-nearest-even; values at
+    or above 2^128 become inf; below 2^-126 (bf16 subnormals) the value is
+    rounded to a multiple of 2^-133.
+    """
+    a = np.asarray(a, dtype=np.float64)
+    u = np.ascontiguousarray(a).view(np.uint64)
+    low = np.uint64((1 << 45) - 1)
+    lsb = (u >> np.uint64(45)) & np.uint64(1)
+    with np.errstate(over="ignore"):
+        r = (u + np.uint64((1 << 44) - 1) + lsb) & ~low
+    out = r.view(np.float64).reshape(a.shape).copy()
+    big = np.abs(out) >= 2.0 ** 128
+    out[big] = np.copysign(np.inf, a[big])
+    small = np.abs(a) < 2.0 ** -126
+    if np.any(small):
+        out[small] = np.round(a[small] * 2.0 ** 133) / 2.0 ** 133
+    nan = np.isnan(a)
+    out[nan] = np.nan
+    return out
+
+
+def f32(a) -> np.ndarray:
+    """Round to float32 (nearest even) and return as float64."""
+    return np.asarray(a, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Row operations
+# ---------------------------------------------------------------------------
+
+def rms_modulate(x, shift, scale, eps: float = 1e-6) -> np.ndarray:
+    """Modulated norm: bf16( x / sqrt(mean(x^2) + eps) * (1 + scale) + shift ).
+
+    TensorFold #949 "What it adds" (block.zig: "modulated norm"); the h3.c
+    README's fused gated-AdaLN paragraph names an RMS over each row.
+    Reading: no learned weight, eps = 1e-6, the adaLN form (1 + scale).
+    Output is a bf16 mid (the projection input is bf16).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    inv = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return bf16(x * inv * (1.0 + np.asarray(scale, np.float64)) + np.asarray(shift, np.float64))
+
+
+def linear(h, w, b=None) -> np.ndarray:
+    """h @ w^T + b with float64 sums of the (bf16) operands, no rounding.
+
+    TensorFold #949 "Precision": bf16 weights and activations, fp32 sums.
+    The oracle sums in float64; the bf16 result rounding is applied by the
+    caller where the method stores bf16.
+    """
+    y = np.asarray(h, np.float64) @ np.asarray(w, np.float64).T
+    if b is not None:
+        y = y + np.asarray(b, np.float64)
+    return y
+
+
+def gelu_erf(x) -> np.ndarray:
+    """GELU(x) = 0.5 x (1 + erf(x / sqrt 2)).
+
+    Reading: the 4x-GELU MLP of the synthetic block shapes; the pages' own
+    checkpoint uses SwiGLU, and no GELU form is printed, so the exact erf form
+    is taken.
+    """
+    x = np.asarray(x, np.float64)
+    return 0.5 * x * (1.0 + _erf(x / math.sqrt(2.0)))
+
+
+def head_rms_norm(x, w, eps: float = 1e-6) -> np.ndarray:
+    """Per-head RMS norm over the last axis (d) times a learned weight w [d].
+
+    h3.c README, Q/K RMS normalization + RoPE paragraph; TensorFold #949
+    "What it adds" (h3_routing.metal: head layout with q/k norm and rotary).
+    """
+    x = np.asarray(x, np.float64)
+    inv = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return x * inv * np.asarray(w, np.float64)
+
+
+def rope(x, positions, theta: float = 10000.0) -> np.ndarray:
+    """Rotary embedding, rotate-half pairing, over the last axis.
+
+    Pairs (c, c + d/2) for c < d/2 are rotated by angle p * theta^(-2c/d),
+    p = the packed row index.  Reading: the pages name "q/k norm and rotary"
+    but give no axes or base; a 1-D rotary over the packed row index with
+    theta = 10,000 is taken.
+    """
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    half = d // 2
+    c = np.arange(half, dtype=np.float64)
+    inv_freq = theta ** (-2.0 * c / d)
+    ang = np.asarray(positions, np.float64)[:, None] * inv_freq[None, :]  # [N, half]
+    cos, sin = np.cos(ang), np.sin(ang)
+    x0, x1 = x[..., :half], x[..., half:]
+    out = np.empty_like(x)
+    out[..., :half] = x0 * cos - x1 * sin
+    out[..., half:] = x1 * cos + x0 * sin
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Router: tile means, tile scores, top-k   (TensorFold #949 "What it adds":
+# h3_routing.metal tile means / tile scores / top-k; "Precision": fp32 tile
+# means, scores and top-k; "Kernel contract": NaN ranks as -inf, ties go to
+# the lower tile)
+# ---------------------------------------------------------------------------
+
+def video_tiles(n_prefix: int, n_video: int, tile: int = 64):
+    """[(first_row, n_valid)] for each video tile; the last may be partial.
+
+    Reading: video rows [P, N) are cut into contiguous 64-row tiles in packed
+    order; the pages' 4x4x4 cube map is a fixed row permutation applied before
+    this step and is not part of these shapes.
+    """
+    return [(n_prefix + t * tile, min(tile, n_video - t * tile))
+            for t in range((n_video + tile - 1) // tile)]
+
+
+def tile_means(X, n_prefix: int, n_video: int, tile: int = 64) -> np.ndarray:
+    """Mean over the valid rows of each video tile: [H, N, d] -> [H, Tv, d] (float64)."""
+    X = np.asarray(X, np.float64)
+    tiles = video_tiles(n_prefix, n_video, tile)
+    out = np.empty((X.shape[0], len(tiles), X.shape[2]))
+    for t, (r0, nv) in enumerate(tiles):
+        out[:, t, :] = X[:, r0:r0 + nv, :].sum(axis=1) / nv
+    return out
+
+
+def tile_scores(mq, mk) -> np.ndarray:
+    """S[h, i, j] = mq[h, i] . mk[h, j], unscaled (float64).
+
+    Reading: the pages do not say whether tile scores carry 1/sqrt(d); the
+    scale does not change the order, so S is unscaled here and the pooled
+    branch applies 1/sqrt(d).
+    """
+    return np.einsum("hid,hjd->hij", np.asarray(mq, np.float64), np.asarray(mk, np.float64))
+
+
+def topk_select(scores, k: int) -> np.ndarray:
+    """Top-k tiles per (h, i) taken on fp32 scores: [H, Tq, T] -> int32 [H, Tq, min(k, T)].
+
+    Rule (TensorFold #949 "Kernel contract"): a NaN score ranks as -inf; among
+    equal scores the lower tile index wins.  The decision is made on scores
+    rounded to fp32 (the routing precision on the pages).  Output indices are
+    sorted ascending.
+    """
+    s = f32(scores)
+    s = np.where(np.isnan(s), -np.inf, s)
+    H, Tq, T = s.shape
+    kk = min(k, T)
+    out = np.empty((H, Tq, kk), dtype=np.int32)
+    j = np.arange(T)
+    for h in range(H):
+        for i in range(Tq):
+            order = np.lexsort((j, -s[h, i]))  # by score descending, then index ascending
+            out[h, i] = np.sort(order[:kk])
+    return out
+
+
+def topk_gap(scores, k: int) -> np.ndarray:
+    """Relative float64 gap between the k-th and (k+1)-th largest score per (h, i).
+
+    Used to classify near-ties (gap < 1e-5): where two correct implementations
+    may choose different tiles.  Returns +inf where k >= T.
+    """
+    s = np.asarray(scores, np.float64)
+    s = np.where(np.isnan(s), -np.inf, s)
+    T = s.shape[-1]
+    if k >= T:
+        return np.full(s.shape[:-1], np.inf)
+    srt = -np.sort(-s, axis=-1)
+    a, b = srt[..., k - 1], srt[..., k]
+    with np.errstate(invalid="ignore"):
+        gap = (a - b) / np.maximum(np.abs(a), 1e-30)
+    return np.where(np.isfinite(gap), gap, np.inf)
+
+
+def topk_set_valid(scores_row, chosen, tol: float = 1e-5) -> bool:
+    """True if ``chosen`` is a top-k set of ``scores_row`` up to a relative tolerance."""
+    s = np.where(np.isnan(scores_row), -np.inf, np.asarray(scores_row, np.float64))
+    chosen = np.asarray(chosen)
+    mask = np.zeros(s.shape[0], bool)
+    mask[chosen] = True
+    if mask.all() or len(set(chosen.tolist())) != len(chosen):
+        return bool(mask.all() and len(set(chosen.tolist())) == len(chosen))
+    lo = s[mask].min()
+    hi = s[~mask].max()
+    return bool(lo >= hi - tol * max(abs(lo), abs(hi), 1e-30))
+
+
+# ---------------------------------------------------------------------------
+# Attention
+# ---------------------------------------------------------------------------
+
+def attend(q, k, v, scale: float, p_bf16: bool = False) -> np.ndarray:
+    """softmax(q k^T * scale) v for one head; bidirectional, no mask.
+
+    With ``p_bf16`` the unnormalised weights exp(s - max) are rounded to bf16
+    before the value product, as TensorFold #949 "Precision" states for the
+    routed attention; the row sum l uses the unrounded weights (reading: the
+    pages do not say which).  Default: exact float64.
+    """
+    s = (np.asarray(q, np.float64) @ np.asarray(k, np.float64).T) * scale
+    m = s.max(axis=1, keepdims=True)
+    p = np.exp(s - m)
+    l = p.sum(axis=1, keepdims=True)
+    if p_bf16:
+        p = bf16(p)
+    return (p @ np.asarray(v, np.float64)) / l
+
+
+def routed_attention(Q, K, V, n_prefix: int, n_video: int, idx, tile: int = 64,
+                     p_bf16: bool = False, tiles=None) -> np.ndarray:
+    """Tile-routed attention, [H, N, d] each -> O [H, N, d] (float64).
+
+    TensorFold #949 "What it adds" (h3_attention.metal: tile-routed attention
+    with fp32 scores and online softmax) and "Receipts" (prefix tiles kept for
+    every query: "8 prefix, 56 video tiles kept a query").
+    * prefix (text + audio) query rows attend densely to all N rows;
+    * a video query row in tile i attends to every prefix row plus the valid
+      rows of the tiles idx[h, i].
+    Scale 1/sqrt(d).  ``tiles`` optionally restricts the work to a list of
+    (h, i) video query tiles (rows elsewhere are left zero).
+    """
+    Q = np.asarray(Q, np.float64)
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    H, N, d = Q.shape
+    scale = 1.0 / math.sqrt(d)
+    O = np.zeros_like(Q)
+    vt = video_tiles(n_prefix, n_video, tile)
+    if tiles is None:
+        for h in range(H):
+            if n_prefix:
+                O[h, :n_prefix] = attend(Q[h, :n_prefix], K[h], V[h], scale, p_bf16)
+        tiles = [(h, i) for h in range(H) for i in range(len(vt))]
+    pre = np.arange(n_prefix)
+    for h, i in tiles:
+        r0, nv = vt[i]
+        keys = [pre] + [np.arange(vt[j][0], vt[j][0] + vt[j][1]) for j in idx[h, i]]
+        kr = np.concatenate(keys)
+        O[h, r0:r0 + nv] = attend(Q[h, r0:r0 + nv], K[h, kr], V[h, kr], scale, p_bf16)
+    return O
+
+
+def pooled_branch(S, mv, head_dim: int) -> np.ndarray:
+    """Pooled branch: op[h, i] = sum_j softmax_j(S[h, i, j] / sqrt(d)) mv[h, j].
+
+    TensorFold #949 "What it adds" ("the pooled branch", h3_routing.metal).
+    Reading: attention of each video query tile's mean over all video tile
+    means, reusing the tile scores (the coarse half of a coarse + fine sparse
+    attention).
+    """
+    z = np.asarray(S, np.float64) / math.sqrt(head_dim)
+    z = z - z.max(axis=-1, keepdims=True)
+    w = np.exp(z)
+    w = w / w.sum(axis=-1, keepdims=True)
+    return w @ np.asarray(mv, np.float64)
+
+
+def gate_mix(O, G, pooled, n_prefix: int, n_video: int, tile: int = 64) -> np.ndarray:
+    """o[r, h*d:(h+1)*d] = O[h, r] + G[r, h*d:(h+1)*d] * pooled[h, tile(r)] for video rows.
+
+    TensorFold #949 "What it adds" ("the routing gate", h3_gate_mix).
+    Reading: the gate is a linear (unsquashed) full-width product; prefix rows
+    get no pooled term.  Returns [N, H*d] float64, not rounded.
+    """
+    O = np.asarray(O, np.float64)
+    H, N, d = O.shape
+    out = O.transpose(1, 0, 2).reshape(N, H * d).copy()
+    if pooled is None or G is None or n_video == 0:
+        return out
+    G = np.asarray(G, np.float64)
+    t_of = (np.arange(n_video) // tile)
+    pb = np.asarray(pooled, np.float64)[:, t_of, :]          # [H, V, d]
+    pb = pb.transpose(1, 0, 2).reshape(n_video, H * d)
+    out[n_prefix:] += G[n_prefix:] * pb
+    return out
+
+
+def attention_layer(Q, K, V, G, n_prefix: int, n_video: int, topk: int, tile: int = 64,
+                    pooled: bool = True, p_bf16: bool = False) -> dict:
+    """Router + routed/dense attention + pooled branch + gate mix.
+
+    Inputs are the bf16 values of Q, K, V [H, N, d] and G [N, H*d] (or None).
+    Returns the intermediates and ``o`` = bf16(mixed output) [N, H*d].
+    """
+    Q = np.asarray(Q, np.float64)
+    d = Q.shape[2]
+    mq = tile_means(Q, n_prefix, n_video, tile)
+    mk = tile_means(K, n_prefix, n_video, tile)
+    mv = tile_means(V, n_prefix, n_video, tile)
+    S = tile_scores(mq, mk)
+    idx = topk_select(S, topk)
+    gap = topk_gap(S, topk)
+    O = routed_attention(Q, K, V, n_prefix, n_video, idx, tile, p_bf16)
+    pb = pooled_branch(S, mv, d) if pooled else None
+    mixed = gate_mix(O, G, pb, n_prefix, n_video, tile)
+    return {"mq": mq, "mk": mk, "mv": mv, "scores": S, "idx": idx, "gap": gap,
+            "O": O, "pooled": pb, "o_f64": mixed, "o": bf16(mixed)}
+
+
+# ---------------------------------------------------------------------------
+# Block
+# ---------------------------------------------------------------------------
+
+def qkv_heads(qkvg, heads: int, head_dim: int, qnorm_w=None, knorm_w=None,
+              eps: float = 1e-6, theta: float = 10000.0, use_rope: bool = True):
+    """Split [N, 4A] projection rows into head-major Q, K, V [H, N, d] and G [N, A].
+
+    q and k get the per-head RMS norm (learned weight) and the rotary, then are
+    rounded to bf16; v and g are the projection's bf16 values.  Column order of
+    the projection: [Q | K | V | G], each A = H*d wide, head-major inside.
+    TensorFold #949 "What it adds" (block.zig "q/k/v and the routing gate,
+    head layout"); h3.c README Q/K RMS + RoPE paragraph.
+    """
+    qkvg = np.asarray(qkvg, np.float64)
+    N = qkvg.shape[0]
+    A = heads * head_dim
+    parts = [qkvg[:, s * A:(s + 1) * A].reshape(N, heads, head_dim).transpose(1, 0, 2)
+             for s in range(3)]
+    q, k, v = parts
+    pos = np.arange(N)
+    if qnorm_w is not None:
+        q = head_rms_norm(q, qnorm_w, eps)
+    if knorm_w is not None:
+        k = head_rms_norm(k, knorm_w, eps)
+    if use_rope:
+        q = rope(q, pos, theta)
+        k = rope(k, pos, theta)
+    return bf16(q), bf16(k), v.copy(), qkvg[:, 3 * A:4 * A].copy()
+
+
+def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
+    """One DiT block on the packed rows x (bf16 values, [N, D]).
+
+    TensorFold #949 "What it adds" (block.zig: modulated norm, q/k/v and the
+    routing gate, head layout, routing, attention, the pooled branch, the out
+    projection and the MLP) and h3.c README (gated residual adds and AdaLN).
+    Reading: the MLP is 4x GELU for the synthetic shapes; gated residuals are
+    x + gate * branch with shift/scale/gate rows of the [6, D] table.
+    ``wts`` holds float64 values of the bf16 weights and the fp32 table.
+    """
+    s = shape
+    mod = np.asarray(wts["mod"], np.float64)
+    shift1, scale1, gate1, shift2, scale2, gate2 = mod
+    x = np.asarray(x, np.float64)
+    h = rms_modulate(x, shift1, scale1, s.rms_eps)
+    qkvg = bf16(linear(h, wts["w_qkvg"], wts["b_qkvg"]))
+    q, k, v, g = qkv_heads(qkvg, s.heads, s.head_dim,
+                           wts.get("qnorm_w") if s.qk_norm else None,
+                           wts.get("knorm_w") if s.qk_norm else None,
+                           s.rms_eps, s.rope_theta, s.rope)
+    att = attention_layer(q, k, v, g if s.pooled else None, s.n_prefix, s.n_video,
+                          s.topk, s.tile, s.pooled, p_bf16)
+    x1 = bf16(x + gate1 * linear(att["o"], wts["w_o"], wts["b_o"]))
+    h2 = rms_modulate(x1, shift2, scale2, s.rms_eps)
+    u = bf16(gelu_erf(linear(h2, wts["w1"], wts["b1"])))
+    x2 = bf16(x1 + gate2 * linear(u, wts["w2"], wts["b2"]))
+    out = dict(att)
+    out.update({"h": h, "qkvg": qkvg, "q": q, "k": k, "v": v, "g": g,
+                "x1": x1, "h2": h2, "u": u, "x2": x2})
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Denoiser step (h3.c README sampler paragraph: first and last passes plus
+# every r-th pass run the model, skipped velocities are extrapolated;
+# H3-metal (zh) control table: 20 steps give 20 / 11 / 8 fresh evaluations
+# at reuse 1 / 2 / 3)
+# ---------------------------------------------------------------------------
+
+def euler_update(z, v, dt: float) -> np.ndarray:
+    """z + dt * v, computed in float64 and stored as fp32 (the latent type)."""
+    return f32(np.asarray(z, np.float64) + dt * np.asarray(v, np.float64))
+
+
+def extrapolate(v_a, v_b, sigma_i: float, sigma_a: float, sigma_b: float) -> np.ndarray:
+    """Linear extrapolation in sigma from the last two fresh velocities.
+
+    v_hat = v_a + (v_a - v_b) * (sigma_i - sigma_a) / (sigma_a - sigma_b).
+    Reading: "extrapolates skipped ... velocities" with the variable taken as
+    sigma.  With no second fresh velocity the caller holds v_a.
+    """
+    v_a = np.asarray(v_a, np.float64)
+    v_b = np.asarray(v_b, np.float64)
+    return v_a + (v_a - v_b) * ((sigma_i - sigma_a) / (sigma_a - sigma_b))
+
+
+def fresh_steps(n_steps: int, reuse: int) -> list:
+    """Steps that run the model: i % reuse == 0, plus the last step."""
+    return [i for i in range(n_steps) if i % reuse == 0 or i == n_steps - 1]
+
+
+def sigma_schedule(n_steps: int) -> np.ndarray:
+    """Reading: uniform sigma_i = 1 - i / n (the released shift is not given)."""
+    return 1.0 - np.arange(n_steps + 1, dtype=np.float64) / n_steps
+
+
+def denoise_forward(z, blocks: list, shape, dt: float, block_ids=None) -> dict:
+    """One fresh step: x0 = bf16(z); run the kept blocks; v = x_L; z' = z + dt v.
+
+    Reading: the synthetic workload has no patch or output layers, so the last
+    hidden rows are the velocity.
+    """
+    ids = list(range(len(blocks))) if block_ids is None else list(block_ids)
+    x = bf16(z)
+    for b in ids:
+        x = block_forward(x, blocks[b], shape)["x2"]
+    v = f32(x)
+    return {"v": v, "z": euler_update(z, v, dt)}
+
+
+def thin_layers(mods, keep: int) -> list:
+    """Block ids kept when thinning to ``keep`` of L blocks.
+
+    h3.c README layer-thinning paragraph: rank the AdaLN gates, protect the
+    first and last blocks.  Reading: score_b = ||gate1_b||_2 + ||gate2_b||_2
+    (rows 2 and 5 of the table), computed in float64; the smallest scores are
+    dropped, ties drop the higher index first.
+    """
+    mods = [np.asarray(m, np.float64) for m in mods]
+    L = len(mods)
+    if keep >= L:
+        return list(range(L))
+    if keep < 2:
+        raise ValueError("keep must be >= 2 (first and last blocks are protected)")
+    score = {b: float(np.linalg.norm(mods[b][2]) + np.linalg.norm(mods[b][5]))
+             for b in range(1, L - 1)}
+    order = sorted(score, key=lambda b: (score[b], -b))  # drop order
+    dropped = set(order[:L - keep])
+    return [b for b in range(L) if b not in dropped]

@@ -1,0 +1,110 @@
+"""Workload shapes.
+
+The packed sequence holds text rows first, then audio rows, then video rows.
+Text and audio rows form the prefix; video rows are cut into 64-row tiles that
+the router selects among.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+
+
+@dataclass(frozen=True)
+class BlockShape:
+    n_text: int
+    n_audio: int
+    n_video: int
+    hidden: int
+    heads: int
+    head_dim: int
+    mlp_width: int
+    topk: int
+    tile: int = 64
+    rms_eps: float = 1e-6
+    rope_theta: float = 10000.0
+    qk_norm: bool = True
+    rope: bool = True
+    pooled: bool = True
+    attn_width_override: int = 0
+
+    @property
+    def n_rows(self) -> int:
+        return self.n_text + self.n_audio + self.n_video
+
+    @property
+    def n_prefix(self) -> int:
+        return self.n_text + self.n_audio
+
+    @property
+    def attn_width(self) -> int:
+        return self.attn_width_override or self.heads * self.head_dim
+
+    @property
+    def n_video_tiles(self) -> int:
+        return (self.n_video + self.tile - 1) // self.tile
+
+    def with_(self, **kw) -> "BlockShape":
+        return replace(self, **kw)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    config_id: int
+    shape: BlockShape
+    description: str
+    n_blocks: int = 1
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def seed(self) -> int:
+        return 0x48334454 + self.config_id
+
+
+# 1: routed attention alone, 1,024 video rows, 4 heads x 64, top-k 4 of 16.
+ATTN_TINY = Workload(
+    "attn_tiny_1024", 1,
+    BlockShape(0, 0, 1024, hidden=256, heads=4, head_dim=64, mlp_width=1024, topk=4,
+               qk_norm=False, rope=False),
+    "routed attention only: 1,024 rows, 4 heads x 64, 16 tiles of 64, top-k 4 + pooled",
+)
+
+# 2: one block shaped like a 512x512 video: 4,096 rows, D = 3,072, 24 x 128.
+BLOCK_4K = Workload(
+    "block_4096_d3072", 2,
+    BlockShape(256, 256, 3584, hidden=3072, heads=24, head_dim=128, mlp_width=4 * 3072, topk=8),
+    "one block: 4,096 rows (256 text, 256 audio, 3,584 video), hidden 3,072, 24 x 128, "
+    "MLP 4x GELU, top-k 8 of 56",
+)
+
+# 3: one block at the long-sequence shape: 15,435 rows, D = 5,120, 40 x 128.
+BLOCK_15K = Workload(
+    "block_15435_d5120", 3,
+    BlockShape(512, 1024, 13899, hidden=5120, heads=40, head_dim=128, mlp_width=4 * 5120, topk=16),
+    "one block: 15,435 rows (512 text, 1,024 audio, 13,899 video), hidden 5,120, 40 x 128, "
+    "MLP 4x GELU, top-k 16 of 218 + pooled",
+)
+
+# 4: 50 blocks of the 15,435-row shape, then one Euler step dt = -1/8.
+FORWARD_50 = Workload(
+    "forward50_15435_d5120", 4, BLOCK_15K.shape,
+    "50-block denoising forward at 15,435 rows (hidden 5,120 block shape), "
+    "then z <- z + dt v with dt = -1/8",
+    n_blocks=50, extra={"dt": -0.125},
+)
+
+# 5: 20-step denoising loop at 4,096 rows, 45 of 50 blocks, reuse 2.
+LOOP_4K = Workload(
+    "loop20_4096_d3072", 5, BLOCK_4K.shape,
+    "20 Euler steps, 45 of 50 blocks, velocity reuse 2 (11 fresh), top-k sweep {4,8,16,32,56}",
+    n_blocks=50, extra={"steps": 20, "reuse": 2, "keep": 45, "topk_sweep": [4, 8, 16, 32, 56]},
+)
+
+CONFIGS = [ATTN_TINY, BLOCK_4K, BLOCK_15K, FORWARD_50, LOOP_4K]
+
+
+def config_by_name(name: str) -> Workload:
+    for w in CONFIGS:
+        if w.name == name:
+            return w
+    raise KeyError(name)

@@ -1,0 +1,402 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test ties one oracle function to a closed form, an invariant, a brute
+force on a tiny input, an independent library routine, or a value printed on
+the pages (tests/golden/).  None of them needs a GPU.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synthetic as S
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+# --------------------------------------------------------------------------- bf16
+def test_bf16_against_torch_conversion():
+    torch = pytest.importorskip("torch")
+    x = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-30, 30, 20000),
+                        [0.0, -0.0, 1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 3.3895e38, -1e-39]])
+    x32 = x.astype(np.float32).astype(np.float64)  # torch converts from fp32
+    want = torch.tensor(x32, dtype=torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.bf16(x32)
+    fin = np.isfinite(want)
+    assert np.array_equal(got[fin], want[fin])
+    assert np.array_equal(np.isinf(got), np.isinf(want))
+
+
+def test_bf16_hand_values():
+    assert O.bf16(1.0) == 1.0
+    assert O.bf16(1.0 + 2 ** -8) == 1.0                 # tie -> even
+    assert O.bf16(1.0 + 3 * 2 ** -8) == 1.0 + 2 ** -6    # tie -> even (up)
+    assert O.bf16(1.0 + 2 ** -8 + 2 ** -30) == 1.0 + 2 ** -7
+    assert np.isnan(O.bf16(np.nan))
+    assert O.bf16(1e39) == np.inf
+
+
+def test_bf16_matches_generator_storage():
+    x = rng.standard_normal(5000).astype(np.float32).astype(np.float64)
+    bits = S.to_bf16_bits(x)
+    assert np.array_equal(S.bf16_bits_to_f64(bits), O.bf16(x))
+
+
+# --------------------------------------------------------------------------- rows
+def test_rms_modulate_closed_forms():
+    eps = 1e-6
+    c = 0.75
+    x = np.full((1, 64), c)
+    h = O.rms_modulate(x, np.zeros(64), np.zeros(64), eps)
+    assert np.all(h == O.bf16(c / math.sqrt(c * c + eps)))
+    a = 2.0
+    x = np.tile([a, -a], (3, 32))
+    shift = np.full(64, 0.25)
+    scale = np.full(64, 1.0)
+    h = O.rms_modulate(x, shift, scale, eps)
+    r = a / math.sqrt(a * a + eps)
+    assert np.all(h[:, 0::2] == O.bf16(2 * r + 0.25))
+    assert np.all(h[:, 1::2] == O.bf16(-2 * r + 0.25))
+    # scale = -1 removes the row: h = shift exactly
+    h = O.rms_modulate(rng.standard_normal((4, 64)), shift, -np.ones(64), eps)
+    assert np.all(h == 0.25)
+
+
+def test_linear_small_integers_exact():
+    a = rng.integers(-8, 9, (37, 96))
+    w = rng.integers(-8, 9, (53, 96))
+    b = rng.integers(-8, 9, 53)
+    want = a.astype(np.int64) @ w.astype(np.int64).T + b
+    assert np.array_equal(O.linear(a, w, b), want.astype(np.float64))
+
+
+def test_gelu_closed_forms():
+    assert O.gelu_erf(0.0) == 0.0
+    x = rng.standard_normal(1000) * 3
+    assert np.allclose(O.gelu_erf(x) - O.gelu_erf(-x), x, rtol=0, atol=1e-14)
+    # GELU(1) = Phi(1), the standard normal CDF at 1 (table value 0.841344746068543)
+    assert abs(float(O.gelu_erf(1.0)) - 0.841344746068543) < 1e-15
+    assert abs(float(O.gelu_erf(-10.0))) < 1e-20
+    assert float(O.gelu_erf(10.0)) == 10.0
+
+
+def test_head_rms_norm_unit_rms():
+    x = rng.standard_normal((3, 10, 128)) * 5
+    y = O.head_rms_norm(x, np.ones(128), 0.0)
+    assert np.allclose(np.mean(y * y, axis=-1), 1.0, atol=1e-13)
+    w = rng.standard_normal(128)
+    assert np.allclose(O.head_rms_norm(x, w, 0.0), y * w, atol=1e-14)
+
+
+def test_rope_closed_form_and_relative_position():
+    # d = 2: one pair, frequency theta^0 = 1, so the angle is the position itself
+    x = np.array([[1.0, 0.0], [0.3, -0.7]])
+    p = np.array([0.0, 2.5])
+    y = O.rope(x, p)
+    assert np.allclose(y[0], [1.0, 0.0])
+    c, s = math.cos(2.5), math.sin(2.5)
+    assert np.allclose(y[1], [0.3 * c + 0.7 * s, -0.7 * c + 0.3 * s])
+    # norm per pair preserved; dot products depend only on the position difference
+    d = 128
+    q = rng.standard_normal((1, d))
+    k = rng.standard_normal((1, d))
+    a = O.rope(q, np.array([17.0]))[0] @ O.rope(k, np.array([5.0]))[0]
+    b = O.rope(q, np.array([1017.0]))[0] @ O.rope(k, np.array([1005.0]))[0]
+    assert abs(a - b) < 1e-9
+    z = O.rope(q, np.array([123.0]))
+    assert abs(np.linalg.norm(z) - np.linalg.norm(q)) < 1e-12
+    # pair c uses frequency theta^(-2c/d): pair 1 of d=4 at position 100 rotates by 100/100
+    x4 = np.array([[0.0, 1.0, 0.0, 0.0]])
+    y4 = O.rope(x4, np.array([100.0]), theta=10000.0)
+    assert np.allclose(y4[0], [0.0, math.cos(1.0), 0.0, math.sin(1.0)])
+
+
+# --------------------------------------------------------------------------- router
+def test_tile_means_brute_force_and_partial_tile():
+    H, P, Vn, d = 2, 64, 150, 8
+    X = rng.standard_normal((H, P + Vn, d))
+    m = O.tile_means(X, P, Vn, 64)
+    assert m.shape == (H, 3, d)
+    for h in range(H):
+        for t in range(3):
+            rows = [r for r in range(P + 64 * t, min(P + 64 * t + 64, P + Vn))]
+            want = [sum(X[h, r, c] for r in rows) / len(rows) for c in range(d)]
+            assert np.allclose(m[h, t], want, atol=1e-14)
+    assert len(O.video_tiles(P, Vn, 64)) == 3 and O.video_tiles(P, Vn, 64)[-1] == (P + 128, 22)
+
+
+def test_tile_scores_brute_force():
+    mq = rng.standard_normal((2, 5, 7))
+    mk = rng.standard_normal((2, 5, 7))
+    s = O.tile_scores(mq, mk)
+    for h, i, j in itertools.product(range(2), range(5), range(5)):
+        assert abs(s[h, i, j] - sum(mq[h, i, c] * mk[h, j, c] for c in range(7))) < 1e-13
+
+
+def _brute_topk(row, k):
+    """The unique k-subset C with: for i in C, j not in C, s_i > s_j or (s_i == s_j and i < j)."""
+    s = [(-math.inf if math.isnan(v) else v) for v in row]
+    T = len(s)
+    found = []
+    for C in itertools.combinations(range(T), k):
+        ok = all(s[i] > s[j] or (s[i] == s[j] and i < j)
+                 for i in C for j in range(T) if j not in C)
+        if ok:
+            found.append(C)
+    assert len(found) == 1
+    return list(found[0])
+
+
+@pytest.mark.parametrize("T,k", [(6, 1), (6, 3), (7, 4), (8, 2), (8, 7)])
+def test_topk_brute_force_with_ties_and_nans(T, k):
+    for trial in range(20):
+        row = rng.integers(-3, 4, T).astype(np.float64)  # many exact ties
+        if trial % 3 == 0:
+            row[rng.integers(0, T, 2)] = np.nan
+        if trial % 5 == 0:
+            row[rng.integers(0, T)] = -np.inf
+        got = O.topk_select(row[None, None, :], k)[0, 0]
+        assert got.tolist() == _brute_topk(row.tolist(), k)
+
+
+def test_topk_nan_regression_exact_k():
+    # A NaN must never let a row keep more than k tiles (TensorFold #949 kernel-contract finding).
+    row = np.array([np.nan, 1.0, np.nan, 2.0, np.nan])
+    got = O.topk_select(row[None, None, :], 2)[0, 0]
+    assert got.tolist() == [1, 3]
+    got = O.topk_select(row[None, None, :], 4)[0, 0]
+    assert got.tolist() == [0, 1, 2, 3]  # NaNs rank as -inf; ties among them go to the lower index
+
+
+def test_topk_all_and_gap():
+    s = rng.standard_normal((2, 3, 5))
+    assert np.array_equal(O.topk_select(s, 5)[0, 0], np.arange(5))
+    assert np.array_equal(O.topk_select(s, 9)[1, 2], np.arange(5))
+    assert np.all(np.isinf(O.topk_gap(s, 5)))
+    t = np.array([[[3.0, 1.0, 2.0, 2.0 + 1e-9]]])
+    assert O.topk_gap(t, 2)[0, 0] < 1e-5
+    assert O.topk_set_valid(t[0, 0], [0, 2]) and O.topk_set_valid(t[0, 0], [0, 3])
+    assert not O.topk_set_valid(t[0, 0], [0, 1])
+
+
+# --------------------------------------------------------------------------- attention
+def _brute_attention(q, K, V, scale):
+    out = []
+    for qi in q:
+        s = [sum(qi[c] * kj[c] for c in range(len(qi))) * scale for kj in K]
+        m = max(s)
+        w = [math.exp(v - m) for v in s]
+        z = sum(w)
+        out.append([sum(w[j] * V[j][c] for j in range(len(K))) / z for c in range(V.shape[1])])
+    return np.array(out)
+
+
+@pytest.mark.parametrize("P", [0, 64])
+def test_routed_all_tiles_equals_dense_brute_force(P):
+    H, Vn, d = 2, 150, 8
+    N = P + Vn
+    Q, K, V = (rng.standard_normal((H, N, d)) for _ in range(3))
+    tv = len(O.video_tiles(P, Vn))
+    idx = O.topk_select(O.tile_scores(O.tile_means(Q, P, Vn), O.tile_means(K, P, Vn)), tv)
+    out = O.routed_attention(Q, K, V, P, Vn, idx)
+    for h in range(H):
+        want = _brute_attention(Q[h], K[h], V[h], 1.0 / math.sqrt(d))
+        assert np.allclose(out[h], want, atol=1e-12)
+
+
+def test_routed_keyset_brute_force():
+    # every video query row attends to the prefix plus exactly its selected tiles
+    H, P, Vn, d, k = 1, 64, 256, 8, 2
+    N = P + Vn
+    Q, K, V = (rng.standard_normal((H, N, d)) for _ in range(3))
+    idx = np.array([[[0, 3], [1, 2], [0, 1], [2, 3]]], dtype=np.int32)
+    out = O.routed_attention(Q, K, V, P, Vn, idx)
+    scale = 1.0 / math.sqrt(d)
+    for i in range(4):
+        keys = list(range(P)) + [P + 64 * j + r for j in idx[0, i] for r in range(64)]
+        rows = range(P + 64 * i, P + 64 * i + 64)
+        for r in list(rows)[:3]:
+            want = _brute_attention(Q[0, [r]], K[0, keys], V[0, keys], scale)
+            assert np.allclose(out[0, r], want[0], atol=1e-12)
+
+
+def test_attention_row_stochastic_and_zero_query():
+    H, P, Vn, d = 2, 64, 200, 16
+    N = P + Vn
+    Q = rng.standard_normal((H, N, d))
+    K = rng.standard_normal((H, N, d))
+    V = np.broadcast_to(rng.standard_normal((H, 1, d)), (H, N, d)).copy()
+    idx = O.topk_select(O.tile_scores(O.tile_means(Q, P, Vn), O.tile_means(K, P, Vn)), 2)
+    out = O.routed_attention(Q, K, V, P, Vn, idx)
+    assert np.allclose(out, V, atol=1e-14)  # weights sum to one
+    V = rng.standard_normal((H, N, d))
+    out = O.routed_attention(np.zeros_like(Q), K, V, P, Vn, idx)
+    assert np.allclose(out[:, :P], V.mean(axis=1, keepdims=True).repeat(P, 1), atol=1e-13)
+    for h in range(H):
+        for i, (r0, nv) in enumerate(O.video_tiles(P, Vn)):
+            kr = list(range(P)) + [r for j in idx[h, i] for r in range(
+                O.video_tiles(P, Vn)[j][0], O.video_tiles(P, Vn)[j][0] + O.video_tiles(P, Vn)[j][1])]
+            assert np.allclose(out[h, r0:r0 + nv], V[h, kr].mean(axis=0), atol=1e-13)
+
+
+def test_router_tile_permutation_equivariance():
+    H, Vn, d, k = 2, 64 * 6, 16, 3
+    Q, K, V = (rng.standard_normal((H, Vn, d)) for _ in range(3))
+    perm = rng.permutation(6)  # new tile t holds old tile perm[t]
+    rows = np.concatenate([np.arange(64 * p, 64 * p + 64) for p in perm])
+    a = O.attention_layer(Q, K, V, None, 0, Vn, k, pooled=False)
+    b = O.attention_layer(Q[:, rows], K[:, rows], V[:, rows], None, 0, Vn, k, pooled=False)
+    inv = np.argsort(perm)
+    for h in range(H):
+        for t in range(6):
+            assert sorted(perm[b["idx"][h, t]].tolist()) == a["idx"][h, perm[t]].tolist()
+    assert np.allclose(b["o_f64"], a["o_f64"][rows], atol=1e-12)
+    # permuting rows inside a tile leaves the means and the selections unchanged
+    inner = np.arange(Vn).reshape(6, 64)
+    inner = np.concatenate([rng.permutation(r) for r in inner])
+    c = O.attention_layer(Q[:, inner], K[:, inner], V[:, inner], None, 0, Vn, k, pooled=False)
+    assert np.array_equal(c["idx"], a["idx"])
+    assert np.allclose(c["mq"], a["mq"], atol=1e-14)
+    assert np.allclose(c["o_f64"], a["o_f64"][inner], atol=1e-12)
+    del inv
+
+
+def test_planted_tie_lower_tile_wins():
+    H, Vn, d = 1, 64 * 4, 8
+    Q, K, V = (rng.standard_normal((H, Vn, d)) for _ in range(3))
+    K[:, 128:192] = K[:, 64:128]  # tiles 1 and 2 identical -> equal scores for every query
+    mq = O.tile_means(Q, 0, Vn)
+    mk = O.tile_means(K, 0, Vn)
+    S_ = O.tile_scores(mq, mk)
+    idx = O.topk_select(S_, 1)
+    for i in range(4):
+        if np.argmax(S_[0, i]) in (1, 2):
+            assert idx[0, i, 0] == 1
+
+
+def test_pooled_closed_forms():
+    mv = rng.standard_normal((2, 1, 8))
+    S_ = rng.standard_normal((2, 1, 1))
+    assert np.allclose(O.pooled_branch(S_, mv, 8), mv, atol=1e-15)
+    mv = np.broadcast_to(rng.standard_normal((2, 1, 8)), (2, 5, 8))
+    S_ = rng.standard_normal((2, 5, 5))
+    assert np.allclose(O.pooled_branch(S_, mv, 8), mv, atol=1e-14)
+    S_ = rng.standard_normal((1, 3, 4))
+    mv = rng.standard_normal((1, 4, 2))
+    got = O.pooled_branch(S_, mv, 16)
+    for i in range(3):
+        w = [math.exp(S_[0, i, j] / 4.0) for j in range(4)]
+        want = [sum(w[j] * mv[0, j, c] for j in range(4)) / sum(w) for c in range(2)]
+        assert np.allclose(got[0, i], want, atol=1e-14)
+
+
+def test_gate_mix_brute_force():
+    H, P, Vn, d = 2, 64, 100, 4
+    N = P + Vn
+    Ov = rng.standard_normal((H, N, d))
+    G = rng.standard_normal((N, H * d))
+    pb = rng.standard_normal((H, 2, d))
+    out = O.gate_mix(Ov, G, pb, P, Vn)
+    for r in range(N):
+        for h in range(H):
+            for c in range(d):
+                want = Ov[h, r, c] + (G[r, h * d + c] * pb[h, (r - P) // 64, c] if r >= P else 0.0)
+                assert abs(out[r, h * d + c] - want) < 1e-14
+
+
+# --------------------------------------------------------------------------- block
+def _tiny_shape(**kw):
+    base = dict(n_text=64, n_audio=64, n_video=150, hidden=64, heads=2, head_dim=32,
+                mlp_width=256, topk=2)
+    base.update(kw)
+    return S.BlockShape(**base)
+
+
+def _weights(shape, seed=7):
+    w = S.block_weights(shape, seed)
+    return {k: (S.bf16_bits_to_f64(v) if v.dtype == np.uint16 else v.astype(np.float64))
+            for k, v in w.items()}
+
+
+def test_block_closed_form_constant_rows():
+    # scale1 = -1 makes every modulated row equal to shift1; without rotary, all q, k, v rows
+    # are then equal, so attention returns that v row and the pooled branch returns it too.
+    shape = _tiny_shape(rope=False)
+    w = _weights(shape)
+    w["mod"][1] = -1.0
+    x = S.bf16_bits_to_f64(S.hidden_rows(shape, 3))
+    out = O.block_forward(x, w, shape)
+    hrow = O.bf16(w["mod"][0])
+    qkvg = O.bf16(O.linear(hrow[None, :], w["w_qkvg"], w["b_qkvg"]))[0]
+    A = shape.attn_width
+    vrow, grow = qkvg[2 * A:3 * A], qkvg[3 * A:]
+    o = np.tile(vrow, (shape.n_rows, 1))
+    o[shape.n_prefix:] += grow * vrow
+    assert np.allclose(out["o_f64"], o, atol=1e-12)
+    x1 = O.bf16(x + w["mod"][2] * O.linear(O.bf16(o), w["w_o"], w["b_o"]))
+    assert np.array_equal(out["x1"], x1)
+
+
+def test_block_zero_gates_pass_residual():
+    shape = _tiny_shape()
+    w = _weights(shape)
+    w["mod"][2] = 0.0
+    w["mod"][5] = 0.0
+    x = S.bf16_bits_to_f64(S.hidden_rows(shape, 3))
+    out = O.block_forward(x, w, shape)
+    assert np.array_equal(out["x1"], x) and np.array_equal(out["x2"], x)
+
+
+def test_block_all_tiles_equals_dense():
+    shape = _tiny_shape(topk=3, pooled=False)
+    w = _weights(shape)
+    x = S.bf16_bits_to_f64(S.hidden_rows(shape, 3))
+    out = O.block_forward(x, w, shape)
+    H, d = shape.heads, shape.head_dim
+    dense = np.stack([O.attend(out["q"][h], out["k"][h], out["v"][h], 1 / math.sqrt(d))
+                      for h in range(H)])
+    assert np.allclose(out["O"], dense, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- denoiser
+def test_euler_power_of_two_exact():
+    z = rng.standard_normal(1000).astype(np.float32)
+    v = O.bf16(rng.standard_normal(1000))
+    got = O.euler_update(z, v, -0.125)
+    want = (z.astype(np.float32) + np.float32(-0.125) * v.astype(np.float32))  # exact product
+    assert np.array_equal(got, want.astype(np.float64))
+
+
+def test_extrapolation_exact_for_linear_velocity():
+    a, b = rng.standard_normal(50), rng.standard_normal(50)
+    v = lambda s: a + b * s  # noqa: E731
+    got = O.extrapolate(v(0.7), v(0.8), 0.65, 0.7, 0.8)
+    assert np.allclose(got, v(0.65), atol=1e-13)
+
+
+def test_fresh_step_counts_golden():
+    with open(os.path.join(GOLDEN, "reuse_fresh_counts.txt")) as f:
+        rows = [list(map(int, ln.split())) for ln in f if ln.strip() and not ln.startswith("#")]
+    assert rows
+    for n, r, want in rows:
+        steps = O.fresh_steps(n, r)
+        assert len(steps) == want and steps[0] == 0 and steps[-1] == n - 1
+
+
+def test_thin_layers_hand_example():
+    D = 4
+    g = [5.0, 1.0, 3.0, 1.0, 0.5, 9.0]  # block 4 smallest, blocks 1 and 3 tie
+    mods = []
+    for s in g:
+        m = np.zeros((6, D))
+        m[2, 0] = s
+        mods.append(m)
+    assert O.thin_layers(mods, 6) == [0, 1, 2, 3, 4, 5]
+    assert O.thin_layers(mods, 5) == [0, 1, 2, 3, 5]
+    assert O.thin_layers(mods, 4) == [0, 1, 2, 5]      # tie 1 vs 3: the higher (3) goes first
+    assert O.thin_layers(mods, 3) == [0, 2, 5]
+    assert O.thin_layers(mods, 2) == [0, 5]
