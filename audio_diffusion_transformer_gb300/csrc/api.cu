@@ -1,0 +1,503 @@
+// api.cu -- the exported C ABI: argument checks, workspace planning, tensor
+// maps and the launch sequence of a block, an attention layer and a denoiser
+// step.  Everything here runs on the host; all arithmetic is in the kernels.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <string.h>
+
+#include "internal.h"
+
+namespace h3 {
+
+// ---------------------------------------------------------------- tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// bf16 row-major [rows, cols], box = 64 columns (128 bytes) x box_rows, 128-byte swizzle.
+bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                  uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 [heads, rows, cols] (cols innermost), box = 64 x 64 x 1, 128-byte swizzle.
+bool make_tmap_3d(CUtensorMap* map, const void* base, uint64_t heads, uint64_t rows,
+                  uint64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {cols, rows, heads};
+  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxRows = 1022 * 64;  // attention key-tile list limit
+
+inline size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+struct Dims {
+  int N, P, V, Tv, ksel, D, H, d, A, F;
+  bool block;  // hidden / mlp widths given
+};
+
+h3dit_status check_attn(const h3dit_shape* s, Dims* o) {
+  if (!s) return H3DIT_ERR_ARG;
+  if (s->n_text < 0 || s->n_audio < 0 || s->n_video < 1) return H3DIT_ERR_SHAPE;
+  if (s->tile != 64) return H3DIT_ERR_SHAPE;
+  const long long N = (long long)s->n_text + s->n_audio + s->n_video;
+  if (N > kMaxRows) return H3DIT_ERR_SHAPE;
+  const int P = s->n_text + s->n_audio;
+  if (P % 64) return H3DIT_ERR_SHAPE;
+  if (s->head_dim != 64 && s->head_dim != 128) return H3DIT_ERR_SHAPE;
+  if (s->heads < 1 || s->heads > 4096) return H3DIT_ERR_SHAPE;
+  if (s->attn_width != s->heads * s->head_dim) return H3DIT_ERR_SHAPE;
+  if (s->topk < 1) return H3DIT_ERR_ARG;
+  const int Tv = (s->n_video + 63) / 64;
+  if ((size_t)(s->head_dim + 3 * Tv) * 4 > 200 * 1024) return H3DIT_ERR_SHAPE;
+  if (!(s->rms_eps >= 0.f)) return H3DIT_ERR_ARG;
+  o->N = (int)N;
+  o->P = P;
+  o->V = s->n_video;
+  o->Tv = Tv;
+  o->ksel = s->topk < Tv ? s->topk : Tv;
+  o->H = s->heads;
+  o->d = s->head_dim;
+  o->A = s->attn_width;
+  o->D = s->hidden;
+  o->F = s->mlp_width;
+  o->block = false;
+  return H3DIT_OK;
+}
+
+h3dit_status check_block(const h3dit_shape* s, Dims* o) {
+  h3dit_status st = check_attn(s, o);
+  if (st != H3DIT_OK) return st;
+  if (s->hidden < 256 || s->hidden % 256 || s->hidden > 8192) return H3DIT_ERR_SHAPE;
+  if (s->attn_width % 256) return H3DIT_ERR_SHAPE;
+  if (s->mlp_width < 256 || s->mlp_width % 256) return H3DIT_ERR_SHAPE;
+  if ((s->flags & H3DIT_ROPE) && (s->rope_theta <= 1.0f)) return H3DIT_ERR_ARG;
+  o->block = true;
+  return H3DIT_OK;
+}
+
+// Workspace layout (all offsets 256-byte aligned).
+struct Ws {
+  size_t status, q, k, v, g, o, u, h, x, rope, means, scores, idx, pooled, total;
+};
+
+Ws plan(const Dims& m) {
+  Ws w;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off += up(bytes);
+    return at;
+  };
+  const size_t NA = (size_t)m.N * m.A * 2;
+  w.status = take(kAlign);
+  w.q = take(NA);
+  w.k = take(NA);
+  w.v = take(NA);
+  w.g = take(NA);
+  w.o = take(NA);
+  w.means = take((size_t)3 * m.H * m.Tv * m.d * 4);
+  w.scores = take((size_t)m.H * m.Tv * m.Tv * 4);
+  w.idx = take((size_t)m.H * m.Tv * m.ksel * 4);
+  w.pooled = take((size_t)m.H * m.Tv * m.d * 4);
+  if (m.block) {
+    const size_t NF = (size_t)m.N * m.F * 2;
+    // u (the MLP inner activations) reuses q..g, which are dead after attention
+    w.u = NF <= 4 * NA ? w.q : take(NF);
+    w.h = take((size_t)m.N * m.D * 2);
+    w.x = take((size_t)m.N * m.D * 2);
+    w.rope = take((size_t)m.N * (m.d / 2) * 8);
+  } else {
+    w.u = w.h = w.x = w.rope = 0;
+  }
+  w.total = off;
+  return w;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+h3dit_status device_ok() {
+  int dev = 0, major = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return H3DIT_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    return H3DIT_ERR_CUDA;
+  return major == 10 ? H3DIT_OK : H3DIT_ERR_UNSUPPORTED;
+}
+
+inline h3dit_status cu(cudaError_t e) { return e == cudaSuccess ? H3DIT_OK : H3DIT_ERR_CUDA; }
+
+#define H3_TRY(expr)                          \
+  do {                                        \
+    h3dit_status _st = (expr);                \
+    if (_st != H3DIT_OK) return _st;          \
+  } while (0)
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+h3dit_status run_attention(const h3dit_shape* s, const Dims& m, const Ws& w, void* ws,
+                           const __nv_bfloat16* q, const __nv_bfloat16* k,
+                           const __nv_bfloat16* v, const __nv_bfloat16* gate,
+                           __nv_bfloat16* out, float* pooled, int* idx, float* scores,
+                           cudaStream_t st) {
+  const bool use_pool = (s->flags & H3DIT_POOLED) && gate != nullptr;
+  RouterArgs r;
+  r.q = q;
+  r.k = k;
+  r.v = v;
+  r.N = m.N;
+  r.H = m.H;
+  r.d = m.d;
+  r.n_prefix = m.P;
+  r.n_video = m.V;
+  r.Tv = m.Tv;
+  r.ksel = m.ksel;
+  r.means = at<float>(ws, w.means);
+  r.scores = scores ? scores : at<float>(ws, w.scores);
+  r.idx = idx ? idx : at<int>(ws, w.idx);
+  r.pooled = use_pool || pooled ? (pooled ? pooled : at<float>(ws, w.pooled)) : nullptr;
+  H3_TRY(cu(launch_router(r, st)));
+  AttnArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.N = m.N;
+  a.H = m.H;
+  a.d = m.d;
+  a.n_prefix = m.P;
+  a.n_video = m.V;
+  a.Tv = m.Tv;
+  a.ksel = m.ksel;
+  a.idx = r.idx;
+  a.gate = use_pool ? gate : nullptr;
+  a.pooled = use_pool ? r.pooled : nullptr;
+  a.out = out;
+  a.status = at<int>(ws, w.status);
+  return cu(launch_attention(a, st));
+}
+
+h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* ws,
+                       const h3dit_block_weights* wt, __nv_bfloat16* x, bool rope_ready,
+                       cudaStream_t st) {
+  const int N = m.N, D = m.D, A = m.A, F = m.F;
+  int* status = at<int>(ws, w.status);
+  __nv_bfloat16* h = at<__nv_bfloat16>(ws, w.h);
+  __nv_bfloat16* q = at<__nv_bfloat16>(ws, w.q);
+  __nv_bfloat16* k = at<__nv_bfloat16>(ws, w.k);
+  __nv_bfloat16* v = at<__nv_bfloat16>(ws, w.v);
+  __nv_bfloat16* g = at<__nv_bfloat16>(ws, w.g);
+  __nv_bfloat16* o = at<__nv_bfloat16>(ws, w.o);
+  __nv_bfloat16* u = at<__nv_bfloat16>(ws, w.u);
+  float2* rope = at<float2>(ws, w.rope);
+  const float* mod = wt->mod;
+  const bool use_rope = (s->flags & H3DIT_ROPE) != 0;
+  if (use_rope && !rope_ready) H3_TRY(cu(launch_rope_table(rope, N, m.d, s->rope_theta, st)));
+
+  // a1: modulated norm 1
+  H3_TRY(cu(launch_rms_modulate(x, mod + 0 * D, mod + 1 * D, h, N, D, s->rms_eps, st)));
+  // a2 + a3: q/k/v/gate projection with q/k norm, rotary and head-major layout
+  GemmArgs ga;
+  memset(&ga, 0, sizeof(ga));
+  ga.a = h;
+  ga.w = static_cast<const __nv_bfloat16*>(wt->w_qkvg);
+  ga.M = N;
+  ga.N = 4 * A;
+  ga.K = D;
+  ga.bias = static_cast<const __nv_bfloat16*>(wt->b_qkvg);
+  ga.heads = m.H;
+  ga.head_dim = m.d;
+  ga.attn_width = A;
+  ga.q = q;
+  ga.k = k;
+  ga.v = v;
+  ga.g = g;
+  if (s->flags & H3DIT_QK_NORM) {
+    ga.qnorm_w = static_cast<const __nv_bfloat16*>(wt->qnorm_w);
+    ga.knorm_w = static_cast<const __nv_bfloat16*>(wt->knorm_w);
+  }
+  ga.rope_cs = use_rope ? rope : nullptr;
+  ga.eps = s->rms_eps;
+  ga.status = status;
+  H3_TRY(cu(launch_gemm(kEpiQkvg, ga, st)));
+  // a4..a9: router, routed + dense attention, pooled branch and gate mix
+  H3_TRY(run_attention(s, m, w, ws, q, k, v, g, o, nullptr, nullptr, nullptr, st));
+  // a10: out projection + gated residual (in place on x)
+  GemmArgs gb;
+  memset(&gb, 0, sizeof(gb));
+  gb.a = o;
+  gb.w = static_cast<const __nv_bfloat16*>(wt->w_o);
+  gb.M = N;
+  gb.N = D;
+  gb.K = A;
+  gb.bias = static_cast<const __nv_bfloat16*>(wt->b_o);
+  gb.y = x;
+  gb.gate = mod + 2 * D;
+  gb.status = status;
+  H3_TRY(cu(launch_gemm(kEpiResid, gb, st)));
+  // a11: modulated norm 2
+  H3_TRY(cu(launch_rms_modulate(x, mod + 3 * D, mod + 4 * D, h, N, D, s->rms_eps, st)));
+  // a12: fc1 + GELU
+  GemmArgs gc;
+  memset(&gc, 0, sizeof(gc));
+  gc.a = h;
+  gc.w = static_cast<const __nv_bfloat16*>(wt->w1);
+  gc.M = N;
+  gc.N = F;
+  gc.K = D;
+  gc.bias = static_cast<const __nv_bfloat16*>(wt->b1);
+  gc.y = u;
+  gc.status = status;
+  H3_TRY(cu(launch_gemm(kEpiGelu, gc, st)));
+  // a13: fc2 + gated residual (in place on x)
+  GemmArgs gd;
+  memset(&gd, 0, sizeof(gd));
+  gd.a = u;
+  gd.w = static_cast<const __nv_bfloat16*>(wt->w2);
+  gd.M = N;
+  gd.N = D;
+  gd.K = F;
+  gd.bias = static_cast<const __nv_bfloat16*>(wt->b2);
+  gd.y = x;
+  gd.gate = mod + 5 * D;
+  gd.status = status;
+  return cu(launch_gemm(kEpiResid, gd, st));
+}
+
+h3dit_status check_weights(const h3dit_shape* s, const h3dit_block_weights* w) {
+  if (!w) return H3DIT_ERR_ARG;
+  const void* req[] = {w->w_qkvg, w->b_qkvg, w->w_o, w->b_o, w->w1, w->b1, w->w2, w->b2, w->mod};
+  for (const void* p : req) {
+    if (!p) return H3DIT_ERR_ARG;
+    if (!aligned16(p)) return H3DIT_ERR_ALIGN;
+  }
+  if (s->flags & H3DIT_QK_NORM) {
+    if (!w->qnorm_w || !w->knorm_w) return H3DIT_ERR_ARG;
+    if (!aligned16(w->qnorm_w) || !aligned16(w->knorm_w)) return H3DIT_ERR_ALIGN;
+  }
+  return H3DIT_OK;
+}
+
+}  // namespace
+}  // namespace h3
+
+using namespace h3;
+
+extern "C" {
+
+const char* h3dit_version(void) { return "h3dit 0.1.0 sm_103a"; }
+
+const char* h3dit_status_string(h3dit_status s) {
+  switch (s) {
+    case H3DIT_OK: return "ok";
+    case H3DIT_ERR_ARG: return "invalid argument";
+    case H3DIT_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case H3DIT_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case H3DIT_ERR_WORKSPACE: return "workspace missing or too small";
+    case H3DIT_ERR_CUDA: return "CUDA call failed";
+    case H3DIT_ERR_TIMEOUT: return "a kernel wait timed out";
+    case H3DIT_ERR_UNSUPPORTED: return "unsupported device or feature";
+  }
+  return "unknown status";
+}
+
+h3dit_status h3dit_check_shape(const h3dit_shape* shape) {
+  Dims m;
+  return check_block(shape, &m);
+}
+
+size_t h3dit_workspace_bytes(const h3dit_shape* shape) {
+  Dims m;
+  if (!shape) return 0;
+  if (shape->hidden == 0 && shape->mlp_width == 0) {
+    if (check_attn(shape, &m) != H3DIT_OK) return 0;
+  } else if (check_block(shape, &m) != H3DIT_OK) {
+    return 0;
+  }
+  return plan(m).total;
+}
+
+h3dit_status h3dit_block_forward(const h3dit_shape* shape, const h3dit_block_weights* w,
+                                 void* x_inout, void* workspace, size_t ws_bytes, void* stream) {
+  Dims m;
+  H3_TRY(check_block(shape, &m));
+  H3_TRY(check_weights(shape, w));
+  if (!x_inout || !workspace) return H3DIT_ERR_ARG;
+  if (!aligned16(x_inout) || !aligned16(workspace)) return H3DIT_ERR_ALIGN;
+  const Ws ws = plan(m);
+  if (ws_bytes < ws.total) return H3DIT_ERR_WORKSPACE;
+  H3_TRY(device_ok());
+  return run_block(shape, m, ws, workspace, w, static_cast<__nv_bfloat16*>(x_inout), false,
+                   static_cast<cudaStream_t>(stream));
+}
+
+h3dit_status h3dit_routed_attention(const h3dit_shape* shape, const void* q, const void* k,
+                                    const void* v, const void* gate_or_null, void* out,
+                                    float* pooled_out_or_null, int* topk_idx_out_or_null,
+                                    float* tile_scores_out_or_null, void* workspace,
+                                    size_t ws_bytes, void* stream) {
+  Dims m;
+  H3_TRY(check_attn(shape, &m));
+  m.block = false;
+  if (!q || !k || !v || !out || !workspace) return H3DIT_ERR_ARG;
+  const void* ptrs[] = {q, k, v, out, workspace, gate_or_null, pooled_out_or_null,
+                        topk_idx_out_or_null, tile_scores_out_or_null};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return H3DIT_ERR_ALIGN;
+  const Ws ws = plan(m);
+  if (ws_bytes < ws.total) return H3DIT_ERR_WORKSPACE;
+  H3_TRY(device_ok());
+  return run_attention(shape, m, ws, workspace, static_cast<const __nv_bfloat16*>(q),
+                       static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
+                       static_cast<const __nv_bfloat16*>(gate_or_null),
+                       static_cast<__nv_bfloat16*>(out), pooled_out_or_null,
+                       topk_idx_out_or_null, tile_scores_out_or_null,
+                       static_cast<cudaStream_t>(stream));
+}
+
+h3dit_status h3dit_denoise_step(const h3dit_shape* shape, const h3dit_block_weights* blocks,
+                                const int* block_ids, int n_blocks, float* z_inout,
+                                float* v_ring, int fresh, float sigma_i, float sigma_a,
+                                float sigma_b, int n_fresh_so_far, float dt, void* workspace,
+                                size_t ws_bytes, void* stream) {
+  Dims m;
+  H3_TRY(check_block(shape, &m));
+  if (!z_inout || !v_ring || !workspace) return H3DIT_ERR_ARG;
+  if (!aligned16(z_inout) || !aligned16(v_ring) || !aligned16(workspace)) return H3DIT_ERR_ALIGN;
+  if (n_fresh_so_far < 0) return H3DIT_ERR_ARG;
+  const Ws ws = plan(m);
+  if (ws_bytes < ws.total) return H3DIT_ERR_WORKSPACE;
+  const size_t n = (size_t)m.N * m.D;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (fresh) {
+    if (!blocks || (n_blocks > 0 && !block_ids) || n_blocks < 0) return H3DIT_ERR_ARG;
+    for (int i = 0; i < n_blocks; ++i) {
+      if (block_ids[i] < 0) return H3DIT_ERR_ARG;
+      H3_TRY(check_weights(shape, &blocks[block_ids[i]]));
+    }
+    H3_TRY(device_ok());
+    __nv_bfloat16* x = at<__nv_bfloat16>(workspace, ws.x);
+    H3_TRY(cu(launch_f32_to_bf16(z_inout, x, n, st)));
+    if (shape->flags & H3DIT_ROPE)
+      H3_TRY(cu(launch_rope_table(at<float2>(workspace, ws.rope), m.N, m.d, shape->rope_theta,
+                                  st)));
+    for (int i = 0; i < n_blocks; ++i)
+      H3_TRY(run_block(shape, m, ws, workspace, &blocks[block_ids[i]], x, true, st));
+    float* slot = v_ring + (size_t)(n_fresh_so_far % 2) * n;
+    return cu(launch_euler_fresh(x, z_inout, slot, dt, n, st));
+  }
+  if (n_fresh_so_far < 1) return H3DIT_ERR_ARG;  // nothing to extrapolate from
+  H3_TRY(device_ok());
+  const float* va = v_ring + (size_t)((n_fresh_so_far - 1) % 2) * n;
+  const float* vb = n_fresh_so_far >= 2 ? v_ring + (size_t)(n_fresh_so_far % 2) * n : nullptr;
+  float coef = 0.f;
+  if (vb) {
+    if (sigma_a == sigma_b) return H3DIT_ERR_ARG;
+    coef = (float)(((double)sigma_i - sigma_a) / ((double)sigma_a - sigma_b));
+  }
+  return cu(launch_euler_extrap(z_inout, va, vb, coef, dt, n, st));
+}
+
+h3dit_status h3dit_select_blocks(const float* mods, int n_blocks, int hidden, int keep,
+                                 int* kept_ids) {
+  if (!mods || !kept_ids || n_blocks < 1 || hidden < 1 || keep < 1) return H3DIT_ERR_ARG;
+  if (keep >= n_blocks) {
+    for (int b = 0; b < n_blocks; ++b) kept_ids[b] = b;
+    return H3DIT_OK;
+  }
+  if (keep < 2) return H3DIT_ERR_ARG;
+  double* score = new double[n_blocks];
+  char* dropped = new char[n_blocks];
+  for (int b = 0; b < n_blocks; ++b) {
+    const float* g1 = mods + ((size_t)b * 6 + 2) * hidden;
+    const float* g2 = mods + ((size_t)b * 6 + 5) * hidden;
+    double s1 = 0.0, s2 = 0.0;
+    for (int c = 0; c < hidden; ++c) {
+      s1 += (double)g1[c] * g1[c];
+      s2 += (double)g2[c] * g2[c];
+    }
+    score[b] = sqrt(s1) + sqrt(s2);
+    dropped[b] = 0;
+  }
+  for (int r = 0; r < n_blocks - keep; ++r) {
+    int best = -1;
+    for (int b = 1; b < n_blocks - 1; ++b) {
+      if (dropped[b]) continue;
+      if (best < 0 || score[b] < score[best] || (score[b] == score[best] && b > best)) best = b;
+    }
+    dropped[best] = 1;
+  }
+  int n = 0;
+  for (int b = 0; b < n_blocks; ++b)
+    if (!dropped[b]) kept_ids[n++] = b;
+  delete[] score;
+  delete[] dropped;
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_linear(const void* a, const void* w, const void* b_or_null, void* y, int M,
+                          int N, int K, void* stream) {
+  if (!a || !w || !y) return H3DIT_ERR_ARG;
+  if (M < 1 || N < 256 || N % 256 || K < 64 || K % 64) return H3DIT_ERR_SHAPE;
+  if (!aligned16(a) || !aligned16(w) || !aligned16(y) || (b_or_null && !aligned16(b_or_null)))
+    return H3DIT_ERR_ALIGN;
+  H3_TRY(device_ok());
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.a = static_cast<const __nv_bfloat16*>(a);
+  g.w = static_cast<const __nv_bfloat16*>(w);
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.bias = static_cast<const __nv_bfloat16*>(b_or_null);
+  g.y = static_cast<__nv_bfloat16*>(y);
+  return cu(launch_gemm(kEpiStore, g, static_cast<cudaStream_t>(stream)));
+}
+
+h3dit_status h3dit_sync_status(void* workspace, size_t ws_bytes, void* stream) {
+  if (!workspace || ws_bytes < sizeof(int)) return H3DIT_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return H3DIT_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return H3DIT_ERR_CUDA;
+  if (v != 0 && cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return H3DIT_ERR_CUDA;
+  return v == 0 ? H3DIT_OK : static_cast<h3dit_status>(v);
+}
+
+}  // extern "C"

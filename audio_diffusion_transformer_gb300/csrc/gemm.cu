@@ -1,0 +1,412 @@
+// gemm.cu -- bf16 projection GEMM on tcgen05 tensor cores with fused epilogues.
+//
+// y[M, N] = a[M, K] * w[N, K]^T with fp32 accumulation in TMEM (TensorFold
+// #949 "Precision": bf16 weights and activations, fp32 sums).  One persistent
+// CTA per SM walks 128 x 256 output tiles in a grouped order (8 row-blocks per
+// group, so a wave of tiles shares A and B panels in L2).  Warp roles:
+//   warp 0      TMA producer: 64-wide K slices of A (128 rows) and W (256 rows)
+//               into a 4-stage shared-memory ring (128-byte swizzle)
+//   warp 1      tcgen05.mma issuer (one thread), M=128 N=256 K=16 per op, into
+//               one of two 256-column TMEM accumulators
+//   warps 2..5  epilogue: TMEM -> registers (warp w reads lanes 32*(w%4)..),
+//               bias / GELU / gated residual / q-k norm + rotary, bf16 stores
+// The double accumulator lets the epilogue of tile i overlap the K loop of
+// tile i+1.  No split-K and no atomics: results are deterministic.
+#include <math.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace h3 {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr int GROUP_M = 8;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+
+struct Params {
+  int M, N, K;
+  const __nv_bfloat16* bias;
+  __nv_bfloat16* y;
+  const float* gate;
+  int heads, head_dim, attn_width;
+  __nv_bfloat16 *q, *k, *v, *g;
+  const __nv_bfloat16 *qnorm_w, *knorm_w;
+  const float2* rope_cs;
+  float eps;
+  int* status;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk,
+                                            int& n_blk) {
+  const int group = tile / (GROUP_M * num_n);
+  const int first_m = group * GROUP_M;
+  const int gm = min(num_m - first_m, GROUP_M);
+  const int in_group = tile - group * GROUP_M * num_n;
+  m_blk = first_m + in_group % gm;
+  n_blk = in_group / gm;
+}
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, float* out) {
+  const uint4* v = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 u = __ldg(v + i);
+    out[8 * i + 0] = bf16_lo(u.x);
+    out[8 * i + 1] = bf16_hi(u.x);
+    out[8 * i + 2] = bf16_lo(u.y);
+    out[8 * i + 3] = bf16_hi(u.y);
+    out[8 * i + 4] = bf16_lo(u.z);
+    out[8 * i + 5] = bf16_hi(u.z);
+    out[8 * i + 6] = bf16_lo(u.w);
+    out[8 * i + 7] = bf16_hi(u.w);
+  }
+}
+
+// Plain (not read-only-cache) load, for data this kernel may also write.
+__device__ __forceinline__ void load_bf16x32_rw(const __nv_bfloat16* p, float* out) {
+  const uint4* v = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 u = v[i];
+    out[8 * i + 0] = bf16_lo(u.x);
+    out[8 * i + 1] = bf16_hi(u.x);
+    out[8 * i + 2] = bf16_lo(u.y);
+    out[8 * i + 3] = bf16_hi(u.y);
+    out[8 * i + 4] = bf16_lo(u.z);
+    out[8 * i + 5] = bf16_hi(u.z);
+    out[8 * i + 6] = bf16_lo(u.w);
+    out[8 * i + 7] = bf16_hi(u.w);
+  }
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 u;
+    u.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+    u.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+    u.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+    u.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+    d[i] = u;
+  }
+}
+
+__device__ __forceinline__ float gelu_erf(float x) {
+  return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+}
+
+// Epilogue of a plain / GELU / residual tile: 8 chunks of 32 columns.
+template <int EPI>
+__device__ __forceinline__ void epilogue_rows(const Params& p, uint32_t t_row, int row, int n0) {
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float v[32];
+    tmem_ld32(t_row + c * 32, v);
+    if (row < p.M) {
+      const int col0 = n0 + c * 32;
+      if (p.bias) {
+        float b[32];
+        load_bf16x32(p.bias + col0, b);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += b[j];
+      }
+      __nv_bfloat16* dst = p.y + (size_t)row * p.N + col0;
+      if (EPI == kEpiGelu) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+      } else if (EPI == kEpiResid) {
+        float r[32];
+        load_bf16x32_rw(dst, r);
+        const float4* g4 = reinterpret_cast<const float4*>(p.gate + col0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 g = __ldg(g4 + j);
+          v[4 * j + 0] = fmaf(g.x, v[4 * j + 0], r[4 * j + 0]);
+          v[4 * j + 1] = fmaf(g.y, v[4 * j + 1], r[4 * j + 1]);
+          v[4 * j + 2] = fmaf(g.z, v[4 * j + 2], r[4 * j + 2]);
+          v[4 * j + 3] = fmaf(g.w, v[4 * j + 3], r[4 * j + 3]);
+        }
+      }
+      store_bf16x32(dst, v);
+    }
+  }
+}
+
+// Epilogue of the fused q/k/v/gate projection: one head (HD columns) at a time.
+template <int HD>
+__device__ __forceinline__ void epilogue_qkvg(const Params& p, uint32_t t_row, int row, int n0) {
+  const int A = p.attn_width;
+  const int slab = n0 / A;  // 0 q, 1 k, 2 v, 3 g  (A is a multiple of BN)
+  const int col_in_slab = n0 - slab * A;
+#pragma unroll 1
+  for (int hh = 0; hh < BN / HD; ++hh) {
+    float v[HD];
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) tmem_ld32(t_row + hh * HD + c * 32, v + c * 32);
+    if (row >= p.M) continue;
+    const int head = (col_in_slab + hh * HD) / HD;
+    const int col0 = n0 + hh * HD;
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) {
+      float b[32];
+      load_bf16x32(p.bias + col0 + c * 32, b);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[c * 32 + j] = bf16_round(v[c * 32 + j] + b[j]);
+    }
+    if (slab <= 1) {
+      const __nv_bfloat16* nw = slab == 0 ? p.qnorm_w : p.knorm_w;
+      if (nw) {
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < HD; ++j) ss = fmaf(v[j], v[j], ss);
+        const float inv = 1.0f / sqrtf(ss / (float)HD + p.eps);
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          float w[32];
+          load_bf16x32(nw + c * 32, w);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[c * 32 + j] = v[c * 32 + j] * inv * w[j];
+        }
+      }
+      if (p.rope_cs) {
+        const float4* cs = reinterpret_cast<const float4*>(p.rope_cs + (size_t)row * (HD / 2));
+#pragma unroll
+        for (int j = 0; j < HD / 4; ++j) {
+          const float4 t = __ldg(cs + j);  // (cos, sin) of pairs 2j and 2j+1
+          const float x0 = v[2 * j], y0 = v[2 * j + HD / 2];
+          const float x1 = v[2 * j + 1], y1 = v[2 * j + 1 + HD / 2];
+          v[2 * j] = x0 * t.x - y0 * t.y;
+          v[2 * j + HD / 2] = y0 * t.x + x0 * t.y;
+          v[2 * j + 1] = x1 * t.z - y1 * t.w;
+          v[2 * j + 1 + HD / 2] = y1 * t.z + x1 * t.w;
+        }
+      }
+    }
+    __nv_bfloat16* dst;
+    if (slab == 3) {
+      dst = p.g + (size_t)row * A + head * HD;
+    } else {
+      __nv_bfloat16* base = slab == 0 ? p.q : (slab == 1 ? p.k : p.v);
+      dst = base + ((size_t)head * p.M + row) * HD;
+    }
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) store_bf16x32(dst + c * 32, v + c * 32);
+  }
+}
+
+template <int EPI, int HD>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* acc_full = bars + 2 * STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_m = (p.M + BM - 1) / BM;
+  const int num_n = p.N / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_k = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        int m_blk, n_blk;
+        tile_coords(tile, num_m, num_n, m_blk, n_blk);
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m_blk * BM);
+          tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, n_blk * BN);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN, false, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * BN;
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + k * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // every MMA this thread issued has completed before TMEM is released
+      umma_commit(drain);
+      mbar_drain(drain, 0);
+    }
+  } else {
+    const int quad = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      int m_blk, n_blk;
+      tile_coords(tile, num_m, num_n, m_blk, n_blk);
+      if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const int row = m_blk * BM + quad * 32 + lane;
+      const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16) + acc * BN;
+      if (EPI == kEpiQkvg)
+        epilogue_qkvg<HD>(p, t_row, row, n_blk * BN);
+      else
+        epilogue_rows<EPI>(p, t_row, row, n_blk * BN);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int EPI, int HD>
+cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
+                       cudaStream_t stream) {
+  auto kern = gemm_kernel<EPI, HD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int tiles = ((p.M + BM - 1) / BM) * (p.N / BN);
+  const int sms = num_sms();
+  const int grid = tiles < sms ? tiles : sms;
+  kern<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
+  if (g.M <= 0 || g.N % BN != 0 || g.N <= 0 || g.K % BK != 0 || g.K <= 0)
+    return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  if (!make_tmap_2d(&ta, g.a, g.M, g.K, BM)) return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&tb, g.w, g.N, g.K, BN)) return cudaErrorInvalidValue;
+  Params p;
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.bias = g.bias;
+  p.y = g.y;
+  p.gate = g.gate;
+  p.heads = g.heads;
+  p.head_dim = g.head_dim;
+  p.attn_width = g.attn_width;
+  p.q = g.q;
+  p.k = g.k;
+  p.v = g.v;
+  p.g = g.g;
+  p.qnorm_w = g.qnorm_w;
+  p.knorm_w = g.knorm_w;
+  p.rope_cs = g.rope_cs;
+  p.eps = g.eps;
+  p.status = g.status;
+  switch (epi) {
+    case kEpiStore:
+      return launch_one<kEpiStore, 128>(ta, tb, p, stream);
+    case kEpiGelu:
+      return launch_one<kEpiGelu, 128>(ta, tb, p, stream);
+    case kEpiResid:
+      return launch_one<kEpiResid, 128>(ta, tb, p, stream);
+    case kEpiQkvg:
+      if (g.head_dim == 128) return launch_one<kEpiQkvg, 128>(ta, tb, p, stream);
+      if (g.head_dim == 64) return launch_one<kEpiQkvg, 64>(ta, tb, p, stream);
+      return cudaErrorInvalidValue;
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace h3

@@ -1,0 +1,83 @@
+// internal.h -- declarations shared by the library's translation units (host side).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "h3dit.h"
+
+namespace h3 {
+
+// ---------------------------------------------------------------- GEMM
+enum Epilogue : int {
+  kEpiStore = 0,  // y = bf16(acc [+ bias])
+  kEpiGelu = 1,   // y = bf16(gelu(acc + bias))
+  kEpiResid = 2,  // y = bf16(y + gate * (acc + bias))   (y is the residual, in place)
+  kEpiQkvg = 3    // split into head-major q/k/v with q/k norm + rotary, and row-major g
+};
+
+struct GemmArgs {
+  const __nv_bfloat16* a;  // [M, K]
+  const __nv_bfloat16* w;  // [N, K]
+  int M, N, K;
+  const __nv_bfloat16* bias;  // [N] or null
+  __nv_bfloat16* y;           // [M, N] (store / gelu / resid)
+  const float* gate;          // [N] fp32 (resid)
+  // qkvg epilogue
+  int heads, head_dim, attn_width;
+  __nv_bfloat16 *q, *k, *v, *g;            // q/k/v [H, M, d], g [M, A]
+  const __nv_bfloat16 *qnorm_w, *knorm_w;  // [d] or null
+  const float2* rope_cs;                   // [M, d/2] (cos, sin) or null
+  float eps;
+  int* status;
+};
+
+cudaError_t launch_gemm(int epi, const GemmArgs& args, cudaStream_t stream);
+
+// ---------------------------------------------------------------- attention
+struct AttnArgs {
+  const __nv_bfloat16 *q, *k, *v;  // [H, N, d]
+  int N, H, d, n_prefix, n_video, Tv, ksel;
+  const int* idx;             // [H, Tv, ksel]
+  const __nv_bfloat16* gate;  // [N, A] or null
+  const float* pooled;        // [H, Tv, d] or null
+  __nv_bfloat16* out;         // [N, A]
+  int* status;
+};
+
+cudaError_t launch_attention(const AttnArgs& args, cudaStream_t stream);
+
+// ---------------------------------------------------------------- router
+struct RouterArgs {
+  const __nv_bfloat16 *q, *k, *v;  // [H, N, d]
+  int N, H, d, n_prefix, n_video, Tv, ksel;
+  float* means;   // [3, H, Tv, d]
+  float* scores;  // [H, Tv, Tv]
+  int* idx;       // [H, Tv, ksel]
+  float* pooled;  // [H, Tv, d] or null (skip)
+};
+
+cudaError_t launch_router(const RouterArgs& args, cudaStream_t stream);
+
+// ---------------------------------------------------------------- row kernels
+cudaError_t launch_rms_modulate(const __nv_bfloat16* x, const float* shift, const float* scale,
+                                __nv_bfloat16* h, int rows, int D, float eps, cudaStream_t s);
+cudaError_t launch_rope_table(float2* cs, int rows, int d, float theta, cudaStream_t s);
+cudaError_t launch_f32_to_bf16(const float* z, __nv_bfloat16* x, size_t n, cudaStream_t s);
+cudaError_t launch_euler_fresh(const __nv_bfloat16* x, float* z, float* v_slot, float dt,
+                               size_t n, cudaStream_t s);
+cudaError_t launch_euler_extrap(float* z, const float* v_a, const float* v_b, float coef,
+                                float dt, size_t n, cudaStream_t s);
+
+// ---------------------------------------------------------------- tensor maps
+bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                  uint32_t box_rows);
+bool make_tmap_3d(CUtensorMap* map, const void* base, uint64_t heads, uint64_t rows,
+                  uint64_t cols);
+
+int num_sms();
+
+}  // namespace h3

@@ -1,0 +1,187 @@
+// rows.cu -- HBM-bound row and elementwise kernels of the block and the sampler.
+//
+//  * rms_modulate: h = bf16(x / sqrt(mean(x^2) + eps) * (1 + scale) + shift),
+//    one 128-thread CTA per row, 16-byte loads kept in registers between the
+//    reduction and the write (TensorFold #949 "What it adds": modulated norm;
+//    h3.c README fused gated-AdaLN paragraph: a per-row RMS).
+//  * rope_table: (cos, sin) of p * theta^(-2c/d) per packed row p and pair c,
+//    evaluated in double precision and stored fp32 for the projection epilogue.
+//  * f32_to_bf16: the sampler's latents -> the bf16 residual stream.
+//  * euler_fresh / euler_extrap: v = fp32(x_L), ring store, z += dt * v; or the
+//    linear extrapolation of the last two fresh velocities (h3.c README sampler
+//    paragraph).
+#include <math.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace h3 {
+
+namespace {
+
+constexpr int ROW_THREADS = 128;
+constexpr int MAXV = 8;  // 16-byte vectors per thread: D <= 8 * 8 * 128 = 8192
+
+__global__ void __launch_bounds__(ROW_THREADS)
+    rms_modulate_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ shift,
+                        const float* __restrict__ scale, __nv_bfloat16* __restrict__ h, int D,
+                        float eps) {
+  __shared__ float wsum[ROW_THREADS / 32];
+  const int row = blockIdx.x;
+  const int nvec = D / 8;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * D);
+  uint4 xv[MAXV];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int v = threadIdx.x + i * ROW_THREADS;
+    if (v < nvec) {
+      xv[i] = src[v];
+      const uint32_t w[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float a = bf16_lo(w[e]), b = bf16_hi(w[e]);
+        ss = fmaf(a, a, ss);
+        ss = fmaf(b, b, ss);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < ROW_THREADS / 32; ++w) tot += wsum[w];
+  const float inv = 1.0f / sqrtf(tot / (float)D + eps);
+  uint4* dst = reinterpret_cast<uint4*>(h + (size_t)row * D);
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int v = threadIdx.x + i * ROW_THREADS;
+    if (v < nvec) {
+      const float4 s0 = reinterpret_cast<const float4*>(scale)[2 * v];
+      const float4 s1 = reinterpret_cast<const float4*>(scale)[2 * v + 1];
+      const float4 b0 = reinterpret_cast<const float4*>(shift)[2 * v];
+      const float4 b1 = reinterpret_cast<const float4*>(shift)[2 * v + 1];
+      const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+      const float sh[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      const uint32_t w[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float a = fmaf(bf16_lo(w[e]) * inv, 1.0f + sc[2 * e], sh[2 * e]);
+        const float b = fmaf(bf16_hi(w[e]) * inv, 1.0f + sc[2 * e + 1], sh[2 * e + 1]);
+        o[e] = pack_bf16x2(a, b);
+      }
+      dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+__global__ void rope_table_kernel(float2* cs, int rows, int half, int d, double log_theta) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (size_t)rows * half) return;
+  const int p = (int)(i / half), c = (int)(i % half);
+  const double inv_freq = exp(-2.0 * (double)c / (double)d * log_theta);
+  double sn, cn;
+  sincos((double)p * inv_freq, &sn, &cn);
+  cs[i] = make_float2((float)cn, (float)sn);
+}
+
+__global__ void f32_to_bf16_kernel(const float4* __restrict__ z, uint2* __restrict__ x, size_t n4) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = z[i];
+    x[i] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+  }
+}
+
+__global__ void euler_fresh_kernel(const uint2* __restrict__ x, float4* __restrict__ z,
+                                   float4* __restrict__ v_slot, float dt, size_t n4) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const uint2 u = x[i];
+    const float4 v = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+    float4 zz = z[i];
+    zz.x = fmaf(dt, v.x, zz.x);
+    zz.y = fmaf(dt, v.y, zz.y);
+    zz.z = fmaf(dt, v.z, zz.z);
+    zz.w = fmaf(dt, v.w, zz.w);
+    v_slot[i] = v;
+    z[i] = zz;
+  }
+}
+
+__global__ void euler_extrap_kernel(float4* __restrict__ z, const float4* __restrict__ va,
+                                    const float4* __restrict__ vb, float coef, float dt,
+                                    size_t n4) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = va[i];
+    float4 v = a;
+    if (vb) {
+      const float4 b = vb[i];
+      v.x = fmaf(a.x - b.x, coef, a.x);
+      v.y = fmaf(a.y - b.y, coef, a.y);
+      v.z = fmaf(a.z - b.z, coef, a.z);
+      v.w = fmaf(a.w - b.w, coef, a.w);
+    }
+    float4 zz = z[i];
+    zz.x = fmaf(dt, v.x, zz.x);
+    zz.y = fmaf(dt, v.y, zz.y);
+    zz.z = fmaf(dt, v.z, zz.z);
+    zz.w = fmaf(dt, v.w, zz.w);
+    z[i] = zz;
+  }
+}
+
+int grid_for(size_t n, int threads) {
+  size_t b = (n + threads - 1) / threads;
+  const size_t cap = (size_t)num_sms() * 16;
+  if (b > cap) b = cap;
+  return b < 1 ? 1 : (int)b;
+}
+
+}  // namespace
+
+cudaError_t launch_rms_modulate(const __nv_bfloat16* x, const float* shift, const float* scale,
+                                __nv_bfloat16* h, int rows, int D, float eps, cudaStream_t s) {
+  if (rows <= 0 || D % 8 != 0 || D > 8 * MAXV * ROW_THREADS) return cudaErrorInvalidValue;
+  rms_modulate_kernel<<<rows, ROW_THREADS, 0, s>>>(x, shift, scale, h, D, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(float2* cs, int rows, int d, float theta, cudaStream_t s) {
+  const int half = d / 2;
+  const size_t n = (size_t)rows * half;
+  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(cs, rows, half, d,
+                                                                 log((double)theta));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f32_to_bf16(const float* z, __nv_bfloat16* x, size_t n, cudaStream_t s) {
+  if (n % 4) return cudaErrorInvalidValue;
+  f32_to_bf16_kernel<<<grid_for(n / 4, 256), 256, 0, s>>>(
+      reinterpret_cast<const float4*>(z), reinterpret_cast<uint2*>(x), n / 4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_euler_fresh(const __nv_bfloat16* x, float* z, float* v_slot, float dt,
+                               size_t n, cudaStream_t s) {
+  if (n % 4) return cudaErrorInvalidValue;
+  euler_fresh_kernel<<<grid_for(n / 4, 256), 256, 0, s>>>(
+      reinterpret_cast<const uint2*>(x), reinterpret_cast<float4*>(z),
+      reinterpret_cast<float4*>(v_slot), dt, n / 4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_euler_extrap(float* z, const float* v_a, const float* v_b, float coef,
+                                float dt, size_t n, cudaStream_t s) {
+  if (n % 4) return cudaErrorInvalidValue;
+  euler_extrap_kernel<<<grid_for(n / 4, 256), 256, 0, s>>>(
+      reinterpret_cast<float4*>(z), reinterpret_cast<const float4*>(v_a),
+      reinterpret_cast<const float4*>(v_b), coef, dt, n / 4);
+  return cudaGetLastError();
+}
+
+}  // namespace h3

@@ -1,0 +1,188 @@
+/*
+ * h3dit.h -- C ABI of the GB300 (sm_103a) routed-attention DiT forward.
+ *
+ * The library runs the denoising forward of a joint video + audio diffusion
+ * transformer of the MiniMax-H3 / FastH3 family: DiT blocks over one packed
+ * sequence of text, audio and video rows, with tile-routed (block-sparse)
+ * attention for the video rows.  Operations follow the pages
+ *   "ashhart/TensorFold pull request #949" (FastH3 denoiser on Metal; cited
+ *   below as TensorFold #949) and
+ *   "Antirez/h3.c: MiniMax H3 inference engine for Mac computers" (cited as
+ *   the h3.c README).
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is caller-owned DEVICE memory unless stated as host.
+ *     The library allocates no device memory; scratch comes from the caller's
+ *     workspace (size from h3dit_workspace_bytes).
+ *   - Calls are asynchronous on the given stream: the status returned reports
+ *     argument errors found on the host before any launch, and launch errors.
+ *     Errors raised inside kernels (a bounded wait that ran out) are recorded
+ *     in a status word inside the workspace; h3dit_sync_status() reads and
+ *     clears it.
+ *   - bf16 tensors are IEEE bfloat16 bit patterns (uint16).  Linear weights
+ *     are stored [out, in] row-major (input features contiguous).
+ *   - Row order of the packed sequence: text rows, then audio rows, then video
+ *     rows.  The prefix (text + audio) must be a multiple of the tile (64).
+ *     Video rows are cut into contiguous 64-row tiles; the last may be partial.
+ *   - Results are deterministic: the same inputs give the same bytes.
+ *   - Pointers must be 16-byte aligned; row pitches are dense.
+ */
+#ifndef H3DIT_H_
+#define H3DIT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  H3DIT_OK = 0,
+  H3DIT_ERR_ARG = 1,          /* null pointer or bad scalar argument            */
+  H3DIT_ERR_SHAPE = 2,        /* unsupported or inconsistent shape              */
+  H3DIT_ERR_ALIGN = 3,        /* pointer not 16-byte aligned                    */
+  H3DIT_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required     */
+  H3DIT_ERR_CUDA = 5,         /* a CUDA runtime / driver call failed            */
+  H3DIT_ERR_TIMEOUT = 6,      /* a kernel's bounded wait ran out (device-side)  */
+  H3DIT_ERR_UNSUPPORTED = 7   /* no sm_100-family GPU, or a feature not built   */
+} h3dit_status;
+
+/* Flags of h3dit_shape.flags */
+#define H3DIT_QK_NORM 0x1u   /* per-head RMS norm of q and k with learned weights */
+#define H3DIT_ROPE    0x2u   /* rotary on q and k over the packed row index        */
+#define H3DIT_POOLED  0x4u   /* pooled branch + gate mix for video rows            */
+
+typedef struct {
+  int n_text, n_audio, n_video; /* packed row counts, in this order               */
+  int hidden;                   /* D: residual width (multiple of 256)            */
+  int heads, head_dim;          /* H, d (d = 64 or 128)                           */
+  int attn_width;               /* A = H * d (multiple of 256)                    */
+  int mlp_width;                /* F: MLP inner width (multiple of 256)           */
+  int tile;                     /* routing tile rows; must be 64                  */
+  int topk;                     /* k video tiles kept per query tile (>= 1);      */
+                                /* k >= number of video tiles means dense         */
+  float rms_eps;                /* epsilon of every RMS norm (e.g. 1e-6)          */
+  float rope_theta;             /* rotary base (e.g. 10000)                       */
+  unsigned flags;               /* H3DIT_QK_NORM | H3DIT_ROPE | H3DIT_POOLED      */
+} h3dit_shape;
+
+/* One block's parameters (device pointers, bf16 unless stated).
+ *   w_qkvg [4A, D], b_qkvg [4A]: rows 0..A-1 -> q, A..2A-1 -> k, 2A..3A-1 -> v,
+ *                                3A..4A-1 -> the routing gate g (head-major).
+ *   w_o [D, A], b_o [D];  w1 [F, D], b1 [F];  w2 [D, F], b2 [D]
+ *   mod  fp32 [6, D]: shift1, scale1, gate1, shift2, scale2, gate2
+ *   qnorm_w, knorm_w [d]: per-head RMS-norm weights (used with H3DIT_QK_NORM) */
+typedef struct {
+  const void *w_qkvg, *b_qkvg, *w_o, *b_o, *w1, *b1, *w2, *b2;
+  const float *mod;
+  const void *qnorm_w, *knorm_w;
+} h3dit_block_weights;
+
+/* Bytes of caller-allocated device workspace that h3dit_block_forward,
+ * h3dit_routed_attention and h3dit_denoise_step need for this shape
+ * (0 if the shape is invalid).  One workspace must not be shared by calls
+ * that may run concurrently. */
+size_t h3dit_workspace_bytes(const h3dit_shape* shape);
+
+/* Checks a shape without touching the GPU. */
+h3dit_status h3dit_check_shape(const h3dit_shape* shape);
+
+/*
+ * h3dit_block_forward -- one DiT block, in place on the residual rows.
+ *
+ * TensorFold #949, "What it adds" (block.zig: modulated norm, q/k/v and the
+ * routing gate, head layout, routing, attention, the pooled branch, the out
+ * projection and the MLP) with the precision of its "Precision" list (bf16
+ * weights and activations, fp32 sums, fp32 routing); gated residual adds as
+ * in the h3.c README's fused gated-AdaLN paragraph.  Per block:
+ *   h  = bf16(rms(x) * (1 + scale1) + shift1)
+ *   [q|k|v|g] = bf16(h W_qkvg^T + b_qkvg); q, k <- bf16(rope(rms_d(.) * w))
+ *   routed attention over video tiles (top-k of tile scores + prefix rows),
+ *   dense attention for prefix rows, pooled branch mixed in through g
+ *   x1 = bf16(x + gate1 * (o W_o^T + b_o))
+ *   h2 = bf16(rms(x1) * (1 + scale2) + shift2)
+ *   x2 = bf16(x1 + gate2 * (gelu(h2 W1^T + b1) W2^T + b2))   [u rounded bf16]
+ * x_inout: bf16 [N, D], overwritten with x2.  Workspace as sized above.
+ */
+h3dit_status h3dit_block_forward(const h3dit_shape* shape, const h3dit_block_weights* w,
+                                 void* x_inout, void* workspace, size_t ws_bytes,
+                                 void* stream /* cudaStream_t; NULL = default */);
+
+/*
+ * h3dit_routed_attention -- router + routed/dense attention + pooled branch.
+ *
+ * TensorFold #949, "What it adds" (h3_routing.metal: tile means, tile scores,
+ * top-k and the pooled branch; h3_attention.metal: tile-routed attention with
+ * fp32 scores and an online softmax), "Precision" (softmax weights rounded to
+ * bf16 before the value product) and "Kernel contract" (top-k: NaN ranks as
+ * -inf, ties go to the lower tile).
+ *   q, k, v       bf16 [H, N, d] head-major (row n of head h at (h*N + n)*d)
+ *   gate_or_null  bf16 [N, A]: routing gate; NULL = no pooled mix
+ *   out           bf16 [N, A]: out[n, h*d + c]
+ *   pooled_out_or_null       fp32 [H, Tv, d]: pooled branch per video tile
+ *   topk_idx_out_or_null     int32 [H, Tv, min(k, Tv)]: selected tiles, ascending
+ *   tile_scores_out_or_null  fp32 [H, Tv, Tv]: unscaled tile-mean dot products
+ * Text/audio (prefix) query rows attend to all N rows; a video row of tile i
+ * attends to all prefix rows plus the rows of its selected tiles.  Scale 1/sqrt(d).
+ * The pooled branch and mix run when H3DIT_POOLED is set and gate is given.
+ */
+h3dit_status h3dit_routed_attention(const h3dit_shape* shape, const void* q, const void* k,
+                                    const void* v, const void* gate_or_null, void* out,
+                                    float* pooled_out_or_null, int* topk_idx_out_or_null,
+                                    float* tile_scores_out_or_null, void* workspace,
+                                    size_t ws_bytes, void* stream);
+
+/*
+ * h3dit_denoise_step -- one Euler step of the denoiser, with velocity reuse.
+ *
+ * h3.c README sampler paragraph: passes that run the model produce a fresh
+ * velocity; skipped passes extrapolate it; the latents stay on the device.
+ *   fresh != 0: x = bf16(z); run blocks[block_ids[i]] for i < n_blocks
+ *               (block_ids is a HOST array, blocks a HOST array of structs);
+ *               v = fp32(x); v_ring[n_fresh_so_far % 2] = v
+ *   fresh == 0: a = slot (n_fresh_so_far - 1) % 2, b = the other slot;
+ *               v = v_a + (v_a - v_b) * (sigma_i - sigma_a) / (sigma_a - sigma_b)
+ *               when n_fresh_so_far >= 2, else v = v_a
+ *   then z <- z + dt * v (fp32).
+ * z_inout fp32 [N, D]; v_ring fp32 [2, N, D].
+ */
+h3dit_status h3dit_denoise_step(const h3dit_shape* shape, const h3dit_block_weights* blocks,
+                                const int* block_ids, int n_blocks, float* z_inout,
+                                float* v_ring, int fresh, float sigma_i, float sigma_a,
+                                float sigma_b, int n_fresh_so_far, float dt, void* workspace,
+                                size_t ws_bytes, void* stream);
+
+/*
+ * h3dit_select_blocks -- layer thinning (host only, no GPU).
+ * h3.c README layer-thinning paragraph: rank the blocks' AdaLN gates and keep
+ * the first and last blocks.  score_b = ||gate1_b||_2 + ||gate2_b||_2 in
+ * double precision; the lowest scores are dropped, ties drop the higher index.
+ *   mods: HOST fp32 [n_blocks, 6, hidden]; keep: blocks to keep (>= 2)
+ *   kept_ids: HOST int32 [keep], ascending.
+ */
+h3dit_status h3dit_select_blocks(const float* mods, int n_blocks, int hidden, int keep,
+                                 int* kept_ids);
+
+/*
+ * h3dit_linear -- plain bf16 GEMM on the tensor cores: y = bf16(a w^T [+ b]).
+ * The projection primitive of the block (TensorFold #949 "Precision": bf16
+ * operands, fp32 sums).  a bf16 [M, K], w bf16 [N, K], b bf16 [N] or NULL,
+ * y bf16 [M, N].  K a multiple of 64, N a multiple of 256, M >= 1.
+ */
+h3dit_status h3dit_linear(const void* a, const void* w, const void* b_or_null, void* y, int M,
+                          int N, int K, void* stream);
+
+/* Synchronises the stream, reads the device status word of this workspace,
+ * clears it and returns it (H3DIT_OK or H3DIT_ERR_TIMEOUT). */
+h3dit_status h3dit_sync_status(void* workspace, size_t ws_bytes, void* stream);
+
+const char* h3dit_status_string(h3dit_status s);
+
+/* Library version, e.g. "h3dit 0.1.0 sm_103a". */
+const char* h3dit_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* H3DIT_H_ */
