@@ -1,0 +1,11 @@
+"""GB300 (sm_103a) routed-attention DiT forward: Python binding of libh3dit.so.
+
+The computation lives in the CUDA library; this package only marshals
+arguments (see ``_binding``).  Importing it does not load the library; the
+first call does, and fails loudly if the library has not been built.
+"""
+from ._binding import (  # noqa: F401
+    EXPORTED, H3DIT_POOLED, H3DIT_QK_NORM, H3DIT_ROPE, BlockWeights, H3DitError, Shape,
+    attn_shape, block_forward, block_weights, check_shape, denoise_step, lib, linear, make_shape,
+    routed_attention, select_blocks, sync_status, version, workspace_bytes,
+)

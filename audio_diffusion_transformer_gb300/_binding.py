@@ -1,0 +1,198 @@
+"""ctypes binding of libh3dit.so: argument marshalling only.
+
+Every function here converts its arguments (torch tensors on the GPU, numpy
+arrays on the host, shape objects) into the plain pointers and structs of
+``include/h3dit.h`` and calls the C entry point of the same name.  No step of
+the computation runs here; if the library is missing the import fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libh3dit.so")
+
+H3DIT_QK_NORM = 0x1
+H3DIT_ROPE = 0x2
+H3DIT_POOLED = 0x4
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported or inconsistent shape",
+          3: "pointer not 16-byte aligned", 4: "workspace missing or too small",
+          5: "CUDA call failed", 6: "a kernel wait timed out",
+          7: "unsupported device or feature"}
+
+
+class H3DitError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn}: {STATUS.get(code, code)} (status {code})")
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("n_text", ctypes.c_int), ("n_audio", ctypes.c_int), ("n_video", ctypes.c_int),
+                ("hidden", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("attn_width", ctypes.c_int), ("mlp_width", ctypes.c_int), ("tile", ctypes.c_int),
+                ("topk", ctypes.c_int), ("rms_eps", ctypes.c_float),
+                ("rope_theta", ctypes.c_float), ("flags", ctypes.c_uint)]
+
+
+class BlockWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w_qkvg", "b_qkvg", "w_o", "b_o", "w1", "b1", "w2", "b2", "mod",
+                 "qnorm_w", "knorm_w")]
+
+
+_lib = None
+
+# (name, restype, argtypes)
+_SIGS = [
+    ("h3dit_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(Shape)]),
+    ("h3dit_check_shape", ctypes.c_int, [ctypes.POINTER(Shape)]),
+    ("h3dit_block_forward", ctypes.c_int,
+     [ctypes.POINTER(Shape), ctypes.POINTER(BlockWeights), ctypes.c_void_p, ctypes.c_void_p,
+      ctypes.c_size_t, ctypes.c_void_p]),
+    ("h3dit_routed_attention", ctypes.c_int,
+     [ctypes.POINTER(Shape)] + [ctypes.c_void_p] * 8 + [ctypes.c_void_p, ctypes.c_size_t,
+                                                        ctypes.c_void_p]),
+    ("h3dit_denoise_step", ctypes.c_int,
+     [ctypes.POINTER(Shape), ctypes.POINTER(BlockWeights), ctypes.POINTER(ctypes.c_int),
+      ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
+      ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_void_p,
+      ctypes.c_size_t, ctypes.c_void_p]),
+    ("h3dit_select_blocks", ctypes.c_int,
+     [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    ("h3dit_linear", ctypes.c_int,
+     [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+      ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    ("h3dit_sync_status", ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    ("h3dit_status_string", ctypes.c_char_p, [ctypes.c_int]),
+    ("h3dit_version", ctypes.c_char_p, []),
+]
+
+EXPORTED = [s[0] for s in _SIGS]
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libh3dit.so from the package directory (raises if it is not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is not built; run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, res, args in _SIGS:
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise H3DitError(fn, code)
+
+
+def make_shape(s, flags=None) -> Shape:
+    """ctypes shape from any object with the BlockShape attributes."""
+    if flags is None:
+        flags = ((H3DIT_QK_NORM if getattr(s, "qk_norm", False) else 0)
+                 | (H3DIT_ROPE if getattr(s, "rope", False) else 0)
+                 | (H3DIT_POOLED if getattr(s, "pooled", False) else 0))
+    return Shape(s.n_text, s.n_audio, s.n_video, s.hidden, s.heads, s.head_dim, s.attn_width,
+                 s.mlp_width, s.tile, s.topk, s.rms_eps, s.rope_theta, flags)
+
+
+def attn_shape(s, flags=None) -> Shape:
+    """Shape for h3dit_routed_attention alone (no hidden / MLP widths)."""
+    sh = make_shape(s, flags)
+    sh.hidden = 0
+    sh.mlp_width = 0
+    return sh
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if hasattr(t, "data_ptr"):
+        if not t.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+        return t.data_ptr()
+    return t
+
+
+def _stream(stream):
+    if stream is not None:
+        return stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def workspace_bytes(shape: Shape) -> int:
+    n = lib().h3dit_workspace_bytes(ctypes.byref(shape))
+    if n == 0:
+        raise H3DitError("h3dit_workspace_bytes", 2)
+    return int(n)
+
+
+def check_shape(shape: Shape) -> int:
+    return int(lib().h3dit_check_shape(ctypes.byref(shape)))
+
+
+def block_weights(w: dict) -> BlockWeights:
+    return BlockWeights(*[_ptr(w.get(n)) for n, _ in BlockWeights._fields_])
+
+
+def block_forward(shape: Shape, weights: dict, x, workspace, stream=None):
+    bw = block_weights(weights)
+    _check("h3dit_block_forward", lib().h3dit_block_forward(
+        ctypes.byref(shape), ctypes.byref(bw), _ptr(x), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def routed_attention(shape: Shape, q, k, v, gate, out, workspace, pooled=None, idx=None,
+                     scores=None, stream=None):
+    _check("h3dit_routed_attention", lib().h3dit_routed_attention(
+        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out), _ptr(pooled),
+        _ptr(idx), _ptr(scores), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def denoise_step(shape: Shape, blocks: list, block_ids, z, v_ring, fresh: bool, sigma_i: float,
+                 sigma_a: float, sigma_b: float, n_fresh_so_far: int, dt: float, workspace,
+                 stream=None, _keep=None):
+    arr = (BlockWeights * max(1, len(blocks)))(*[block_weights(b) for b in blocks])
+    ids = (ctypes.c_int * max(1, len(block_ids)))(*[int(i) for i in block_ids])
+    _check("h3dit_denoise_step", lib().h3dit_denoise_step(
+        ctypes.byref(shape), arr, ids, len(block_ids), _ptr(z), _ptr(v_ring), int(bool(fresh)),
+        sigma_i, sigma_a, sigma_b, int(n_fresh_so_far), dt, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def select_blocks(mods: np.ndarray, keep: int) -> list:
+    m = np.ascontiguousarray(mods, dtype=np.float32)
+    L, six, D = m.shape
+    assert six == 6
+    out = np.zeros(max(keep, 1) if keep < L else L, dtype=np.int32)
+    _check("h3dit_select_blocks", lib().h3dit_select_blocks(
+        m.ctypes.data, L, D, keep, out.ctypes.data))
+    return out.tolist()
+
+
+def linear(a, w, b, y, stream=None):
+    M, K = a.shape
+    N = w.shape[0]
+    _check("h3dit_linear", lib().h3dit_linear(_ptr(a), _ptr(w), _ptr(b), _ptr(y), M, N, K,
+                                              _stream(stream)))
+
+
+def sync_status(workspace, stream=None) -> int:
+    return int(lib().h3dit_sync_status(_ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream)))
+
+
+def version() -> str:
+    return lib().h3dit_version().decode()

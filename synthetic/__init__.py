@@ -64,27 +64,40 @@ def uniform(seed: int, name: str, count: int, start: int = 0) -> np.ndarray:
     return ((bits >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
 
 
+_CHUNK = 1 << 18  # pairs per chunk: temporaries stay small and are reused
+
+
 def normal(seed: int, name: str, shape, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
-    """Standard-normal draws (Box-Muller on the uniform stream), float64."""
+    """Standard-normal draws (Box-Muller on the uniform stream), float64.
+
+    Drawn in fixed-size chunks of uniform pairs; the values do not depend on
+    the chunking (every draw is addressed by its counter).
+    """
     n = int(np.prod(shape)) if len(tuple(np.atleast_1d(shape))) else 1
     pairs = (n + 1) // 2
-    u = uniform(seed, name, 2 * pairs)
-    u1, u2 = u[0::2], u[1::2]
-    r = np.sqrt(-2.0 * np.log(u1))
-    t = 2.0 * np.pi * u2
     z = np.empty(2 * pairs, dtype=np.float64)
-    z[0::2] = r * np.cos(t)
-    z[1::2] = r * np.sin(t)
-    return (mean + std * z[:n]).reshape(shape)
+    for p0 in range(0, pairs, _CHUNK):
+        p1 = min(pairs, p0 + _CHUNK)
+        u = uniform(seed, name, 2 * (p1 - p0), start=2 * p0)
+        r = np.sqrt(-2.0 * np.log(u[0::2]))
+        t = 2.0 * np.pi * u[1::2]
+        z[2 * p0:2 * p1:2] = r * np.cos(t)
+        z[2 * p0 + 1:2 * p1:2] = r * np.sin(t)
+    out = z[:n]
+    if std != 1.0:
+        out *= std
+    if mean != 0.0:
+        out += mean
+    return out.reshape(shape)
 
 
 def to_bf16_bits(a: np.ndarray) -> np.ndarray:
     """float -> bf16 storage bits (uint16), round to nearest even via float32."""
     f = np.ascontiguousarray(a, dtype=np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
+    u = f.view(np.uint32)
     nan = np.isnan(f)
-    u = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
-    out = u.astype(np.uint16)
+    r = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+    out = r.astype(np.uint16)
     out[nan] = np.uint16(0x7FC0)
     return out.reshape(np.shape(a))
 
@@ -96,7 +109,27 @@ def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
 
 
 def normal_bf16(seed: int, name: str, shape, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
-    return to_bf16_bits(normal(seed, name, shape, mean, std))
+    """bf16 bits of ``normal(seed, name, shape, mean, std)``, drawn chunk by chunk."""
+    n = int(np.prod(shape)) if len(tuple(np.atleast_1d(shape))) else 1
+    out = np.empty(n, dtype=np.uint16)
+    step = 2 * _CHUNK
+    for e0 in range(0, n, step):
+        e1 = min(n, e0 + step)
+        # draws e0..e1-1 of the stream: pairs e0/2 .. ceil(e1/2)
+        p0, p1 = e0 // 2, (e1 + 1) // 2
+        u = uniform(seed, name, 2 * (p1 - p0), start=2 * p0)
+        r = np.sqrt(-2.0 * np.log(u[0::2]))
+        t = 2.0 * np.pi * u[1::2]
+        z = np.empty(2 * (p1 - p0))
+        z[0::2] = r * np.cos(t)
+        z[1::2] = r * np.sin(t)
+        z = z[:e1 - e0]
+        if std != 1.0:
+            z *= std
+        if mean != 0.0:
+            z += mean
+        out[e0:e1] = to_bf16_bits(z)
+    return out.reshape(shape)
 
 
 # ---------------------------------------------------------------------------

@@ -1,0 +1,278 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bars: top-k index sets bit-exact except near-ties (relative gap < 1e-5),
+outputs within relative L2 2e-2 and cosine 0.998 of the float64 oracle (plus
+tighter per-stage bounds where the arithmetic allows), exact results where the
+float arithmetic is exact, and two runs byte-identical.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic as S
+from helpers import (assert_close, compare_topk, dev_bf16, dev_f32, host_f64, weights_to_device,
+                     weights_to_f64)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def h3():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+    __graft_entry__.build()
+    import audio_diffusion_transformer_gb300 as pkg
+    return pkg
+
+
+def empty_bf16(*shape):
+    return torch.empty(*shape, dtype=torch.bfloat16, device="cuda")
+
+
+# ----------------------------------------------------------------------------- GEMM
+@pytest.mark.parametrize("M,N,K", [(300, 512, 320), (128, 256, 64), (1, 256, 128), (515, 768, 1024)])
+def test_linear_small_integers_bit_exact(h3, M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    a = rng.integers(-8, 9, (M, K)).astype(np.float32)
+    w = rng.integers(-8, 9, (N, K)).astype(np.float32)
+    b = rng.integers(-8, 9, N).astype(np.float32)
+    ad, wd, bd = (dev_bf16(S.to_bf16_bits(x)) for x in (a, w, b))
+    y = empty_bf16(M, N)
+    h3.linear(ad, wd, bd, y)
+    torch.cuda.synchronize()
+    want = oracle.bf16(oracle.linear(a, w, b))  # fp32 sums of small integers are exact
+    assert np.array_equal(host_f64(y), want)
+    y2 = empty_bf16(M, N)
+    h3.linear(ad, wd, None, y2)
+    assert np.array_equal(host_f64(y2), oracle.bf16(oracle.linear(a, w)))
+
+
+def test_linear_random_close(h3):
+    M, N, K = 1000, 1024, 3072
+    a = S.normal_bf16(5, "a", (M, K))
+    w = S.normal_bf16(5, "w", (N, K), std=0.02)
+    y = empty_bf16(M, N)
+    h3.linear(dev_bf16(a), dev_bf16(w), None, y)
+    torch.cuda.synchronize()
+    ref = oracle.linear(S.bf16_bits_to_f64(a), S.bf16_bits_to_f64(w))
+    got = host_f64(y)
+    assert_close(got, ref, "linear", rel=4e-3, cos=0.99999)
+    # within one bf16 ulp of the exact value almost everywhere
+    ulp = np.abs(ref) * 2.0 ** -8 + 1e-30
+    assert np.mean(np.abs(got - ref) <= ulp) > 0.999
+
+
+# ----------------------------------------------------------------------------- attention
+def run_attention(h3, shp, inp, with_gate=True, flags=None):
+    cs = h3.attn_shape(shp, flags)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    q, k, v = (dev_bf16(inp[n]) for n in ("q", "k", "v"))
+    g = dev_bf16(inp["gate"]) if with_gate else None
+    tv, ks = shp.n_video_tiles, min(shp.topk, shp.n_video_tiles)
+    out = empty_bf16(shp.n_rows, shp.attn_width)
+    idx = torch.empty(shp.heads, tv, ks, dtype=torch.int32, device="cuda")
+    sc = torch.empty(shp.heads, tv, tv, dtype=torch.float32, device="cuda")
+    pooled = torch.empty(shp.heads, tv, shp.head_dim, dtype=torch.float32, device="cuda")
+    h3.routed_attention(cs, q, k, v, g, out, ws, pooled=pooled, idx=idx, scores=sc)
+    torch.cuda.synchronize()
+    assert h3.sync_status(ws) == 0
+    return {"o": host_f64(out), "idx": idx.cpu().numpy(), "scores": sc.cpu().double().numpy(),
+            "pooled": pooled.cpu().double().numpy(), "out_t": out}
+
+
+def oracle_attention(shp, inp, with_gate=True, pooled=True, p_bf16=False):
+    q, k, v = (S.bf16_bits_to_f64(inp[n]) for n in ("q", "k", "v"))
+    g = S.bf16_bits_to_f64(inp["gate"]) if with_gate else None
+    return oracle.attention_layer(q, k, v, g, shp.n_prefix, shp.n_video, shp.topk, shp.tile,
+                                  pooled, p_bf16)
+
+
+ATTN_CASES = [
+    # (name, shape, structured)
+    ("tiny_k4", S.CONFIGS[0].shape, 0.0),
+    ("tiny_k4_structured", S.CONFIGS[0].shape, 0.5),
+    ("tiny_k16_dense", S.CONFIGS[0].shape.with_(topk=16), 0.0),
+    ("prefix_ragged_d128", S.BlockShape(64, 64, 300, hidden=256, heads=2, head_dim=128,
+                                        mlp_width=1024, topk=2), 0.3),
+    ("prefix_odd_tiles_d64", S.BlockShape(128, 64, 5 * 64 + 1, hidden=256, heads=3, head_dim=64,
+                                          mlp_width=1024, topk=3), 0.3),
+]
+
+
+@pytest.mark.parametrize("name,shp,structured", ATTN_CASES, ids=[c[0] for c in ATTN_CASES])
+def test_routed_attention_matches_oracle(h3, name, shp, structured):
+    inp = S.attention_inputs(shp, 0x48334455, structured=structured)
+    got = run_attention(h3, shp, inp)
+    ref = oracle_attention(shp, inp)
+    ks = min(shp.topk, shp.n_video_tiles)
+    assert np.allclose(got["scores"], ref["scores"], rtol=1e-4, atol=1e-6)
+    n_tie = compare_topk(got["idx"], ref["idx"], ref["scores"], ks)
+    if n_tie:  # recompute the oracle with the GPU's selections where near-ties differ
+        q, k, v = (S.bf16_bits_to_f64(inp[n]) for n in ("q", "k", "v"))
+        O = oracle.routed_attention(q, k, v, shp.n_prefix, shp.n_video, got["idx"], shp.tile)
+        ref["o_f64"] = oracle.gate_mix(O, S.bf16_bits_to_f64(inp["gate"]), ref["pooled"],
+                                       shp.n_prefix, shp.n_video, shp.tile)
+    assert np.allclose(got["pooled"], ref["pooled"], rtol=1e-4, atol=1e-6)
+    assert_close(got["o"], ref["o_f64"], name)
+    # tighter: against the oracle that also rounds P to bf16
+    refp = oracle_attention(shp, inp, p_bf16=True)
+    if not n_tie:
+        assert_close(got["o"], refp["o_f64"], name + " (bf16 P)", rel=5e-3, cos=0.99995)
+
+
+def test_routed_all_tiles_equals_dense_attention(h3):
+    shp = S.CONFIGS[0].shape.with_(topk=16)
+    inp = S.attention_inputs(shp, 77)
+    got = run_attention(h3, shp, inp, with_gate=False)
+    q, k, v = (S.bf16_bits_to_f64(inp[n]) for n in ("q", "k", "v"))
+    d = shp.head_dim
+    dense = np.stack([oracle.attend(q[h], k[h], v[h], 1 / np.sqrt(d)) for h in range(shp.heads)])
+    dense = dense.transpose(1, 0, 2).reshape(shp.n_rows, -1)
+    assert_close(got["o"], dense, "dense", rel=5e-3, cos=0.99995)
+
+
+def test_attention_constant_v_and_row_stochastic(h3):
+    shp = S.BlockShape(64, 0, 256 + 40, hidden=256, heads=2, head_dim=128, mlp_width=1024, topk=2)
+    inp = S.attention_inputs(shp, 9, with_gate=False)
+    vrow = S.normal_bf16(9, "vrow", (shp.heads, 1, shp.head_dim))
+    inp["v"] = np.ascontiguousarray(np.broadcast_to(vrow, (shp.heads, shp.n_rows, shp.head_dim)))
+    got = run_attention(h3, shp, inp, with_gate=False)
+    want = np.broadcast_to(S.bf16_bits_to_f64(vrow).transpose(1, 0, 2).reshape(1, -1),
+                           got["o"].shape)
+    # P rounded to bf16 but l from unrounded P: |o - v| <= 2^-8 |v| per element
+    assert np.all(np.abs(got["o"] - want) <= 2.0 ** -8 * np.abs(want) + 1e-6)
+
+
+def test_topk_nan_and_tie_rule(h3):
+    # identical K tiles 1 and 2 give equal scores for every query: the lower tile must win
+    shp = S.BlockShape(0, 0, 64 * 6, hidden=256, heads=1, head_dim=64, mlp_width=1024, topk=2)
+    inp = S.attention_inputs(shp, 3, structured=0.5, with_gate=False)
+    k = inp["k"].copy()
+    k[:, 128:192] = k[:, 64:128]
+    inp["k"] = k
+    got = run_attention(h3, shp, inp, with_gate=False)
+    ref = oracle_attention(shp, inp, with_gate=False, pooled=False)
+    assert np.array_equal(got["idx"], ref["idx"])
+    # NaN rows: a NaN in K's tile mean ranks as -inf and never adds a tile
+    k[:, 64 * 3 + 5, 7] = np.uint16(0x7FC0)
+    inp["k"] = k
+    got = run_attention(h3, shp, inp, with_gate=False)
+    ref = oracle_attention(shp, inp, with_gate=False, pooled=False)
+    assert np.array_equal(got["idx"], ref["idx"])
+    assert not np.any(got["idx"] == 3)
+
+
+def test_attention_deterministic(h3):
+    shp = ATTN_CASES[3][1]
+    inp = S.attention_inputs(shp, 21, structured=0.3)
+    a = run_attention(h3, shp, inp)["out_t"]
+    b = run_attention(h3, shp, inp)["out_t"]
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ----------------------------------------------------------------------------- block
+def run_block(h3, shp, seed, x_bits=None, wts=None):
+    w = wts if wts is not None else S.block_weights(shp, seed)
+    xb = x_bits if x_bits is not None else S.hidden_rows(shp, seed)
+    cs = h3.make_shape(shp)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    x = dev_bf16(xb)
+    h3.block_forward(cs, weights_to_device(w), x, ws)
+    torch.cuda.synchronize()
+    assert h3.sync_status(ws) == 0
+    return x, w, xb
+
+
+BLOCK_CASES = [
+    ("tiny_d128", S.BlockShape(64, 64, 192 + 17, hidden=256, heads=2, head_dim=128,
+                               mlp_width=1024, topk=2)),
+    ("tiny_d64_norope", S.BlockShape(0, 128, 300, hidden=512, heads=4, head_dim=64,
+                                     mlp_width=1024, topk=3, rope=False)),
+    ("tiny_dense_nopool", S.BlockShape(64, 0, 256, hidden=256, heads=2, head_dim=128,
+                                       mlp_width=512, topk=8, pooled=False)),
+]
+
+
+@pytest.mark.parametrize("name,shp", BLOCK_CASES, ids=[c[0] for c in BLOCK_CASES])
+def test_block_forward_small(h3, name, shp):
+    x, w, xb = run_block(h3, shp, 31)
+    ref = oracle.block_forward(S.bf16_bits_to_f64(xb), weights_to_f64(w), shp)
+    got = host_f64(x)
+    assert_close(got, ref["x2"], name, rel=2e-3, cos=0.99999)
+    # the residual update itself (x2 - x) must match as well
+    x0 = S.bf16_bits_to_f64(xb)
+    assert_close(got - x0, ref["x2"] - x0, name + " update", rel=3e-2, cos=0.999)
+
+
+def test_block_forward_4096_rows(h3):
+    wl = S.CONFIGS[1]
+    shp = wl.shape
+    x, w, xb = run_block(h3, shp, wl.seed)
+    ref = oracle.block_forward(S.bf16_bits_to_f64(xb), weights_to_f64(w), shp)
+    got = host_f64(x)
+    x0 = S.bf16_bits_to_f64(xb)
+    assert_close(got, ref["x2"], "block 4096")
+    assert_close(got - x0, ref["x2"] - x0, "block 4096 update", rel=5e-2, cos=0.998)
+
+
+def test_block_forward_deterministic(h3):
+    shp = BLOCK_CASES[0][1]
+    a = run_block(h3, shp, 5)[0]
+    b = run_block(h3, shp, 5)[0]
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ----------------------------------------------------------------------------- denoiser
+def test_denoise_fresh_and_extrapolated_steps(h3):
+    shp = BLOCK_CASES[0][1]
+    blocks = [S.block_weights(shp, 100 + b) for b in range(3)]
+    dblocks = [weights_to_device(b) for b in blocks]
+    z0 = S.latents(shp, 7)
+    z = dev_f32(z0)
+    ring = torch.zeros(2, shp.n_rows, shp.hidden, dtype=torch.float32, device="cuda")
+    cs = h3.make_shape(shp)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    ids = [0, 2]
+    sig = oracle.sigma_schedule(4)
+    dt = -0.25
+    # step 0 fresh, step 1 fresh, step 2 skipped (extrapolated), step 3 fresh
+    wo = [weights_to_f64(b) for b in blocks]
+    zr = z0.astype(np.float64)
+    vs = []
+    n_fresh = 0
+    for i, fresh in enumerate([True, True, False, True]):
+        if fresh:
+            h3.denoise_step(cs, dblocks, ids, z, ring, True, sig[i], 0, 0, n_fresh, dt, ws)
+            r = oracle.denoise_forward(zr, wo, shp, dt, ids)
+            vs.append((sig[i], r["v"]))
+            zr = r["z"]
+            n_fresh += 1
+        else:
+            h3.denoise_step(cs, dblocks, ids, z, ring, False, sig[i], vs[-1][0], vs[-2][0],
+                            n_fresh, dt, ws)
+            vh = oracle.extrapolate(vs[-1][1], vs[-2][1], sig[i], vs[-1][0], vs[-2][0])
+            zr = oracle.euler_update(zr, vh, dt)
+        torch.cuda.synchronize()
+        assert h3.sync_status(ws) == 0
+        got = z.cpu().double().numpy()
+        assert_close(got, zr, f"z after step {i}", rel=2e-3, cos=0.99999)
+        # the ring holds the most recent fresh velocity exactly as fp32 of the bf16 rows
+        slot = (n_fresh - 1) % 2
+        vring = ring[slot].cpu().double().numpy()
+        assert_close(vring, vs[-1][1], f"v ring step {i}", rel=2e-2, cos=0.998)
+
+
+def test_euler_step_bit_exact_given_velocity(h3):
+    # with zero blocks the velocity is bf16(z) itself, and z + (-1/8) v is exact in fp32
+    shp = BLOCK_CASES[0][1]
+    z0 = S.latents(shp, 8)
+    z = dev_f32(z0)
+    ring = torch.zeros(2, shp.n_rows, shp.hidden, dtype=torch.float32, device="cuda")
+    cs = h3.make_shape(shp)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    h3.denoise_step(cs, [], [], z, ring, True, 1.0, 0, 0, 0, -0.125, ws)
+    torch.cuda.synchronize()
+    want = oracle.euler_update(z0, oracle.bf16(z0.astype(np.float64)), -0.125)
+    assert np.array_equal(z.cpu().double().numpy(), want)

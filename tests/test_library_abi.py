@@ -1,0 +1,96 @@
+"""Host-only checks of the C-ABI library: it loads, exports every declared entry
+point, rejects bad arguments before touching a GPU, and its host-side layer
+thinning agrees with the oracle."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "h3dit.h")
+
+
+@pytest.fixture(scope="module")
+def h3():
+    import __graft_entry__
+    __graft_entry__.build()
+    import audio_diffusion_transformer_gb300 as pkg
+    return pkg
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(h3dit_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(h3):
+    lib = h3.lib()
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(h3.EXPORTED)
+    assert h3.version().startswith("h3dit")
+
+
+def test_shape_checks_on_host(h3):
+    good = S.CONFIGS[1].shape
+    assert h3.check_shape(h3.make_shape(good)) == 0
+    bad = [good.with_(tile=32), good.with_(n_text=100), good.with_(head_dim=96),
+           good.with_(hidden=3000), good.with_(mlp_width=1000), good.with_(n_video=0),
+           good.with_(attn_width_override=2048)]
+    for b in bad:
+        assert h3.check_shape(h3.make_shape(b)) != 0, b
+    assert h3.check_shape(h3.make_shape(good.with_(topk=0))) == 1
+
+
+def test_workspace_sizes(h3):
+    for wl in S.CONFIGS:
+        s = wl.shape
+        if wl.config_id == 1:
+            n = h3.workspace_bytes(h3.attn_shape(s))
+        else:
+            n = h3.workspace_bytes(h3.make_shape(s))
+        assert n > 0 and n % 256 == 0
+    s3 = S.CONFIGS[2].shape
+    n = h3.workspace_bytes(h3.make_shape(s3))
+    # q, k, v, g, o, h, x at least: 7 * N * D * 2 bytes
+    assert n >= 7 * s3.n_rows * s3.hidden * 2
+    with pytest.raises(h3.H3DitError):
+        h3.workspace_bytes(h3.make_shape(s3.with_(tile=16)))
+
+
+def test_entry_points_reject_bad_arguments_without_gpu(h3):
+    import ctypes
+    lib = h3.lib()
+    s = h3.make_shape(S.CONFIGS[1].shape)
+    # null pointers are refused before any CUDA call
+    assert lib.h3dit_block_forward(ctypes.byref(s), None, None, None, 0, None) == 1
+    assert lib.h3dit_routed_attention(ctypes.byref(s), *([None] * 8), None, 0, None) == 1
+    assert lib.h3dit_linear(None, None, None, None, 1, 256, 64, None) == 1
+    assert lib.h3dit_linear(16, 16, None, 16, 1, 255, 64, None) == 2   # N not a multiple of 256
+    assert lib.h3dit_linear(17, 16, None, 16, 1, 256, 64, None) == 3   # misaligned
+    bad = h3.make_shape(S.CONFIGS[1].shape.with_(n_audio=100))
+    assert lib.h3dit_block_forward(ctypes.byref(bad), None, None, None, 0, None) == 2
+
+
+@pytest.mark.parametrize("L,keep", [(50, 45), (50, 40), (6, 3), (5, 5), (3, 2)])
+def test_select_blocks_matches_oracle(h3, L, keep):
+    rng = np.random.default_rng(L * 100 + keep)
+    mods = (rng.standard_normal((L, 6, 64)) * 0.1).astype(np.float32)
+    got = h3.select_blocks(mods, keep)
+    want = oracle.thin_layers([m.astype(np.float64) for m in mods], keep)
+    assert got == want
+
+
+def test_select_blocks_ties_drop_higher_index(h3):
+    mods = np.zeros((6, 6, 4), np.float32)
+    for b, g in enumerate([5.0, 1.0, 3.0, 1.0, 0.5, 9.0]):
+        mods[b, 2, 0] = g
+    assert h3.select_blocks(mods, 4) == [0, 1, 2, 5]
+    assert h3.select_blocks(mods, 4) == oracle.thin_layers(list(mods.astype(np.float64)), 4)
