@@ -70,7 +70,12 @@ _SIGS = [
     ("h3dit_sync_status", ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     ("h3dit_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("h3dit_version", ctypes.c_char_p, []),
+    ("h3dit_profile_begin", ctypes.c_int, [ctypes.c_int]),
+    ("h3dit_profile_end", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]),
+    ("h3dit_launch_count", ctypes.c_ulonglong, []),
 ]
+
+STAGES = ["norm1", "qkvg", "router", "attention", "out_proj", "norm2", "fc1", "fc2", "sampler"]
 
 EXPORTED = [s[0] for s in _SIGS]
 
@@ -192,6 +197,23 @@ def sync_status(workspace, stream=None) -> int:
     return int(lib().h3dit_sync_status(_ptr(workspace),
                                        workspace.numel() * workspace.element_size(),
                                        _stream(stream)))
+
+
+def profile_begin(max_records: int = 65536):
+    _check("h3dit_profile_begin", lib().h3dit_profile_begin(int(max_records)))
+
+
+def profile_end() -> dict:
+    """{stage: (milliseconds, kernel launches)} summed over the profiled calls."""
+    ms = np.zeros(len(STAGES), np.float32)
+    n = np.zeros(len(STAGES), np.int32)
+    _check("h3dit_profile_end", lib().h3dit_profile_end(ms.ctypes.data, n.ctypes.data,
+                                                        len(STAGES)))
+    return {s: (float(ms[i]), int(n[i])) for i, s in enumerate(STAGES)}
+
+
+def launch_count() -> int:
+    return int(lib().h3dit_launch_count())
 
 
 def version() -> str:

@@ -5,6 +5,9 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+#include <vector>
+
 #include "internal.h"
 
 namespace h3 {
@@ -59,6 +62,43 @@ int num_sms() {
 }
 
 namespace {
+
+// ---------------------------------------------------------------- tracing
+std::atomic<unsigned long long> g_launches{0};
+
+struct Profiler {
+  bool on = false;
+  int max = 0, used = 0;
+  std::vector<cudaEvent_t> ev;   // 2 per record
+  std::vector<int> stage, nlaunch;
+};
+Profiler g_prof;
+
+// Records an event pair around one stage when profiling is on.
+struct StageScope {
+  int rec = -1;
+  unsigned long long l0;
+  cudaStream_t st;
+  StageScope(int id, cudaStream_t s) : st(s) {
+    l0 = g_launches.load();
+    if (g_prof.on && g_prof.used < g_prof.max) {
+      rec = g_prof.used++;
+      g_prof.stage[rec] = id;
+      cudaEventRecord(g_prof.ev[2 * rec], st);
+    }
+  }
+  ~StageScope() {
+    if (rec >= 0) {
+      cudaEventRecord(g_prof.ev[2 * rec + 1], st);
+      g_prof.nlaunch[rec] = (int)(g_launches.load() - l0);
+    }
+  }
+};
+
+inline cudaError_t counted(cudaError_t e, int n) {
+  if (e == cudaSuccess) g_launches += n;
+  return e;
+}
 
 constexpr size_t kAlign = 256;
 constexpr int kMaxRows = 1022 * 64;  // attention key-tile list limit
@@ -192,7 +232,10 @@ h3dit_status run_attention(const h3dit_shape* s, const Dims& m, const Ws& w, voi
   r.scores = scores ? scores : at<float>(ws, w.scores);
   r.idx = idx ? idx : at<int>(ws, w.idx);
   r.pooled = use_pool || pooled ? (pooled ? pooled : at<float>(ws, w.pooled)) : nullptr;
-  H3_TRY(cu(launch_router(r, st)));
+  {
+    StageScope sc(H3DIT_STAGE_ROUTER, st);
+    H3_TRY(cu(counted(launch_router(r, st), 2)));
+  }
   AttnArgs a;
   a.q = q;
   a.k = k;
@@ -209,7 +252,8 @@ h3dit_status run_attention(const h3dit_shape* s, const Dims& m, const Ws& w, voi
   a.pooled = use_pool ? r.pooled : nullptr;
   a.out = out;
   a.status = at<int>(ws, w.status);
-  return cu(launch_attention(a, st));
+  StageScope sc(H3DIT_STAGE_ATTN, st);
+  return cu(counted(launch_attention(a, st), 1));
 }
 
 h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* ws,
@@ -227,10 +271,16 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   float2* rope = at<float2>(ws, w.rope);
   const float* mod = wt->mod;
   const bool use_rope = (s->flags & H3DIT_ROPE) != 0;
-  if (use_rope && !rope_ready) H3_TRY(cu(launch_rope_table(rope, N, m.d, s->rope_theta, st)));
+  if (use_rope && !rope_ready) {
+    StageScope sc(H3DIT_STAGE_SAMPLER, st);
+    H3_TRY(cu(counted(launch_rope_table(rope, N, m.d, s->rope_theta, st), 1)));
+  }
 
   // a1: modulated norm 1
-  H3_TRY(cu(launch_rms_modulate(x, mod + 0 * D, mod + 1 * D, h, N, D, s->rms_eps, st)));
+  {
+    StageScope sc(H3DIT_STAGE_NORM1, st);
+    H3_TRY(cu(counted(launch_rms_modulate(x, mod + 0 * D, mod + 1 * D, h, N, D, s->rms_eps, st), 1)));
+  }
   // a2 + a3: q/k/v/gate projection with q/k norm, rotary and head-major layout
   GemmArgs ga;
   memset(&ga, 0, sizeof(ga));
@@ -254,7 +304,10 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   ga.rope_cs = use_rope ? rope : nullptr;
   ga.eps = s->rms_eps;
   ga.status = status;
-  H3_TRY(cu(launch_gemm(kEpiQkvg, ga, st)));
+  {
+    StageScope sc(H3DIT_STAGE_QKVG, st);
+    H3_TRY(cu(counted(launch_gemm(kEpiQkvg, ga, st), 1)));
+  }
   // a4..a9: router, routed + dense attention, pooled branch and gate mix
   H3_TRY(run_attention(s, m, w, ws, q, k, v, g, o, nullptr, nullptr, nullptr, st));
   // a10: out projection + gated residual (in place on x)
@@ -269,9 +322,15 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   gb.y = x;
   gb.gate = mod + 2 * D;
   gb.status = status;
-  H3_TRY(cu(launch_gemm(kEpiResid, gb, st)));
+  {
+    StageScope sc(H3DIT_STAGE_OUT, st);
+    H3_TRY(cu(counted(launch_gemm(kEpiResid, gb, st), 1)));
+  }
   // a11: modulated norm 2
-  H3_TRY(cu(launch_rms_modulate(x, mod + 3 * D, mod + 4 * D, h, N, D, s->rms_eps, st)));
+  {
+    StageScope sc(H3DIT_STAGE_NORM2, st);
+    H3_TRY(cu(counted(launch_rms_modulate(x, mod + 3 * D, mod + 4 * D, h, N, D, s->rms_eps, st), 1)));
+  }
   // a12: fc1 + GELU
   GemmArgs gc;
   memset(&gc, 0, sizeof(gc));
@@ -283,7 +342,10 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   gc.bias = static_cast<const __nv_bfloat16*>(wt->b1);
   gc.y = u;
   gc.status = status;
-  H3_TRY(cu(launch_gemm(kEpiGelu, gc, st)));
+  {
+    StageScope sc(H3DIT_STAGE_FC1, st);
+    H3_TRY(cu(counted(launch_gemm(kEpiGelu, gc, st), 1)));
+  }
   // a13: fc2 + gated residual (in place on x)
   GemmArgs gd;
   memset(&gd, 0, sizeof(gd));
@@ -296,7 +358,8 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   gd.y = x;
   gd.gate = mod + 5 * D;
   gd.status = status;
-  return cu(launch_gemm(kEpiResid, gd, st));
+  StageScope sc(H3DIT_STAGE_FC2, st);
+  return cu(counted(launch_gemm(kEpiResid, gd, st), 1));
 }
 
 h3dit_status check_weights(const h3dit_shape* s, const h3dit_block_weights* w) {
@@ -412,14 +475,18 @@ h3dit_status h3dit_denoise_step(const h3dit_shape* shape, const h3dit_block_weig
     }
     H3_TRY(device_ok());
     __nv_bfloat16* x = at<__nv_bfloat16>(workspace, ws.x);
-    H3_TRY(cu(launch_f32_to_bf16(z_inout, x, n, st)));
-    if (shape->flags & H3DIT_ROPE)
-      H3_TRY(cu(launch_rope_table(at<float2>(workspace, ws.rope), m.N, m.d, shape->rope_theta,
-                                  st)));
+    {
+      StageScope sc(H3DIT_STAGE_SAMPLER, st);
+      H3_TRY(cu(counted(launch_f32_to_bf16(z_inout, x, n, st), 1)));
+      if (shape->flags & H3DIT_ROPE)
+        H3_TRY(cu(counted(launch_rope_table(at<float2>(workspace, ws.rope), m.N, m.d,
+                                            shape->rope_theta, st), 1)));
+    }
     for (int i = 0; i < n_blocks; ++i)
       H3_TRY(run_block(shape, m, ws, workspace, &blocks[block_ids[i]], x, true, st));
     float* slot = v_ring + (size_t)(n_fresh_so_far % 2) * n;
-    return cu(launch_euler_fresh(x, z_inout, slot, dt, n, st));
+    StageScope sc(H3DIT_STAGE_SAMPLER, st);
+    return cu(counted(launch_euler_fresh(x, z_inout, slot, dt, n, st), 1));
   }
   if (n_fresh_so_far < 1) return H3DIT_ERR_ARG;  // nothing to extrapolate from
   H3_TRY(device_ok());
@@ -430,7 +497,8 @@ h3dit_status h3dit_denoise_step(const h3dit_shape* shape, const h3dit_block_weig
     if (sigma_a == sigma_b) return H3DIT_ERR_ARG;
     coef = (float)(((double)sigma_i - sigma_a) / ((double)sigma_a - sigma_b));
   }
-  return cu(launch_euler_extrap(z_inout, va, vb, coef, dt, n, st));
+  StageScope sc(H3DIT_STAGE_SAMPLER, st);
+  return cu(counted(launch_euler_extrap(z_inout, va, vb, coef, dt, n, st), 1));
 }
 
 h3dit_status h3dit_select_blocks(const float* mods, int n_blocks, int hidden, int keep,
@@ -486,7 +554,55 @@ h3dit_status h3dit_linear(const void* a, const void* w, const void* b_or_null, v
   g.K = K;
   g.bias = static_cast<const __nv_bfloat16*>(b_or_null);
   g.y = static_cast<__nv_bfloat16*>(y);
-  return cu(launch_gemm(kEpiStore, g, static_cast<cudaStream_t>(stream)));
+  return cu(counted(launch_gemm(kEpiStore, g, static_cast<cudaStream_t>(stream)), 1));
+}
+
+unsigned long long h3dit_launch_count(void) { return g_launches.load(); }
+
+h3dit_status h3dit_profile_begin(int max_records) {
+  if (g_prof.on || max_records < 1 || max_records > (1 << 20)) return H3DIT_ERR_ARG;
+  g_prof.ev.assign(2 * (size_t)max_records, nullptr);
+  for (auto& e : g_prof.ev) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      for (auto& f : g_prof.ev)
+        if (f) cudaEventDestroy(f);
+      g_prof.ev.clear();
+      return H3DIT_ERR_CUDA;
+    }
+  }
+  g_prof.stage.assign(max_records, -1);
+  g_prof.nlaunch.assign(max_records, 0);
+  g_prof.max = max_records;
+  g_prof.used = 0;
+  g_prof.on = true;
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_profile_end(float* stage_ms, int* stage_launches, int n_stages) {
+  if (!g_prof.on) return H3DIT_ERR_ARG;
+  g_prof.on = false;
+  h3dit_status rc = H3DIT_OK;
+  for (int i = 0; i < n_stages; ++i) {
+    if (stage_ms) stage_ms[i] = 0.f;
+    if (stage_launches) stage_launches[i] = 0;
+  }
+  for (int r = 0; r < g_prof.used; ++r) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(g_prof.ev[2 * r + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_prof.ev[2 * r], g_prof.ev[2 * r + 1]) != cudaSuccess) {
+      rc = H3DIT_ERR_CUDA;
+      continue;
+    }
+    const int sidx = g_prof.stage[r];
+    if (sidx >= 0 && sidx < n_stages) {
+      if (stage_ms) stage_ms[sidx] += ms;
+      if (stage_launches) stage_launches[sidx] += g_prof.nlaunch[r];
+    }
+  }
+  for (auto& e : g_prof.ev) cudaEventDestroy(e);
+  g_prof.ev.clear();
+  g_prof.used = g_prof.max = 0;
+  return rc;
 }
 
 h3dit_status h3dit_sync_status(void* workspace, size_t ws_bytes, void* stream) {

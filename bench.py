@@ -1,0 +1,442 @@
+#!/usr/bin/env python
+"""Throughput of the routed-attention DiT denoising forward on GB300.
+
+One step = one fresh denoiser step through the C ABI (h3dit_denoise_step):
+bf16(z) -> all DiT blocks of the workload -> v = x_L -> z += dt v.  The
+default workload is 50 blocks at 15,435 packed rows (512 text, 1,024 audio,
+13,899 video; hidden 5,120, 40 heads x 128, MLP 4x GELU, top-k 16 of 218
+video tiles + pooled branch), dt = -1/8.
+
+Prints one JSON line (rank 0).  ``value`` = packed rows/s per DiT block over
+the whole job (rows x blocks x steps x ranks / max-over-ranks time).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload forward50_15435_d5120|block_15435_d5120|block_4096_d3072]
+
+--impl reference times the CPU oracle (float64, numpy) on a bounded sample of
+the same workload on this host's cores.  Multi-GPU runs are independent
+replicas (one per rank, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic as S  # noqa: E402
+
+METRIC = ("packed rows/s per DiT block and s per 50-block forward, % of bf16 TC peak")
+UNIT = "packed rows/s per block"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
+KERNEL_SOURCES = {"gemm": ["gemm.cu", "ptx.cuh"], "attention": ["attention.cu", "ptx.cuh"]}
+
+
+# ----------------------------------------------------------------------------- helpers
+def workload(name):
+    wl = S.config_by_name(name)
+    n_blocks = wl.n_blocks if wl.config_id == 4 else 1
+    return wl, n_blocks
+
+
+def block_flops(s):
+    """Algorithmic flops of one block (2 per MAC): the four projections plus
+    the attention the method performs (prefix rows over all N keys, video rows
+    over the prefix and k selected tiles of 64 rows)."""
+    N, D, A, F = s.n_rows, s.hidden, s.attn_width, s.mlp_width
+    gemm = 2.0 * N * (D * 4 * A + A * D + D * F + F * D)
+    k = min(s.topk, s.n_video_tiles)
+    attn = 4.0 * s.head_dim * s.heads * (s.n_prefix * N + s.n_video * (s.n_prefix + k * 64))
+    return gemm, attn
+
+
+def stage_flops(s):
+    N, D, A, F = s.n_rows, s.hidden, s.attn_width, s.mlp_width
+    _, attn = block_flops(s)
+    return {"qkvg": 2.0 * N * D * 4 * A, "out_proj": 2.0 * N * A * D, "fc1": 2.0 * N * D * F,
+            "fc2": 2.0 * N * F * D, "attention": attn}
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return FALLBACK_PEAKS, "fallback"
+
+
+def source_sha(kernel):
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(kernel, []):
+        with open(os.path.join(ROOT, "audio_diffusion_transformer_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, stage, workload_name):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source
+    is unchanged since it was captured; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            for ln in f:
+                if ln.startswith("#") or not ln.strip():
+                    continue
+                k, st, wl, sha, nbytes = ln.split()[:5]
+                if k == kernel and st == stage and wl == workload_name and sha == source_sha(kernel):
+                    return int(float(nbytes))
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) < 10:
+                    continue
+                if self.bus_id and self.bus_id[-12:] not in parts[1].lower():
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = sorted(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None,
+                "sm_max_mhz": float(rows[0][3]) if rows[0][3].replace(".", "").isdigit() else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_block_sample(shape, rng_seed=0):
+    """Times the oracle on a bounded sample of one block of ``shape`` and scales it
+    to the whole block.  Returns (seconds per block, description)."""
+    import numpy as np
+
+    import oracle as O
+    rng = np.random.default_rng(rng_seed)
+    s = shape
+    N, D, A, F, H, d = s.n_rows, s.hidden, s.attn_width, s.mlp_width, s.heads, s.head_dim
+    R = 64
+    w = {"w_qkvg": O.bf16(rng.standard_normal((4 * A, D)) * 0.02),
+         "b_qkvg": O.bf16(rng.standard_normal(4 * A) * 0.02),
+         "w_o": O.bf16(rng.standard_normal((D, A)) * 0.02), "b_o": np.zeros(D),
+         "w1": O.bf16(rng.standard_normal((F, D)) * 0.02), "b1": np.zeros(F),
+         "w2": O.bf16(rng.standard_normal((D, F)) * 0.02), "b2": np.zeros(D),
+         "mod": rng.standard_normal((6, D)) * 0.1}
+    x = O.bf16(rng.standard_normal((R, D)))
+    # row-local stages on R rows
+    t0 = time.perf_counter()
+    h = O.rms_modulate(x, w["mod"][0], w["mod"][1])
+    qkvg = O.bf16(O.linear(h, w["w_qkvg"], w["b_qkvg"]))
+    O.qkv_heads(qkvg, H, d, np.ones(d), np.ones(d))
+    o = O.bf16(qkvg[:, :A])
+    x1 = O.bf16(x + w["mod"][2] * O.linear(o, w["w_o"], w["b_o"]))
+    h2 = O.rms_modulate(x1, w["mod"][3], w["mod"][4])
+    u = O.bf16(O.gelu_erf(O.linear(h2, w["w1"], w["b1"])))
+    O.bf16(x1 + w["mod"][5] * O.linear(u, w["w2"], w["b2"]))
+    t_rows = (time.perf_counter() - t0) * N / R
+    # router over all tiles, attention for a sample of query tiles of a few heads
+    hs = min(H, 4)
+    Q = O.bf16(rng.standard_normal((hs, N, d)))
+    K = O.bf16(rng.standard_normal((hs, N, d)))
+    V = O.bf16(rng.standard_normal((hs, N, d)))
+    t0 = time.perf_counter()
+    mq = O.tile_means(Q, s.n_prefix, s.n_video)
+    mk = O.tile_means(K, s.n_prefix, s.n_video)
+    mv = O.tile_means(V, s.n_prefix, s.n_video)
+    Sc = O.tile_scores(mq, mk)
+    idx = O.topk_select(Sc, s.topk)
+    O.pooled_branch(Sc, mv, d)
+    t_router = (time.perf_counter() - t0) * H / hs
+    tv = s.n_video_tiles
+    vt = [(h, i) for h in range(hs) for i in (0, tv // 2)]
+    t0 = time.perf_counter()
+    O.routed_attention(Q, K, V, s.n_prefix, s.n_video, idx, tiles=vt)
+    t_vid = (time.perf_counter() - t0) * (H * tv) / len(vt)
+    t_pre = 0.0
+    if s.n_prefix:
+        t0 = time.perf_counter()
+        for h in range(hs):
+            O.attend(Q[h, :64], K[h], V[h], 1.0 / math.sqrt(d))
+        t_pre = (time.perf_counter() - t0) * (H * s.n_prefix / 64) / hs
+    total = t_rows + t_router + t_vid + t_pre
+    desc = (f"one block of the {N}-row shape, float64 oracle: row-local stages on {R} rows "
+            f"(x{N / R:.0f}), router on {hs} of {H} heads (x{H / hs:.0f}), attention on "
+            f"{len(vt)} video query tiles (x{H * tv / len(vt):.0f}) and {hs} prefix 64-row "
+            f"chunks (x{H * s.n_prefix / 64 / hs:.0f}); scaled to the whole block")
+    return total, desc
+
+
+def blas_threads():
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(v, "").isdigit():
+            return int(os.environ[v])
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(shape, samples=1):
+    best = None
+    desc = ""
+    for _ in range(samples):
+        t, desc = oracle_block_sample(shape)
+        best = t if best is None else min(best, t)
+    return {"value": shape.n_rows / best, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": desc, "s_per_block": best}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def make_blocks(torch, shape, n_blocks, seed, dev):
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    D, A, F, d = shape.hidden, shape.attn_width, shape.mlp_width, shape.head_dim
+    blocks = []
+
+    def rn(*sz, std=0.02, mean=0.0, dtype=torch.bfloat16):
+        t = torch.randn(*sz, generator=g, device=dev, dtype=torch.float32)
+        return (t * std + mean).to(dtype).contiguous()
+
+    for _ in range(n_blocks):
+        blocks.append({"w_qkvg": rn(4 * A, D), "b_qkvg": rn(4 * A), "w_o": rn(D, A), "b_o": rn(D),
+                       "w1": rn(F, D), "b1": rn(F), "w2": rn(D, F), "b2": rn(D),
+                       "mod": rn(6, D, std=0.1, dtype=torch.float32),
+                       "qnorm_w": rn(d, mean=1.0), "knorm_w": rn(d, mean=1.0)})
+    return blocks
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import audio_diffusion_transformer_gb300 as h3
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl, n_blocks = workload(args.workload)
+    shape = wl.shape
+    N, D = shape.n_rows, shape.hidden
+    cs = h3.make_shape(shape)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device=dev)
+    blocks = make_blocks(torch, shape, n_blocks, wl.seed + 1000 * rank, dev)
+    ids = list(range(n_blocks))
+    gz = torch.Generator(device=dev)
+    gz.manual_seed(wl.seed + 7 + 1000 * rank)
+    z0 = torch.randn(N, D, generator=gz, device=dev, dtype=torch.float32)
+    z = z0.clone()
+    ring = torch.zeros(2, N, D, dtype=torch.float32, device=dev)
+    dt = -0.125
+    stream = torch.cuda.current_stream()
+
+    def step():
+        h3.denoise_step(cs, blocks, ids, z, ring, True, 1.0, 0.0, 0.0, 0, dt, ws,
+                        stream=stream.cuda_stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        z.copy_(z0)
+        step()
+    torch.cuda.synchronize()
+    if h3.sync_status(ws) != 0:
+        raise SystemExit("device status error after warm-up")
+    barrier()
+    torch.cuda.synchronize()
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except AttributeError:
+        pass
+    sampler = ClockSampler(bus)
+    sampler.start()
+    time.sleep(0.3)
+    h3.profile_begin(16 * n_blocks * args.steps + 64)
+    l0 = h3.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    stages = h3.profile_end()
+    launches = h3.launch_count() - l0
+    clocks = sampler.stop()
+    barrier()
+    ms = e0.elapsed_time(e1)
+    if h3.sync_status(ws) != 0:
+        raise SystemExit("device status error in the timed region")
+    ms_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(t.item())
+
+    # end to end through the C ABI with host buffers: H2D z, the step, D2H z
+    z_host = z0.cpu().pin_memory()
+    z_back = torch.empty_like(z_host).pin_memory()
+    e2e_ms = None
+    if not args.no_e2e:
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            z.copy_(z_host, non_blocking=True)
+            step()
+            z_back.copy_(z, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_ms = (time.perf_counter() - t0) * 1e3
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        assert torch.isfinite(z_back).all().item()
+
+    if rank != 0:
+        return None
+    K = args.steps
+    rows_blocks = N * n_blocks * K * world
+    value = rows_blocks / (ms_max / 1e3)
+    gemm_f, attn_f = block_flops(shape)
+    step_flops = n_blocks * (gemm_f + attn_f)
+    pk, pk_kind = peaks()
+    peak_tc = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    achieved_total = step_flops * K / (ms_max / 1e3) / 1e12
+    sf = stage_flops(shape)
+    # dominant kernel: the stage with the largest total time
+    dom = max(stages, key=lambda k: stages[k][0])
+    tc_stage = dom if dom in sf else max((k for k in sf), key=lambda k: stages[k][0])
+    st_ms, st_n = stages[tc_stage]
+    per_launch_ms = st_ms / max(st_n, 1)
+    kernel = "attention" if tc_stage == "attention" else "gemm"
+    roofline = {"bound": "tensor", "kernel": f"{kernel}:{tc_stage}",
+                "achieved": sf[tc_stage] / (per_launch_ms / 1e3) / 1e12, "peak": peak_tc,
+                "peak_kind": f"bf16 sustained, {pk_kind}", "unit": "TFLOP/s",
+                "traffic": recorded_traffic(kernel, tc_stage, wl.name),
+                "launch_ms": per_launch_ms}
+    roofline["frac"] = roofline["achieved"] / peak_tc
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_max / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "n_rows": N, "n_text": shape.n_text,
+                   "n_audio": shape.n_audio, "n_video": shape.n_video, "n_blocks": n_blocks,
+                   "hidden": D, "heads": shape.heads, "head_dim": shape.head_dim,
+                   "mlp": f"{shape.mlp_width // D}x GELU", "topk": shape.topk, "tile": shape.tile,
+                   "dt": dt, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (each block reads its own 682 MB of weights)"},
+        "s_per_forward": ms_max / K / 1e3 * (50 / n_blocks),
+        "tc_frac_of_peak": achieved_total / peak_tc,
+        "achieved_tflops": achieved_total,
+        "roofline": roofline,
+        "stages_ms_per_step": {k: v[0] / K for k, v in stages.items()},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    if e2e_ms is not None:
+        out["e2e"] = {"value": rows_blocks / (e2e_ms / 1e3), "unit": UNIT,
+                      "h2d_bytes_per_step": N * D * 4, "d2h_bytes_per_step": N * D * 4}
+    if not args.no_cpu_baseline and world == 1:
+        out["cpu_baseline"] = cpu_baseline(shape)
+        out["cpu_baseline"].pop("s_per_block")
+    return out
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    wl, n_blocks = workload(args.workload)
+    shape = wl.shape
+    for _ in range(args.warmup):
+        oracle_block_sample(shape)
+    tot = 0.0
+    desc = ""
+    for _ in range(args.steps):
+        t, desc = oracle_block_sample(shape)
+        tot += t
+    value = shape.n_rows * args.steps / tot
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot / args.steps * 1e3 * n_blocks, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "n_rows": shape.n_rows, "n_blocks": n_blocks},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="forward50_15435_d5120")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl")
+        out = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

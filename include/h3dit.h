@@ -173,6 +173,32 @@ h3dit_status h3dit_select_blocks(const float* mods, int n_blocks, int hidden, in
 h3dit_status h3dit_linear(const void* a, const void* w, const void* b_or_null, void* y, int M,
                           int N, int K, void* stream);
 
+/*
+ * Stage timing (tracing).  Between h3dit_profile_begin and h3dit_profile_end
+ * the block, attention and denoiser entry points record a CUDA event pair on
+ * the caller's stream around each stage below; h3dit_profile_end waits for
+ * the recorded events, writes the summed milliseconds and the number of
+ * kernel launches per stage, and releases the events.  Off by default; one
+ * profiling session per process at a time (not thread-safe).
+ */
+#define H3DIT_N_STAGES 9
+enum {
+  H3DIT_STAGE_NORM1 = 0,   /* modulated norm before attention            */
+  H3DIT_STAGE_QKVG = 1,    /* q/k/v/gate projection + heads epilogue      */
+  H3DIT_STAGE_ROUTER = 2,  /* tile means, scores, top-k, pooled branch    */
+  H3DIT_STAGE_ATTN = 3,    /* routed + dense attention + gate mix         */
+  H3DIT_STAGE_OUT = 4,     /* out projection + gated residual             */
+  H3DIT_STAGE_NORM2 = 5,   /* modulated norm before the MLP               */
+  H3DIT_STAGE_FC1 = 6,     /* fc1 + GELU                                  */
+  H3DIT_STAGE_FC2 = 7,     /* fc2 + gated residual                        */
+  H3DIT_STAGE_SAMPLER = 8  /* rotary table, latent cast, Euler/extrapolate */
+};
+h3dit_status h3dit_profile_begin(int max_records);
+h3dit_status h3dit_profile_end(float* stage_ms, int* stage_launches, int n_stages);
+
+/* Number of kernels this library has launched in this process so far. */
+unsigned long long h3dit_launch_count(void);
+
 /* Synchronises the stream, reads the device status word of this workspace,
  * clears it and returns it (H3DIT_OK or H3DIT_ERR_TIMEOUT). */
 h3dit_status h3dit_sync_status(void* workspace, size_t ws_bytes, void* stream);
