@@ -57,6 +57,8 @@ _SIGS = [
     ("h3dit_routed_attention", ctypes.c_int,
      [ctypes.POINTER(Shape)] + [ctypes.c_void_p] * 8 + [ctypes.c_void_p, ctypes.c_size_t,
                                                         ctypes.c_void_p]),
+    ("h3dit_routed_attention_static", ctypes.c_int,
+     [ctypes.POINTER(Shape)] + [ctypes.c_void_p] * 8 + [ctypes.c_void_p]),
     ("h3dit_denoise_step", ctypes.c_int,
      [ctypes.POINTER(Shape), ctypes.POINTER(BlockWeights), ctypes.POINTER(ctypes.c_int),
       ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
@@ -163,6 +165,14 @@ def routed_attention(shape: Shape, q, k, v, gate, out, workspace, pooled=None, i
         ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out), _ptr(pooled),
         _ptr(idx), _ptr(scores), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def routed_attention_static(shape: Shape, q, k, v, gate, out, pooled=None, idx=None,
+                            scores=None, stream=None):
+    """h3dit_routed_attention on the library's fixed scratch array (no workspace)."""
+    _check("h3dit_routed_attention_static", lib().h3dit_routed_attention_static(
+        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out), _ptr(pooled),
+        _ptr(idx), _ptr(scores), _stream(stream)))
 
 
 def denoise_step(shape: Shape, blocks: list, block_ids, z, v_ring, fresh: bool, sigma_i: float,

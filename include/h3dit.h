@@ -134,6 +134,37 @@ h3dit_status h3dit_routed_attention(const h3dit_shape* shape, const void* q, con
                                     size_t ws_bytes, void* stream);
 
 /*
+ * h3dit_routed_attention_static -- h3dit_routed_attention without a workspace.
+ *
+ * No counterpart on the pages: this is a library convenience.  It is meant for
+ * callers that cannot call cudaMalloc: code inside a framework that owns all
+ * device memory, plugins that may not touch the host process's allocator, or
+ * code under a fixed memory budget where an allocation would synchronise the
+ * device.  Same arguments and results as h3dit_routed_attention, minus the
+ * workspace: scratch comes from a 4 MiB array compiled into the library, which
+ * every GPU that loads the library holds until the process exits.
+ *   - Returns H3DIT_ERR_WORKSPACE, before any launch, when the shape needs more
+ *     than 4 MiB of scratch (the attention-only h3dit_workspace_bytes of the
+ *     shape, i.e. with hidden = mlp_width = 0, must be <= 4 MiB; for example
+ *     1,024 rows x 4 heads x 64 fits, 4,096 rows x 24 heads x 128 does not).
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree.
+ *   - All calls share the array and it keeps the previous call's contents; the
+ *     call clears the part that must start at zero (the device status word) on
+ *     its stream.  Calls whose kernels overlap on the GPU (other streams, other
+ *     host threads) race on the array: serialise them.
+ *   - Device-side wait timeouts are not reported (h3dit_sync_status needs a
+ *     workspace); the status word is cleared by the next call.
+ */
+h3dit_status h3dit_routed_attention_static(const h3dit_shape* shape, const void* q,
+                                           const void* k, const void* v,
+                                           const void* gate_or_null, void* out,
+                                           float* pooled_out_or_null,
+                                           int* topk_idx_out_or_null,
+                                           float* tile_scores_out_or_null, void* stream);
+
+/*
  * h3dit_denoise_step -- one Euler step of the denoiser, with velocity reuse.
  *
  * h3.c README sampler paragraph: passes that run the model produce a fresh
