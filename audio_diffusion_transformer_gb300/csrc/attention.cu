@@ -11,17 +11,21 @@
 //     key tile carries a 2-bit mask saying which of the two query tiles chose
 //     it; scores of the other half are masked to -inf, so every row sees
 //     exactly its own key set.
-// The KV loop walks the key-tile list two 64-row tiles (128 keys) per step.
+// CTAs are ordered head-major (all units of head 0, then head 1, ...), so a
+// wave of CTAs shares one head's K/V in L2.  The KV loop walks the key-tile
+// list two 64-row tiles (128 keys) per step.
 // K and V tiles are gathered per step with one TMA box per 64 x 64 piece into
 // a 2-stage ring (128-byte swizzle, no multicast).
 //   warp 0      TMA producer (Q once, then K and V per step)
 //   warp 1      MMA issuer: S = Q K^T (M=128, N=128, fp32 in TMEM, double
 //               buffered) and O += P V (M=128, N=d, V read as an MN-major operand)
-//   warps 2..5  softmax: thread = query row (TMEM lane); scores scaled into the
-//               log2 domain; lazily rescaled running max (O is rescaled in TMEM
-//               only when the row max grows by more than 2^8); P = exp2(s - m)
-//               rounded to bf16 and written to shared memory in the swizzled
-//               K-major layout the MMA reads; l sums the unrounded weights.
+//   warps 2..5  softmax: thread = query row (TMEM lane); one TMEM read of the
+//               row's 128 scores per step, scaled into the log2 domain; lazily
+//               rescaled running max (O is rescaled in TMEM only when the row
+//               max grows by more than 2^8); P = exp2(s - m) rounded to bf16,
+//               computed before waiting for the previous step's PV, then
+//               written to shared memory in the swizzled K-major layout the MMA
+//               reads; l sums the unrounded weights.
 //               Epilogue: O / l, + gate * pooled for video rows, bf16 store.
 #include <math.h>
 
@@ -92,8 +96,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.x % p.H;
-  const int unit = blockIdx.x / p.H;
+  // head-major order: a wave of CTAs works on one or two heads, so their K/V stay in L2
+  const int n_units = p.n_pre_units + (p.Tv + 1) / 2;
+  const int h = blockIdx.x / n_units;
+  const int unit = blockIdx.x % n_units;
   const bool is_prefix = unit < p.n_pre_units;
   const int vu = unit - p.n_pre_units;
   const int ta = 2 * vu, tb = 2 * vu + 1;  // video query tiles of a video unit
@@ -268,22 +274,32 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int nva = ((e0 >> half) & 1) ? min(64, p.N - (e0 >> 2)) : 0;
       const int nvb = ((e1 >> half) & 1) ? min(64, p.N - (e1 >> 2)) : 0;
       const uint32_t s_addr = t_lane + sb * 128;
-      // pass 1: row max of the scaled, masked scores
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float s[32];
-        tmem_ld32(s_addr + c * 32, s);
-        const int nv = c < 2 ? nva : nvb;
-        const int j0 = (c & 1) * 32;
+      // scores of this row for the step's 128 keys, scaled to the log2 domain and masked
+      float sv[128];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j0 + j < nv) mx = fmaxf(mx, s[j] * sl2);
-        }
+      for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sv + c * 32);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 128; ++j) {
+        const bool valid = (j < 64) ? (j < nva) : (j - 64 < nvb);
+        sv[j] = valid ? sv[j] * sl2 : -INFINITY;
+        mx = fmaxf(mx, sv[j]);
       }
       const bool need = mx > m_run + kRescaleLog2;
       const float m_new = need ? mx : m_run;
       const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      // P = exp2(s - m) rounded to bf16; l sums the unrounded weights
+      uint32_t pk[64];
+      float lsum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 128; j += 2) {
+        const float p0 = ex2_approx(sv[j] - m_use);
+        const float p1 = ex2_approx(sv[j + 1] - m_use);
+        lsum += p0;
+        lsum += p1;
+        pk[j >> 1] = pack_bf16x2(p0, p1);
+      }
       if (t > 0) {
         // PV of the previous step must be done: it reads the single P buffer and updates O
         if (!mbar_wait(pv_done, (t - 1) & 1, abort_flag, p.status)) {
@@ -302,33 +318,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      l_run *= alpha;
+      l_run = l_run * alpha;
       m_run = m_new;
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      // pass 2: P = exp2(s - m) -> bf16 -> swizzled shared memory; l += sum of unrounded P
-      float lsum = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float s[32];
-        tmem_ld32(s_addr + c * 32, s);
-        const int nv = c < 2 ? nva : nvb;
-        const int j0 = (c & 1) * 32;
-        uint32_t pk[16];
+      // keys 64b..64b+63 -> column block b; 16-byte unit u holds keys 8u..8u+7 of the block
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float p0 = (j0 + j < nv) ? ex2_approx(fmaf(s[j], sl2, -m_use)) : 0.f;
-          const float p1 = (j0 + j + 1 < nv) ? ex2_approx(fmaf(s[j + 1], sl2, -m_use)) : 0.f;
-          lsum += p0;
-          lsum += p1;
-          pk[j >> 1] = pack_bf16x2(p0, p1);
-        }
-        // keys 32c..32c+31 -> 64-key column block c/2, 16-byte units (c&1)*4 .. +3
-        uint8_t* rowp = sP + (c >> 1) * L::CHUNK + row * 128;
+      for (int b = 0; b < 2; ++b) {
+        uint8_t* rowp = sP + b * L::CHUNK + row * 128;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int unit16 = (c & 1) * 4 + u;
-          uint4 val = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-          *reinterpret_cast<uint4*>(rowp + ((unit16 ^ (row & 7)) << 4)) = val;
+        for (int u = 0; u < 8; ++u) {
+          const int w0 = b * 32 + u * 4;
+          *reinterpret_cast<uint4*>(rowp + ((u ^ (row & 7)) << 4)) =
+              make_uint4(pk[w0], pk[w0 + 1], pk[w0 + 2], pk[w0 + 3]);
         }
       }
       l_run += lsum;

@@ -8,11 +8,14 @@
 // Kernel 1 (tile_means): one CTA per (video tile, head, tensor of q/k/v),
 //   thread c sums column c over the tile's valid rows in row order and divides
 //   by the valid-row count.  Reads each video row of q, k, v once (HBM-bound).
-// Kernel 2 (route): one CTA per (query tile i, head h):
-//   S[h,i,j] = sum_c mq[h,i,c] mk[h,j,c] (fp32 FMA chain, c ascending);
+// Kernel 2 (route): one CTA (8 warps) per (query tile i, head h):
+//   S[h,i,j] = sum_c mq[h,i,c] mk[h,j,c]: one warp per j, lane l sums dims
+//   4l..4l+3 in order, then a fixed xor-shuffle tree across the lanes;
 //   rank_j = #{j' : s_j' > s_j or (s_j' == s_j and j' < j)} with NaN -> -inf;
 //   tile j is kept iff rank_j < k; kept tiles are written ascending;
-//   pooled[h,i,:] = sum_j softmax_j(S[h,i,j] / sqrt(d)) mv[h,j,:] (sums in j order).
+//   pooled[h,i,:] = sum_j softmax_j(S[h,i,j] / sqrt(d)) mv[h,j,:]: max and
+//   denominator by fixed block reductions, the weighted sum in j order over
+//   contiguous j ranges whose partial sums are added in range order.
 // Every reduction has a fixed order, so results are deterministic.
 #include <math.h>
 
@@ -43,31 +46,71 @@ __global__ void tile_means_kernel(const __nv_bfloat16* __restrict__ q,
 
 __device__ __forceinline__ float rank_key(float s) { return isnan(s) ? -INFINITY : s; }
 
+// Fixed-order block reductions over ROUTE_THREADS threads (8 warps).
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < ROUTE_THREADS / 32; ++w) r = fmaxf(r, red[w]);
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < ROUTE_THREADS / 32; ++w) r += red[w];
+  __syncthreads();
+  return r;
+}
+
 __global__ void __launch_bounds__(ROUTE_THREADS)
     route_kernel(const float* __restrict__ means, float* __restrict__ scores,
                  int* __restrict__ idx, float* __restrict__ pooled, int H, int d, int Tv,
                  int ksel) {
   extern __shared__ float sh[];
-  float* mq = sh;         // [d]
-  float* s = sh + d;      // [Tv]
-  float* w = s + Tv;      // [Tv]
+  float* s = sh;                               // [Tv] scores
+  float* w = s + Tv;                           // [Tv] pooled weights
   int* keep = reinterpret_cast<int*>(w + Tv);  // [Tv]
-  __shared__ float red[2];
+  float* part = reinterpret_cast<float*>(keep + Tv);  // [ROUTE_THREADS] pooled partials
+  __shared__ float red[ROUTE_THREADS / 32];
   const int i = blockIdx.x, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* mQ = means + ((size_t)0 * H + h) * Tv * d;
   const float* mK = means + ((size_t)1 * H + h) * Tv * d;
   const float* mV = means + ((size_t)2 * H + h) * Tv * d;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) mq[c] = mQ[(size_t)i * d + c];
-  __syncthreads();
-  for (int j = threadIdx.x; j < Tv; j += blockDim.x) {
-    const float* kr = mK + (size_t)j * d;
+  // scores: one warp per key tile j; lane l holds dims 4l..4l+3 (+128 per round), then a
+  // fixed xor-tree across lanes
+  const int d4 = d >> 2;
+  const float4* q4 = reinterpret_cast<const float4*>(mQ + (size_t)i * d);
+  float4 qa = lane < d4 ? __ldg(q4 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = warp; j < Tv; j += ROUTE_THREADS / 32) {
+    const float4* k4 = reinterpret_cast<const float4*>(mK + (size_t)j * d);
     float acc = 0.f;
-    for (int c = 0; c < d; ++c) acc = fmaf(mq[c], kr[c], acc);
-    s[j] = acc;
-    scores[((size_t)h * Tv + i) * Tv + j] = acc;
+    if (lane < d4) {
+      const float4 kb = __ldg(k4 + lane);
+      acc = fmaf(qa.x, kb.x, acc);
+      acc = fmaf(qa.y, kb.y, acc);
+      acc = fmaf(qa.z, kb.z, acc);
+      acc = fmaf(qa.w, kb.w, acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      s[j] = acc;
+      scores[((size_t)h * Tv + i) * Tv + j] = acc;
+    }
   }
   __syncthreads();
-  for (int j = threadIdx.x; j < Tv; j += blockDim.x) {
+  // top-k by rank: rank_j = #{j' : s_j' > s_j or (s_j' == s_j and j' < j)}, NaN as -inf
+  for (int j = threadIdx.x; j < Tv; j += ROUTE_THREADS) {
     const float sj = rank_key(s[j]);
     int rank = 0;
     for (int j2 = 0; j2 < Tv; ++j2) {
@@ -77,44 +120,56 @@ __global__ void __launch_bounds__(ROUTE_THREADS)
     keep[j] = rank < ksel ? 1 : 0;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int n = 0;
-    int* out = idx + ((size_t)h * Tv + i) * ksel;
-    for (int j = 0; j < Tv && n < ksel; ++j)
-      if (keep[j]) out[n++] = j;
-    if (pooled) {
-      const float sc = 1.0f / sqrtf((float)d);
-      float mx = -INFINITY;
-      for (int j = 0; j < Tv; ++j) mx = fmaxf(mx, s[j] * sc);
-      float sum = 0.f;
-      for (int j = 0; j < Tv; ++j) {
-        const float e = expf(s[j] * sc - mx);
-        w[j] = e;
-        sum += e;
-      }
-      red[0] = sum;
+  // ascending compaction: a kept tile's slot is the number of kept tiles before it
+  int* out = idx + ((size_t)h * Tv + i) * ksel;
+  for (int j = threadIdx.x; j < Tv; j += ROUTE_THREADS) {
+    if (keep[j]) {
+      int pos = 0;
+      for (int j2 = 0; j2 < j; ++j2) pos += keep[j2];
+      if (pos < ksel) out[pos] = j;
     }
   }
   if (!pooled) return;
+  // pooled branch: softmax over all video tiles of S / sqrt(d), then weights . mean(v)
+  const float sc = 1.0f / sqrtf((float)d);
+  float mx = -INFINITY;
+  for (int j = threadIdx.x; j < Tv; j += ROUTE_THREADS) mx = fmaxf(mx, s[j] * sc);
+  mx = block_max(mx, red);
+  float sum = 0.f;
+  for (int j = threadIdx.x; j < Tv; j += ROUTE_THREADS) {
+    const float e = expf(s[j] * sc - mx);
+    w[j] = e;
+    sum += e;
+  }
+  sum = block_sum(sum, red);  // ends with __syncthreads: w[] complete
+  // two halves of the key tiles per column, summed in j order, combined in a fixed order
+  const int c = threadIdx.x % d;
+  const int half = threadIdx.x / d;  // d = 64: 4 quarters; d = 128: 2 halves
+  const int parts = ROUTE_THREADS / d;
+  const int per = (Tv + parts - 1) / parts;
+  const int j0 = half * per, j1 = min(Tv, j0 + per);
+  float acc = 0.f;
+#pragma unroll 4
+  for (int j = j0; j < j1; ++j) acc = fmaf(w[j], __ldg(mV + (size_t)j * d + c), acc);
+  part[half * d + c] = acc;
   __syncthreads();
-  const float inv = 1.0f / red[0];
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    float acc = 0.f;
-    for (int j = 0; j < Tv; ++j) acc = fmaf(w[j], mV[(size_t)j * d + c], acc);
-    pooled[((size_t)h * Tv + i) * d + c] = acc * inv;
+  if (threadIdx.x < d) {
+    float tot = 0.f;
+    for (int p = 0; p < parts; ++p) tot += part[p * d + threadIdx.x];
+    pooled[((size_t)h * Tv + i) * d + threadIdx.x] = tot / sum;
   }
 }
 
 }  // namespace
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream) {
-  if (a.Tv <= 0 || a.d <= 0 || a.d > 1024 || a.ksel <= 0) return cudaErrorInvalidValue;
+  if (a.Tv <= 0 || (a.d != 64 && a.d != 128) || a.ksel <= 0) return cudaErrorInvalidValue;
   dim3 g1(a.Tv, a.H, 3);
   tile_means_kernel<<<g1, a.d, 0, stream>>>(a.q, a.k, a.v, a.means, a.N, a.H, a.d, a.n_prefix,
                                             a.n_video, a.Tv);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t shm = (size_t)(a.d + 3 * a.Tv) * 4;
+  const size_t shm = (size_t)(3 * a.Tv + 4 * a.d) * 4;
   if (shm > 200 * 1024) return cudaErrorInvalidValue;
   if (shm > 48 * 1024) {
     e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -30,7 +30,8 @@ __all__ = [
     "bf16", "f32", "rms_modulate", "linear", "gelu_erf", "head_rms_norm", "rope",
     "video_tiles", "tile_means", "tile_scores", "topk_select", "topk_gap",
     "topk_set_valid", "attend", "routed_attention", "pooled_branch", "gate_mix",
-    "attention_layer", "qkv_heads", "block_forward", "euler_update", "extrapolate",
+    "attention_layer", "qkv_heads", "block_forward", "block_forward_rows", "euler_update",
+    "extrapolate",
     "fresh_steps", "sigma_schedule", "denoise_forward", "thin_layers",
 ]
 
@@ -407,6 +408,61 @@ def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
     out.update({"h": h, "qkvg": qkvg, "q": q, "k": k, "v": v, "g": g,
                 "x1": x1, "h2": h2, "u": u, "x2": x2})
     return out
+
+
+def block_forward_rows(x, wts: dict, shape, rows) -> dict:
+    """``block_forward`` evaluated for a subset of output rows (for full-size checks).
+
+    The same steps in the same order as ``block_forward``; only the work that
+    the requested rows depend on is done: the projection of every row (keys,
+    values and the video query rows that feed the tile means), the router over
+    all tiles, attention for the requested rows' query rows / tiles, and the
+    out projection and MLP for the requested rows.
+    """
+    s = shape
+    mod = np.asarray(wts["mod"], np.float64)
+    shift1, scale1, gate1, shift2, scale2, gate2 = mod
+    x = np.asarray(x, np.float64)
+    rows = np.array(sorted(set(int(r) for r in rows)))
+    h = rms_modulate(x, shift1, scale1, s.rms_eps)
+    qkvg = bf16(linear(h, wts["w_qkvg"], wts["b_qkvg"]))
+    q, k, v, g = qkv_heads(qkvg, s.heads, s.head_dim,
+                           wts.get("qnorm_w") if s.qk_norm else None,
+                           wts.get("knorm_w") if s.qk_norm else None,
+                           s.rms_eps, s.rope_theta, s.rope)
+    del qkvg
+    P, Vn, tile, d = s.n_prefix, s.n_video, s.tile, s.head_dim
+    mq = tile_means(q, P, Vn, tile)
+    mk = tile_means(k, P, Vn, tile)
+    mv = tile_means(v, P, Vn, tile)
+    S = tile_scores(mq, mk)
+    idx = topk_select(S, s.topk)
+    H = s.heads
+    O = np.zeros((H, len(rows), d))
+    scale = 1.0 / math.sqrt(d)
+    vt = video_tiles(P, Vn, tile)
+    for n, r in enumerate(rows):
+        for hh in range(H):
+            if r < P:
+                keys = np.arange(s.n_rows)
+            else:
+                i = (r - P) // tile
+                keys = np.concatenate([np.arange(P)] + [np.arange(vt[j][0], vt[j][0] + vt[j][1])
+                                                        for j in idx[hh, i]])
+            O[hh, n] = attend(q[hh, [r]], k[hh, keys], v[hh, keys], scale)[0]
+    o = O.transpose(1, 0, 2).reshape(len(rows), H * d)
+    if s.pooled:
+        pb = pooled_branch(S, mv, d)
+        for n, r in enumerate(rows):
+            if r >= P:
+                i = (r - P) // tile
+                o[n] += g[r] * pb[:, i, :].reshape(H * d)
+    o = bf16(o)
+    x1 = bf16(x[rows] + gate1 * linear(o, wts["w_o"], wts["b_o"]))
+    h2 = rms_modulate(x1, shift2, scale2, s.rms_eps)
+    u = bf16(gelu_erf(linear(h2, wts["w1"], wts["b1"])))
+    x2 = bf16(x1 + gate2 * linear(u, wts["w2"], wts["b2"]))
+    return {"rows": rows, "x1": x1, "x2": x2, "idx": idx, "scores": S, "o": o}
 
 
 # ---------------------------------------------------------------------------

@@ -1,0 +1,159 @@
+"""Full-size GPU parity at the 15,435-row shape (hidden 5,120, 40 heads x 128,
+top-k 16 of 218 video tiles, last video tile 11 rows), in the launch
+configuration bench.py times.  The oracle computes sampled outputs one by one
+(sampled query tiles and rows); routing is compared over every (head, tile)."""
+import os
+import time
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic as S
+from helpers import assert_close, compare_topk, dev_bf16, dev_f32, host_f64, weights_to_device, \
+    weights_to_f64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+WL = S.config_by_name("block_15435_d5120")
+SHAPE = WL.shape
+
+
+@pytest.fixture(scope="module")
+def h3():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+    __graft_entry__.build()
+    import audio_diffusion_transformer_gb300 as pkg
+    return pkg
+
+
+def _log(msg):
+    os.makedirs("gpurun_out", exist_ok=True)
+    with open(os.path.join("gpurun_out", "fullsize_timing.log"), "a") as f:
+        f.write(msg + "\n")
+
+
+def sample_rows(shp):
+    P, N = shp.n_prefix, shp.n_rows
+    rows = {0, 1, shp.n_text - 1, shp.n_text, P - 1, P, P + 63, P + 64, N // 2, N - 12, N - 11,
+            N - 1}
+    return sorted(r for r in rows if 0 <= r < N)
+
+
+def test_routed_attention_fullsize(h3):
+    shp = SHAPE
+    t0 = time.time()
+    inp = S.attention_inputs(shp, WL.seed)
+    q64, k64, v64, g64 = (S.bf16_bits_to_f64(inp[n]) for n in ("q", "k", "v", "gate"))
+    _log(f"attention inputs {time.time() - t0:.1f}s")
+    cs = h3.attn_shape(shp)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    tv = shp.n_video_tiles
+    out = torch.empty(shp.n_rows, shp.attn_width, dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty(shp.heads, tv, shp.topk, dtype=torch.int32, device="cuda")
+    sc = torch.empty(shp.heads, tv, tv, dtype=torch.float32, device="cuda")
+    pooled = torch.empty(shp.heads, tv, shp.head_dim, dtype=torch.float32, device="cuda")
+    h3.routed_attention(cs, *(dev_bf16(inp[n]) for n in ("q", "k", "v", "gate")), out, ws,
+                        pooled=pooled, idx=idx, scores=sc)
+    torch.cuda.synchronize()
+    assert h3.sync_status(ws) == 0
+    t0 = time.time()
+    P, Vn = shp.n_prefix, shp.n_video
+    mq, mk, mv = (oracle.tile_means(a, P, Vn) for a in (q64, k64, v64))
+    Sref = oracle.tile_scores(mq, mk)
+    idx_ref = oracle.topk_select(Sref, shp.topk)
+    gi = idx.cpu().numpy()
+    n_tie = compare_topk(gi, idx_ref, Sref, shp.topk)
+    _log(f"router oracle {time.time() - t0:.1f}s, near-tie rows that differ: {n_tie} "
+         f"of {shp.heads * tv}")
+    assert np.allclose(sc.cpu().numpy(), Sref, rtol=1e-4, atol=1e-6)
+    pref = oracle.pooled_branch(Sref, mv, shp.head_dim)
+    assert np.allclose(pooled.cpu().double().numpy(), pref, rtol=1e-4, atol=1e-6)
+    # sampled outputs: a few (head, video tile) pairs incl. the partial last tile, using the
+    # GPU's selections (identical to the oracle's except counted near-ties)
+    tiles = [(0, 0), (7, 100), (39, tv - 1), (20, tv - 2), (33, 57)]
+    O = oracle.routed_attention(q64, k64, v64, P, Vn, gi, tiles=tiles)
+    got = host_f64(out)
+    for h, i in tiles:
+        r0, nv = oracle.video_tiles(P, Vn)[i]
+        d = shp.head_dim
+        want = O[h, r0:r0 + nv] + g64[r0:r0 + nv, h * d:(h + 1) * d] * pref[h, i]
+        assert_close(got[r0:r0 + nv, h * d:(h + 1) * d], want, f"video tile ({h},{i})")
+    # sampled dense prefix rows
+    for r in (0, shp.n_text, P - 1):
+        for h in (0, 19, 39):
+            d = shp.head_dim
+            want = oracle.attend(q64[h, [r]], k64[h], v64[h], 1 / np.sqrt(d))[0]
+            assert_close(got[r, h * d:(h + 1) * d], want, f"prefix row {r} head {h}")
+    _log(f"attention sampled oracle {time.time() - t0:.1f}s")
+
+
+def test_block_forward_fullsize_sampled(h3):
+    shp = SHAPE
+    t0 = time.time()
+    w = S.block_weights(shp, WL.seed)
+    xb = S.hidden_rows(shp, WL.seed)
+    _log(f"block inputs {time.time() - t0:.1f}s")
+    cs = h3.make_shape(shp)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    x = dev_bf16(xb)
+    h3.block_forward(cs, weights_to_device(w), x, ws)
+    torch.cuda.synchronize()
+    assert h3.sync_status(ws) == 0
+    got = host_f64(x)
+    rows = sample_rows(shp)
+    t0 = time.time()
+    ref = oracle.block_forward_rows(S.bf16_bits_to_f64(xb), weights_to_f64(w), shp, rows)
+    _log(f"block sampled oracle {time.time() - t0:.1f}s")
+    x0 = S.bf16_bits_to_f64(xb)[rows]
+    assert_close(got[rows], ref["x2"], "block x2 (sampled rows)")
+    assert_close(got[rows] - x0, ref["x2"] - x0, "block update (sampled rows)", rel=5e-2,
+                 cos=0.998)
+    assert np.all(np.isfinite(got))
+
+
+def test_block_forward_fullsize_deterministic(h3):
+    shp = SHAPE
+    w = weights_to_device(S.block_weights(shp, WL.seed + 1))
+    xb = S.hidden_rows(shp, WL.seed + 1)
+    cs = h3.make_shape(shp)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        x = dev_bf16(xb)
+        h3.block_forward(cs, w, x, ws)
+        torch.cuda.synchronize()
+        outs.append(x.view(torch.int16).clone())
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_denoise_two_blocks_fullsize(h3):
+    """The 50-block forward's velocity path, checked on its first 2 blocks:
+    v = x_2 after two blocks of bf16(z), then z' = z - v/8 (bit-exact given v)."""
+    shp = SHAPE
+    blocks = [S.block_weights(shp, WL.seed + 10 + b) for b in range(2)]
+    z0 = S.latents(shp, WL.seed)
+    cs = h3.make_shape(shp)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    z = dev_f32(z0)
+    ring = torch.zeros(2, shp.n_rows, shp.hidden, dtype=torch.float32, device="cuda")
+    h3.denoise_step(cs, [weights_to_device(b) for b in blocks], [0, 1], z, ring, True, 1.0, 0.0,
+                    0.0, 0, -0.125, ws)
+    torch.cuda.synchronize()
+    assert h3.sync_status(ws) == 0
+    v_gpu = ring[0].cpu().double().numpy()
+    z_gpu = z.cpu().double().numpy()
+    # Euler step exact given the GPU's own velocity
+    assert np.array_equal(z_gpu, oracle.euler_update(z0, v_gpu, -0.125))
+    # velocity against the oracle: block 0 in full, block 1 on sampled rows
+    t0 = time.time()
+    wo = [weights_to_f64(b) for b in blocks]
+    x1 = oracle.block_forward(oracle.bf16(z0.astype(np.float64)), wo[0], shp)["x2"]
+    _log(f"denoise block0 full oracle {time.time() - t0:.1f}s")
+    rows = sample_rows(shp)
+    ref = oracle.block_forward_rows(x1, wo[1], shp, rows)
+    _log(f"denoise block1 sampled oracle {time.time() - t0:.1f}s")
+    assert_close(v_gpu[rows], ref["x2"], "velocity after 2 blocks (sampled rows)")

@@ -400,3 +400,20 @@ def test_thin_layers_hand_example():
     assert O.thin_layers(mods, 4) == [0, 1, 2, 5]      # tie 1 vs 3: the higher (3) goes first
     assert O.thin_layers(mods, 3) == [0, 2, 5]
     assert O.thin_layers(mods, 2) == [0, 5]
+
+
+def test_block_rows_equals_full_block():
+    # the sampled evaluation must reproduce the full evaluation on the sampled rows exactly
+    shape = _tiny_shape()
+    w = _weights(shape)
+    x = S.bf16_bits_to_f64(S.hidden_rows(shape, 4))
+    full = O.block_forward(x, w, shape)
+    rows = [0, 63, 64, 127, 128, 200, shape.n_rows - 1]
+    part = O.block_forward_rows(x, w, shape, rows)
+    # the same arithmetic; only BLAS blocking of a 1-row vs a 64-row product may differ
+    # in the last float64 bit, which can move a bf16 rounding by one ulp
+    ref = full["x2"][rows]
+    ulp = np.abs(ref) * 2.0 ** -7
+    assert np.all(np.abs(part["x2"] - ref) <= ulp)
+    assert np.mean(part["x2"] == ref) > 0.99
+    assert np.array_equal(part["idx"], full["idx"])
