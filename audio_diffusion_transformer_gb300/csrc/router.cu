@@ -9,7 +9,7 @@
 //   thread c sums column c over the tile's valid rows in row order and divides
 //   by the valid-row count.  Reads each video row of q, k, v once (HBM-bound).
 // Kernel 2 (route): one CTA (8 warps) per (query tile i, head h):
-//   S[h,i,j] = sum_c mq[h,i,c] mk[h,j,c]: one warp per j, lane l sums dims
+//   S[h,i,j] = sum_c mq[h,i,c] mk[h,j,c]: one warp per j (four j's in flight), lane l sums dims
 //   4l..4l+3 in order, then a fixed xor-shuffle tree across the lanes;
 //   rank_j = #{j' : s_j' > s_j or (s_j' == s_j and j' < j)} with NaN -> -inf;
 //   tile j is kept iff rank_j < k; kept tiles are written ascending;
@@ -40,7 +40,15 @@ __global__ void tile_means_kernel(const __nv_bfloat16* __restrict__ q,
   const int nv = min(64, n_video - 64 * t);
   const __nv_bfloat16* src = X + ((size_t)h * N + r0) * d + c;
   float s = 0.f;
-  for (int r = 0; r < nv; ++r) s += __bfloat162float(src[(size_t)r * d]);
+  int r = 0;
+  for (; r + 8 <= nv; r += 8) {  // eight rows in flight, summed in row order
+    float x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) x[u] = __bfloat162float(src[(size_t)(r + u) * d]);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) s += x[u];
+  }
+  for (; r < nv; ++r) s += __bfloat162float(src[(size_t)r * d]);
   means[(((size_t)which * H + h) * Tv + t) * d + c] = s / (float)nv;
 }
 
@@ -91,21 +99,36 @@ __global__ void __launch_bounds__(ROUTE_THREADS)
   const int d4 = d >> 2;
   const float4* q4 = reinterpret_cast<const float4*>(mQ + (size_t)i * d);
   float4 qa = lane < d4 ? __ldg(q4 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = warp; j < Tv; j += ROUTE_THREADS / 32) {
-    const float4* k4 = reinterpret_cast<const float4*>(mK + (size_t)j * d);
-    float acc = 0.f;
-    if (lane < d4) {
-      const float4 kb = __ldg(k4 + lane);
-      acc = fmaf(qa.x, kb.x, acc);
-      acc = fmaf(qa.y, kb.y, acc);
-      acc = fmaf(qa.z, kb.z, acc);
-      acc = fmaf(qa.w, kb.w, acc);
+  constexpr int NW = ROUTE_THREADS / 32;
+  constexpr int U = 4;  // key tiles in flight per warp (independent loads before the reductions)
+  for (int jb = warp * U; jb < Tv; jb += NW * U) {
+    float acc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = jb + u;
+      acc[u] = 0.f;
+      if (j < Tv && lane < d4) {
+        const float4 kb = __ldg(reinterpret_cast<const float4*>(mK + (size_t)j * d) + lane);
+        acc[u] = fmaf(qa.x, kb.x, acc[u]);
+        acc[u] = fmaf(qa.y, kb.y, acc[u]);
+        acc[u] = fmaf(qa.z, kb.z, acc[u]);
+        acc[u] = fmaf(qa.w, kb.w, acc[u]);
+      }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
+    }
     if (lane == 0) {
-      s[j] = acc;
-      scores[((size_t)h * Tv + i) * Tv + j] = acc;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = jb + u;
+        if (j < Tv) {
+          s[j] = acc[u];
+          scores[((size_t)h * Tv + i) * Tv + j] = acc[u];
+        }
+      }
     }
   }
   __syncthreads();
@@ -149,8 +172,15 @@ __global__ void __launch_bounds__(ROUTE_THREADS)
   const int per = (Tv + parts - 1) / parts;
   const int j0 = half * per, j1 = min(Tv, j0 + per);
   float acc = 0.f;
-#pragma unroll 4
-  for (int j = j0; j < j1; ++j) acc = fmaf(w[j], __ldg(mV + (size_t)j * d + c), acc);
+  int j = j0;
+  for (; j + 8 <= j1; j += 8) {  // eight loads in flight, then the sums in j order
+    float m[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) m[u] = __ldg(mV + (size_t)(j + u) * d + c);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc = fmaf(w[j + u], m[u], acc);
+  }
+  for (; j < j1; ++j) acc = fmaf(w[j], __ldg(mV + (size_t)j * d + c), acc);
   part[half * d + c] = acc;
   __syncthreads();
   if (threadIdx.x < d) {
