@@ -274,32 +274,48 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int nva = ((e0 >> half) & 1) ? min(64, p.N - (e0 >> 2)) : 0;
       const int nvb = ((e1 >> half) & 1) ? min(64, p.N - (e1 >> 2)) : 0;
       const uint32_t s_addr = t_lane + sb * 128;
-      // scores of this row for the step's 128 keys, scaled to the log2 domain and masked
+      // scores of this row for the step's 128 keys, scaled to the log2 domain and masked;
+      // eight independent max / sum chains, combined in a fixed order
       float sv[128];
+      tmem_ld128(s_addr, sv);
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sv + c * 32);
-      float mx = -INFINITY;
+      for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+      if (nva == 64 && nvb == 64) {  // warp-uniform: every key of the step is visible
 #pragma unroll
-      for (int j = 0; j < 128; ++j) {
-        const bool valid = (j < 64) ? (j < nva) : (j - 64 < nvb);
-        sv[j] = valid ? sv[j] * sl2 : -INFINITY;
-        mx = fmaxf(mx, sv[j]);
+        for (int j = 0; j < 128; ++j) {
+          sv[j] *= sl2;
+          mx8[j & 7] = fmaxf(mx8[j & 7], sv[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 128; ++j) {
+          const bool valid = (j < 64) ? (j < nva) : (j - 64 < nvb);
+          sv[j] = valid ? sv[j] * sl2 : -INFINITY;
+          mx8[j & 7] = fmaxf(mx8[j & 7], sv[j]);
+        }
       }
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const bool need = mx > m_run + kRescaleLog2;
       const float m_new = need ? mx : m_run;
       const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       // P = exp2(s - m) rounded to bf16; l sums the unrounded weights
       uint32_t pk[64];
-      float lsum = 0.f;
+      float ls8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ls8[u] = 0.f;
 #pragma unroll
       for (int j = 0; j < 128; j += 2) {
         const float p0 = ex2_approx(sv[j] - m_use);
         const float p1 = ex2_approx(sv[j + 1] - m_use);
-        lsum += p0;
-        lsum += p1;
+        ls8[(j >> 1) & 7] += p0;
+        ls8[(j >> 1) & 7] += p1;
         pk[j >> 1] = pack_bf16x2(p0, p1);
       }
+      const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) +
+                         ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       if (t > 0) {
         // PV of the previous step must be done: it reads the single P buffer and updates O
         if (!mbar_wait(pv_done, (t - 1) & 1, abort_flag, p.status)) {
