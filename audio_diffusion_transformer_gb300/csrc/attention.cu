@@ -13,20 +13,23 @@
 //     exactly its own key set.
 // CTAs are ordered head-major (all units of head 0, then head 1, ...), so a
 // wave of CTAs shares one head's K/V in L2.  The KV loop walks the key-tile
-// list two 64-row tiles (128 keys) per step.
-// K and V tiles are gathered per step with one TMA box per 64 x 64 piece into
-// a 2-stage ring (128-byte swizzle, no multicast).
+// list two 64-row tiles ("slots" 0 and 1, 128 keys) per step.  K and V tiles
+// are gathered per step with one TMA box per 64 x 64 piece into a 2-stage ring
+// (128-byte swizzle, no multicast).
 //   warp 0      TMA producer (Q once, then K and V per step)
 //   warp 1      MMA issuer: S = Q K^T (M=128, N=128, fp32 in TMEM, double
-//               buffered) and O += P V (M=128, N=d, V read as an MN-major operand)
-//   warps 2..5  softmax: thread = query row (TMEM lane); one TMEM read of the
-//               row's 128 scores per step, scaled into the log2 domain; lazily
-//               rescaled running max (O is rescaled in TMEM only when the row
-//               max grows by more than 2^8); P = exp2(s - m) rounded to bf16,
-//               computed before waiting for the previous step's PV, then
-//               written to shared memory in the swizzled K-major layout the MMA
-//               reads; l sums the unrounded weights.
-//               Epilogue: O / l, + gate * pooled for video rows, bf16 store.
+//               buffered); O_c += P[:, slot c] V[slot c] for c = 0, 1 (two
+//               fp32 TMEM accumulators, V read as an MN-major operand)
+//   warps 2..9  softmax, two warps per TMEM lane quarter: warp (q, c) owns rows
+//               32q..32q+31 and key slot c.  Each runs its own online softmax
+//               over the keys of its slot (split-K): one 64-column TMEM read of
+//               S per step, row max on the raw scores, P = exp2(s*scale*log2e -
+//               m) rounded to bf16 into the swizzled K-major P tile in shared
+//               memory, l summing the unrounded weights, O_c rescaled in TMEM
+//               only when the max grows by more than 2^8.  The epilogue merges
+//               the two slots' (m, l, O) per row, divides, adds gate * pooled
+//               for video rows and stores bf16; each warp of a pair writes half
+//               of the head dimensions.
 #include <math.h>
 
 #include "internal.h"
@@ -36,7 +39,7 @@ namespace h3 {
 
 namespace {
 
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;
 constexpr int MAX_TILES = 1024;  // key tiles per unit: N <= 65,536 rows
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -52,10 +55,14 @@ struct Layout {
   static constexpr int STAGE_STRIDE = 2 * KV_BYTES;
   static constexpr int P_OFF = K_OFF0 + 2 * STAGE_STRIDE;
   static constexpr int TILES_OFF = P_OFF + P_BYTES;
-  static constexpr int BAR_OFF = TILES_OFF + MAX_TILES * 4;
+  static constexpr int MERGE_OFF = TILES_OFF + MAX_TILES * 4;  // float2 [2][128]
+  static constexpr int BAR_OFF = MERGE_OFF + 2 * 128 * 8;
   static constexpr int USED = BAR_OFF + 256;
   // keep one CTA per SM (the kernel allocates 512 TMEM columns)
   static constexpr int SMEM = (USED + 1024) > 120 * 1024 ? (USED + 1024) : 120 * 1024;
+  static constexpr uint32_t S_COL = 0;          // two 128-column score buffers
+  static constexpr uint32_t O_COL0 = 256;       // slot-0 accumulator
+  static constexpr uint32_t O_COL1 = 256 + HD;  // slot-1 accumulator
 };
 
 struct Params {
@@ -70,6 +77,18 @@ struct Params {
 };
 
 template <int HD>
+__device__ __forceinline__ void rescale_rows(uint32_t taddr, float alpha) {
+#pragma unroll 1
+  for (int c = 0; c < HD / 32; ++c) {
+    float o[32];
+    tmem_ld32(taddr + c * 32, o);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) o[j] *= alpha;
+    tmem_st32(taddr + c * 32, o);
+  }
+}
+
+template <int HD>
 __global__ void __launch_bounds__(THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK,
@@ -81,6 +100,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sQ = smem + L::Q_OFF;
   uint8_t* sP = smem + L::P_OFF;
   int* tiles = reinterpret_cast<int*>(smem + L::TILES_OFF);
+  float2* merge_ml = reinterpret_cast<float2*>(smem + L::MERGE_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;    // [2]
@@ -90,7 +110,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* p_full = bars + 9;
   uint64_t* pv_done = bars + 10;
   uint64_t* drain = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* merge_bar = bars + 12;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
   int* n_steps_s = reinterpret_cast<int*>(tmem_slot + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
@@ -145,9 +166,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&kv_empty[s], 1);
       mbar_init(&s_full[s], 1);
     }
-    mbar_init(p_full, 4);
+    mbar_init(p_full, 8);
     mbar_init(pv_done, 1);
     mbar_init(drain, 1);
+    mbar_init(merge_bar, 8);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -160,7 +182,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int n_steps = *n_steps_s;
-  constexpr uint32_t O_COL = 256;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -215,8 +236,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
           const uint32_t off = (ks >> 2) * L::CHUNK + (ks & 3) * 32;
-          umma_bf16(tmem, sdesc_sw128(q0 + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024),
-                    idesc_s, ks > 0 ? 1u : 0u);
+          umma_bf16(tmem + L::S_COL, sdesc_sw128(q0 + off, 16, 1024),
+                    sdesc_sw128(k0 + off, 16, 1024), idesc_s, ks > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[0]);
       }
@@ -230,7 +251,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int ks = 0; ks < HD / 16; ++ks) {
             const uint32_t off = (ks >> 2) * L::CHUNK + (ks & 3) * 32;
-            umma_bf16(tmem + sn * 128, sdesc_sw128(q0 + off, 16, 1024),
+            umma_bf16(tmem + L::S_COL + sn * 128, sdesc_sw128(q0 + off, 16, 1024),
                       sdesc_sw128(k0 + off, 16, 1024), idesc_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(&s_full[sn]);
@@ -241,11 +262,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t v0 = smem_u32(smem + L::V_OFF0 + st * L::STAGE_STRIDE);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
+          // keys 16ks..16ks+15: slot ks/4 -> accumulator O_(ks/4)
           const uint32_t aoff = (ks >> 2) * L::CHUNK + (ks & 3) * 32;
+          const uint32_t obuf = tmem + (ks < 4 ? L::O_COL0 : L::O_COL1);
           // V: MN-major; LBO = next 64-dim column block, SBO = next 8 keys
-          umma_bf16(tmem + O_COL, sdesc_sw128(p0 + aoff, 16, 1024),
+          umma_bf16(obuf, sdesc_sw128(p0 + aoff, 16, 1024),
                     sdesc_sw128(v0 + ks * 2048, L::CHUNK, 1024), idesc_pv,
-                    (t > 0 || ks > 0) ? 1u : 0u);
+                    (t > 0 || (ks & 3) > 0) ? 1u : 0u);
         }
         umma_commit(&kv_empty[st]);
         umma_commit(pv_done);
@@ -256,9 +279,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ---------------------------------------------------------------- softmax
     const int quad = warp & 3;
+    const int slot = (warp - 2) >> 2;  // warps 2..5 -> slot 0, warps 6..9 -> slot 1
     const int row = quad * 32 + lane;
     const int half = row >> 6;
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t o_mine = t_lane + (slot ? L::O_COL1 : L::O_COL0);
     const float sl2 = p.scale_log2;
     float m_run = -INFINITY;
     float l_run = 0.f;
@@ -270,92 +295,85 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      const int e0 = tiles[2 * t], e1 = tiles[2 * t + 1];
-      const int nva = ((e0 >> half) & 1) ? min(64, p.N - (e0 >> 2)) : 0;
-      const int nvb = ((e1 >> half) & 1) ? min(64, p.N - (e1 >> 2)) : 0;
-      const uint32_t s_addr = t_lane + sb * 128;
-      // scores of this row for the step's 128 keys, scaled to the log2 domain and masked;
-      // eight independent max / sum chains, combined in a fixed order
-      float sv[128];
-      tmem_ld128(s_addr, sv);
+      const int e = tiles[2 * t + slot];
+      const int nv = ((e >> half) & 1) ? min(64, p.N - (e >> 2)) : 0;
+      // this slot's 64 raw scores; max on the raw values (the scale is positive)
+      float sv[64];
+      tmem_ld64(t_lane + L::S_COL + sb * 128 + slot * 64, sv);
       float mx8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
-      if (nva == 64 && nvb == 64) {  // warp-uniform: every key of the step is visible
+      if (nv == 64) {  // warp-uniform: every key of the slot is visible to these rows
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
-          sv[j] *= sl2;
-          mx8[j & 7] = fmaxf(mx8[j & 7], sv[j]);
-        }
+        for (int j = 0; j < 64; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], sv[j]);
       } else {
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
-          const bool valid = (j < 64) ? (j < nva) : (j - 64 < nvb);
-          sv[j] = valid ? sv[j] * sl2 : -INFINITY;
+        for (int j = 0; j < 64; ++j) {
+          sv[j] = j < nv ? sv[j] : -INFINITY;
           mx8[j & 7] = fmaxf(mx8[j & 7], sv[j]);
         }
       }
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
       const bool need = mx > m_run + kRescaleLog2;
       const float m_new = need ? mx : m_run;
       const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      // P = exp2(s - m) rounded to bf16; l sums the unrounded weights
-      uint32_t pk[64];
+      // P = exp2(s * scale - m) rounded to bf16; l sums the unrounded weights
+      uint32_t pk[32];
       float ls8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) ls8[u] = 0.f;
 #pragma unroll
-      for (int j = 0; j < 128; j += 2) {
-        const float p0 = ex2_approx(sv[j] - m_use);
-        const float p1 = ex2_approx(sv[j + 1] - m_use);
-        ls8[(j >> 1) & 7] += p0;
-        ls8[(j >> 1) & 7] += p1;
-        pk[j >> 1] = pack_bf16x2(p0, p1);
+      for (int j = 0; j < 64; j += 2) {
+        const float e0 = ex2_approx(fmaf(sv[j], sl2, -m_use));
+        const float e1 = ex2_approx(fmaf(sv[j + 1], sl2, -m_use));
+        ls8[(j >> 1) & 7] += e0;
+        ls8[(j >> 1) & 7] += e1;
+        pk[j >> 1] = pack_bf16x2(e0, e1);
       }
       const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) +
                          ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       if (t > 0) {
-        // PV of the previous step must be done: it reads the single P buffer and updates O
+        // the previous step's PV reads the single P tile and updates O: wait for it
         if (!mbar_wait(pv_done, (t - 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
-            float o[32];
-            tmem_ld32(t_lane + O_COL + c * 32, o);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] *= alpha;
-            tmem_st32(t_lane + O_COL + c * 32, o);
-          }
-        }
+        if (__any_sync(0xffffffffu, need)) rescale_rows<HD>(o_mine, alpha);
       }
-      l_run = l_run * alpha;
+      l_run = fmaf(l_run, alpha, lsum);
       m_run = m_new;
-      // keys 64b..64b+63 -> column block b; 16-byte unit u holds keys 8u..8u+7 of the block
+      // keys of this slot -> column block `slot`; 16-byte unit u holds keys 8u..8u+7
+      uint8_t* rowp = sP + slot * L::CHUNK + row * 128;
 #pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        uint8_t* rowp = sP + b * L::CHUNK + row * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int w0 = b * 32 + u * 4;
-          *reinterpret_cast<uint4*>(rowp + ((u ^ (row & 7)) << 4)) =
-              make_uint4(pk[w0], pk[w0 + 1], pk[w0 + 2], pk[w0 + 3]);
-        }
+      for (int u = 0; u < 8; ++u) {
+        *reinterpret_cast<uint4*>(rowp + ((u ^ (row & 7)) << 4)) =
+            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       }
-      l_run += lsum;
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
     if (ok && n_steps > 0) {
-      if (mbar_wait(pv_done, (n_steps - 1) & 1, abort_flag, p.status)) {
+      bool done = mbar_wait(pv_done, (n_steps - 1) & 1, abort_flag, p.status);
+      if (done) {
+        // merge the two slots' online-softmax states of each row
+        merge_ml[slot * 128 + row] = make_float2(m_run, l_run);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(merge_bar);
+        done = mbar_wait(merge_bar, 0, abort_flag, p.status);
+      }
+      if (done) {
         tc_fence_after();
+        const float2 a = merge_ml[row], b = merge_ml[128 + row];
+        const float m = fmaxf(a.x, b.x);
+        const float sa = (a.x == -INFINITY) ? 0.f : ex2_approx(a.x - m);
+        const float sbb = (b.x == -INFINITY) ? 0.f : ex2_approx(b.x - m);
+        const float l = fmaf(a.y, sa, b.y * sbb);
+        const float inv_l = l > 0.f ? 1.0f / l : 0.f;
         int grow, tile = -1;
         bool store;
         if (is_prefix) {
@@ -366,21 +384,24 @@ __global__ void __launch_bounds__(THREADS, 1)
           grow = p.n_prefix + 64 * tile + (row & 63);
           store = tile < p.Tv && grow < p.N;
         }
-        const float inv_l = 1.0f / l_run;
         const int A = p.H * HD;
         const bool mix = !is_prefix && p.gate != nullptr && p.pooled != nullptr;
+        // this warp writes head dims [slot * HD/2, (slot + 1) * HD/2)
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
-          float o[32];
-          tmem_ld32(t_lane + O_COL + c * 32, o);
+        for (int c = 0; c < HD / 64; ++c) {
+          const int d0 = slot * (HD / 2) + c * 32;
+          float o0[32], o1[32];
+          tmem_ld32(t_lane + L::O_COL0 + d0, o0);
+          tmem_ld32(t_lane + L::O_COL1 + d0, o1);
           if (store) {
+            float o[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] *= inv_l;
+            for (int j = 0; j < 32; ++j) o[j] = fmaf(o0[j], sa, o1[j] * sbb) * inv_l;
             if (mix) {
               const uint4* g4 =
-                  reinterpret_cast<const uint4*>(p.gate + (size_t)grow * A + h * HD + c * 32);
+                  reinterpret_cast<const uint4*>(p.gate + (size_t)grow * A + h * HD + d0);
               const float4* pb4 = reinterpret_cast<const float4*>(
-                  p.pooled + ((size_t)h * p.Tv + tile) * HD + c * 32);
+                  p.pooled + ((size_t)h * p.Tv + tile) * HD + d0);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const uint4 g = __ldg(g4 + i);
@@ -395,7 +416,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 o[8 * i + 7] = fmaf(bf16_hi(g.w), b1.w, o[8 * i + 7]);
               }
             }
-            uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t)grow * A + h * HD + c * 32);
+            uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t)grow * A + h * HD + d0);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               dst[i] = make_uint4(pack_bf16x2(o[8 * i + 0], o[8 * i + 1]),
