@@ -14,8 +14,10 @@
 // CTAs are ordered head-major (all units of head 0, then head 1, ...), so a
 // wave of CTAs shares one head's K/V in L2.  The KV loop walks the key-tile
 // list two 64-row tiles ("slots" 0 and 1, 128 keys) per step.  K and V tiles
-// are gathered per step with one TMA box per 64 x 64 piece into a 2-stage ring
-// (128-byte swizzle, no multicast).
+// are gathered per step with one TMA box per 64 x 64 piece into 2-stage K and V
+// rings (128-byte swizzle, no multicast); a K stage is released as soon as its
+// S MMA completes and the producer loads K one step ahead of V, so the next
+// step's keys arrive while the current step's softmax runs.
 //   warp 0      TMA producer (Q once, then K and V per step)
 //   warp 1      MMA issuer: S = Q K^T (M=128, N=128, fp32 in TMEM, double
 //               buffered); O_c += P[:, slot c] V[slot c] for c = 0, 1 (two
@@ -105,13 +107,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;    // [2]
   uint64_t* v_full = bars + 3;    // [2]
-  uint64_t* kv_empty = bars + 5;  // [2]
+  uint64_t* k_empty = bars + 5;   // [2] K stage free: its S MMA completed
   uint64_t* s_full = bars + 7;    // [2]
   uint64_t* p_full = bars + 9;
   uint64_t* pv_done = bars + 10;
   uint64_t* drain = bars + 11;
   uint64_t* merge_bar = bars + 12;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  uint64_t* v_empty = bars + 13;  // [2] V stage free: its PV MMA completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   int* n_steps_s = reinterpret_cast<int*>(tmem_slot + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
@@ -163,7 +166,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
     }
     mbar_init(p_full, 8);
@@ -202,23 +206,38 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_3d(sQ + c * L::CHUNK, &tmQ, q_full, 64 * c, qrow0, h);
         tma_load_3d(sQ + c * L::CHUNK + 8192, &tmQ, q_full, 64 * c, qrow1, h);
       }
-      for (int t = 0; t < n_steps; ++t) {
+      // K runs one step ahead of V: K_t is needed for S_t, V_t only after softmax(t)
+      auto load_k = [&](int t) {
         const int st = t & 1;
-        if (!mbar_wait(&kv_empty[st], ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
-        const int r0 = tiles[2 * t] >> 2, r1 = tiles[2 * t + 1] >> 2;
         uint8_t* sK = smem + L::K_OFF0 + st * L::STAGE_STRIDE;
-        uint8_t* sV = smem + L::V_OFF0 + st * L::STAGE_STRIDE;
+        const int r0 = tiles[2 * t] >> 2, r1 = tiles[2 * t + 1] >> 2;
         mbar_arrive_expect_tx(&k_full[st], L::KV_BYTES);
 #pragma unroll
         for (int c = 0; c < HD / 64; ++c) {
           tma_load_3d(sK + c * L::CHUNK, &tmK, &k_full[st], 64 * c, r0, h);
           tma_load_3d(sK + c * L::CHUNK + 8192, &tmK, &k_full[st], 64 * c, r1, h);
         }
+      };
+      auto load_v = [&](int t) {
+        const int st = t & 1;
+        uint8_t* sV = smem + L::V_OFF0 + st * L::STAGE_STRIDE;
+        const int r0 = tiles[2 * t] >> 2, r1 = tiles[2 * t + 1] >> 2;
         mbar_arrive_expect_tx(&v_full[st], L::KV_BYTES);
 #pragma unroll
         for (int c = 0; c < HD / 64; ++c) {
           tma_load_3d(sV + c * L::CHUNK, &tmV, &v_full[st], 64 * c, r0, h);
           tma_load_3d(sV + c * L::CHUNK + 8192, &tmV, &v_full[st], 64 * c, r1, h);
+        }
+      };
+      for (int t = 0; t <= n_steps; ++t) {
+        if (t < n_steps) {
+          if (!mbar_wait(&k_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+          load_k(t);
+        }
+        if (t >= 1) {
+          const int tv = t - 1;
+          if (!mbar_wait(&v_empty[tv & 1], ((tv >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+          load_v(tv);
         }
       }
     }
@@ -239,6 +258,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           umma_bf16(tmem + L::S_COL, sdesc_sw128(q0 + off, 16, 1024),
                     sdesc_sw128(k0 + off, 16, 1024), idesc_s, ks > 0 ? 1u : 0u);
         }
+        umma_commit(&k_empty[0]);
         umma_commit(&s_full[0]);
       }
       for (int t = 0; ok && t < n_steps; ++t) {
@@ -254,6 +274,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             umma_bf16(tmem + L::S_COL + sn * 128, sdesc_sw128(q0 + off, 16, 1024),
                       sdesc_sw128(k0 + off, 16, 1024), idesc_s, ks > 0 ? 1u : 0u);
           }
+          umma_commit(&k_empty[sn]);
           umma_commit(&s_full[sn]);
         }
         if (!mbar_wait(p_full, t & 1, abort_flag, p.status)) break;
@@ -270,7 +291,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     sdesc_sw128(v0 + ks * 2048, L::CHUNK, 1024), idesc_pv,
                     (t > 0 || (ks & 3) > 0) ? 1u : 0u);
         }
-        umma_commit(&kv_empty[st]);
+        umma_commit(&v_empty[st]);
         umma_commit(pv_done);
       }
       umma_commit(drain);
