@@ -14,8 +14,10 @@
 //   per CTA in chunks of 32 tiles:
 //   S[h,i,j] = sum_c mq[h,i,c] mk[h,j,c]: lane l sums dims 4l..4l+3 in order,
 //   then a fixed xor-shuffle tree across the lanes;
-//   rank_j = #{j' : s_j' > s_j or (s_j' == s_j and j' < j)} with NaN -> -inf;
-//   tile j is kept iff rank_j < k; kept tiles are written ascending (ballots);
+//   top-k by k rounds of warp-wide arg-max under the total order (score
+//   descending, tile index ascending), NaN ranking as -inf -- the same set as
+//   "rank_j < k" with rank_j = #{j' : s_j' > s_j or (s_j' == s_j and j' < j)};
+//   kept tiles are written ascending (ballots);
 //   pooled[h,i,:] = sum_j softmax_j(S[h,i,j] / sqrt(d)) mv[h,j,:]: max and
 //   denominator by fixed warp reductions, the weighted sum in j order.
 // Every reduction has a fixed order, so results are deterministic.
@@ -147,26 +149,47 @@ __global__ void __launch_bounds__(ROUTE_THREADS)
   if (active) {
     float* srow_out = scores + ((size_t)h * Tv + i) * Tv;
     for (int j = lane; j < Tv; j += 32) srow_out[j] = s[j];
-    // top-k by rank: rank_j = #{j' : s_j' > s_j or (s_j' == s_j and j' < j)}, NaN as -inf;
-    // kept tiles are written in ascending order via warp ballots
+    // top-k: k rounds of a warp-wide arg-max under the total order (score desc, index asc),
+    // NaN ranking as -inf; lane l owns tiles l, l + 32, ... (bit m of `taken` = tile l + 32m).
+    // Selected tiles are then written in ascending order via ballots.
     int* out = idx + ((size_t)h * Tv + i) * ksel;
-    int base = 0;
-    for (int j0 = 0; j0 < Tv; j0 += 32) {
-      const int j = j0 + lane;
-      bool keep = false;
-      if (j < Tv) {
-        const float sj = rank_key(s[j]);
-        int rank = 0;
-        for (int j2 = 0; j2 < Tv; ++j2) {
-          const float s2 = rank_key(s[j2]);
-          rank += (s2 > sj || (s2 == sj && j2 < j)) ? 1 : 0;
+    unsigned taken = 0u;
+    if (ksel >= Tv) {
+      for (int m = 0; lane + 32 * m < Tv; ++m) taken |= 1u << m;
+    } else {
+      for (int r = 0; r < ksel; ++r) {
+        float bs = -INFINITY;
+        int bj = 0x7fffffff;
+        for (int m = 0; lane + 32 * m < Tv; ++m) {
+          const int j = lane + 32 * m;
+          if ((taken >> m) & 1u) continue;
+          const float v = rank_key(s[j]);
+          if (bj == 0x7fffffff || v > bs || (v == bs && j < bj)) {
+            bs = v;
+            bj = j;
+          }
         }
-        keep = rank < ksel;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+          const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+          const bool better = oj != 0x7fffffff &&
+                              (bj == 0x7fffffff || os > bs || (os == bs && oj < bj));
+          if (better) {
+            bs = os;
+            bj = oj;
+          }
+        }
+        if (bj != 0x7fffffff && (bj & 31) == lane) taken |= 1u << (bj >> 5);
       }
-      const unsigned m = __ballot_sync(0xffffffffu, keep);
-      const int pos = base + __popc(m & ((1u << lane) - 1u));
-      if (keep && pos < ksel) out[pos] = j;
-      base += __popc(m);
+    }
+    int base = 0;
+    for (int m = 0; 32 * m < Tv; ++m) {
+      const bool keep = (taken >> m) & 1u;
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      const int pos = base + __popc(bal & ((1u << lane) - 1u));
+      if (keep && pos < ksel) out[pos] = lane + 32 * m;
+      base += __popc(bal);
     }
   }
   if (!pooled) return;
@@ -213,7 +236,9 @@ __global__ void __launch_bounds__(ROUTE_THREADS)
 }  // namespace
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream) {
-  if (a.Tv <= 0 || (a.d != 64 && a.d != 128) || a.ksel <= 0) return cudaErrorInvalidValue;
+  // the top-k keeps one bit per tile in a 32-bit mask per lane: at most 1,024 video tiles
+  if (a.Tv <= 0 || a.Tv > 1024 || (a.d != 64 && a.d != 128) || a.ksel <= 0)
+    return cudaErrorInvalidValue;
   dim3 g1(a.Tv, a.H, 3);
   if (a.d == 128)
     tile_means_kernel<128><<<g1, 128, 0, stream>>>(a.q, a.k, a.v, a.means, a.N, a.H, a.n_prefix,
