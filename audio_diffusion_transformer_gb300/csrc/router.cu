@@ -12,8 +12,8 @@
 // Kernel 2 (route): one CTA per (head h, 8 query tiles), one warp per query
 //   tile; the head's key / value tile means pass through shared memory once
 //   per CTA in chunks of 32 tiles:
-//   S[h,i,j] = sum_c mq[h,i,c] mk[h,j,c]: lane l sums dims 4l..4l+3 in order,
-//   then a fixed xor-shuffle tree across the lanes;
+//   S[h,i,j] = sum_c mq[h,i,c] mk[h,j,c]: one lane per key tile, four
+//   interleaved partial sums over c (c mod 4) added as ((p0 + p1) + (p2 + p3));
 //   top-k by k rounds of warp-wide arg-max under the total order (score
 //   descending, tile index ascending), NaN ranking as -inf -- the same set as
 //   "rank_j < k" with rank_j = #{j' : s_j' > s_j or (s_j' == s_j and j' < j)};
@@ -110,39 +110,40 @@ __global__ void __launch_bounds__(ROUTE_THREADS)
     route_kernel(const float* __restrict__ means, float* __restrict__ scores,
                  int* __restrict__ idx, float* __restrict__ pooled, int H, int Tv, int ksel) {
   extern __shared__ float sh[];
-  float* stage = sh;                                  // [KCHUNK][D] staged means
-  float* srow = stage + KCHUNK * D;                   // [8][Tv] scores, then pooled weights
+  float* stage = sh;                                  // [KCHUNK][D + 1] staged means
+  float* qrow = stage + KCHUNK * (D + 1);             // [8][D] query means, one row per warp
+  float* srow = qrow + TILES_PER_CTA * D;             // [8][Tv] scores, then pooled weights
   const int h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * TILES_PER_CTA + warp;
   const bool active = i < Tv;
   float* s = srow + warp * Tv;
+  float* mq = qrow + warp * D;
   const float* mQ = means + ((size_t)0 * H + h) * Tv * D;
   const float* mK = means + ((size_t)1 * H + h) * Tv * D;
   const float* mV = means + ((size_t)2 * H + h) * Tv * D;
   constexpr int D4 = D / 4;  // float4 lanes per row (<= 32)
-  float4 qa = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (active && lane < D4) qa = reinterpret_cast<const float4*>(mQ + (size_t)i * D)[lane];
-  // scores: stage KCHUNK key means, then each warp dots its query mean with them
+  for (int c = lane; c < D; c += 32) mq[c] = active ? mQ[(size_t)i * D + c] : 0.f;
+  // scores: stage 32 key means (row stride D + 1: conflict-free column reads), then lane l
+  // of each warp computes the whole dot product for key tile j0 + l with four interleaved
+  // partial sums over the dimensions (c mod 4), added as ((p0 + p1) + (p2 + p3))
   for (int j0 = 0; j0 < Tv; j0 += KCHUNK) {
     const int nj = min(KCHUNK, Tv - j0);
     __syncthreads();
-    for (int e = threadIdx.x; e < nj * D4; e += ROUTE_THREADS)
-      reinterpret_cast<float4*>(stage)[e] = __ldg(reinterpret_cast<const float4*>(mK + (size_t)j0 * D) + e);
+    for (int e = threadIdx.x; e < nj * D; e += ROUTE_THREADS)
+      stage[(e / D) * (D + 1) + (e % D)] = __ldg(mK + (size_t)j0 * D + e);
     __syncthreads();
-    if (active) {
-      for (int jj = 0; jj < nj; ++jj) {
-        float acc = 0.f;
-        if (lane < D4) {
-          const float4 kb = reinterpret_cast<const float4*>(stage + jj * D)[lane];
-          acc = fmaf(qa.x, kb.x, acc);
-          acc = fmaf(qa.y, kb.y, acc);
-          acc = fmaf(qa.z, kb.z, acc);
-          acc = fmaf(qa.w, kb.w, acc);
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) s[j0 + jj] = acc;
+    if (active && lane < nj) {
+      const float* kr = stage + lane * (D + 1);
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 8
+      for (int c = 0; c < D; c += 4) {
+        a0 = fmaf(mq[c], kr[c], a0);
+        a1 = fmaf(mq[c + 1], kr[c + 1], a1);
+        a2 = fmaf(mq[c + 2], kr[c + 2], a2);
+        a3 = fmaf(mq[c + 3], kr[c + 3], a3);
       }
+      s[j0 + lane] = (a0 + a1) + (a2 + a3);
     }
   }
   __syncwarp();
@@ -248,7 +249,7 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream) {
                                                   a.n_video, a.Tv);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t shm = (size_t)(KCHUNK * a.d + TILES_PER_CTA * a.Tv) * 4;
+  const size_t shm = (size_t)(KCHUNK * (a.d + 1) + TILES_PER_CTA * (a.d + a.Tv)) * 4;
   if (shm > 200 * 1024) return cudaErrorInvalidValue;
   auto kern = a.d == 128 ? route_kernel<128> : route_kernel<64>;
   if (shm > 48 * 1024) {
