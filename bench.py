@@ -11,7 +11,11 @@ Prints one JSON line (rank 0).  ``value`` = packed rows/s per DiT block over
 the whole job (rows x blocks x steps x ranks / max-over-ranks time).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload forward50_15435_d5120|block_15435_d5120|block_4096_d3072]
+                  [--workload forward50_15435_d5120|block_15435_d5120|block_4096_d3072|
+                              loop20_4096_d3072]
+
+The loop workload (20 Euler steps, 45 of 50 blocks, reuse 2) also prints a
+top-k density sweep {4, 8, 16, 32, all 56 tiles} of one block.
 
 --impl reference times the CPU oracle (float64, numpy) on a bounded sample of
 the same workload on this host's cores.  Multi-GPU runs are independent
@@ -393,6 +397,119 @@ def run_ours(args, rank, world, local_rank):
     return out
 
 
+def fresh_schedule(n_steps, reuse):
+    """Passes that run the model: every reuse-th pass and the last one."""
+    return [i % reuse == 0 or i == n_steps - 1 for i in range(n_steps)]
+
+
+def run_loop(args, rank, world, local_rank):
+    """The 20-step denoising loop at 4,096 rows: 45 of 50 blocks kept by layer thinning,
+    velocity reuse 2 (11 fresh passes), plus a top-k density sweep of one block."""
+    import numpy as np
+    import torch
+
+    import audio_diffusion_transformer_gb300 as h3
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = S.config_by_name(args.workload)
+    shape = wl.shape
+    N, D = shape.n_rows, shape.hidden
+    n_steps, reuse, keep = wl.extra["steps"], wl.extra["reuse"], wl.extra["keep"]
+    cs = h3.make_shape(shape)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device=dev)
+    blocks = make_blocks(torch, shape, wl.n_blocks, wl.seed + 1000 * rank, dev)
+    mods = np.stack([b["mod"].cpu().numpy() for b in blocks])
+    ids = h3.select_blocks(mods, keep)
+    gz = torch.Generator(device=dev)
+    gz.manual_seed(wl.seed + 7 + 1000 * rank)
+    z0 = torch.randn(N, D, generator=gz, device=dev, dtype=torch.float32)
+    z = z0.clone()
+    ring = torch.zeros(2, N, D, dtype=torch.float32, device=dev)
+    sig = [1.0 - i / n_steps for i in range(n_steps + 1)]
+    dt = -1.0 / n_steps
+    fresh = fresh_schedule(n_steps, reuse)
+    stream = torch.cuda.current_stream()
+
+    def loop():
+        z.copy_(z0)
+        nf, fs = 0, []
+        for i in range(n_steps):
+            if fresh[i]:
+                h3.denoise_step(cs, blocks, ids, z, ring, True, sig[i], 0.0, 0.0, nf, dt, ws,
+                                stream=stream.cuda_stream)
+                nf += 1
+                fs.append(sig[i])
+            else:
+                sb = fs[-2] if len(fs) > 1 else fs[-1]
+                h3.denoise_step(cs, blocks, ids, z, ring, False, sig[i], fs[-1], sb, nf, dt, ws,
+                                stream=stream.cuda_stream)
+
+    for _ in range(args.warmup):
+        loop()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler = ClockSampler()
+    sampler.start()
+    time.sleep(0.3)
+    l0 = h3.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        loop()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = h3.launch_count() - l0
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    if h3.sync_status(ws) != 0:
+        raise SystemExit("device status error in the timed region")
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    n_fresh = sum(fresh)
+    block_evals = n_fresh * len(ids)
+    # top-k density sweep: one block of this shape per k, rows/s per block
+    sweep = {}
+    x0 = torch.randn(N, D, generator=gz, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    for k in wl.extra["topk_sweep"]:
+        csk = h3.make_shape(shape.with_(topk=k))
+        x = x0.clone()
+        for _ in range(3):
+            h3.block_forward(csk, blocks[0], x, ws, stream=stream.cuda_stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for r in range(10):
+            h3.block_forward(csk, blocks[r % len(blocks)], x, ws, stream=stream.cuda_stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        t_ms = a.elapsed_time(b) / 10
+        gf, af = block_flops(shape.with_(topk=k))
+        sweep[str(k)] = {"rows_per_s": N / (t_ms / 1e3), "ms_per_block": t_ms,
+                         "attention_gflop": af / 1e9, "tflops": (gf + af) / (t_ms / 1e3) / 1e12}
+    if rank != 0:
+        return None
+    pk, pk_kind = peaks()
+    gf, af = block_flops(shape)
+    achieved = block_evals * (gf + af) * args.steps / (ms / 1e3) / 1e12
+    return {
+        "metric": METRIC, "value": N * block_evals * args.steps * world / (ms / 1e3),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "n_rows": N, "hidden": D, "heads": shape.heads,
+                   "head_dim": shape.head_dim, "topk": shape.topk, "denoise_steps": n_steps,
+                   "reuse": reuse, "fresh_passes": n_fresh, "blocks_kept": len(ids),
+                   "blocks_total": wl.n_blocks, "kept_ids": ids,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (45 blocks x 113 MB of weights per pass)"},
+        "tc_frac_of_peak": achieved / pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
+        "achieved_tflops": achieved, "topk_sweep": sweep, "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -439,7 +556,10 @@ def main():
             import torch
             torch.cuda.set_device(local_rank)
             torch.distributed.init_process_group("nccl")
-        out = run_ours(args, rank, world, local_rank)
+        if S.config_by_name(args.workload).config_id == 5:
+            out = run_loop(args, rank, world, local_rank)
+        else:
+            out = run_ours(args, rank, world, local_rank)
         if world > 1:
             import torch
             torch.distributed.destroy_process_group()

@@ -32,7 +32,7 @@ __all__ = [
     "topk_set_valid", "attend", "routed_attention", "pooled_branch", "gate_mix",
     "attention_layer", "qkv_heads", "block_forward", "block_forward_rows", "euler_update",
     "extrapolate",
-    "fresh_steps", "sigma_schedule", "denoise_forward", "thin_layers",
+    "fresh_steps", "sigma_schedule", "denoise_forward", "denoise_loop", "thin_layers",
 ]
 
 
@@ -511,6 +511,33 @@ def denoise_forward(z, blocks: list, shape, dt: float, block_ids=None) -> dict:
         x = block_forward(x, blocks[b], shape)["x2"]
     v = f32(x)
     return {"v": v, "z": euler_update(z, v, dt)}
+
+
+def denoise_loop(z, blocks: list, shape, n_steps: int, reuse: int, block_ids=None) -> dict:
+    """A whole sampler run: n_steps Euler steps on the uniform schedule, fresh
+    velocities on ``fresh_steps(n_steps, reuse)``, linear extrapolation in sigma
+    otherwise (holding the only fresh velocity while there is one).
+    Returns the final latents and the fresh-step indices.
+    """
+    sig = sigma_schedule(n_steps)
+    dt = -1.0 / n_steps
+    fresh = set(fresh_steps(n_steps, reuse))
+    z = np.asarray(z, np.float64)
+    hist = []  # (sigma, v) of fresh steps, most recent last
+    for i in range(n_steps):
+        if i in fresh:
+            r = denoise_forward(z, blocks, shape, dt, block_ids)
+            hist.append((sig[i], r["v"]))
+            z = r["z"]
+        else:
+            (sa, va) = hist[-1]
+            if len(hist) > 1:
+                (sb, vb) = hist[-2]
+                v = extrapolate(va, vb, sig[i], sa, sb)
+            else:
+                v = va
+            z = euler_update(z, v, dt)
+    return {"z": z, "fresh": sorted(fresh)}
 
 
 def thin_layers(mods, keep: int) -> list:

@@ -276,3 +276,35 @@ def test_euler_step_bit_exact_given_velocity(h3):
     torch.cuda.synchronize()
     want = oracle.euler_update(z0, oracle.bf16(z0.astype(np.float64)), -0.125)
     assert np.array_equal(z.cpu().double().numpy(), want)
+
+
+def test_denoise_loop_reuse_and_layer_thinning(h3):
+    """Six Euler steps with reuse 2 (fresh passes 0, 2, 4, 5) over 3 of 4 blocks chosen
+    by layer thinning, driven through h3dit_denoise_step, against the oracle's loop."""
+    shp = BLOCK_CASES[0][1]
+    blocks = [S.block_weights(shp, 300 + b) for b in range(4)]
+    ids = h3.select_blocks(np.stack([b["mod"] for b in blocks]), 3)
+    assert ids == oracle.thin_layers([b["mod"] for b in blocks], 3)
+    z0 = S.latents(shp, 17)
+    z = dev_f32(z0)
+    ring = torch.zeros(2, shp.n_rows, shp.hidden, dtype=torch.float32, device="cuda")
+    cs = h3.make_shape(shp)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    dblocks = [weights_to_device(b) for b in blocks]
+    n_steps, reuse = 6, 2
+    sig = oracle.sigma_schedule(n_steps)
+    fresh = oracle.fresh_steps(n_steps, reuse)
+    assert fresh == [0, 2, 4, 5]
+    nf, fs = 0, []
+    for i in range(n_steps):
+        if i in fresh:
+            h3.denoise_step(cs, dblocks, ids, z, ring, True, sig[i], 0, 0, nf, -1 / n_steps, ws)
+            nf += 1
+            fs.append(sig[i])
+        else:
+            h3.denoise_step(cs, dblocks, ids, z, ring, False, sig[i], fs[-1],
+                            fs[-2] if len(fs) > 1 else fs[-1], nf, -1 / n_steps, ws)
+    torch.cuda.synchronize()
+    assert h3.sync_status(ws) == 0
+    ref = oracle.denoise_loop(z0, [weights_to_f64(b) for b in blocks], shp, n_steps, reuse, ids)
+    assert_close(z.cpu().double().numpy(), ref["z"], "z after the loop", rel=2e-3, cos=0.99999)

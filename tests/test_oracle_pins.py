@@ -417,3 +417,25 @@ def test_block_rows_equals_full_block():
     assert np.all(np.abs(part["x2"] - ref) <= ulp)
     assert np.mean(part["x2"] == ref) > 0.99
     assert np.array_equal(part["idx"], full["idx"])
+
+
+def test_denoise_loop_orchestration_without_blocks():
+    # with no blocks the velocity is bf16(z): check which velocities and sigmas the loop
+    # combines, step by step, against a hand-written schedule for n = 8, reuse = 2
+    z0 = rng.standard_normal(64).astype(np.float32).astype(np.float64)
+    out = O.denoise_loop(z0, [], None, 8, 2, [])
+    assert out["fresh"] == [0, 2, 4, 6, 7]
+    z = z0.copy()
+    sig = [1 - i / 8 for i in range(9)]
+    hist = []
+    for i in range(8):
+        if i in (0, 2, 4, 6, 7):
+            v = O.bf16(z)
+            hist.append((sig[i], v))
+        else:
+            (sa, va), (sb, vb) = hist[-1], (hist[-2] if len(hist) > 1 else hist[-1])
+            v = va if len(hist) == 1 else va + (va - vb) * (sig[i] - sa) / (sa - sb)
+        z = (z + (-0.125) * v).astype(np.float32).astype(np.float64)
+    assert np.array_equal(out["z"], z)
+    # step 1 holds the single fresh velocity; step 3 extrapolates from passes 2 and 0
+    assert abs((sig[3] - sig[2]) / (sig[2] - sig[0]) - 0.5) < 1e-15  # v = v2 + 0.5 (v2 - v0)
