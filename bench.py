@@ -154,23 +154,32 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- CPU oracle
+_SAMPLE_INPUTS = {}
+
+
 def oracle_block_sample(shape, rng_seed=0):
     """Times the oracle on a bounded sample of one block of ``shape`` and scales it
     to the whole block.  Returns (seconds per block, description)."""
     import numpy as np
 
     import oracle as O
-    rng = np.random.default_rng(rng_seed)
     s = shape
     N, D, A, F, H, d = s.n_rows, s.hidden, s.attn_width, s.mlp_width, s.heads, s.head_dim
-    R = 64
-    w = {"w_qkvg": O.bf16(rng.standard_normal((4 * A, D)) * 0.02),
-         "b_qkvg": O.bf16(rng.standard_normal(4 * A) * 0.02),
-         "w_o": O.bf16(rng.standard_normal((D, A)) * 0.02), "b_o": np.zeros(D),
-         "w1": O.bf16(rng.standard_normal((F, D)) * 0.02), "b1": np.zeros(F),
-         "w2": O.bf16(rng.standard_normal((D, F)) * 0.02), "b2": np.zeros(D),
-         "mod": rng.standard_normal((6, D)) * 0.1}
-    x = O.bf16(rng.standard_normal((R, D)))
+    R = min(N, 1024)   # rows through the row-local stages
+    HS = min(H, 8)     # heads through the router and attention
+    key = (N, D, A, F, H, d, rng_seed)
+    if key not in _SAMPLE_INPUTS:  # drawn once per process; only the oracle's work is timed
+        rng = np.random.default_rng(rng_seed)
+        _SAMPLE_INPUTS[key] = (
+            {"w_qkvg": O.bf16(rng.standard_normal((4 * A, D)) * 0.02),
+             "b_qkvg": O.bf16(rng.standard_normal(4 * A) * 0.02),
+             "w_o": O.bf16(rng.standard_normal((D, A)) * 0.02), "b_o": np.zeros(D),
+             "w1": O.bf16(rng.standard_normal((F, D)) * 0.02), "b1": np.zeros(F),
+             "w2": O.bf16(rng.standard_normal((D, F)) * 0.02), "b2": np.zeros(D),
+             "mod": rng.standard_normal((6, D)) * 0.1},
+            O.bf16(rng.standard_normal((R, D))),
+            [O.bf16(rng.standard_normal((HS, N, d))) for _ in range(3)])
+    w, x, (Q, K, V) = _SAMPLE_INPUTS[key]
     # row-local stages on R rows
     t0 = time.perf_counter()
     h = O.rms_modulate(x, w["mod"][0], w["mod"][1])
@@ -183,10 +192,7 @@ def oracle_block_sample(shape, rng_seed=0):
     O.bf16(x1 + w["mod"][5] * O.linear(u, w["w2"], w["b2"]))
     t_rows = (time.perf_counter() - t0) * N / R
     # router over all tiles, attention for a sample of query tiles of a few heads
-    hs = min(H, 4)
-    Q = O.bf16(rng.standard_normal((hs, N, d)))
-    K = O.bf16(rng.standard_normal((hs, N, d)))
-    V = O.bf16(rng.standard_normal((hs, N, d)))
+    hs = HS
     t0 = time.perf_counter()
     mq = O.tile_means(Q, s.n_prefix, s.n_video)
     mk = O.tile_means(K, s.n_prefix, s.n_video)
@@ -196,21 +202,23 @@ def oracle_block_sample(shape, rng_seed=0):
     O.pooled_branch(Sc, mv, d)
     t_router = (time.perf_counter() - t0) * H / hs
     tv = s.n_video_tiles
-    vt = [(h, i) for h in range(hs) for i in (0, tv // 2)]
+    vt = [(h, i) for h in range(hs) for i in range(0, tv, max(1, tv // 8))][:8 * hs]
     t0 = time.perf_counter()
     O.routed_attention(Q, K, V, s.n_prefix, s.n_video, idx, tiles=vt)
     t_vid = (time.perf_counter() - t0) * (H * tv) / len(vt)
     t_pre = 0.0
     if s.n_prefix:
         t0 = time.perf_counter()
+        n_chunks = min(2, s.n_prefix // 64)
         for h in range(hs):
-            O.attend(Q[h, :64], K[h], V[h], 1.0 / math.sqrt(d))
-        t_pre = (time.perf_counter() - t0) * (H * s.n_prefix / 64) / hs
+            for c in range(n_chunks):
+                O.attend(Q[h, 64 * c:64 * c + 64], K[h], V[h], 1.0 / math.sqrt(d))
+        t_pre = (time.perf_counter() - t0) * (H * s.n_prefix / 64) / (hs * n_chunks)
     total = t_rows + t_router + t_vid + t_pre
     desc = (f"one block of the {N}-row shape, float64 oracle: row-local stages on {R} rows "
             f"(x{N / R:.0f}), router on {hs} of {H} heads (x{H / hs:.0f}), attention on "
-            f"{len(vt)} video query tiles (x{H * tv / len(vt):.0f}) and {hs} prefix 64-row "
-            f"chunks (x{H * s.n_prefix / 64 / hs:.0f}); scaled to the whole block")
+            f"{len(vt)} video query tiles (x{H * tv / len(vt):.0f}) and {2 * hs} prefix 64-row "
+            f"chunks (x{H * s.n_prefix / 64 / (2 * hs):.0f}); scaled to the whole block")
     return total, desc
 
 
