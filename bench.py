@@ -424,7 +424,9 @@ def run_loop(args, rank, world, local_rank):
     N, D = shape.n_rows, shape.hidden
     n_steps, reuse, keep = wl.extra["steps"], wl.extra["reuse"], wl.extra["keep"]
     cs = h3.make_shape(shape)
-    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device=dev)
+    ws_bytes = max(h3.workspace_bytes(h3.make_shape(shape.with_(topk=k)))
+                   for k in [shape.topk] + list(wl.extra["topk_sweep"]))
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     blocks = make_blocks(torch, shape, wl.n_blocks, wl.seed + 1000 * rank, dev)
     mods = np.stack([b["mod"].cpu().numpy() for b in blocks])
     ids = h3.select_blocks(mods, keep)
