@@ -165,8 +165,8 @@ def oracle_block_sample(shape, rng_seed=0):
     import oracle as O
     s = shape
     N, D, A, F, H, d = s.n_rows, s.hidden, s.attn_width, s.mlp_width, s.heads, s.head_dim
-    R = min(N, 1024)   # rows through the row-local stages
-    HS = min(H, 8)     # heads through the router and attention
+    R = min(N, 2048)   # rows through the row-local stages
+    HS = min(H, 12)    # heads through the router and attention
     key = (N, D, A, F, H, d, rng_seed)
     if key not in _SAMPLE_INPUTS:  # drawn once per process; only the oracle's work is timed
         rng = np.random.default_rng(rng_seed)
@@ -202,7 +202,7 @@ def oracle_block_sample(shape, rng_seed=0):
     O.pooled_branch(Sc, mv, d)
     t_router = (time.perf_counter() - t0) * H / hs
     tv = s.n_video_tiles
-    vt = [(h, i) for h in range(hs) for i in range(0, tv, max(1, tv // 8))][:8 * hs]
+    vt = [(h, i) for h in range(hs) for i in range(0, tv, max(1, tv // 12))][:12 * hs]
     t0 = time.perf_counter()
     O.routed_attention(Q, K, V, s.n_prefix, s.n_video, idx, tiles=vt)
     t_vid = (time.perf_counter() - t0) * (H * tv) / len(vt)
