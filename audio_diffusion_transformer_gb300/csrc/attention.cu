@@ -11,8 +11,9 @@
 //     key tile carries a 2-bit mask saying which of the two query tiles chose
 //     it; scores of the other half are masked to -inf, so every row sees
 //     exactly its own key set.
-// CTAs are ordered head-major (all units of head 0, then head 1, ...), so a
-// wave of CTAs shares one head's K/V in L2.  The KV loop walks the key-tile
+// CTAs run the long prefix units first (all heads), then the video units
+// head-major, so a wave of video CTAs shares one or two heads' K/V in L2 and no
+// long unit starts at the end of the grid.  The KV loop walks the key-tile
 // list one 64-row tile per step.  K and V tiles arrive by TMA (one box per
 // 64 x 64 piece, 128-byte swizzle, no multicast) into 2-stage K and V rings; a
 // K stage is released as soon as its S MMA completes and the producer loads K
@@ -112,10 +113,19 @@ __global__ void __launch_bounds__(THREADS, 2)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // head-major order: a wave of CTAs works on one or two heads, so their K/V stay in L2
-  const int n_units = p.n_pre_units + (p.Tv + 1) / 2;
-  const int h = blockIdx.x / n_units;
-  const int unit = blockIdx.x % n_units;
+  // longest work first: all prefix units (each walks every key tile), head-major, then all
+  // video units, head-major (a wave of video CTAs shares one or two heads' K/V in L2)
+  const int n_vid_units = (p.Tv + 1) / 2;
+  const int n_pre_ctas = p.n_pre_units * p.H;
+  int h, unit;
+  if ((int)blockIdx.x < n_pre_ctas) {
+    h = blockIdx.x / p.n_pre_units;
+    unit = blockIdx.x % p.n_pre_units;
+  } else {
+    const int b = blockIdx.x - n_pre_ctas;
+    h = b / n_vid_units;
+    unit = p.n_pre_units + b % n_vid_units;
+  }
   const bool is_prefix = unit < p.n_pre_units;
   const int vu = unit - p.n_pre_units;
   const int ta = 2 * vu, tb = 2 * vu + 1;  // video query tiles of a video unit
