@@ -21,13 +21,19 @@ namespace h3 {
 
 namespace {
 
+#ifndef H3_GEMM_STAGES
+#define H3_GEMM_STAGES 4
+#endif
+#ifndef H3_GEMM_GROUP_M
+#define H3_GEMM_GROUP_M 8
+#endif
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 4;
+constexpr int STAGES = H3_GEMM_STAGES;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
-constexpr int GROUP_M = 8;
+constexpr int GROUP_M = H3_GEMM_GROUP_M;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 
 struct Params {
