@@ -2,8 +2,8 @@
 //
 // y[M, N] = a[M, K] * w[N, K]^T with fp32 accumulation in TMEM (TensorFold
 // #949 "Precision": bf16 weights and activations, fp32 sums).  One persistent
-// CTA per SM walks 128 x 256 output tiles in a grouped order (8 row-blocks per
-// group, so a wave of tiles shares A and B panels in L2).  Warp roles:
+// CTA per SM walks 128 x 256 output tiles in a grouped order (8 or 16 row-blocks
+// per group, so a wave of tiles shares A and B panels in L2).  Warp roles:
 //   warp 0      TMA producer: 64-wide K slices of A (128 rows) and W (256 rows)
 //               into a 4-stage shared-memory ring (128-byte swizzle)
 //   warp 1      tcgen05.mma issuer (one thread), M=128 N=256 K=16 per op, into
@@ -24,20 +24,18 @@ namespace {
 #ifndef H3_GEMM_STAGES
 #define H3_GEMM_STAGES 4
 #endif
-#ifndef H3_GEMM_GROUP_M
-#define H3_GEMM_GROUP_M 8
-#endif
+
 constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int STAGES = H3_GEMM_STAGES;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
-constexpr int GROUP_M = H3_GEMM_GROUP_M;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 
 struct Params {
   int M, N, K;
+  int group;  // row-blocks per raster group
   const __nv_bfloat16* bias;
   __nv_bfloat16* y;
   const float* gate;
@@ -49,13 +47,13 @@ struct Params {
   int* status;
 };
 
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk,
-                                            int& n_blk) {
-  const int group = tile / (GROUP_M * num_n);
-  const int first_m = group * GROUP_M;
-  const int gm = min(num_m - first_m, GROUP_M);
-  const int in_group = tile - group * GROUP_M * num_n;
-  m_blk = first_m + in_group % gm;
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int group,
+                                            int& m_blk, int& n_blk) {
+  const int g = tile / (group * num_n);
+  const int first = g * group;
+  const int gm = min(num_m - first, group);
+  const int in_group = tile - g * group * num_n;
+  m_blk = first + in_group % gm;
   n_blk = in_group / gm;
 }
 
@@ -266,7 +264,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         int m_blk, n_blk;
-        tile_coords(tile, num_m, num_n, m_blk, n_blk);
+        tile_coords(tile, num_m, num_n, p.group, m_blk, n_blk);
         for (int kb = 0; kb < num_k; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
             ok = false;
@@ -331,7 +329,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       int m_blk, n_blk;
-      tile_coords(tile, num_m, num_n, m_blk, n_blk);
+      tile_coords(tile, num_m, num_n, p.group, m_blk, n_blk);
       if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
       const int row = m_blk * BM + quad * 32 + lane;
@@ -381,6 +379,9 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   if (!make_tmap_2d(&ta, g.a, g.M, g.K, BM)) return cudaErrorInvalidValue;
   if (!make_tmap_2d(&tb, g.w, g.N, g.K, BN)) return cudaErrorInvalidValue;
   Params p;
+  // raster group: 16 row-blocks when N or K is long (the measured best at 15,435 rows:
+  // N = 20,480 and K = 20,480), else 8 (N = K = 5,120)
+  p.group = (g.N >= 16384 || g.K >= 16384) ? 16 : 8;
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
