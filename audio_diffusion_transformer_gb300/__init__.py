@@ -8,5 +8,5 @@ from ._binding import (  # noqa: F401
     EXPORTED, H3DIT_POOLED, H3DIT_QK_NORM, H3DIT_ROPE, BlockWeights, H3DitError, Shape,
     attn_shape, block_forward, block_weights, check_shape, denoise_step, lib, linear, make_shape,
     routed_attention, routed_attention_static, select_blocks, sync_status, version, workspace_bytes, STAGES, profile_begin,
-    profile_end, launch_count,
+    profile_end, launch_count, selftest_timeout,
 )

@@ -75,6 +75,8 @@ _SIGS = [
     ("h3dit_profile_begin", ctypes.c_int, [ctypes.c_int]),
     ("h3dit_profile_end", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]),
     ("h3dit_launch_count", ctypes.c_ulonglong, []),
+    ("h3dit_selftest_timeout", ctypes.c_int,
+     [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]),
 ]
 
 STAGES = ["norm1", "qkvg", "router", "attention", "out_proj", "norm2", "fc1", "fc2", "sampler"]
@@ -220,6 +222,12 @@ def profile_end() -> dict:
     _check("h3dit_profile_end", lib().h3dit_profile_end(ms.ctypes.data, n.ctypes.data,
                                                         len(STAGES)))
     return {s: (float(ms[i]), int(n[i])) for i, s in enumerate(STAGES)}
+
+
+def selftest_timeout(workspace, limit_ms: int = 200, stream=None):
+    _check("h3dit_selftest_timeout", lib().h3dit_selftest_timeout(
+        _ptr(workspace), workspace.numel() * workspace.element_size(), int(limit_ms),
+        _stream(stream)))
 
 
 def launch_count() -> int:

@@ -230,6 +230,18 @@ h3dit_status h3dit_profile_end(float* stage_ms, int* stage_launches, int n_stage
 /* Number of kernels this library has launched in this process so far. */
 unsigned long long h3dit_launch_count(void);
 
+/*
+ * h3dit_selftest_timeout -- checks the device-side failure path (diagnostics).
+ * Launches one CTA that waits, through the same bounded mbarrier wait every
+ * tensor-core kernel uses, on a barrier that nothing signals, with a limit of
+ * limit_ms milliseconds (1..10000).  The wait runs out, the kernel records
+ * H3DIT_ERR_TIMEOUT in the workspace status word and returns; read it with
+ * h3dit_sync_status.  No fault or trap is raised: the context stays usable.
+ * workspace: device memory of at least 256 bytes whose first int is the status.
+ */
+h3dit_status h3dit_selftest_timeout(void* workspace, size_t ws_bytes, int limit_ms,
+                                    void* stream);
+
 /* Synchronises the stream, reads the device status word of this workspace,
  * clears it and returns it (H3DIT_OK or H3DIT_ERR_TIMEOUT). */
 h3dit_status h3dit_sync_status(void* workspace, size_t ws_bytes, void* stream);

@@ -94,3 +94,23 @@ def test_select_blocks_ties_drop_higher_index(h3):
         mods[b, 2, 0] = g
     assert h3.select_blocks(mods, 4) == [0, 1, 2, 5]
     assert h3.select_blocks(mods, 4) == oracle.thin_layers(list(mods.astype(np.float64)), 4)
+
+
+def test_workspace_too_small_and_bad_weights_refused_on_host(h3):
+    import ctypes
+    lib = h3.lib()
+    s = h3.make_shape(S.CONFIGS[1].shape)
+    fake = {n: 4096 for n, _ in h3.BlockWeights._fields_}  # aligned, never dereferenced
+    bw = h3.BlockWeights(*[fake[n] for n, _ in h3.BlockWeights._fields_])
+    need = h3.workspace_bytes(s)
+    assert lib.h3dit_block_forward(ctypes.byref(s), ctypes.byref(bw), 4096, 4096, need - 256,
+                                   None) == 4  # H3DIT_ERR_WORKSPACE
+    bw.w1 = 4097  # misaligned weight pointer
+    assert lib.h3dit_block_forward(ctypes.byref(s), ctypes.byref(bw), 4096, 4096, need,
+                                   None) == 3  # H3DIT_ERR_ALIGN
+    bw.w1 = None
+    assert lib.h3dit_block_forward(ctypes.byref(s), ctypes.byref(bw), 4096, 4096, need,
+                                   None) == 1  # H3DIT_ERR_ARG
+    assert lib.h3dit_selftest_timeout(None, 0, 100, None) == 1
+    assert lib.h3dit_denoise_step(ctypes.byref(s), None, None, 0, 4096, 4096, 0, 0.5, 0.6, 0.7,
+                                  0, -0.1, 4096, need, None) == 1  # nothing to extrapolate
