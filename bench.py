@@ -239,6 +239,22 @@ def cpu_baseline(shape, samples=1):
             "sample": desc, "s_per_block": best}
 
 
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(value: float, world: int, device) -> float:
+    """Largest value across the replicas (the job's wall time is the slowest rank's)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(rows_per_rank: float, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank's rows over the slowest rank's time."""
+    return rows_per_rank * world / (max_ms / 1e3)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def make_blocks(torch, shape, n_blocks, seed, dev):
     g = torch.Generator(device=dev)
@@ -320,11 +336,7 @@ def run_ours(args, rank, world, local_rank):
     ms = e0.elapsed_time(e1)
     if h3.sync_status(ws) != 0:
         raise SystemExit("device status error in the timed region")
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, world, dev)
 
     # end to end through the C ABI with host buffers: H2D z, the step, D2H z
     z_host = z0.cpu().pin_memory()
@@ -339,18 +351,14 @@ def run_ours(args, rank, world, local_rank):
             step()
             z_back.copy_(z, non_blocking=True)
         torch.cuda.synchronize()
-        e2e_ms = (time.perf_counter() - t0) * 1e3
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world, dev)
         assert torch.isfinite(z_back).all().item()
 
     if rank != 0:
         return None
     K = args.steps
     rows_blocks = N * n_blocks * K * world
-    value = rows_blocks / (ms_max / 1e3)
+    value = job_rows_per_s(N * n_blocks * K, world, ms_max)
     gemm_f, attn_f = block_flops(shape)
     step_flops = n_blocks * (gemm_f + attn_f)
     pk, pk_kind = peaks()
@@ -474,10 +482,7 @@ def run_loop(args, rank, world, local_rank):
     ms = e0.elapsed_time(e1)
     if h3.sync_status(ws) != 0:
         raise SystemExit("device status error in the timed region")
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     n_fresh = sum(fresh)
     block_evals = n_fresh * len(ids)
     # top-k density sweep: one block of this shape per k, rows/s per block
@@ -504,7 +509,7 @@ def run_loop(args, rank, world, local_rank):
     gf, af = block_flops(shape)
     achieved = block_evals * (gf + af) * args.steps / (ms / 1e3) / 1e12
     return {
-        "metric": METRIC, "value": N * block_evals * args.steps * world / (ms / 1e3),
+        "metric": METRIC, "value": job_rows_per_s(N * block_evals * args.steps, world, ms),
         "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
