@@ -261,8 +261,9 @@ def routed_attention(Q, K, V, n_prefix: int, n_video: int, idx, tile: int = 64,
     """Tile-routed attention, [H, N, d] each -> O [H, N, d] (float64).
 
     TensorFold #949 "What it adds" (h3_attention.metal: tile-routed attention
-    with fp32 scores and online softmax) and "Receipts" (prefix tiles kept for
-    every query: "8 prefix, 56 video tiles kept a query").
+    with fp32 scores and online softmax) and "Receipts" (the tile count puts 8
+    prefix tiles beside the 56 video tiles each query keeps: prefix tiles are
+    kept for every query).
     * prefix (text + audio) query rows attend densely to all N rows;
     * a video query row in tile i attends to every prefix row plus the valid
       rows of the tiles idx[h, i].
