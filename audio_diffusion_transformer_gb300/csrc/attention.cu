@@ -16,10 +16,13 @@
 // long unit starts at the end of the grid.  The KV loop walks the key-tile
 // list one 64-row tile per step.  K and V tiles arrive by TMA (one box per
 // 64 x 64 piece, 128-byte swizzle, no multicast) into 2-stage K and V rings; a
-// K stage is released as soon as its S MMA completes and the producer loads K
-// one step ahead of V.  A CTA needs ~101 KB of shared memory and 256 TMEM
-// columns, so two CTAs share an SM and each hides the other's latencies.
-//   warp 0      TMA producer (Q once, then K and V per step)
+// K stage is released as soon as its S MMA completes, a V stage as soon as its
+// PV MMA completes, and each ring has its own producer warp, so a key tile is
+// requested two steps before its S MMA.  A CTA needs ~101 KB of shared memory
+// and 256 TMEM columns, so two CTAs share an SM and each hides the other's
+// latencies.
+//   warp 0      TMA producer: Q once, then the K ring
+//   warp 6      TMA producer: the V ring
 //   warp 1      MMA issuer: S = Q K^T (M=128, N=64, fp32 in TMEM, double
 //               buffered) and O += P V (M=128, N=d, K=64) with P read from TMEM
 //               and V from shared memory as an MN-major operand
@@ -38,7 +41,7 @@ namespace h3 {
 
 namespace {
 
-constexpr int THREADS = 192;
+constexpr int THREADS = 224;  // 7 warps: K/Q producer, MMA, 4 softmax, V producer
 constexpr int MAX_TILES = 1024;  // key tiles per unit: N <= 65,536 rows
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -202,28 +205,30 @@ __global__ void __launch_bounds__(THREADS, 2)
         tma_load_3d(sQ + c * L::QCHUNK, &tmQ, q_full, 64 * c, qrow0, h);
         tma_load_3d(sQ + c * L::QCHUNK + 8192, &tmQ, q_full, 64 * c, qrow1, h);
       }
-      // K runs one step ahead of V: K_t is needed for S_t, V_t only after softmax(t)
-      for (int t = 0; t <= n_steps; ++t) {
-        if (t < n_steps) {
-          const int st = t & 1;
-          if (!mbar_wait(&k_empty[st], ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
-          uint8_t* sK = smem + L::K_OFF0 + st * L::KV_BYTES;
-          const int r0 = tiles[t] >> 2;
-          mbar_arrive_expect_tx(&k_full[st], L::KV_BYTES);
+      // K ring: a stage is refilled as soon as its S MMA completes (V has its own producer)
+      for (int t = 0; t < n_steps; ++t) {
+        const int st = t & 1;
+        if (!mbar_wait(&k_empty[st], ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        uint8_t* sK = smem + L::K_OFF0 + st * L::KV_BYTES;
+        const int r0 = tiles[t] >> 2;
+        mbar_arrive_expect_tx(&k_full[st], L::KV_BYTES);
 #pragma unroll
-          for (int c = 0; c < HD / 64; ++c)
-            tma_load_3d(sK + c * L::KCHUNK, &tmK, &k_full[st], 64 * c, r0, h);
-        }
-        if (t >= 1) {
-          const int tv = t - 1, st = tv & 1;
-          if (!mbar_wait(&v_empty[st], ((tv >> 1) & 1) ^ 1, abort_flag, p.status)) break;
-          uint8_t* sV = smem + L::V_OFF0 + st * L::KV_BYTES;
-          const int r0 = tiles[tv] >> 2;
-          mbar_arrive_expect_tx(&v_full[st], L::KV_BYTES);
+        for (int c = 0; c < HD / 64; ++c)
+          tma_load_3d(sK + c * L::KCHUNK, &tmK, &k_full[st], 64 * c, r0, h);
+      }
+    }
+  } else if (warp == 6) {
+    if (lane == 0) {
+      // V ring: a stage is refilled as soon as its PV MMA completes
+      for (int t = 0; t < n_steps; ++t) {
+        const int st = t & 1;
+        if (!mbar_wait(&v_empty[st], ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        uint8_t* sV = smem + L::V_OFF0 + st * L::KV_BYTES;
+        const int r0 = tiles[t] >> 2;
+        mbar_arrive_expect_tx(&v_full[st], L::KV_BYTES);
 #pragma unroll
-          for (int c = 0; c < HD / 64; ++c)
-            tma_load_3d(sV + c * L::KCHUNK, &tmV, &v_full[st], 64 * c, r0, h);
-        }
+        for (int c = 0; c < HD / 64; ++c)
+          tma_load_3d(sV + c * L::KCHUNK, &tmV, &v_full[st], 64 * c, r0, h);
       }
     }
   } else if (warp == 1) {
@@ -275,7 +280,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       umma_commit(drain);
       mbar_drain(drain, 0);
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ---------------------------------------------------------------- softmax
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
