@@ -104,11 +104,12 @@ __global__ void __launch_bounds__(THREADS, 2)
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;    // [2]
   uint64_t* v_full = bars + 3;    // [2]
-  uint64_t* k_empty = bars + 5;   // [2] K stage free: its S MMA completed
-  uint64_t* v_empty = bars + 7;   // [2] V stage free: its PV MMA completed
-  uint64_t* s_full = bars + 9;    // [2]
+  // s_done[st]: S of the step in stage st is in TMEM and its K stage is free (one commit,
+  // waited by the softmax warps and the K producer); pv_done[st]: the step's PV completed,
+  // so its V stage is free and O is stable (waited by the V producer and the softmax)
+  uint64_t* s_done = bars + 5;    // [2]
+  uint64_t* pv_done = bars + 7;   // [2]
   uint64_t* p_full = bars + 11;
-  uint64_t* pv_done = bars + 12;
   uint64_t* drain = bars + 13;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   int* n_steps_s = reinterpret_cast<int*>(tmem_slot + 1);
@@ -166,12 +167,10 @@ __global__ void __launch_bounds__(THREADS, 2)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
-      mbar_init(&s_full[s], 1);
+      mbar_init(&s_done[s], 1);
+      mbar_init(&pv_done[s], 1);
     }
     mbar_init(p_full, 4);
-    mbar_init(pv_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -208,7 +207,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       // K ring: a stage is refilled as soon as its S MMA completes (V has its own producer)
       for (int t = 0; t < n_steps; ++t) {
         const int st = t & 1;
-        if (!mbar_wait(&k_empty[st], ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        if (!mbar_wait(&s_done[st], ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         uint8_t* sK = smem + L::K_OFF0 + st * L::KV_BYTES;
         const int r0 = tiles[t] >> 2;
         mbar_arrive_expect_tx(&k_full[st], L::KV_BYTES);
@@ -222,7 +221,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       // V ring: a stage is refilled as soon as its PV MMA completes
       for (int t = 0; t < n_steps; ++t) {
         const int st = t & 1;
-        if (!mbar_wait(&v_empty[st], ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        if (!mbar_wait(&pv_done[st], ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         uint8_t* sV = smem + L::V_OFF0 + st * L::KV_BYTES;
         const int r0 = tiles[t] >> 2;
         mbar_arrive_expect_tx(&v_full[st], L::KV_BYTES);
@@ -246,8 +245,7 @@ __global__ void __launch_bounds__(THREADS, 2)
           umma_bf16(tmem + L::S_COL + st * 64, sdesc_sw128(q0 + qoff, 16, 1024),
                     sdesc_sw128(k0 + koff, 16, 1024), idesc_s, ks > 0 ? 1u : 0u);
         }
-        umma_commit(&k_empty[st]);
-        umma_commit(&s_full[st]);
+        umma_commit(&s_done[st]);
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
       if (ok && n_steps > 0) ok = mbar_wait(&k_full[0], 0, abort_flag, p.status);
@@ -274,8 +272,7 @@ __global__ void __launch_bounds__(THREADS, 2)
                        sdesc_sw128(v0 + ks * 2048, L::KCHUNK, 1024), idesc_pv,
                        (t > 0 || ks > 0) ? 1u : 0u);
         }
-        umma_commit(&v_empty[st]);
-        umma_commit(pv_done);
+        umma_commit(&pv_done[st]);
       }
       umma_commit(drain);
       mbar_drain(drain, 0);
@@ -292,7 +289,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     bool ok = true;
     for (int t = 0; t < n_steps; ++t) {
       const int sb = t & 1;
-      if (!mbar_wait(&s_full[sb], (t >> 1) & 1, abort_flag, p.status)) {
+      if (!mbar_wait(&s_done[sb], (t >> 1) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
@@ -340,7 +337,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       tmem_st32_u(s_addr, pk);
       if (t > 0) {
         // O must not change under a rescale while the previous step's PV runs
-        if (!mbar_wait(pv_done, (t - 1) & 1, abort_flag, p.status)) {
+        if (!mbar_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -353,7 +350,8 @@ __global__ void __launch_bounds__(THREADS, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    if (ok && n_steps > 0 && mbar_wait(pv_done, (n_steps - 1) & 1, abort_flag, p.status)) {
+    if (ok && n_steps > 0 &&
+        mbar_wait(&pv_done[(n_steps - 1) & 1], ((n_steps - 1) >> 1) & 1, abort_flag, p.status)) {
       tc_fence_after();
       int grow, tile = -1;
       bool store;
