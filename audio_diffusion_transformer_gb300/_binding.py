@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libh3dit.so")
 H3DIT_QK_NORM = 0x1
 H3DIT_ROPE = 0x2
 H3DIT_POOLED = 0x4
+H3DIT_SWIGLU = 0x8
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported or inconsistent shape",
           3: "pointer not 16-byte aligned", 4: "workspace missing or too small",
@@ -109,7 +110,8 @@ def make_shape(s, flags=None) -> Shape:
     if flags is None:
         flags = ((H3DIT_QK_NORM if getattr(s, "qk_norm", False) else 0)
                  | (H3DIT_ROPE if getattr(s, "rope", False) else 0)
-                 | (H3DIT_POOLED if getattr(s, "pooled", False) else 0))
+                 | (H3DIT_POOLED if getattr(s, "pooled", False) else 0)
+                 | (H3DIT_SWIGLU if getattr(s, "mlp", "gelu") == "swiglu" else 0))
     return Shape(s.n_text, s.n_audio, s.n_video, s.hidden, s.heads, s.head_dim, s.attn_width,
                  s.mlp_width, s.tile, s.topk, s.rms_eps, s.rope_theta, flags)
 

@@ -144,7 +144,12 @@ h3dit_status check_block(const h3dit_shape* s, Dims* o) {
   if (st != H3DIT_OK) return st;
   if (s->hidden < 256 || s->hidden % 256 || s->hidden > 8192) return H3DIT_ERR_SHAPE;
   if (s->attn_width % 256) return H3DIT_ERR_SHAPE;
-  if (s->mlp_width < 256 || s->mlp_width % 256) return H3DIT_ERR_SHAPE;
+  if (s->flags & H3DIT_SWIGLU) {
+    if (s->mlp_width < 128 || s->mlp_width % 128) return H3DIT_ERR_SHAPE;  // fc1 N = 2F
+    if (s->mlp_width % 64) return H3DIT_ERR_SHAPE;                         // fc2 K = F
+  } else if (s->mlp_width < 256 || s->mlp_width % 256) {
+    return H3DIT_ERR_SHAPE;
+  }
   if ((s->flags & H3DIT_ROPE) && (s->rope_theta <= 1.0f)) return H3DIT_ERR_ARG;
   o->block = true;
   return H3DIT_OK;
@@ -331,20 +336,21 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
     StageScope sc(H3DIT_STAGE_NORM2, st);
     H3_TRY(cu(counted(launch_rms_modulate(x, mod + 3 * D, mod + 4 * D, h, N, D, s->rms_eps, st), 1)));
   }
-  // a12: fc1 + GELU
+  // a12: fc1 + GELU, or the gate/up projection + SwiGLU
+  const bool swiglu = (s->flags & H3DIT_SWIGLU) != 0;
   GemmArgs gc;
   memset(&gc, 0, sizeof(gc));
   gc.a = h;
   gc.w = static_cast<const __nv_bfloat16*>(wt->w1);
   gc.M = N;
-  gc.N = F;
+  gc.N = swiglu ? 2 * F : F;
   gc.K = D;
   gc.bias = static_cast<const __nv_bfloat16*>(wt->b1);
   gc.y = u;
   gc.status = status;
   {
     StageScope sc(H3DIT_STAGE_FC1, st);
-    H3_TRY(cu(counted(launch_gemm(kEpiGelu, gc, st), 1)));
+    H3_TRY(cu(counted(launch_gemm(swiglu ? kEpiSwiglu : kEpiGelu, gc, st), 1)));
   }
   // a13: fc2 + gated residual (in place on x)
   GemmArgs gd;

@@ -9,7 +9,7 @@
 //   warp 1      tcgen05.mma issuer (one thread), M=128 N=256 K=16 per op, into
 //               one of two 256-column TMEM accumulators
 //   warps 2..5  epilogue: TMEM -> registers (warp w reads lanes 32*(w%4)..),
-//               bias / GELU / gated residual / q-k norm + rotary, bf16 stores
+//               bias / GELU / SwiGLU / gated residual / q-k norm + rotary, bf16 stores
 // The double accumulator lets the epilogue of tile i overlap the K loop of
 // tile i+1.  No split-K and no atomics: results are deterministic.
 #include <math.h>
@@ -140,6 +140,29 @@ __device__ __forceinline__ void epilogue_rows(const Params& p, uint32_t t_row, i
         }
       }
       store_bf16x32(dst, v);
+    }
+  }
+}
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+
+// Epilogue of the SwiGLU fc1: tile columns 0..127 are gate, 128..255 up, for the 128
+// activated outputs 128 * (n0 / 256) ..; y has N / 2 columns.
+__device__ __forceinline__ void epilogue_swiglu(const Params& p, uint32_t t_row, int row, int n0) {
+  const int F = p.N / 2;
+  const int out0 = n0 / 2;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float g[32], u[32];
+    tmem_ld32(t_row + c * 32, g);
+    tmem_ld32(t_row + 128 + c * 32, u);
+    if (row < p.M) {
+      float bg[32], bu[32];
+      load_bf16x32(p.bias + n0 + c * 32, bg);
+      load_bf16x32(p.bias + n0 + 128 + c * 32, bu);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) g[j] = silu(g[j] + bg[j]) * (u[j] + bu[j]);
+      store_bf16x32(p.y + (size_t)row * F + out0 + c * 32, g);
     }
   }
 }
@@ -336,6 +359,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16) + acc * BN;
       if (EPI == kEpiQkvg)
         epilogue_qkvg<HD>(p, t_row, row, n_blk * BN);
+      else if (EPI == kEpiSwiglu)
+        epilogue_swiglu(p, t_row, row, n_blk * BN);
       else
         epilogue_rows<EPI>(p, t_row, row, n_blk * BN);
       tc_fence_before();
@@ -407,6 +432,9 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
       return launch_one<kEpiGelu, 128>(ta, tb, p, stream);
     case kEpiResid:
       return launch_one<kEpiResid, 128>(ta, tb, p, stream);
+    case kEpiSwiglu:
+      if (!g.bias) return cudaErrorInvalidValue;
+      return launch_one<kEpiSwiglu, 128>(ta, tb, p, stream);
     case kEpiQkvg:
       if (g.head_dim == 128) return launch_one<kEpiQkvg, 128>(ta, tb, p, stream);
       if (g.head_dim == 64) return launch_one<kEpiQkvg, 64>(ta, tb, p, stream);

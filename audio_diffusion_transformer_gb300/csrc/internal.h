@@ -16,7 +16,8 @@ enum Epilogue : int {
   kEpiStore = 0,  // y = bf16(acc [+ bias])
   kEpiGelu = 1,   // y = bf16(gelu(acc + bias))
   kEpiResid = 2,  // y = bf16(y + gate * (acc + bias))   (y is the residual, in place)
-  kEpiQkvg = 3    // split into head-major q/k/v with q/k norm + rotary, and row-major g
+  kEpiQkvg = 3,   // split into head-major q/k/v with q/k norm + rotary, and row-major g
+  kEpiSwiglu = 4  // y[:, 128j + c] = bf16(silu(acc_g + b_g) * (acc_u + b_u)), y is [M, N/2]
 };
 
 struct GemmArgs {

@@ -12,7 +12,8 @@ the whole job (rows x blocks x steps x ranks / max-over-ranks time).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload forward50_15435_d5120|block_15435_d5120|block_4096_d3072|
-                              loop20_4096_d3072]
+                              loop20_4096_d3072|block_15435_d5376_swiglu|
+                              forward50_15435_d5376_swiglu]
 
 The loop workload (20 Euler steps, 45 of 50 blocks, reuse 2) also prints a
 top-k density sweep {4, 8, 16, 32, all 56 tiles} of one block.
@@ -49,8 +50,13 @@ KERNEL_SOURCES = {"gemm": ["gemm.cu", "ptx.cuh"], "attention": ["attention.cu", 
 # ----------------------------------------------------------------------------- helpers
 def workload(name):
     wl = S.config_by_name(name)
-    n_blocks = wl.n_blocks if wl.config_id == 4 else 1
+    n_blocks = wl.n_blocks if wl.extra.get("forward") else 1
     return wl, n_blocks
+
+
+def fc1_width(s):
+    """Rows of the fc1 weight: 2F for the SwiGLU MLP (gate and up), F for GELU."""
+    return 2 * s.mlp_width if s.mlp == "swiglu" else s.mlp_width
 
 
 def block_flops(s):
@@ -58,7 +64,7 @@ def block_flops(s):
     the attention the method performs (prefix rows over all N keys, video rows
     over the prefix and k selected tiles of 64 rows)."""
     N, D, A, F = s.n_rows, s.hidden, s.attn_width, s.mlp_width
-    gemm = 2.0 * N * (D * 4 * A + A * D + D * F + F * D)
+    gemm = 2.0 * N * (D * 4 * A + A * D + D * fc1_width(s) + F * D)
     k = min(s.topk, s.n_video_tiles)
     attn = 4.0 * s.head_dim * s.heads * (s.n_prefix * N + s.n_video * (s.n_prefix + k * 64))
     return gemm, attn
@@ -67,8 +73,8 @@ def block_flops(s):
 def stage_flops(s):
     N, D, A, F = s.n_rows, s.hidden, s.attn_width, s.mlp_width
     _, attn = block_flops(s)
-    return {"qkvg": 2.0 * N * D * 4 * A, "out_proj": 2.0 * N * A * D, "fc1": 2.0 * N * D * F,
-            "fc2": 2.0 * N * F * D, "attention": attn}
+    return {"qkvg": 2.0 * N * D * 4 * A, "out_proj": 2.0 * N * A * D,
+            "fc1": 2.0 * N * D * fc1_width(s), "fc2": 2.0 * N * F * D, "attention": attn}
 
 
 def peaks():
@@ -167,14 +173,15 @@ def oracle_block_sample(shape, rng_seed=0):
     N, D, A, F, H, d = s.n_rows, s.hidden, s.attn_width, s.mlp_width, s.heads, s.head_dim
     R = min(N, 2048)   # rows through the row-local stages
     HS = min(H, 12)    # heads through the router and attention
-    key = (N, D, A, F, H, d, rng_seed)
+    key = (N, D, A, F, H, d, s.mlp, rng_seed)
     if key not in _SAMPLE_INPUTS:  # drawn once per process; only the oracle's work is timed
         rng = np.random.default_rng(rng_seed)
         _SAMPLE_INPUTS[key] = (
             {"w_qkvg": O.bf16(rng.standard_normal((4 * A, D)) * 0.02),
              "b_qkvg": O.bf16(rng.standard_normal(4 * A) * 0.02),
              "w_o": O.bf16(rng.standard_normal((D, A)) * 0.02), "b_o": np.zeros(D),
-             "w1": O.bf16(rng.standard_normal((F, D)) * 0.02), "b1": np.zeros(F),
+             "w1": O.bf16(rng.standard_normal((2 * F if s.mlp == "swiglu" else F, D)) * 0.02),
+             "b1": np.zeros(2 * F if s.mlp == "swiglu" else F),
              "w2": O.bf16(rng.standard_normal((D, F)) * 0.02), "b2": np.zeros(D),
              "mod": rng.standard_normal((6, D)) * 0.1},
             O.bf16(rng.standard_normal((R, D))),
@@ -188,7 +195,7 @@ def oracle_block_sample(shape, rng_seed=0):
     o = O.bf16(qkvg[:, :A])
     x1 = O.bf16(x + w["mod"][2] * O.linear(o, w["w_o"], w["b_o"]))
     h2 = O.rms_modulate(x1, w["mod"][3], w["mod"][4])
-    u = O.bf16(O.gelu_erf(O.linear(h2, w["w1"], w["b1"])))
+    u = O.mlp_inner(h2, w, s.mlp)
     O.bf16(x1 + w["mod"][5] * O.linear(u, w["w2"], w["b2"]))
     t_rows = (time.perf_counter() - t0) * N / R
     # router over all tiles, attention for a sample of query tiles of a few heads
@@ -267,8 +274,9 @@ def make_blocks(torch, shape, n_blocks, seed, dev):
         return (t * std + mean).to(dtype).contiguous()
 
     for _ in range(n_blocks):
+        F1 = fc1_width(shape)
         blocks.append({"w_qkvg": rn(4 * A, D), "b_qkvg": rn(4 * A), "w_o": rn(D, A), "b_o": rn(D),
-                       "w1": rn(F, D), "b1": rn(F), "w2": rn(D, F), "b2": rn(D),
+                       "w1": rn(F1, D), "b1": rn(F1), "w2": rn(D, F), "b2": rn(D),
                        "mod": rn(6, D, std=0.1, dtype=torch.float32),
                        "qnorm_w": rn(d, mean=1.0), "knorm_w": rn(d, mean=1.0)})
     return blocks
@@ -392,7 +400,12 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": wl.name, "n_rows": N, "n_text": shape.n_text,
                    "n_audio": shape.n_audio, "n_video": shape.n_video, "n_blocks": n_blocks,
                    "hidden": D, "heads": shape.heads, "head_dim": shape.head_dim,
-                   "mlp": f"{shape.mlp_width // D}x GELU", "topk": shape.topk, "tile": shape.tile,
+                   "attn_width": shape.attn_width,
+                   "mlp": (f"SwiGLU {shape.mlp_width}" if shape.mlp == "swiglu"
+                           else f"{shape.mlp_width // D}x GELU"),
+                   "params_b": n_blocks * (D * 4 * shape.attn_width + shape.attn_width * D
+                                           + D * fc1_width(shape) + shape.mlp_width * D) / 1e9,
+                   "topk": shape.topk, "tile": shape.tile,
                    "dt": dt, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (each block reads its own 682 MB of weights)"},
         "s_per_forward": ms_max / K / 1e3 * (50 / n_blocks),

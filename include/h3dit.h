@@ -52,6 +52,8 @@ typedef enum {
 #define H3DIT_QK_NORM 0x1u   /* per-head RMS norm of q and k with learned weights */
 #define H3DIT_ROPE    0x2u   /* rotary on q and k over the packed row index        */
 #define H3DIT_POOLED  0x4u   /* pooled branch + gate mix for video rows            */
+#define H3DIT_SWIGLU  0x8u   /* MLP u = silu(h W_gate^T + b_g) * (h W_up^T + b_u)   */
+                             /* (else u = gelu(h W1^T + b1)); see w1 below          */
 
 typedef struct {
   int n_text, n_audio, n_video; /* packed row counts, in this order               */
@@ -71,6 +73,10 @@ typedef struct {
  *   w_qkvg [4A, D], b_qkvg [4A]: rows 0..A-1 -> q, A..2A-1 -> k, 2A..3A-1 -> v,
  *                                3A..4A-1 -> the routing gate g (head-major).
  *   w_o [D, A], b_o [D];  w1 [F, D], b1 [F];  w2 [D, F], b2 [D]
+ *   with H3DIT_SWIGLU, w1 [2F, D] and b1 [2F] hold the gate and up projections
+ *   interleaved in groups of 128 rows: rows 256j .. 256j+127 are the gate rows of
+ *   outputs 128j .. 128j+127 and rows 256j+128 .. 256j+255 their up rows (F a
+ *   multiple of 128); mlp_width is F, the activated width.
  *   mod  fp32 [6, D]: shift1, scale1, gate1, shift2, scale2, gate2
  *   qnorm_w, knorm_w [d]: per-head RMS-norm weights (used with H3DIT_QK_NORM) */
 typedef struct {
@@ -102,7 +108,9 @@ h3dit_status h3dit_check_shape(const h3dit_shape* shape);
  *   dense attention for prefix rows, pooled branch mixed in through g
  *   x1 = bf16(x + gate1 * (o W_o^T + b_o))
  *   h2 = bf16(rms(x1) * (1 + scale2) + shift2)
- *   x2 = bf16(x1 + gate2 * (gelu(h2 W1^T + b1) W2^T + b2))   [u rounded bf16]
+ *   x2 = bf16(x1 + gate2 * (u W2^T + b2)),  u = bf16(gelu(h2 W1^T + b1)), or with
+ *   H3DIT_SWIGLU u = bf16(silu(h2 Wg^T + bg) * (h2 Wu^T + bu)) (the pages' MLP:
+ *   the h3.c README's FC1 gate/up + SwiGLU paragraph; TensorFold #949 h3_swiglu)
  * x_inout: bf16 [N, D], overwritten with x2.  Workspace as sized above.
  */
 h3dit_status h3dit_block_forward(const h3dit_shape* shape, const h3dit_block_weights* w,

@@ -27,7 +27,8 @@ import numpy as np
 from scipy.special import erf as _erf
 
 __all__ = [
-    "bf16", "f32", "rms_modulate", "linear", "gelu_erf", "head_rms_norm", "rope",
+    "bf16", "f32", "rms_modulate", "linear", "gelu_erf", "silu", "swiglu_split", "mlp_inner",
+    "head_rms_norm", "rope",
     "video_tiles", "tile_means", "tile_scores", "topk_select", "topk_gap",
     "topk_set_valid", "attend", "routed_attention", "pooled_branch", "gate_mix",
     "attention_layer", "qkv_heads", "block_forward", "block_forward_rows", "euler_update",
@@ -110,6 +111,40 @@ def gelu_erf(x) -> np.ndarray:
     """
     x = np.asarray(x, np.float64)
     return 0.5 * x * (1.0 + _erf(x / math.sqrt(2.0)))
+
+
+def silu(x) -> np.ndarray:
+    """SiLU(x) = x / (1 + exp(-x)), the activation of the SwiGLU gate."""
+    x = np.asarray(x, np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def swiglu_split(w1, b1):
+    """Gate and up halves of a SwiGLU fc1 stored [2F, D] with gate/up rows interleaved in
+    groups of 128 (the library's storage convention): returns (Wg, bg, Wu, bu), [F, D] / [F]."""
+    w1 = np.asarray(w1, np.float64)
+    b1 = np.asarray(b1, np.float64)
+    F2, D = w1.shape
+    g = w1.reshape(F2 // 256, 2, 128, D)
+    bb = b1.reshape(F2 // 256, 2, 128)
+    return (g[:, 0].reshape(-1, D), bb[:, 0].reshape(-1), g[:, 1].reshape(-1, D),
+            bb[:, 1].reshape(-1))
+
+
+def mlp_inner(h2, wts: dict, mlp: str = "gelu") -> np.ndarray:
+    """The MLP's inner activations u, rounded to bf16.
+
+    "gelu": u = GELU(h2 W1^T + b1) (the synthetic 4x shapes).
+    "swiglu": u = SiLU(h2 Wg^T + bg) * (h2 Wu^T + bu), the pages' MLP (h3.c README:
+    the FC1 gate/up products feed SwiGLU and only the activated intermediate is
+    written; TensorFold #949 "What it adds": h3_swiglu).  No rounding between the
+    two products and the activation.
+    """
+    if mlp == "swiglu":
+        wg, bg, wu, bu = swiglu_split(wts["w1"], wts["b1"])
+        return bf16(silu(linear(h2, wg, bg)) * linear(h2, wu, bu))
+    return bf16(gelu_erf(linear(h2, wts["w1"], wts["b1"])))
 
 
 def head_rms_norm(x, w, eps: float = 1e-6) -> np.ndarray:
@@ -385,8 +420,9 @@ def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
     TensorFold #949 "What it adds" (block.zig: modulated norm, q/k/v and the
     routing gate, head layout, routing, attention, the pooled branch, the out
     projection and the MLP) and h3.c README (gated residual adds and AdaLN).
-    Reading: the MLP is 4x GELU for the synthetic shapes; gated residuals are
-    x + gate * branch with shift/scale/gate rows of the [6, D] table.
+    Reading: the MLP is 4x GELU for the synthetic shapes and SwiGLU for the
+    pages' own shape; gated residuals are x + gate * branch with shift/scale/gate
+    rows of the [6, D] table.
     ``wts`` holds float64 values of the bf16 weights and the fp32 table.
     """
     s = shape
@@ -403,7 +439,7 @@ def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
                           s.topk, s.tile, s.pooled, p_bf16)
     x1 = bf16(x + gate1 * linear(att["o"], wts["w_o"], wts["b_o"]))
     h2 = rms_modulate(x1, shift2, scale2, s.rms_eps)
-    u = bf16(gelu_erf(linear(h2, wts["w1"], wts["b1"])))
+    u = mlp_inner(h2, wts, getattr(s, "mlp", "gelu"))
     x2 = bf16(x1 + gate2 * linear(u, wts["w2"], wts["b2"]))
     out = dict(att)
     out.update({"h": h, "qkvg": qkvg, "q": q, "k": k, "v": v, "g": g,
@@ -461,7 +497,7 @@ def block_forward_rows(x, wts: dict, shape, rows) -> dict:
     o = bf16(o)
     x1 = bf16(x[rows] + gate1 * linear(o, wts["w_o"], wts["b_o"]))
     h2 = rms_modulate(x1, shift2, scale2, s.rms_eps)
-    u = bf16(gelu_erf(linear(h2, wts["w1"], wts["b1"])))
+    u = mlp_inner(h2, wts, getattr(s, "mlp", "gelu"))
     x2 = bf16(x1 + gate2 * linear(u, wts["w2"], wts["b2"]))
     return {"rows": rows, "x1": x1, "x2": x2, "idx": idx, "scores": S, "o": o}
 

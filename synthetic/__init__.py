@@ -168,19 +168,21 @@ def block_weights(shape: BlockShape, seed: int, block: int = 0) -> dict:
     """One block's synthetic parameters.
 
     Linear weights are stored [out, in] (row-major, the input dimension
-    contiguous).  Weights and biases bf16 ~ N(0, 0.02); modulation table fp32
+    contiguous).  With a SwiGLU MLP, fc1 holds 2F rows: the gate and up rows of
+    each group of 128 outputs, one after the other.  Weights and biases bf16 ~ N(0, 0.02); modulation table fp32
     [6, D] ~ N(0, 0.1^2) in the order shift1, scale1, gate1, shift2, scale2,
     gate2; q/k norm weights bf16 = 1 + N(0, 0.02).
     """
     D, A, F = shape.hidden, shape.attn_width, shape.mlp_width
+    F1 = 2 * F if shape.mlp == "swiglu" else F  # fc1 rows: gate/up interleaved by 128
     p = f"blk{block}."
     return {
         "w_qkvg": normal_bf16(seed, p + "w_qkvg", (4 * A, D), std=0.02),
         "b_qkvg": normal_bf16(seed, p + "b_qkvg", (4 * A,), std=0.02),
         "w_o": normal_bf16(seed, p + "w_o", (D, A), std=0.02),
         "b_o": normal_bf16(seed, p + "b_o", (D,), std=0.02),
-        "w1": normal_bf16(seed, p + "w1", (F, D), std=0.02),
-        "b1": normal_bf16(seed, p + "b1", (F,), std=0.02),
+        "w1": normal_bf16(seed, p + "w1", (F1, D), std=0.02),
+        "b1": normal_bf16(seed, p + "b1", (F1,), std=0.02),
         "w2": normal_bf16(seed, p + "w2", (D, F), std=0.02),
         "b2": normal_bf16(seed, p + "b2", (D,), std=0.02),
         "mod": normal(seed, p + "mod", (6, D), std=0.1).astype(np.float32),

@@ -26,6 +26,7 @@ class BlockShape:
     rope: bool = True
     pooled: bool = True
     attn_width_override: int = 0
+    mlp: str = "gelu"  # "gelu": fc1 [F, D]; "swiglu": fc1 [2F, D] gate/up interleaved by 128 rows
 
     @property
     def n_rows(self) -> int:
@@ -90,7 +91,7 @@ FORWARD_50 = Workload(
     "forward50_15435_d5120", 4, BLOCK_15K.shape,
     "50-block denoising forward at 15,435 rows (hidden 5,120 block shape), "
     "then z <- z + dt v with dt = -1/8",
-    n_blocks=50, extra={"dt": -0.125},
+    n_blocks=50, extra={"dt": -0.125, "forward": True},
 )
 
 # 5: 20-step denoising loop at 4,096 rows, 45 of 50 blocks, reuse 2.
@@ -100,7 +101,23 @@ LOOP_4K = Workload(
     n_blocks=50, extra={"steps": 20, "reuse": 2, "keep": 45, "topk_sweep": [4, 8, 16, 32, 56]},
 )
 
-CONFIGS = [ATTN_TINY, BLOCK_4K, BLOCK_15K, FORWARD_50, LOOP_4K]
+# The pages' own block shape: hidden 5,376, attention width 7,168 (56 x 128), SwiGLU MLP
+# 14,336 wide; 50 such blocks hold 21.2 B parameters (42 GB bf16).
+PAGES_SHAPE = BlockShape(512, 1024, 13899, hidden=5376, heads=56, head_dim=128,
+                         mlp_width=14336, topk=16, mlp="swiglu")
+BLOCK_PAGES = Workload(
+    "block_15435_d5376_swiglu", 6, PAGES_SHAPE,
+    "one block of the pages' shape: 15,435 rows, hidden 5,376, 56 x 128 heads (attention "
+    "width 7,168), SwiGLU MLP 14,336, top-k 16 + pooled",
+)
+FORWARD_PAGES = Workload(
+    "forward50_15435_d5376_swiglu", 7, PAGES_SHAPE,
+    "50-block denoising forward of the pages' shape (21.2 B parameters, 42 GB bf16) at "
+    "15,435 rows, then z <- z + dt v with dt = -1/8",
+    n_blocks=50, extra={"dt": -0.125, "forward": True},
+)
+
+CONFIGS = [ATTN_TINY, BLOCK_4K, BLOCK_15K, FORWARD_50, LOOP_4K, BLOCK_PAGES, FORWARD_PAGES]
 
 
 def config_by_name(name: str) -> Workload:

@@ -157,3 +157,27 @@ def test_denoise_two_blocks_fullsize(h3):
     ref = oracle.block_forward_rows(x1, wo[1], shp, rows)
     _log(f"denoise block1 sampled oracle {time.time() - t0:.1f}s")
     assert_close(v_gpu[rows], ref["x2"], "velocity after 2 blocks (sampled rows)")
+
+
+def test_pages_shape_block_sampled(h3):
+    """The pages' own block shape at 15,435 rows: hidden 5,376, attention width 7,168
+    (56 x 128), SwiGLU 14,336, checked on sampled rows."""
+    wl = S.config_by_name("block_15435_d5376_swiglu")
+    shp = wl.shape
+    t0 = time.time()
+    w = S.block_weights(shp, wl.seed)
+    xb = S.hidden_rows(shp, wl.seed)
+    cs = h3.make_shape(shp)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    x = dev_bf16(xb)
+    h3.block_forward(cs, weights_to_device(w), x, ws)
+    torch.cuda.synchronize()
+    assert h3.sync_status(ws) == 0
+    got = host_f64(x)
+    rows = sample_rows(shp)
+    ref = oracle.block_forward_rows(S.bf16_bits_to_f64(xb), weights_to_f64(w), shp, rows)
+    _log(f"pages-shape block sampled oracle {time.time() - t0:.1f}s")
+    x0 = S.bf16_bits_to_f64(xb)[rows]
+    assert_close(got[rows], ref["x2"], "pages-shape x2 (sampled rows)")
+    assert_close(got[rows] - x0, ref["x2"] - x0, "pages-shape update (sampled rows)", rel=5e-2,
+                 cos=0.998)

@@ -308,3 +308,22 @@ def test_denoise_loop_reuse_and_layer_thinning(h3):
     assert h3.sync_status(ws) == 0
     ref = oracle.denoise_loop(z0, [weights_to_f64(b) for b in blocks], shp, n_steps, reuse, ids)
     assert_close(z.cpu().double().numpy(), ref["z"], "z after the loop", rel=2e-3, cos=0.99999)
+
+
+SWIGLU_CASES = [
+    ("swiglu_attn_wider_than_hidden", S.BlockShape(64, 64, 200, hidden=256, heads=4, head_dim=128,
+                                                   mlp_width=384, topk=2, mlp="swiglu")),
+    ("swiglu_d64", S.BlockShape(0, 128, 130, hidden=512, heads=4, head_dim=64, mlp_width=256,
+                                topk=1, mlp="swiglu")),
+]
+
+
+@pytest.mark.parametrize("name,shp", SWIGLU_CASES, ids=[c[0] for c in SWIGLU_CASES])
+def test_block_forward_swiglu_small(h3, name, shp):
+    assert shp.attn_width != shp.hidden or shp.head_dim == 64
+    x, w, xb = run_block(h3, shp, 61)
+    ref = oracle.block_forward(S.bf16_bits_to_f64(xb), weights_to_f64(w), shp)
+    got = host_f64(x)
+    x0 = S.bf16_bits_to_f64(xb)
+    assert_close(got, ref["x2"], name, rel=2e-3, cos=0.99999)
+    assert_close(got - x0, ref["x2"] - x0, name + " update", rel=3e-2, cos=0.999)

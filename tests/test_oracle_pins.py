@@ -439,3 +439,34 @@ def test_denoise_loop_orchestration_without_blocks():
     assert np.array_equal(out["z"], z)
     # step 1 holds the single fresh velocity; step 3 extrapolates from passes 2 and 0
     assert abs((sig[3] - sig[2]) / (sig[2] - sig[0]) - 0.5) < 1e-15  # v = v2 + 0.5 (v2 - v0)
+
+
+def test_silu_closed_forms():
+    assert O.silu(0.0) == 0.0
+    x = rng.standard_normal(1000) * 4
+    assert np.allclose(O.silu(x) - O.silu(-x), x, rtol=0, atol=1e-13)  # sigmoid(x)+sigmoid(-x)=1
+    assert abs(float(O.silu(1.0)) - 0.7310585786300049) < 1e-15  # 1 / (1 + e^-1)
+    assert float(O.silu(-800.0)) == 0.0
+
+
+def test_swiglu_split_layout_and_block():
+    F, D = 256, 8
+    gate = rng.standard_normal((F, D))
+    up = rng.standard_normal((F, D))
+    w1 = np.empty((2 * F, D))
+    for j in range(F // 128):  # the storage convention written out by loops
+        w1[256 * j:256 * j + 128] = gate[128 * j:128 * j + 128]
+        w1[256 * j + 128:256 * j + 256] = up[128 * j:128 * j + 128]
+    bg, bu = rng.standard_normal(F), rng.standard_normal(F)
+    b1 = np.concatenate([np.concatenate([bg[128 * j:128 * j + 128], bu[128 * j:128 * j + 128]])
+                         for j in range(F // 128)])
+    wg, bg2, wu, bu2 = O.swiglu_split(w1, b1)
+    assert np.array_equal(wg, gate) and np.array_equal(wu, up)
+    assert np.array_equal(bg2, bg) and np.array_equal(bu2, bu)
+    h = rng.standard_normal((3, D))
+    u = O.mlp_inner(h, {"w1": w1, "b1": b1}, "swiglu")
+    for r in range(3):
+        for c in range(0, F, 37):
+            a = h[r] @ gate[c] + bg[c]
+            b = h[r] @ up[c] + bu[c]
+            assert u[r, c] == O.bf16(a / (1 + math.exp(-a)) * b)
