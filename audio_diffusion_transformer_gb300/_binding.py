@@ -43,7 +43,12 @@ class Shape(ctypes.Structure):
 class BlockWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w_qkvg", "b_qkvg", "w_o", "b_o", "w1", "b1", "w2", "b2", "mod",
-                 "qnorm_w", "knorm_w")]
+                 "qnorm_w", "knorm_w", "mod_prefix")]
+
+
+class Schedule(ctypes.Structure):
+    _fields_ = [("sigma_i", ctypes.c_float), ("sigma_a", ctypes.c_float),
+                ("sigma_b", ctypes.c_float), ("dt", ctypes.c_float)]
 
 
 _lib = None
@@ -62,9 +67,9 @@ _SIGS = [
      [ctypes.POINTER(Shape)] + [ctypes.c_void_p] * 8 + [ctypes.c_void_p]),
     ("h3dit_denoise_step", ctypes.c_int,
      [ctypes.POINTER(Shape), ctypes.POINTER(BlockWeights), ctypes.POINTER(ctypes.c_int),
-      ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
-      ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_void_p,
-      ctypes.c_size_t, ctypes.c_void_p]),
+      ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(Schedule),
+      ctypes.POINTER(Schedule), ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+      ctypes.c_void_p]),
     ("h3dit_select_blocks", ctypes.c_int,
      [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     ("h3dit_linear", ctypes.c_int,
@@ -179,15 +184,18 @@ def routed_attention_static(shape: Shape, q, k, v, gate, out, pooled=None, idx=N
         _ptr(idx), _ptr(scores), _stream(stream)))
 
 
-def denoise_step(shape: Shape, blocks: list, block_ids, z, v_ring, fresh: bool, sigma_i: float,
-                 sigma_a: float, sigma_b: float, n_fresh_so_far: int, dt: float, workspace,
-                 stream=None, _keep=None):
+def denoise_step(shape: Shape, blocks: list, block_ids, z, v_ring, fresh: bool, video,
+                 n_fresh_so_far: int, workspace, prefix=None, stream=None):
+    """One sampler step.  ``video`` and ``prefix`` are (sigma_i, sigma_a, sigma_b, dt)
+    tuples; ``prefix`` (the text and audio rows' schedule) defaults to ``video``."""
     arr = (BlockWeights * max(1, len(blocks)))(*[block_weights(b) for b in blocks])
     ids = (ctypes.c_int * max(1, len(block_ids)))(*[int(i) for i in block_ids])
+    sv = Schedule(*[float(x) for x in video])
+    sp = Schedule(*[float(x) for x in prefix]) if prefix is not None else None
     _check("h3dit_denoise_step", lib().h3dit_denoise_step(
         ctypes.byref(shape), arr, ids, len(block_ids), _ptr(z), _ptr(v_ring), int(bool(fresh)),
-        sigma_i, sigma_a, sigma_b, int(n_fresh_so_far), dt, _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+        ctypes.byref(sv), ctypes.byref(sp) if sp is not None else None, int(n_fresh_so_far),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def select_blocks(mods: np.ndarray, keep: int) -> list:

@@ -275,6 +275,8 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   __nv_bfloat16* u = at<__nv_bfloat16>(ws, w.u);
   float2* rope = at<float2>(ws, w.rope);
   const float* mod = wt->mod;
+  const float* modp = wt->mod_prefix;  // null: every row uses mod
+  const int P = m.P;
   const bool use_rope = (s->flags & H3DIT_ROPE) != 0;
   if (use_rope && !rope_ready) {
     StageScope sc(H3DIT_STAGE_SAMPLER, st);
@@ -284,7 +286,9 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   // a1: modulated norm 1
   {
     StageScope sc(H3DIT_STAGE_NORM1, st);
-    H3_TRY(cu(counted(launch_rms_modulate(x, mod + 0 * D, mod + 1 * D, h, N, D, s->rms_eps, st), 1)));
+    H3_TRY(cu(counted(launch_rms_modulate(x, mod + 0 * D, mod + 1 * D, modp ? modp + 0 * D : nullptr,
+                                          modp ? modp + 1 * D : nullptr, P, h, N, D, s->rms_eps,
+                                          st), 1)));
   }
   // a2 + a3: q/k/v/gate projection with q/k norm, rotary and head-major layout
   GemmArgs ga;
@@ -326,6 +330,8 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   gb.bias = static_cast<const __nv_bfloat16*>(wt->b_o);
   gb.y = x;
   gb.gate = mod + 2 * D;
+  gb.gate_prefix = modp ? modp + 2 * D : nullptr;
+  gb.n_prefix = P;
   gb.status = status;
   {
     StageScope sc(H3DIT_STAGE_OUT, st);
@@ -334,7 +340,9 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   // a11: modulated norm 2
   {
     StageScope sc(H3DIT_STAGE_NORM2, st);
-    H3_TRY(cu(counted(launch_rms_modulate(x, mod + 3 * D, mod + 4 * D, h, N, D, s->rms_eps, st), 1)));
+    H3_TRY(cu(counted(launch_rms_modulate(x, mod + 3 * D, mod + 4 * D, modp ? modp + 3 * D : nullptr,
+                                          modp ? modp + 4 * D : nullptr, P, h, N, D, s->rms_eps,
+                                          st), 1)));
   }
   // a12: fc1 + GELU, or the gate/up projection + SwiGLU
   const bool swiglu = (s->flags & H3DIT_SWIGLU) != 0;
@@ -363,6 +371,8 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   gd.bias = static_cast<const __nv_bfloat16*>(wt->b2);
   gd.y = x;
   gd.gate = mod + 5 * D;
+  gd.gate_prefix = modp ? modp + 5 * D : nullptr;
+  gd.n_prefix = P;
   gd.status = status;
   StageScope sc(H3DIT_STAGE_FC2, st);
   return cu(counted(launch_gemm(kEpiResid, gd, st), 1));
@@ -379,6 +389,7 @@ h3dit_status check_weights(const h3dit_shape* s, const h3dit_block_weights* w) {
     if (!w->qnorm_w || !w->knorm_w) return H3DIT_ERR_ARG;
     if (!aligned16(w->qnorm_w) || !aligned16(w->knorm_w)) return H3DIT_ERR_ALIGN;
   }
+  if (w->mod_prefix && !aligned16(w->mod_prefix)) return H3DIT_ERR_ALIGN;
   return H3DIT_OK;
 }
 
@@ -461,17 +472,19 @@ h3dit_status h3dit_routed_attention(const h3dit_shape* shape, const void* q, con
 
 h3dit_status h3dit_denoise_step(const h3dit_shape* shape, const h3dit_block_weights* blocks,
                                 const int* block_ids, int n_blocks, float* z_inout,
-                                float* v_ring, int fresh, float sigma_i, float sigma_a,
-                                float sigma_b, int n_fresh_so_far, float dt, void* workspace,
-                                size_t ws_bytes, void* stream) {
+                                float* v_ring, int fresh, const h3dit_schedule* video,
+                                const h3dit_schedule* prefix_or_null, int n_fresh_so_far,
+                                void* workspace, size_t ws_bytes, void* stream) {
   Dims m;
   H3_TRY(check_block(shape, &m));
-  if (!z_inout || !v_ring || !workspace) return H3DIT_ERR_ARG;
+  if (!z_inout || !v_ring || !workspace || !video) return H3DIT_ERR_ARG;
   if (!aligned16(z_inout) || !aligned16(v_ring) || !aligned16(workspace)) return H3DIT_ERR_ALIGN;
   if (n_fresh_so_far < 0) return H3DIT_ERR_ARG;
+  const h3dit_schedule* pre = prefix_or_null ? prefix_or_null : video;
   const Ws ws = plan(m);
   if (ws_bytes < ws.total) return H3DIT_ERR_WORKSPACE;
   const size_t n = (size_t)m.N * m.D;
+  const size_t n_pre = (size_t)m.P * m.D;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (fresh) {
     if (!blocks || (n_blocks > 0 && !block_ids) || n_blocks < 0) return H3DIT_ERR_ARG;
@@ -492,19 +505,23 @@ h3dit_status h3dit_denoise_step(const h3dit_shape* shape, const h3dit_block_weig
       H3_TRY(run_block(shape, m, ws, workspace, &blocks[block_ids[i]], x, true, st));
     float* slot = v_ring + (size_t)(n_fresh_so_far % 2) * n;
     StageScope sc(H3DIT_STAGE_SAMPLER, st);
-    return cu(counted(launch_euler_fresh(x, z_inout, slot, dt, n, st), 1));
+    return cu(counted(launch_euler_fresh(x, z_inout, slot, video->dt, pre->dt, n_pre, n, st), 1));
   }
   if (n_fresh_so_far < 1) return H3DIT_ERR_ARG;  // nothing to extrapolate from
-  H3_TRY(device_ok());
   const float* va = v_ring + (size_t)((n_fresh_so_far - 1) % 2) * n;
   const float* vb = n_fresh_so_far >= 2 ? v_ring + (size_t)(n_fresh_so_far % 2) * n : nullptr;
-  float coef = 0.f;
+  float coef_v = 0.f, coef_p = 0.f;
+  if (vb && (video->sigma_a == video->sigma_b || pre->sigma_a == pre->sigma_b))
+    return H3DIT_ERR_ARG;  // no slope to extrapolate along
+  H3_TRY(device_ok());
   if (vb) {
-    if (sigma_a == sigma_b) return H3DIT_ERR_ARG;
-    coef = (float)(((double)sigma_i - sigma_a) / ((double)sigma_a - sigma_b));
+    coef_v = (float)(((double)video->sigma_i - video->sigma_a) /
+                     ((double)video->sigma_a - video->sigma_b));
+    coef_p = (float)(((double)pre->sigma_i - pre->sigma_a) / ((double)pre->sigma_a - pre->sigma_b));
   }
   StageScope sc(H3DIT_STAGE_SAMPLER, st);
-  return cu(counted(launch_euler_extrap(z_inout, va, vb, coef, dt, n, st), 1));
+  return cu(counted(launch_euler_extrap(z_inout, va, vb, coef_v, video->dt, coef_p, pre->dt, n_pre,
+                                        n, st), 1));
 }
 
 h3dit_status h3dit_select_blocks(const float* mods, int n_blocks, int hidden, int keep,

@@ -39,6 +39,8 @@ struct Params {
   const __nv_bfloat16* bias;
   __nv_bfloat16* y;
   const float* gate;
+  const float* gate_prefix;  // rows < n_prefix use this gate when set
+  int n_prefix;
   int heads, head_dim, attn_width;
   __nv_bfloat16 *q, *k, *v, *g;
   const __nv_bfloat16 *qnorm_w, *knorm_w;
@@ -129,7 +131,8 @@ __device__ __forceinline__ void epilogue_rows(const Params& p, uint32_t t_row, i
       } else if (EPI == kEpiResid) {
         float r[32];
         load_bf16x32_rw(dst, r);
-        const float4* g4 = reinterpret_cast<const float4*>(p.gate + col0);
+        const float* gsel = (p.gate_prefix != nullptr && row < p.n_prefix) ? p.gate_prefix : p.gate;
+        const float4* g4 = reinterpret_cast<const float4*>(gsel + col0);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float4 g = __ldg(g4 + j);
@@ -413,6 +416,8 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   p.bias = g.bias;
   p.y = g.y;
   p.gate = g.gate;
+  p.gate_prefix = g.gate_prefix;
+  p.n_prefix = g.n_prefix;
   p.heads = g.heads;
   p.head_dim = g.head_dim;
   p.attn_width = g.attn_width;

@@ -27,6 +27,8 @@ struct GemmArgs {
   const __nv_bfloat16* bias;  // [N] or null
   __nv_bfloat16* y;           // [M, N] (store / gelu / resid)
   const float* gate;          // [N] fp32 (resid)
+  const float* gate_prefix;   // [N] fp32 for rows < n_prefix (resid), or null = gate
+  int n_prefix;
   // qkvg epilogue
   int heads, head_dim, attn_width;
   __nv_bfloat16 *q, *k, *v, *g;            // q/k/v [H, M, d], g [M, A]
@@ -64,14 +66,18 @@ struct RouterArgs {
 cudaError_t launch_router(const RouterArgs& args, cudaStream_t stream);
 
 // ---------------------------------------------------------------- row kernels
+// rows < n_prefix use (shift_p, scale_p) when shift_p is not null
 cudaError_t launch_rms_modulate(const __nv_bfloat16* x, const float* shift, const float* scale,
+                                const float* shift_p, const float* scale_p, int n_prefix,
                                 __nv_bfloat16* h, int rows, int D, float eps, cudaStream_t s);
 cudaError_t launch_rope_table(float2* cs, int rows, int d, float theta, cudaStream_t s);
 cudaError_t launch_f32_to_bf16(const float* z, __nv_bfloat16* x, size_t n, cudaStream_t s);
+// elements [0, n_pre) follow the prefix step dt_p (coef_p), the rest dt (coef)
 cudaError_t launch_euler_fresh(const __nv_bfloat16* x, float* z, float* v_slot, float dt,
-                               size_t n, cudaStream_t s);
+                               float dt_p, size_t n_pre, size_t n, cudaStream_t s);
 cudaError_t launch_euler_extrap(float* z, const float* v_a, const float* v_b, float coef,
-                                float dt, size_t n, cudaStream_t s);
+                                float dt, float coef_p, float dt_p, size_t n_pre, size_t n,
+                                cudaStream_t s);
 
 // ---------------------------------------------------------------- tensor maps
 bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,

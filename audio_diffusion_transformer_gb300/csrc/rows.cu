@@ -1,6 +1,7 @@
 // rows.cu -- HBM-bound row and elementwise kernels of the block and the sampler.
 //
-//  * rms_modulate: h = bf16(x / sqrt(mean(x^2) + eps) * (1 + scale) + shift),
+//  * rms_modulate: h = bf16(x / sqrt(mean(x^2) + eps) * (1 + scale) + shift), with
+//    the prefix (text + audio) rows optionally on their own (shift, scale),
 //    one 128-thread CTA per row, 16-byte loads kept in registers between the
 //    reduction and the write (TensorFold #949 "What it adds": modulated norm;
 //    h3.c README fused gated-AdaLN paragraph: a per-row RMS).
@@ -9,7 +10,7 @@
 //  * f32_to_bf16: the sampler's latents -> the bf16 residual stream.
 //  * euler_fresh / euler_extrap: v = fp32(x_L), ring store, z += dt * v; or the
 //    linear extrapolation of the last two fresh velocities (h3.c README sampler
-//    paragraph).
+//    paragraph); prefix rows and video rows each on their own schedule.
 #include <math.h>
 
 #include "internal.h"
@@ -23,11 +24,15 @@ constexpr int ROW_THREADS = 128;
 constexpr int MAXV = 8;  // 16-byte vectors per thread: D <= 8 * 8 * 128 = 8192
 
 __global__ void __launch_bounds__(ROW_THREADS)
-    rms_modulate_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ shift,
-                        const float* __restrict__ scale, __nv_bfloat16* __restrict__ h, int D,
-                        float eps) {
+    rms_modulate_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ shift_v,
+                        const float* __restrict__ scale_v, const float* __restrict__ shift_p,
+                        const float* __restrict__ scale_p, int n_prefix,
+                        __nv_bfloat16* __restrict__ h, int D, float eps) {
   __shared__ float wsum[ROW_THREADS / 32];
   const int row = blockIdx.x;
+  const bool pre = shift_p != nullptr && row < n_prefix;
+  const float* shift = pre ? shift_p : shift_v;
+  const float* scale = pre ? scale_p : scale_v;
   const int nvec = D / 8;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * D);
   uint4 xv[MAXV];
@@ -97,9 +102,11 @@ __global__ void f32_to_bf16_kernel(const float4* __restrict__ z, uint2* __restri
 }
 
 __global__ void euler_fresh_kernel(const uint2* __restrict__ x, float4* __restrict__ z,
-                                   float4* __restrict__ v_slot, float dt, size_t n4) {
+                                   float4* __restrict__ v_slot, float dt_v, float dt_p,
+                                   size_t n4_pre, size_t n4) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (size_t)gridDim.x * blockDim.x) {
+    const float dt = i < n4_pre ? dt_p : dt_v;
     const uint2 u = x[i];
     const float4 v = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
     float4 zz = z[i];
@@ -113,10 +120,13 @@ __global__ void euler_fresh_kernel(const uint2* __restrict__ x, float4* __restri
 }
 
 __global__ void euler_extrap_kernel(float4* __restrict__ z, const float4* __restrict__ va,
-                                    const float4* __restrict__ vb, float coef, float dt,
-                                    size_t n4) {
+                                    const float4* __restrict__ vb, float coef_v, float dt_v,
+                                    float coef_p, float dt_p, size_t n4_pre, size_t n4) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (size_t)gridDim.x * blockDim.x) {
+    const bool pre = i < n4_pre;
+    const float coef = pre ? coef_p : coef_v;
+    const float dt = pre ? dt_p : dt_v;
     const float4 a = va[i];
     float4 v = a;
     if (vb) {
@@ -145,9 +155,11 @@ int grid_for(size_t n, int threads) {
 }  // namespace
 
 cudaError_t launch_rms_modulate(const __nv_bfloat16* x, const float* shift, const float* scale,
+                                const float* shift_p, const float* scale_p, int n_prefix,
                                 __nv_bfloat16* h, int rows, int D, float eps, cudaStream_t s) {
   if (rows <= 0 || D % 8 != 0 || D > 8 * MAXV * ROW_THREADS) return cudaErrorInvalidValue;
-  rms_modulate_kernel<<<rows, ROW_THREADS, 0, s>>>(x, shift, scale, h, D, eps);
+  rms_modulate_kernel<<<rows, ROW_THREADS, 0, s>>>(x, shift, scale, shift_p, scale_p, n_prefix, h,
+                                                   D, eps);
   return cudaGetLastError();
 }
 
@@ -167,20 +179,21 @@ cudaError_t launch_f32_to_bf16(const float* z, __nv_bfloat16* x, size_t n, cudaS
 }
 
 cudaError_t launch_euler_fresh(const __nv_bfloat16* x, float* z, float* v_slot, float dt,
-                               size_t n, cudaStream_t s) {
-  if (n % 4) return cudaErrorInvalidValue;
+                               float dt_p, size_t n_pre, size_t n, cudaStream_t s) {
+  if (n % 4 || n_pre % 4) return cudaErrorInvalidValue;
   euler_fresh_kernel<<<grid_for(n / 4, 256), 256, 0, s>>>(
       reinterpret_cast<const uint2*>(x), reinterpret_cast<float4*>(z),
-      reinterpret_cast<float4*>(v_slot), dt, n / 4);
+      reinterpret_cast<float4*>(v_slot), dt, dt_p, n_pre / 4, n / 4);
   return cudaGetLastError();
 }
 
 cudaError_t launch_euler_extrap(float* z, const float* v_a, const float* v_b, float coef,
-                                float dt, size_t n, cudaStream_t s) {
-  if (n % 4) return cudaErrorInvalidValue;
+                                float dt, float coef_p, float dt_p, size_t n_pre, size_t n,
+                                cudaStream_t s) {
+  if (n % 4 || n_pre % 4) return cudaErrorInvalidValue;
   euler_extrap_kernel<<<grid_for(n / 4, 256), 256, 0, s>>>(
       reinterpret_cast<float4*>(z), reinterpret_cast<const float4*>(v_a),
-      reinterpret_cast<const float4*>(v_b), coef, dt, n / 4);
+      reinterpret_cast<const float4*>(v_b), coef, dt, coef_p, dt_p, n_pre / 4, n / 4);
   return cudaGetLastError();
 }
 

@@ -279,6 +279,8 @@ def make_blocks(torch, shape, n_blocks, seed, dev):
                        "w1": rn(F1, D), "b1": rn(F1), "w2": rn(D, F), "b2": rn(D),
                        "mod": rn(6, D, std=0.1, dtype=torch.float32),
                        "qnorm_w": rn(d, mean=1.0), "knorm_w": rn(d, mean=1.0)})
+        if getattr(shape, "prefix_mod", False):
+            blocks[-1]["mod_prefix"] = rn(6, D, std=0.1, dtype=torch.float32)
     return blocks
 
 
@@ -306,7 +308,7 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     def step():
-        h3.denoise_step(cs, blocks, ids, z, ring, True, 1.0, 0.0, 0.0, 0, dt, ws,
+        h3.denoise_step(cs, blocks, ids, z, ring, True, (1.0, 0.0, 0.0, dt), 0, ws,
                         stream=stream.cuda_stream)
 
     def barrier():
@@ -466,14 +468,14 @@ def run_loop(args, rank, world, local_rank):
         nf, fs = 0, []
         for i in range(n_steps):
             if fresh[i]:
-                h3.denoise_step(cs, blocks, ids, z, ring, True, sig[i], 0.0, 0.0, nf, dt, ws,
+                h3.denoise_step(cs, blocks, ids, z, ring, True, (sig[i], 0.0, 0.0, dt), nf, ws,
                                 stream=stream.cuda_stream)
                 nf += 1
                 fs.append(sig[i])
             else:
                 sb = fs[-2] if len(fs) > 1 else fs[-1]
-                h3.denoise_step(cs, blocks, ids, z, ring, False, sig[i], fs[-1], sb, nf, dt, ws,
-                                stream=stream.cuda_stream)
+                h3.denoise_step(cs, blocks, ids, z, ring, False, (sig[i], fs[-1], sb, dt), nf,
+                                ws, stream=stream.cuda_stream)
 
     for _ in range(args.warmup):
         loop()

@@ -78,12 +78,24 @@ typedef struct {
  *   outputs 128j .. 128j+127 and rows 256j+128 .. 256j+255 their up rows (F a
  *   multiple of 128); mlp_width is F, the activated width.
  *   mod  fp32 [6, D]: shift1, scale1, gate1, shift2, scale2, gate2
- *   qnorm_w, knorm_w [d]: per-head RMS-norm weights (used with H3DIT_QK_NORM) */
+ *   qnorm_w, knorm_w [d]: per-head RMS-norm weights (used with H3DIT_QK_NORM)
+ *   mod_prefix fp32 [6, D] or NULL: the modulation of the text and audio rows when
+ *     they are conditioned on their own timestep (the h3.c README runs video and
+ *     audio on independent schedules); NULL = every row uses mod */
 typedef struct {
   const void *w_qkvg, *b_qkvg, *w_o, *b_o, *w1, *b1, *w2, *b2;
   const float *mod;
   const void *qnorm_w, *knorm_w;
+  const float *mod_prefix;
 } h3dit_block_weights;
+
+/* One modality's position on its noise schedule for one sampler step. */
+typedef struct {
+  float sigma_i;  /* sigma of this step                                        */
+  float sigma_a;  /* sigma of the most recent fresh step (extrapolation only)  */
+  float sigma_b;  /* sigma of the fresh step before it (extrapolation only)    */
+  float dt;       /* step: z <- z + dt * v                                     */
+} h3dit_schedule;
 
 /* Bytes of caller-allocated device workspace that h3dit_block_forward,
  * h3dit_routed_attention and h3dit_denoise_step need for this shape
@@ -176,7 +188,8 @@ h3dit_status h3dit_routed_attention_static(const h3dit_shape* shape, const void*
  * h3dit_denoise_step -- one Euler step of the denoiser, with velocity reuse.
  *
  * h3.c README sampler paragraph: passes that run the model produce a fresh
- * velocity; skipped passes extrapolate it; the latents stay on the device.
+ * velocity; skipped passes extrapolate it, video and audio on their own
+ * schedules; the latents stay on the device.
  *   fresh != 0: x = bf16(z); run blocks[block_ids[i]] for i < n_blocks
  *               (block_ids is a HOST array, blocks a HOST array of structs);
  *               v = fp32(x); v_ring[n_fresh_so_far % 2] = v
@@ -184,13 +197,15 @@ h3dit_status h3dit_routed_attention_static(const h3dit_shape* shape, const void*
  *               v = v_a + (v_a - v_b) * (sigma_i - sigma_a) / (sigma_a - sigma_b)
  *               when n_fresh_so_far >= 2, else v = v_a
  *   then z <- z + dt * v (fp32).
+ * video: the schedule of the video rows (HOST struct); prefix_or_null: the
+ * schedule of the text and audio rows (NULL = the video schedule for all rows).
  * z_inout fp32 [N, D]; v_ring fp32 [2, N, D].
  */
 h3dit_status h3dit_denoise_step(const h3dit_shape* shape, const h3dit_block_weights* blocks,
                                 const int* block_ids, int n_blocks, float* z_inout,
-                                float* v_ring, int fresh, float sigma_i, float sigma_a,
-                                float sigma_b, int n_fresh_so_far, float dt, void* workspace,
-                                size_t ws_bytes, void* stream);
+                                float* v_ring, int fresh, const h3dit_schedule* video,
+                                const h3dit_schedule* prefix_or_null, int n_fresh_so_far,
+                                void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * h3dit_select_blocks -- layer thinning (host only, no GPU).

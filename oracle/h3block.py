@@ -414,6 +414,34 @@ def qkv_heads(qkvg, heads: int, head_dim: int, qnorm_w=None, knorm_w=None,
     return bf16(q), bf16(k), v.copy(), qkvg[:, 3 * A:4 * A].copy()
 
 
+def modulate_rows(x, mod, mod_prefix, n_prefix: int, k_shift: int, k_scale: int,
+                  eps: float = 1e-6, rows=None) -> np.ndarray:
+    """``rms_modulate`` with the text and audio rows (packed index < n_prefix) on their
+    own table when ``mod_prefix`` is given (independent audio conditioning; reading:
+    text rows share the audio rows' table).  ``rows`` are the packed indices of x."""
+    mod = np.asarray(mod, np.float64)
+    if mod_prefix is None:
+        return rms_modulate(x, mod[k_shift], mod[k_scale], eps)
+    modp = np.asarray(mod_prefix, np.float64)
+    r = np.arange(np.shape(x)[0]) if rows is None else np.asarray(rows)
+    pre = r < n_prefix
+    out = np.empty(np.shape(x))
+    if pre.any():
+        out[pre] = rms_modulate(np.asarray(x)[pre], modp[k_shift], modp[k_scale], eps)
+    if (~pre).any():
+        out[~pre] = rms_modulate(np.asarray(x)[~pre], mod[k_shift], mod[k_scale], eps)
+    return out
+
+
+def gate_rows(mod, mod_prefix, n_prefix: int, k: int, rows) -> np.ndarray:
+    """Gate row k of the modulation for each packed row index in ``rows``: [R, D] or [D]."""
+    mod = np.asarray(mod, np.float64)
+    if mod_prefix is None:
+        return mod[k]
+    pre = (np.asarray(rows) < n_prefix)[:, None]
+    return np.where(pre, np.asarray(mod_prefix, np.float64)[k], mod[k])
+
+
 def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
     """One DiT block on the packed rows x (bf16 values, [N, D]).
 
@@ -427,9 +455,11 @@ def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
     """
     s = shape
     mod = np.asarray(wts["mod"], np.float64)
-    shift1, scale1, gate1, shift2, scale2, gate2 = mod
+    modp = wts.get("mod_prefix")
+    P = s.n_prefix
     x = np.asarray(x, np.float64)
-    h = rms_modulate(x, shift1, scale1, s.rms_eps)
+    allr = np.arange(x.shape[0])
+    h = modulate_rows(x, mod, modp, P, 0, 1, s.rms_eps)
     qkvg = bf16(linear(h, wts["w_qkvg"], wts["b_qkvg"]))
     q, k, v, g = qkv_heads(qkvg, s.heads, s.head_dim,
                            wts.get("qnorm_w") if s.qk_norm else None,
@@ -437,10 +467,10 @@ def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
                            s.rms_eps, s.rope_theta, s.rope)
     att = attention_layer(q, k, v, g if s.pooled else None, s.n_prefix, s.n_video,
                           s.topk, s.tile, s.pooled, p_bf16)
-    x1 = bf16(x + gate1 * linear(att["o"], wts["w_o"], wts["b_o"]))
-    h2 = rms_modulate(x1, shift2, scale2, s.rms_eps)
+    x1 = bf16(x + gate_rows(mod, modp, P, 2, allr) * linear(att["o"], wts["w_o"], wts["b_o"]))
+    h2 = modulate_rows(x1, mod, modp, P, 3, 4, s.rms_eps)
     u = mlp_inner(h2, wts, getattr(s, "mlp", "gelu"))
-    x2 = bf16(x1 + gate2 * linear(u, wts["w2"], wts["b2"]))
+    x2 = bf16(x1 + gate_rows(mod, modp, P, 5, allr) * linear(u, wts["w2"], wts["b2"]))
     out = dict(att)
     out.update({"h": h, "qkvg": qkvg, "q": q, "k": k, "v": v, "g": g,
                 "x1": x1, "h2": h2, "u": u, "x2": x2})
@@ -458,10 +488,10 @@ def block_forward_rows(x, wts: dict, shape, rows) -> dict:
     """
     s = shape
     mod = np.asarray(wts["mod"], np.float64)
-    shift1, scale1, gate1, shift2, scale2, gate2 = mod
+    modp = wts.get("mod_prefix")
     x = np.asarray(x, np.float64)
     rows = np.array(sorted(set(int(r) for r in rows)))
-    h = rms_modulate(x, shift1, scale1, s.rms_eps)
+    h = modulate_rows(x, mod, modp, s.n_prefix, 0, 1, s.rms_eps)
     qkvg = bf16(linear(h, wts["w_qkvg"], wts["b_qkvg"]))
     q, k, v, g = qkv_heads(qkvg, s.heads, s.head_dim,
                            wts.get("qnorm_w") if s.qk_norm else None,
@@ -495,10 +525,11 @@ def block_forward_rows(x, wts: dict, shape, rows) -> dict:
                 i = (r - P) // tile
                 o[n] += g[r] * pb[:, i, :].reshape(H * d)
     o = bf16(o)
-    x1 = bf16(x[rows] + gate1 * linear(o, wts["w_o"], wts["b_o"]))
-    h2 = rms_modulate(x1, shift2, scale2, s.rms_eps)
+    x1 = bf16(x[rows] + gate_rows(mod, modp, s.n_prefix, 2, rows) *
+              linear(o, wts["w_o"], wts["b_o"]))
+    h2 = modulate_rows(x1, mod, modp, s.n_prefix, 3, 4, s.rms_eps, rows)
     u = mlp_inner(h2, wts, getattr(s, "mlp", "gelu"))
-    x2 = bf16(x1 + gate2 * linear(u, wts["w2"], wts["b2"]))
+    x2 = bf16(x1 + gate_rows(mod, modp, s.n_prefix, 5, rows) * linear(u, wts["w2"], wts["b2"]))
     return {"rows": rows, "x1": x1, "x2": x2, "idx": idx, "scores": S, "o": o}
 
 
@@ -509,21 +540,36 @@ def block_forward_rows(x, wts: dict, shape, rows) -> dict:
 # at reuse 1 / 2 / 3)
 # ---------------------------------------------------------------------------
 
-def euler_update(z, v, dt: float) -> np.ndarray:
-    """z + dt * v, computed in float64 and stored as fp32 (the latent type)."""
-    return f32(np.asarray(z, np.float64) + dt * np.asarray(v, np.float64))
+def _per_row(value_v, value_p, n_rows: int, n_prefix: int):
+    """A per-row column of a schedule value: value_p for the first n_prefix rows."""
+    if value_p is None or n_prefix == 0:
+        return value_v
+    return np.where((np.arange(n_rows) < n_prefix)[:, None], value_p, value_v)
 
 
-def extrapolate(v_a, v_b, sigma_i: float, sigma_a: float, sigma_b: float) -> np.ndarray:
+def euler_update(z, v, dt: float, dt_prefix=None, n_prefix: int = 0) -> np.ndarray:
+    """z + dt * v, computed in float64 and stored as fp32 (the latent type); the text and
+    audio rows (index < n_prefix) step by ``dt_prefix`` when given (their own schedule)."""
+    z = np.asarray(z, np.float64)
+    dtr = _per_row(dt, dt_prefix, z.shape[0], n_prefix) if z.ndim == 2 else dt
+    return f32(z + dtr * np.asarray(v, np.float64))
+
+
+def extrapolate(v_a, v_b, sigma_i: float, sigma_a: float, sigma_b: float,
+                prefix=None, n_prefix: int = 0) -> np.ndarray:
     """Linear extrapolation in sigma from the last two fresh velocities.
 
     v_hat = v_a + (v_a - v_b) * (sigma_i - sigma_a) / (sigma_a - sigma_b).
     Reading: "extrapolates skipped ... velocities" with the variable taken as
-    sigma.  With no second fresh velocity the caller holds v_a.
+    sigma; ``prefix`` = (sigma_i, sigma_a, sigma_b) of the text/audio rows' own
+    schedule.  With no second fresh velocity the caller holds v_a.
     """
     v_a = np.asarray(v_a, np.float64)
     v_b = np.asarray(v_b, np.float64)
-    return v_a + (v_a - v_b) * ((sigma_i - sigma_a) / (sigma_a - sigma_b))
+    c = (sigma_i - sigma_a) / (sigma_a - sigma_b)
+    cp = None if prefix is None else (prefix[0] - prefix[1]) / (prefix[1] - prefix[2])
+    coef = _per_row(c, cp, v_a.shape[0], n_prefix) if v_a.ndim == 2 else c
+    return v_a + (v_a - v_b) * coef
 
 
 def fresh_steps(n_steps: int, reuse: int) -> list:
@@ -531,12 +577,17 @@ def fresh_steps(n_steps: int, reuse: int) -> list:
     return [i for i in range(n_steps) if i % reuse == 0 or i == n_steps - 1]
 
 
-def sigma_schedule(n_steps: int) -> np.ndarray:
-    """Reading: uniform sigma_i = 1 - i / n (the released shift is not given)."""
-    return 1.0 - np.arange(n_steps + 1, dtype=np.float64) / n_steps
+def sigma_schedule(n_steps: int, shift: float = 1.0) -> np.ndarray:
+    """sigma_i for i = 0..n: uniform 1 - i/n, then the time shift s*t / (1 + (s-1)*t).
+
+    Reading: the pages speak of a released shifted video/audio schedule without
+    its formula or values; shift = 1 gives the uniform grid.
+    """
+    t = 1.0 - np.arange(n_steps + 1, dtype=np.float64) / n_steps
+    return shift * t / (1.0 + (shift - 1.0) * t)
 
 
-def denoise_forward(z, blocks: list, shape, dt: float, block_ids=None) -> dict:
+def denoise_forward(z, blocks: list, shape, dt: float, block_ids=None, dt_prefix=None) -> dict:
     """One fresh step: x0 = bf16(z); run the kept blocks; v = x_L; z' = z + dt v.
 
     Reading: the synthetic workload has no patch or output layers, so the last
@@ -547,33 +598,39 @@ def denoise_forward(z, blocks: list, shape, dt: float, block_ids=None) -> dict:
     for b in ids:
         x = block_forward(x, blocks[b], shape)["x2"]
     v = f32(x)
-    return {"v": v, "z": euler_update(z, v, dt)}
+    P = shape.n_prefix if shape is not None else 0
+    return {"v": v, "z": euler_update(z, v, dt, dt_prefix, P)}
 
 
-def denoise_loop(z, blocks: list, shape, n_steps: int, reuse: int, block_ids=None) -> dict:
-    """A whole sampler run: n_steps Euler steps on the uniform schedule, fresh
-    velocities on ``fresh_steps(n_steps, reuse)``, linear extrapolation in sigma
-    otherwise (holding the only fresh velocity while there is one).
+def denoise_loop(z, blocks: list, shape, n_steps: int, reuse: int, block_ids=None,
+                 sig_video=None, sig_prefix=None) -> dict:
+    """A whole sampler run: n_steps Euler steps, fresh velocities on
+    ``fresh_steps(n_steps, reuse)``, linear extrapolation in sigma otherwise (holding
+    the only fresh velocity while there is one).  ``sig_video`` / ``sig_prefix`` are the
+    n_steps + 1 sigmas of the video rows and of the text/audio rows (default: uniform;
+    the prefix defaults to the video schedule); dt_i = sigma_{i+1} - sigma_i.
     Returns the final latents and the fresh-step indices.
     """
-    sig = sigma_schedule(n_steps)
-    dt = -1.0 / n_steps
+    sv = sigma_schedule(n_steps) if sig_video is None else np.asarray(sig_video, np.float64)
+    sp = sv if sig_prefix is None else np.asarray(sig_prefix, np.float64)
+    P = shape.n_prefix if shape is not None else 0
     fresh = set(fresh_steps(n_steps, reuse))
     z = np.asarray(z, np.float64)
-    hist = []  # (sigma, v) of fresh steps, most recent last
+    hist = []  # (index, v) of fresh steps, most recent last
     for i in range(n_steps):
+        dtv, dtp = sv[i + 1] - sv[i], sp[i + 1] - sp[i]
         if i in fresh:
-            r = denoise_forward(z, blocks, shape, dt, block_ids)
-            hist.append((sig[i], r["v"]))
+            r = denoise_forward(z, blocks, shape, dtv, block_ids, dtp)
+            hist.append((i, r["v"]))
             z = r["z"]
         else:
-            (sa, va) = hist[-1]
+            (ia, va) = hist[-1]
             if len(hist) > 1:
-                (sb, vb) = hist[-2]
-                v = extrapolate(va, vb, sig[i], sa, sb)
+                (ib, vb) = hist[-2]
+                v = extrapolate(va, vb, sv[i], sv[ia], sv[ib], (sp[i], sp[ia], sp[ib]), P)
             else:
                 v = va
-            z = euler_update(z, v, dt)
+            z = euler_update(z, v, dtv, dtp, P)
     return {"z": z, "fresh": sorted(fresh)}
 
 

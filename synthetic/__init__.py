@@ -169,14 +169,16 @@ def block_weights(shape: BlockShape, seed: int, block: int = 0) -> dict:
 
     Linear weights are stored [out, in] (row-major, the input dimension
     contiguous).  With a SwiGLU MLP, fc1 holds 2F rows: the gate and up rows of
-    each group of 128 outputs, one after the other.  Weights and biases bf16 ~ N(0, 0.02); modulation table fp32
-    [6, D] ~ N(0, 0.1^2) in the order shift1, scale1, gate1, shift2, scale2,
-    gate2; q/k norm weights bf16 = 1 + N(0, 0.02).
+    each group of 128 outputs, one after the other.  Weights and biases bf16
+    ~ N(0, 0.02); modulation table fp32 [6, D] ~ N(0, 0.1^2) in the order shift1,
+    scale1, gate1, shift2, scale2, gate2; with ``prefix_mod`` the text and audio
+    rows get their own table "mod_prefix" of the same kind; q/k norm weights bf16
+    = 1 + N(0, 0.02).
     """
     D, A, F = shape.hidden, shape.attn_width, shape.mlp_width
     F1 = 2 * F if shape.mlp == "swiglu" else F  # fc1 rows: gate/up interleaved by 128
     p = f"blk{block}."
-    return {
+    out = {
         "w_qkvg": normal_bf16(seed, p + "w_qkvg", (4 * A, D), std=0.02),
         "b_qkvg": normal_bf16(seed, p + "b_qkvg", (4 * A,), std=0.02),
         "w_o": normal_bf16(seed, p + "w_o", (D, A), std=0.02),
@@ -189,6 +191,9 @@ def block_weights(shape: BlockShape, seed: int, block: int = 0) -> dict:
         "qnorm_w": normal_bf16(seed, p + "qnorm_w", (shape.head_dim,), mean=1.0, std=0.02),
         "knorm_w": normal_bf16(seed, p + "knorm_w", (shape.head_dim,), mean=1.0, std=0.02),
     }
+    if shape.prefix_mod:  # the text/audio rows' own modulation table, same distribution
+        out["mod_prefix"] = normal(seed, p + "mod_prefix", (6, D), std=0.1).astype(np.float32)
+    return out
 
 
 def hidden_rows(shape: BlockShape, seed: int) -> np.ndarray:

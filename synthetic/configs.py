@@ -27,6 +27,7 @@ class BlockShape:
     pooled: bool = True
     attn_width_override: int = 0
     mlp: str = "gelu"  # "gelu": fc1 [F, D]; "swiglu": fc1 [2F, D] gate/up interleaved by 128 rows
+    prefix_mod: bool = False  # text/audio rows modulated by their own [6, D] table
 
     @property
     def n_rows(self) -> int:
@@ -104,7 +105,7 @@ LOOP_4K = Workload(
 # The pages' own block shape: hidden 5,376, attention width 7,168 (56 x 128), SwiGLU MLP
 # 14,336 wide; 50 such blocks hold 21.2 B parameters (42 GB bf16).
 PAGES_SHAPE = BlockShape(512, 1024, 13899, hidden=5376, heads=56, head_dim=128,
-                         mlp_width=14336, topk=16, mlp="swiglu")
+                         mlp_width=14336, topk=16, mlp="swiglu", prefix_mod=True)
 BLOCK_PAGES = Workload(
     "block_15435_d5376_swiglu", 6, PAGES_SHAPE,
     "one block of the pages' shape: 15,435 rows, hidden 5,376, 56 x 128 heads (attention "

@@ -140,8 +140,8 @@ def test_denoise_two_blocks_fullsize(h3):
     ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
     z = dev_f32(z0)
     ring = torch.zeros(2, shp.n_rows, shp.hidden, dtype=torch.float32, device="cuda")
-    h3.denoise_step(cs, [weights_to_device(b) for b in blocks], [0, 1], z, ring, True, 1.0, 0.0,
-                    0.0, 0, -0.125, ws)
+    h3.denoise_step(cs, [weights_to_device(b) for b in blocks], [0, 1], z, ring, True,
+                    (1.0, 0.0, 0.0, -0.125), 0, ws)
     torch.cuda.synchronize()
     assert h3.sync_status(ws) == 0
     v_gpu = ring[0].cpu().double().numpy()

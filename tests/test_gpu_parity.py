@@ -244,14 +244,14 @@ def test_denoise_fresh_and_extrapolated_steps(h3):
     n_fresh = 0
     for i, fresh in enumerate([True, True, False, True]):
         if fresh:
-            h3.denoise_step(cs, dblocks, ids, z, ring, True, sig[i], 0, 0, n_fresh, dt, ws)
+            h3.denoise_step(cs, dblocks, ids, z, ring, True, (sig[i], 0, 0, dt), n_fresh, ws)
             r = oracle.denoise_forward(zr, wo, shp, dt, ids)
             vs.append((sig[i], r["v"]))
             zr = r["z"]
             n_fresh += 1
         else:
-            h3.denoise_step(cs, dblocks, ids, z, ring, False, sig[i], vs[-1][0], vs[-2][0],
-                            n_fresh, dt, ws)
+            h3.denoise_step(cs, dblocks, ids, z, ring, False, (sig[i], vs[-1][0], vs[-2][0], dt),
+                            n_fresh, ws)
             vh = oracle.extrapolate(vs[-1][1], vs[-2][1], sig[i], vs[-1][0], vs[-2][0])
             zr = oracle.euler_update(zr, vh, dt)
         torch.cuda.synchronize()
@@ -272,7 +272,7 @@ def test_euler_step_bit_exact_given_velocity(h3):
     ring = torch.zeros(2, shp.n_rows, shp.hidden, dtype=torch.float32, device="cuda")
     cs = h3.make_shape(shp)
     ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
-    h3.denoise_step(cs, [], [], z, ring, True, 1.0, 0, 0, 0, -0.125, ws)
+    h3.denoise_step(cs, [], [], z, ring, True, (1.0, 0, 0, -0.125), 0, ws)
     torch.cuda.synchronize()
     want = oracle.euler_update(z0, oracle.bf16(z0.astype(np.float64)), -0.125)
     assert np.array_equal(z.cpu().double().numpy(), want)
@@ -298,12 +298,13 @@ def test_denoise_loop_reuse_and_layer_thinning(h3):
     nf, fs = 0, []
     for i in range(n_steps):
         if i in fresh:
-            h3.denoise_step(cs, dblocks, ids, z, ring, True, sig[i], 0, 0, nf, -1 / n_steps, ws)
+            h3.denoise_step(cs, dblocks, ids, z, ring, True, (sig[i], 0, 0, -1 / n_steps), nf, ws)
             nf += 1
             fs.append(sig[i])
         else:
-            h3.denoise_step(cs, dblocks, ids, z, ring, False, sig[i], fs[-1],
-                            fs[-2] if len(fs) > 1 else fs[-1], nf, -1 / n_steps, ws)
+            h3.denoise_step(cs, dblocks, ids, z, ring, False,
+                            (sig[i], fs[-1], fs[-2] if len(fs) > 1 else fs[-1], -1 / n_steps),
+                            nf, ws)
     torch.cuda.synchronize()
     assert h3.sync_status(ws) == 0
     ref = oracle.denoise_loop(z0, [weights_to_f64(b) for b in blocks], shp, n_steps, reuse, ids)
@@ -327,3 +328,89 @@ def test_block_forward_swiglu_small(h3, name, shp):
     x0 = S.bf16_bits_to_f64(xb)
     assert_close(got, ref["x2"], name, rel=2e-3, cos=0.99999)
     assert_close(got - x0, ref["x2"] - x0, name + " update", rel=3e-2, cos=0.999)
+
+
+# ----------------------------------------------------------------------------- per-modality
+PREFIX_MOD_CASES = [
+    ("prefix_table_gelu", BLOCK_CASES[0][1].with_(prefix_mod=True)),
+    ("prefix_table_swiglu", SWIGLU_CASES[0][1].with_(prefix_mod=True)),
+]
+
+
+@pytest.mark.parametrize("name,shp", PREFIX_MOD_CASES, ids=[c[0] for c in PREFIX_MOD_CASES])
+def test_block_forward_prefix_table(h3, name, shp):
+    """Text and audio rows on their own modulation table (norm shift/scale and gates)."""
+    x, w, xb = run_block(h3, shp, 71)
+    assert "mod_prefix" in w
+    ref = oracle.block_forward(S.bf16_bits_to_f64(xb), weights_to_f64(w), shp)
+    got = host_f64(x)
+    x0 = S.bf16_bits_to_f64(xb)
+    P = shp.n_prefix
+    assert_close(got, ref["x2"], name, rel=2e-3, cos=0.99999)
+    for part, sl in (("prefix", slice(0, P)), ("video", slice(P, None))):
+        assert_close(got[sl] - x0[sl], ref["x2"][sl] - x0[sl], f"{name} {part} update",
+                     rel=3e-2, cos=0.999)
+
+
+def test_block_prefix_table_zero_gates_leave_prefix_rows(h3):
+    shp = PREFIX_MOD_CASES[0][1]
+    w = S.block_weights(shp, 72)
+    w["mod_prefix"][2] = 0.0
+    w["mod_prefix"][5] = 0.0
+    x, _, xb = run_block(h3, shp, 72, wts=w)
+    got = x.view(torch.int16).cpu().numpy()
+    P = shp.n_prefix
+    assert np.array_equal(got[:P], xb[:P].view(np.int16))
+    assert not np.array_equal(got[P:], xb[P:].view(np.int16))
+
+
+def test_denoise_loop_per_modality_schedules(h3):
+    """Video rows on the uniform schedule, text/audio rows on a shifted one (shift 3),
+    reuse 2 over 5 steps, both modulation tables, against the oracle's loop."""
+    shp = PREFIX_MOD_CASES[0][1]
+    blocks = [S.block_weights(shp, 400 + b) for b in range(2)]
+    ids = [0, 1]
+    z0 = S.latents(shp, 19)
+    z = dev_f32(z0)
+    ring = torch.zeros(2, shp.n_rows, shp.hidden, dtype=torch.float32, device="cuda")
+    cs = h3.make_shape(shp)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    dblocks = [weights_to_device(b) for b in blocks]
+    n_steps, reuse = 5, 2
+    sv, sp = oracle.sigma_schedule(n_steps), oracle.sigma_schedule(n_steps, 3.0)
+    fresh = oracle.fresh_steps(n_steps, reuse)
+    hist = []
+    for i in range(n_steps):
+        dv, dp = sv[i + 1] - sv[i], sp[i + 1] - sp[i]
+        if i in fresh:
+            h3.denoise_step(cs, dblocks, ids, z, ring, True, (sv[i], 0, 0, dv), len(hist), ws,
+                            prefix=(sp[i], 0, 0, dp))
+            hist.append(i)
+        else:
+            a, b = hist[-1], hist[-2] if len(hist) > 1 else hist[-1]
+            h3.denoise_step(cs, dblocks, ids, z, ring, False, (sv[i], sv[a], sv[b], dv),
+                            len(hist), ws, prefix=(sp[i], sp[a], sp[b], dp))
+    torch.cuda.synchronize()
+    assert h3.sync_status(ws) == 0
+    ref = oracle.denoise_loop(z0, [weights_to_f64(b) for b in blocks], shp, n_steps, reuse, ids,
+                              sig_video=sv, sig_prefix=sp)
+    got = z.cpu().double().numpy()
+    P = shp.n_prefix
+    assert_close(got[:P], ref["z"][:P], "prefix rows after the loop", rel=2e-3, cos=0.99999)
+    assert_close(got[P:], ref["z"][P:], "video rows after the loop", rel=2e-3, cos=0.99999)
+
+
+def test_euler_per_modality_bit_exact_given_velocity(h3):
+    # zero blocks: v = bf16(z); prefix rows step by -1/4, video rows by -1/8, both exact
+    shp = BLOCK_CASES[0][1]
+    z0 = S.latents(shp, 9)
+    z = dev_f32(z0)
+    ring = torch.zeros(2, shp.n_rows, shp.hidden, dtype=torch.float32, device="cuda")
+    cs = h3.make_shape(shp)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    h3.denoise_step(cs, [], [], z, ring, True, (1.0, 0, 0, -0.125), 0, ws,
+                    prefix=(1.0, 0, 0, -0.25))
+    torch.cuda.synchronize()
+    want = oracle.euler_update(z0, oracle.bf16(z0.astype(np.float64)), -0.125, -0.25,
+                               shp.n_prefix)
+    assert np.array_equal(z.cpu().double().numpy(), want)

@@ -112,5 +112,11 @@ def test_workspace_too_small_and_bad_weights_refused_on_host(h3):
     assert lib.h3dit_block_forward(ctypes.byref(s), ctypes.byref(bw), 4096, 4096, need,
                                    None) == 1  # H3DIT_ERR_ARG
     assert lib.h3dit_selftest_timeout(None, 0, 100, None) == 1
-    assert lib.h3dit_denoise_step(ctypes.byref(s), None, None, 0, 4096, 4096, 0, 0.5, 0.6, 0.7,
-                                  0, -0.1, 4096, need, None) == 1  # nothing to extrapolate
+    sv = h3.Schedule(0.5, 0.6, 0.7, -0.1)
+    assert lib.h3dit_denoise_step(ctypes.byref(s), None, None, 0, 4096, 4096, 0, ctypes.byref(sv),
+                                  None, 0, 4096, need, None) == 1  # nothing to extrapolate
+    assert lib.h3dit_denoise_step(ctypes.byref(s), None, None, 0, 4096, 4096, 1, None, None, 0,
+                                  4096, need, None) == 1  # no video schedule
+    bad = h3.Schedule(0.5, 0.6, 0.6, -0.1)  # sigma_a == sigma_b: no extrapolation slope
+    assert lib.h3dit_denoise_step(ctypes.byref(s), None, None, 0, 4096, 4096, 0, ctypes.byref(bad),
+                                  None, 2, 4096, need, None) == 1

@@ -362,6 +362,58 @@ def test_block_all_tiles_equals_dense():
     assert np.allclose(out["O"], dense, atol=1e-12)
 
 
+def test_block_prefix_table_zero_gates_split_by_modality():
+    # zero gates on one table leave exactly that modality's rows untouched
+    shape = _tiny_shape(prefix_mod=True)
+    x = S.bf16_bits_to_f64(S.hidden_rows(shape, 3))
+    P = shape.n_prefix
+    for zeroed, same, moved in (("mod_prefix", slice(0, P), slice(P, None)),
+                                ("mod", slice(P, None), slice(0, P))):
+        w = _weights(shape)
+        w[zeroed][2] = 0.0
+        w[zeroed][5] = 0.0
+        out = O.block_forward(x, w, shape)
+        assert np.array_equal(out["x2"][same], x[same])
+        assert not np.array_equal(out["x2"][moved], x[moved])
+
+
+def test_block_prefix_table_norm_applies_to_its_rows():
+    # scale1 = -1 on one table makes that modality's modulated rows all equal to its shift1;
+    # with no rotary and every tile selected (dense), those rows' queries are equal, so
+    # their attention outputs are equal too, while the other modality's are not
+    for table, rows, other in (("mod_prefix", slice(0, 128), slice(128, None)),
+                               ("mod", slice(128, None), slice(0, 128))):
+        shape = _tiny_shape(rope=False, pooled=False, topk=3, prefix_mod=True)
+        w = _weights(shape)
+        w[table][1] = -1.0
+        x = S.bf16_bits_to_f64(S.hidden_rows(shape, 5))
+        o = O.block_forward(x, w, shape)["o_f64"]
+        assert np.allclose(o[rows], o[rows][:1], atol=1e-12, rtol=0)
+        assert np.abs(o[other] - o[other][:1]).max() > 1e-3
+
+
+def test_block_prefix_table_equal_to_shared_table():
+    shape = _tiny_shape(prefix_mod=True)
+    w = _weights(shape)
+    w["mod_prefix"] = w["mod"].copy()
+    x = S.bf16_bits_to_f64(S.hidden_rows(shape, 6))
+    a = O.block_forward(x, w, shape)["x2"]
+    w.pop("mod_prefix")
+    assert np.array_equal(a, O.block_forward(x, w, shape)["x2"])
+
+
+def test_block_rows_equals_full_block_with_prefix_table():
+    shape = _tiny_shape(prefix_mod=True, mlp="swiglu")
+    w = _weights(shape)
+    x = S.bf16_bits_to_f64(S.hidden_rows(shape, 4))
+    full = O.block_forward(x, w, shape)
+    rows = [0, 64, 127, 128, 200, shape.n_rows - 1]
+    part = O.block_forward_rows(x, w, shape, rows)
+    ref = full["x2"][rows]
+    assert np.all(np.abs(part["x2"] - ref) <= np.abs(ref) * 2.0 ** -7)
+    assert np.mean(part["x2"] == ref) > 0.99
+
+
 # --------------------------------------------------------------------------- denoiser
 def test_euler_power_of_two_exact():
     z = rng.standard_normal(1000).astype(np.float32)
@@ -376,6 +428,57 @@ def test_extrapolation_exact_for_linear_velocity():
     v = lambda s: a + b * s  # noqa: E731
     got = O.extrapolate(v(0.7), v(0.8), 0.65, 0.7, 0.8)
     assert np.allclose(got, v(0.65), atol=1e-13)
+
+
+def test_euler_and_extrapolation_per_modality_rows():
+    P = 3
+    z = np.zeros((7, 4))
+    got = O.euler_update(z, np.ones((7, 4)), -0.25, -0.5, P)
+    assert np.all(got[:P] == -0.5) and np.all(got[P:] == -0.25)
+    # velocities linear in each modality's own sigma are extrapolated exactly
+    a, b = rng.standard_normal((7, 4)), rng.standard_normal((7, 4))
+    sv, sp = (0.65, 0.7, 0.8), (0.5, 0.55, 0.7)
+    va = np.where(np.arange(7)[:, None] < P, a + b * sp[1], a + b * sv[1])
+    vb = np.where(np.arange(7)[:, None] < P, a + b * sp[2], a + b * sv[2])
+    got = O.extrapolate(va, vb, *sv, prefix=sp, n_prefix=P)
+    assert np.allclose(got[:P], (a + b * sp[0])[:P], atol=1e-13)
+    assert np.allclose(got[P:], (a + b * sv[0])[P:], atol=1e-13)
+
+
+def test_sigma_schedule_shift_endpoints_and_composition():
+    for n in (1, 4, 30):
+        for s in (1.0, 0.5, 3.0, 5.0):
+            sig = O.sigma_schedule(n, s)
+            assert sig[0] == 1.0 and sig[-1] == 0.0 and np.all(np.diff(sig) < 0)
+    assert np.array_equal(O.sigma_schedule(8), 1 - np.arange(9) / 8)
+    # a larger shift keeps more of the run at high noise: every interior sigma rises
+    assert np.all(O.sigma_schedule(10, 3.0)[1:-1] > O.sigma_schedule(10)[1:-1])
+    # the map t -> s t / (1 + (s - 1) t) composes multiplicatively in s (a Moebius family)
+    t = O.sigma_schedule(12)
+    f = lambda s, u: s * u / (1 + (s - 1) * u)  # noqa: E731
+    assert np.allclose(f(2.0, f(1.5, t)), O.sigma_schedule(12, 3.0), atol=1e-15)
+    assert np.allclose(O.sigma_schedule(12, 0.25), f(0.5, f(0.5, t)), atol=1e-15)
+
+
+def test_denoise_loop_per_modality_without_blocks():
+    # with no blocks v = bf16(z) and the rows are independent: each modality follows the
+    # Euler product prod(1 + dt_i) of its own schedule up to bf16/fp32 rounding
+    class Shp:
+        n_prefix = 5
+    n = 6
+    z0 = rng.standard_normal((12, 8)).astype(np.float32).astype(np.float64)
+    sv, sp = O.sigma_schedule(n), O.sigma_schedule(n, 3.0)
+    out = O.denoise_loop(z0, [], Shp, n, 1, [], sig_video=sv, sig_prefix=sp)
+    for rows, sig in ((slice(0, 5), sp), (slice(5, None), sv)):
+        want = z0[rows] * np.prod(1 + np.diff(sig))
+        assert np.allclose(out["z"][rows], want, rtol=n * 2.0 ** -8, atol=0)
+    # reuse 2: the video rows do not depend on the prefix schedule, and equal sigmas give
+    # the default run
+    a = O.denoise_loop(z0, [], Shp, n, 2, [], sig_video=sv, sig_prefix=sp)
+    b = O.denoise_loop(z0, [], Shp, n, 2, [], sig_video=sv, sig_prefix=sv)
+    c = O.denoise_loop(z0, [], Shp, n, 2, [])
+    assert np.array_equal(a["z"][5:], b["z"][5:]) and np.array_equal(b["z"], c["z"])
+    assert not np.array_equal(a["z"][:5], b["z"][:5])
 
 
 def test_fresh_step_counts_golden():
