@@ -37,7 +37,9 @@ class Shape(ctypes.Structure):
                 ("hidden", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("attn_width", ctypes.c_int), ("mlp_width", ctypes.c_int), ("tile", ctypes.c_int),
                 ("topk", ctypes.c_int), ("rms_eps", ctypes.c_float),
-                ("rope_theta", ctypes.c_float), ("flags", ctypes.c_uint)]
+                ("rope_theta", ctypes.c_float), ("flags", ctypes.c_uint),
+                ("video_t", ctypes.c_int), ("video_h", ctypes.c_int), ("video_w", ctypes.c_int),
+                ("cube_t", ctypes.c_int), ("cube_h", ctypes.c_int), ("cube_w", ctypes.c_int)]
 
 
 class BlockWeights(ctypes.Structure):
@@ -72,6 +74,9 @@ _SIGS = [
       ctypes.c_void_p]),
     ("h3dit_select_blocks", ctypes.c_int,
      [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    ("h3dit_tile_spans", ctypes.c_int,
+     [ctypes.POINTER(Shape), ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]),
+    ("h3dit_video_order", ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_void_p]),
     ("h3dit_linear", ctypes.c_int,
      [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
       ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
@@ -117,8 +122,11 @@ def make_shape(s, flags=None) -> Shape:
                  | (H3DIT_ROPE if getattr(s, "rope", False) else 0)
                  | (H3DIT_POOLED if getattr(s, "pooled", False) else 0)
                  | (H3DIT_SWIGLU if getattr(s, "mlp", "gelu") == "swiglu" else 0))
+    grid = getattr(s, "video_grid", None) or (0, 0, 0)
+    cube = getattr(s, "cube", None) if getattr(s, "video_grid", None) else None
+    cube = cube or (0, 0, 0)
     return Shape(s.n_text, s.n_audio, s.n_video, s.hidden, s.heads, s.head_dim, s.attn_width,
-                 s.mlp_width, s.tile, s.topk, s.rms_eps, s.rope_theta, flags)
+                 s.mlp_width, s.tile, s.topk, s.rms_eps, s.rope_theta, flags, *grid, *cube)
 
 
 def attn_shape(s, flags=None) -> Shape:
@@ -196,6 +204,26 @@ def denoise_step(shape: Shape, blocks: list, block_ids, z, v_ring, fresh: bool, 
         ctypes.byref(shape), arr, ids, len(block_ids), _ptr(z), _ptr(v_ring), int(bool(fresh)),
         ctypes.byref(sv), ctypes.byref(sp) if sp is not None else None, int(n_fresh_so_far),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tile_spans(shape: Shape):
+    """(first_row, n_rows) int32 arrays of the shape's video routing tiles."""
+    n = ctypes.c_int(0)
+    lib().h3dit_tile_spans(ctypes.byref(shape), None, None, ctypes.byref(n))
+    if n.value <= 0:
+        _check("h3dit_tile_spans", lib().h3dit_check_shape(ctypes.byref(shape)))
+    first = np.zeros(max(n.value, 1), np.int32)
+    rows = np.zeros(max(n.value, 1), np.int32)
+    _check("h3dit_tile_spans", lib().h3dit_tile_spans(ctypes.byref(shape), first.ctypes.data,
+                                                      rows.ctypes.data, ctypes.byref(n)))
+    return first[:n.value], rows[:n.value]
+
+
+def video_order(shape: Shape) -> np.ndarray:
+    """int32 [n_video]: raster index of each video row in the library's row order."""
+    out = np.zeros(shape.n_video, np.int32)
+    _check("h3dit_video_order", lib().h3dit_video_order(ctypes.byref(shape), out.ctypes.data))
+    return out
 
 
 def select_blocks(mods: np.ndarray, keep: int) -> list:

@@ -107,8 +107,35 @@ inline size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct Dims {
   int N, P, V, Tv, ksel, D, H, d, A, F;
+  TileGeom geom;
   bool block;  // hidden / mlp widths given
 };
+
+// The video tile geometry of a shape; false if the grid or cube fields are inconsistent.
+bool make_geom(const h3dit_shape* s, TileGeom* g) {
+  memset(g, 0, sizeof(*g));
+  g->P = s->n_text + s->n_audio;
+  g->V = s->n_video;
+  const int grid[3] = {s->video_t, s->video_h, s->video_w};
+  const int cube[3] = {s->cube_t, s->cube_h, s->cube_w};
+  bool any = false;
+  for (int i = 0; i < 3; ++i) any = any || grid[i] != 0 || cube[i] != 0;
+  if (!any) return true;
+  for (int i = 0; i < 3; ++i)
+    if (grid[i] < 1 || cube[i] < 1 || grid[i] > (1 << 20)) return false;
+  if ((long long)grid[0] * grid[1] * grid[2] != s->n_video) return false;
+  if (cube[0] * cube[1] * cube[2] != s->tile) return false;
+  g->gt = grid[0];
+  g->gh = grid[1];
+  g->gw = grid[2];
+  g->ct = cube[0];
+  g->ch = cube[1];
+  g->cw = cube[2];
+  g->nt = (grid[0] + cube[0] - 1) / cube[0];
+  g->nh = (grid[1] + cube[1] - 1) / cube[1];
+  g->nw = (grid[2] + cube[2] - 1) / cube[2];
+  return true;
+}
 
 h3dit_status check_attn(const h3dit_shape* s, Dims* o) {
   if (!s) return H3DIT_ERR_ARG;
@@ -117,12 +144,12 @@ h3dit_status check_attn(const h3dit_shape* s, Dims* o) {
   const long long N = (long long)s->n_text + s->n_audio + s->n_video;
   if (N > kMaxRows) return H3DIT_ERR_SHAPE;
   const int P = s->n_text + s->n_audio;
-  if (P % 64) return H3DIT_ERR_SHAPE;
   if (s->head_dim != 64 && s->head_dim != 128) return H3DIT_ERR_SHAPE;
   if (s->heads < 1 || s->heads > 4096) return H3DIT_ERR_SHAPE;
   if (s->attn_width != s->heads * s->head_dim) return H3DIT_ERR_SHAPE;
   if (s->topk < 1) return H3DIT_ERR_ARG;
-  const int Tv = (s->n_video + 63) / 64;
+  if (!make_geom(s, &o->geom)) return H3DIT_ERR_SHAPE;
+  const int Tv = tile_count_of(o->geom);
   if ((size_t)(s->head_dim + 3 * Tv) * 4 > 200 * 1024) return H3DIT_ERR_SHAPE;
   if (!(s->rms_eps >= 0.f)) return H3DIT_ERR_ARG;
   o->N = (int)N;
@@ -232,6 +259,7 @@ h3dit_status run_attention(const h3dit_shape* s, const Dims& m, const Ws& w, voi
   r.n_prefix = m.P;
   r.n_video = m.V;
   r.Tv = m.Tv;
+  r.geom = m.geom;
   r.ksel = m.ksel;
   r.means = at<float>(ws, w.means);
   r.scores = scores ? scores : at<float>(ws, w.scores);
@@ -251,6 +279,7 @@ h3dit_status run_attention(const h3dit_shape* s, const Dims& m, const Ws& w, voi
   a.n_prefix = m.P;
   a.n_video = m.V;
   a.Tv = m.Tv;
+  a.geom = m.geom;
   a.ksel = m.ksel;
   a.idx = r.idx;
   a.gate = use_pool ? gate : nullptr;
@@ -280,7 +309,7 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   const bool use_rope = (s->flags & H3DIT_ROPE) != 0;
   if (use_rope && !rope_ready) {
     StageScope sc(H3DIT_STAGE_SAMPLER, st);
-    H3_TRY(cu(counted(launch_rope_table(rope, N, m.d, s->rope_theta, st), 1)));
+    H3_TRY(cu(counted(launch_rope_table(rope, N, m.d, s->rope_theta, m.geom, st), 1)));
   }
 
   // a1: modulated norm 1
@@ -499,7 +528,7 @@ h3dit_status h3dit_denoise_step(const h3dit_shape* shape, const h3dit_block_weig
       H3_TRY(cu(counted(launch_f32_to_bf16(z_inout, x, n, st), 1)));
       if (shape->flags & H3DIT_ROPE)
         H3_TRY(cu(counted(launch_rope_table(at<float2>(workspace, ws.rope), m.N, m.d,
-                                            shape->rope_theta, st), 1)));
+                                            shape->rope_theta, m.geom, st), 1)));
     }
     for (int i = 0; i < n_blocks; ++i)
       H3_TRY(run_block(shape, m, ws, workspace, &blocks[block_ids[i]], x, true, st));
@@ -558,6 +587,35 @@ h3dit_status h3dit_select_blocks(const float* mods, int n_blocks, int hidden, in
     if (!dropped[b]) kept_ids[n++] = b;
   delete[] score;
   delete[] dropped;
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_tile_spans(const h3dit_shape* shape, int* first_row, int* n_rows,
+                              int* n_tiles_inout) {
+  if (!shape || !n_tiles_inout) return H3DIT_ERR_ARG;
+  Dims m;
+  H3_TRY(check_attn(shape, &m));
+  const int cap = *n_tiles_inout;
+  *n_tiles_inout = m.Tv;
+  if (cap < m.Tv || !first_row || !n_rows) return H3DIT_ERR_ARG;
+  for (int t = 0; t < m.Tv; ++t) tile_span(m.geom, t, &first_row[t], &n_rows[t]);
+  return H3DIT_OK;
+}
+
+h3dit_status h3dit_video_order(const h3dit_shape* shape, int* raster_index) {
+  if (!shape || !raster_index) return H3DIT_ERR_ARG;
+  Dims m;
+  H3_TRY(check_attn(shape, &m));
+  const TileGeom& g = m.geom;
+  for (int i = 0; i < m.V; ++i) {
+    if (g.gt == 0) {
+      raster_index[i] = i;
+    } else {
+      int t, h, w;
+      video_coord(g, i, &t, &h, &w);
+      raster_index[i] = (t * g.gh + h) * g.gw + w;
+    }
+  }
   return H3DIT_OK;
 }
 

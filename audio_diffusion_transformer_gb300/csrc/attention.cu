@@ -6,8 +6,10 @@
 //
 // One CTA owns 128 query rows of one head:
 //   * a prefix unit: 128 text/audio rows, attending to all N rows;
-//   * a video unit: two 64-row video query tiles (2u, 2u+1), attending to all
-//     prefix rows plus the union of the two tiles' selected key tiles.  Each
+//   * a video unit: two video query tiles (2u, 2u+1) of up to 64 rows each (a
+//     64-row slice or a clipped 4x4x4 cube, contiguous in the library's row
+//     order), attending to all prefix rows plus the union of the two tiles'
+//     selected key tiles; a key tile with fewer than 64 rows masks the rest.  Each
 //     key tile carries a 2-bit mask saying which of the two query tiles chose
 //     it; scores of the other half are masked to -inf, so every row sees
 //     exactly its own key set.
@@ -68,6 +70,7 @@ struct Layout {
 struct Params {
   int N, H, n_prefix, n_video, Tv, ksel;
   int n_pre_units;
+  TileGeom geom;
   const int* idx;
   const __nv_bfloat16* gate;
   const float* pooled;
@@ -135,12 +138,15 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int ta = 2 * vu, tb = 2 * vu + 1;  // video query tiles of a video unit
 
   if (threadIdx.x == 0) {
-    // key-tile list: entry = first_row << 2 | mask (bit 0: rows 0-63 use it, bit 1: rows 64-127)
+    // key-tile list: entry = first_row << 9 | rows << 2 | mask (rows: 1..64 keys from
+    // first_row; mask bit 0: query rows 0-63 use it, bit 1: query rows 64-127)
     int nt = 0;
     if (is_prefix) {
-      for (int r0 = 0; r0 < p.N && nt < MAX_TILES; r0 += 64) tiles[nt++] = (r0 << 2) | 3;
+      for (int r0 = 0; r0 < p.N && nt < MAX_TILES; r0 += 64)
+        tiles[nt++] = (r0 << 9) | (min(64, p.N - r0) << 2) | 3;
     } else {
-      for (int r0 = 0; r0 < p.n_prefix && nt < MAX_TILES; r0 += 64) tiles[nt++] = (r0 << 2) | 3;
+      for (int r0 = 0; r0 < p.n_prefix && nt < MAX_TILES; r0 += 64)
+        tiles[nt++] = (r0 << 9) | (min(64, p.n_prefix - r0) << 2) | 3;
       const int* ia = p.idx + ((size_t)h * p.Tv + ta) * p.ksel;
       const int* ib = p.idx + ((size_t)h * p.Tv + tb) * p.ksel;
       const int na = p.ksel, nb = tb < p.Tv ? p.ksel : 0;
@@ -159,7 +165,9 @@ __global__ void __launch_bounds__(THREADS, 2)
           m = 3;
         }
         t = min(max(t, 0), p.Tv - 1);  // indices come from the router; clamp defensively
-        tiles[nt++] = ((p.n_prefix + 64 * t) << 2) | m;
+        int f, c;
+        tile_span(p.geom, t, &f, &c);
+        tiles[nt++] = (f << 9) | (c << 2) | m;
       }
     }
     *n_steps_s = nt;
@@ -195,8 +203,10 @@ __global__ void __launch_bounds__(THREADS, 2)
         qrow0 = unit * 128;
         qrow1 = unit * 128 + 64;
       } else {
-        qrow0 = p.n_prefix + 64 * ta;
-        qrow1 = p.n_prefix + 64 * tb;
+        int c;
+        tile_span(p.geom, ta, &qrow0, &c);
+        qrow1 = qrow0;  // an odd tile count leaves the second half without a tile
+        if (tb < p.Tv) tile_span(p.geom, tb, &qrow1, &c);
       }
       mbar_arrive_expect_tx(q_full, L::Q_BYTES);
 #pragma unroll
@@ -209,7 +219,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         const int st = t & 1;
         if (!mbar_wait(&s_done[st], ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         uint8_t* sK = smem + L::K_OFF0 + st * L::KV_BYTES;
-        const int r0 = tiles[t] >> 2;
+        const int r0 = tiles[t] >> 9;
         mbar_arrive_expect_tx(&k_full[st], L::KV_BYTES);
 #pragma unroll
         for (int c = 0; c < HD / 64; ++c)
@@ -223,7 +233,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         const int st = t & 1;
         if (!mbar_wait(&pv_done[st], ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         uint8_t* sV = smem + L::V_OFF0 + st * L::KV_BYTES;
-        const int r0 = tiles[t] >> 2;
+        const int r0 = tiles[t] >> 9;
         mbar_arrive_expect_tx(&v_full[st], L::KV_BYTES);
 #pragma unroll
         for (int c = 0; c < HD / 64; ++c)
@@ -295,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       }
       tc_fence_after();
       const int e = tiles[t];
-      const int nv = ((e >> half) & 1) ? min(64, p.N - (e >> 2)) : 0;
+      const int nv = ((e >> half) & 1) ? ((e >> 2) & 127) : 0;
       const uint32_t s_addr = t_lane + L::S_COL + sb * 64;
       float sv[64];
       tmem_ld64(s_addr, sv);
@@ -360,8 +370,10 @@ __global__ void __launch_bounds__(THREADS, 2)
         store = grow < p.n_prefix;
       } else {
         tile = half ? tb : ta;
-        grow = p.n_prefix + 64 * tile + (row & 63);
-        store = tile < p.Tv && grow < p.N;
+        int f = 0, c = 0;
+        if (tile < p.Tv) tile_span(p.geom, tile, &f, &c);
+        grow = f + (row & 63);
+        store = (row & 63) < c;
       }
       const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
       const int A = p.H * HD;
@@ -428,6 +440,7 @@ cudaError_t launch_hd(const AttnArgs& a, cudaStream_t stream) {
   p.Tv = a.Tv;
   p.ksel = a.ksel;
   p.n_pre_units = (a.n_prefix + 127) / 128;
+  p.geom = a.geom;
   p.idx = a.idx;
   p.gate = a.gate;
   p.pooled = a.pooled;

@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include "h3dit.h"
+#include "tiles.cuh"
 
 namespace h3 {
 
@@ -44,6 +45,7 @@ cudaError_t launch_gemm(int epi, const GemmArgs& args, cudaStream_t stream);
 struct AttnArgs {
   const __nv_bfloat16 *q, *k, *v;  // [H, N, d]
   int N, H, d, n_prefix, n_video, Tv, ksel;
+  TileGeom geom;              // rows of each video tile
   const int* idx;             // [H, Tv, ksel]
   const __nv_bfloat16* gate;  // [N, A] or null
   const float* pooled;        // [H, Tv, d] or null
@@ -57,6 +59,7 @@ cudaError_t launch_attention(const AttnArgs& args, cudaStream_t stream);
 struct RouterArgs {
   const __nv_bfloat16 *q, *k, *v;  // [H, N, d]
   int N, H, d, n_prefix, n_video, Tv, ksel;
+  TileGeom geom;  // rows of each video tile
   float* means;   // [3, H, Tv, d]
   float* scores;  // [H, Tv, Tv]
   int* idx;       // [H, Tv, ksel]
@@ -70,7 +73,10 @@ cudaError_t launch_router(const RouterArgs& args, cudaStream_t stream);
 cudaError_t launch_rms_modulate(const __nv_bfloat16* x, const float* shift, const float* scale,
                                 const float* shift_p, const float* scale_p, int n_prefix,
                                 __nv_bfloat16* h, int rows, int D, float eps, cudaStream_t s);
-cudaError_t launch_rope_table(float2* cs, int rows, int d, float theta, cudaStream_t s);
+// (cos, sin) per row and rotary pair: 1-D over the packed index, or 3-D (t, h, w) when
+// the geometry has a video grid
+cudaError_t launch_rope_table(float2* cs, int rows, int d, float theta, const TileGeom& g,
+                              cudaStream_t s);
 cudaError_t launch_f32_to_bf16(const float* z, __nv_bfloat16* x, size_t n, cudaStream_t s);
 // elements [0, n_pre) follow the prefix step dt_p (coef_p), the rest dt (coef)
 cudaError_t launch_euler_fresh(const __nv_bfloat16* x, float* z, float* v_slot, float dt,

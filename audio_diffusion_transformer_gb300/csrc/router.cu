@@ -6,8 +6,9 @@
 // the lower tile; a row never keeps more than k tiles).
 //
 // Kernel 1 (tile_means): one CTA per (video tile, head, tensor of q/k/v); four
-//   warps sum 16-row blocks of the tile's valid rows in row order, the block
-//   sums are added in order and divided by the valid-row count.  Reads each
+//   warps sum 16-row blocks of the tile's rows (a contiguous run of at most 64
+//   rows: a 64-row slice, or a clipped 4x4x4 cube) in row order, the block sums
+//   are added in order and divided by the tile's row count.  Reads each
 //   video row of q, k, v once (HBM-bound).
 // Kernel 2 (route): one CTA per (head h, 8 query tiles), one warp per query
 //   tile; the head's key / value tile means pass through shared memory once
@@ -39,14 +40,14 @@ template <int D>
 __global__ void __launch_bounds__(128)
     tile_means_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                       const __nv_bfloat16* __restrict__ v, float* __restrict__ means, int N, int H,
-                      int n_prefix, int n_video, int Tv) {
+                      const TileGeom geom, int Tv) {
   constexpr int CPL = D / 32;  // columns per lane: 4 (d = 128) or 2 (d = 64)
   __shared__ float part[4][D];
   const int t = blockIdx.x, h = blockIdx.y, which = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const __nv_bfloat16* X = which == 0 ? q : (which == 1 ? k : v);
-  const int r0 = n_prefix + 64 * t;
-  const int nv = min(64, n_video - 64 * t);
+  int r0, nv;
+  tile_span(geom, t, &r0, &nv);
   const int ra = warp * 16, rb = min(nv, ra + 16);
   float acc[CPL];
 #pragma unroll
@@ -242,11 +243,11 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   dim3 g1(a.Tv, a.H, 3);
   if (a.d == 128)
-    tile_means_kernel<128><<<g1, 128, 0, stream>>>(a.q, a.k, a.v, a.means, a.N, a.H, a.n_prefix,
-                                                   a.n_video, a.Tv);
+    tile_means_kernel<128><<<g1, 128, 0, stream>>>(a.q, a.k, a.v, a.means, a.N, a.H, a.geom,
+                                                   a.Tv);
   else
-    tile_means_kernel<64><<<g1, 128, 0, stream>>>(a.q, a.k, a.v, a.means, a.N, a.H, a.n_prefix,
-                                                  a.n_video, a.Tv);
+    tile_means_kernel<64><<<g1, 128, 0, stream>>>(a.q, a.k, a.v, a.means, a.N, a.H, a.geom,
+                                                  a.Tv);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t shm = (size_t)(KCHUNK * (a.d + 1) + TILES_PER_CTA * (a.d + a.Tv)) * 4;

@@ -5,8 +5,11 @@
 //    one 128-thread CTA per row, 16-byte loads kept in registers between the
 //    reduction and the write (TensorFold #949 "What it adds": modulated norm;
 //    h3.c README fused gated-AdaLN paragraph: a per-row RMS).
-//  * rope_table: (cos, sin) of p * theta^(-2c/d) per packed row p and pair c,
-//    evaluated in double precision and stored fp32 for the projection epilogue.
+//  * rope_table: (cos, sin) per packed row and rotary pair, evaluated in double
+//    precision and stored fp32 for the projection epilogue: p * theta^(-2c/d)
+//    over the packed index p, or with a video grid a 3-D rotary whose pairs are
+//    split into time, height and width groups, each with its own frequency
+//    ladder, at the row's latent (t, h, w) (text and audio rows: (p, p, p)).
 //  * f32_to_bf16: the sampler's latents -> the bf16 residual stream.
 //  * euler_fresh / euler_extrap: v = fp32(x_L), ring store, z += dt * v; or the
 //    linear extrapolation of the last two fresh velocities (h3.c README sampler
@@ -83,13 +86,32 @@ __global__ void __launch_bounds__(ROW_THREADS)
   }
 }
 
-__global__ void rope_table_kernel(float2* cs, int rows, int half, int d, double log_theta) {
+__global__ void rope_table_kernel(float2* cs, int rows, int half, int d, double log_theta,
+                                  const TileGeom g) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (size_t)rows * half) return;
   const int p = (int)(i / half), c = (int)(i % half);
-  const double inv_freq = exp(-2.0 * (double)c / (double)d * log_theta);
+  double pos, expo;
+  if (g.gt == 0) {  // 1-D: pair c turns by p * theta^(-2c/d)
+    pos = (double)p;
+    expo = 2.0 * (double)c / (double)d;
+  } else {  // 3-D: pairs [0, mt) time, [mt, mt + ms) height, the rest width
+    const int ms = half / 3, mt = half - 2 * ms;
+    int tt = p, hh = p, ww = p;  // text and audio rows: the packed index on every axis
+    if (p >= g.P) video_coord(g, p - g.P, &tt, &hh, &ww);
+    int axis_pos, j, m;
+    if (c < mt) {
+      axis_pos = tt, j = c, m = mt;
+    } else if (c < mt + ms) {
+      axis_pos = hh, j = c - mt, m = ms;
+    } else {
+      axis_pos = ww, j = c - mt - ms, m = ms;
+    }
+    pos = (double)axis_pos;
+    expo = (double)j / (double)m;
+  }
   double sn, cn;
-  sincos((double)p * inv_freq, &sn, &cn);
+  sincos(pos * exp(-expo * log_theta), &sn, &cn);
   cs[i] = make_float2((float)cn, (float)sn);
 }
 
@@ -163,11 +185,12 @@ cudaError_t launch_rms_modulate(const __nv_bfloat16* x, const float* shift, cons
   return cudaGetLastError();
 }
 
-cudaError_t launch_rope_table(float2* cs, int rows, int d, float theta, cudaStream_t s) {
+cudaError_t launch_rope_table(float2* cs, int rows, int d, float theta, const TileGeom& g,
+                              cudaStream_t s) {
   const int half = d / 2;
   const size_t n = (size_t)rows * half;
   rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(cs, rows, half, d,
-                                                                 log((double)theta));
+                                                                 log((double)theta), g);
   return cudaGetLastError();
 }
 

@@ -59,14 +59,22 @@ def fc1_width(s):
     return 2 * s.mlp_width if s.mlp == "swiglu" else s.mlp_width
 
 
+def block_weight_bytes(s):
+    D, A, F = s.hidden, s.attn_width, s.mlp_width
+    return 2 * (D * 4 * A + A * D + D * fc1_width(s) + F * D)
+
+
 def block_flops(s):
     """Algorithmic flops of one block (2 per MAC): the four projections plus
     the attention the method performs (prefix rows over all N keys, video rows
-    over the prefix and k selected tiles of 64 rows)."""
+    over the prefix and k selected tiles of V / Tv rows on average: 64-row slices,
+    or clipped 4x4x4 cubes)."""
     N, D, A, F = s.n_rows, s.hidden, s.attn_width, s.mlp_width
     gemm = 2.0 * N * (D * 4 * A + A * D + D * fc1_width(s) + F * D)
-    k = min(s.topk, s.n_video_tiles)
-    attn = 4.0 * s.head_dim * s.heads * (s.n_prefix * N + s.n_video * (s.n_prefix + k * 64))
+    tv = s.n_video_tiles
+    k = min(s.topk, tv)
+    attn = 4.0 * s.head_dim * s.heads * (s.n_prefix * N + s.n_video * (s.n_prefix
+                                                                       + k * s.n_video / tv))
     return gemm, attn
 
 
@@ -408,8 +416,14 @@ def run_ours(args, rank, world, local_rank):
                    "params_b": n_blocks * (D * 4 * shape.attn_width + shape.attn_width * D
                                            + D * fc1_width(shape) + shape.mlp_width * D) / 1e9,
                    "topk": shape.topk, "tile": shape.tile,
+                   "video_tiles": (f"{shape.n_video_tiles} cubes "
+                                   f"{'x'.join(map(str, shape.cube))} of a "
+                                   f"{'x'.join(map(str, shape.video_grid))} grid, 3-D rotary"
+                                   if shape.video_grid else
+                                   f"{shape.n_video_tiles} slices of 64 rows"),
                    "dt": dt, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (each block reads its own 682 MB of weights)"},
+                   "l2": f"inputs larger than L2 (each block reads its own "
+                         f"{block_weight_bytes(shape) / 1e6:.0f} MB of weights)"},
         "s_per_forward": ms_max / K / 1e3 * (50 / n_blocks),
         "tc_frac_of_peak": achieved_total / peak_tc,
         "achieved_tflops": achieved_total,

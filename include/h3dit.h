@@ -50,7 +50,8 @@ typedef enum {
 
 /* Flags of h3dit_shape.flags */
 #define H3DIT_QK_NORM 0x1u   /* per-head RMS norm of q and k with learned weights */
-#define H3DIT_ROPE    0x2u   /* rotary on q and k over the packed row index        */
+#define H3DIT_ROPE    0x2u   /* rotary on q and k: over the packed row index, or   */
+                             /* 3-D (t, h, w) when a video grid is given below      */
 #define H3DIT_POOLED  0x4u   /* pooled branch + gate mix for video rows            */
 #define H3DIT_SWIGLU  0x8u   /* MLP u = silu(h W_gate^T + b_g) * (h W_up^T + b_u)   */
                              /* (else u = gelu(h W1^T + b1)); see w1 below          */
@@ -67,6 +68,21 @@ typedef struct {
   float rms_eps;                /* epsilon of every RMS norm (e.g. 1e-6)          */
   float rope_theta;             /* rotary base (e.g. 10000)                       */
   unsigned flags;               /* H3DIT_QK_NORM | H3DIT_ROPE | H3DIT_POOLED      */
+  /* Video layout.  All zero: video rows form contiguous 64-row tiles in packed
+   * order (the last may be partial).  Otherwise the video rows are the latent grid
+   * video_t x video_h x video_w (n_video = t * h * w) cut into cubes of
+   * cube_t x cube_h x cube_w = tile tokens, edge cubes clipped (TensorFold #949
+   * "Receipts": 280 tiles from 4 x 4 x 4 cubes at 864 x 480 x 124), and every
+   * buffer holds them in CUBE ORDER: cubes in raster (cube_t, cube_h, cube_w)
+   * order, each cube's tokens in raster (t, h, w) order, so every tile is a
+   * contiguous run of rows (h3dit_video_order gives the permutation).  With
+   * H3DIT_ROPE the rotary is then 3-D: rotary pairs c < d/2 split into
+   * m_t = d/2 - 2 m_s time pairs, then m_s height and m_s width pairs
+   * (m_s = floor(d/6)); pair c of axis a with local index j turns by
+   * pos_a * theta^(-j / m_a), pos = (t, h, w) for video rows and (p, p, p) for
+   * a text or audio row at packed index p. */
+  int video_t, video_h, video_w;
+  int cube_t, cube_h, cube_w;
 } h3dit_shape;
 
 /* One block's parameters (device pointers, bf16 unless stated).
@@ -217,6 +233,25 @@ h3dit_status h3dit_denoise_step(const h3dit_shape* shape, const h3dit_block_weig
  */
 h3dit_status h3dit_select_blocks(const float* mods, int n_blocks, int hidden, int keep,
                                  int* kept_ids);
+
+/*
+ * h3dit_tile_spans -- the routing tiles of a shape (host only, no GPU).
+ * first_row[t], n_rows[t] (HOST int32 [number of video tiles]): tile t is the
+ * packed rows first_row[t] .. first_row[t] + n_rows[t] - 1.  n_tiles_inout: in,
+ * the capacity of both arrays; out, the number of video tiles.
+ */
+h3dit_status h3dit_tile_spans(const h3dit_shape* shape, int* first_row, int* n_rows,
+                              int* n_tiles_inout);
+
+/*
+ * h3dit_video_order -- the library's video row order (host only, no GPU).
+ * raster_index (HOST int32 [n_video]): for the i-th video row as the library
+ * stores it, the raster index (t * video_h + h) * video_w + w of its latent
+ * token; the identity without a video grid.  A caller holding video rows in
+ * raster order gathers row raster_index[i] into row i before the call and
+ * scatters back after it.
+ */
+h3dit_status h3dit_video_order(const h3dit_shape* shape, int* raster_index);
 
 /*
  * h3dit_linear -- plain bf16 GEMM on the tensor cores: y = bf16(a w^T [+ b]).

@@ -28,8 +28,8 @@ from scipy.special import erf as _erf
 
 __all__ = [
     "bf16", "f32", "rms_modulate", "linear", "gelu_erf", "silu", "swiglu_split", "mlp_inner",
-    "head_rms_norm", "rope",
-    "video_tiles", "tile_means", "tile_scores", "topk_select", "topk_gap",
+    "head_rms_norm", "rope", "rope_axis_split", "rope_3d", "rope_coords",
+    "video_tiles", "cube_tiles", "tile_sets", "shape_tiles", "tile_means", "tile_scores", "topk_select", "topk_gap",
     "topk_set_valid", "attend", "routed_attention", "pooled_branch", "gate_mix",
     "attention_layer", "qkv_heads", "block_forward", "block_forward_rows", "euler_update",
     "extrapolate",
@@ -158,25 +158,72 @@ def head_rms_norm(x, w, eps: float = 1e-6) -> np.ndarray:
     return x * inv * np.asarray(w, np.float64)
 
 
+def _rotate_half(x, ang) -> np.ndarray:
+    """Turn pairs (c, c + d/2) of the last axis by ang[..., row, c]."""
+    x = np.asarray(x, np.float64)
+    half = x.shape[-1] // 2
+    cos, sin = np.cos(ang), np.sin(ang)
+    x0, x1 = x[..., :half], x[..., half:]
+    out = np.empty_like(x)
+    out[..., :half] = x0 * cos - x1 * sin
+    out[..., half:] = x1 * cos + x0 * sin
+    return out
+
+
 def rope(x, positions, theta: float = 10000.0) -> np.ndarray:
     """Rotary embedding, rotate-half pairing, over the last axis.
 
     Pairs (c, c + d/2) for c < d/2 are rotated by angle p * theta^(-2c/d),
     p = the packed row index.  Reading: the pages name "q/k norm and rotary"
     but give no axes or base; a 1-D rotary over the packed row index with
-    theta = 10,000 is taken.
+    theta = 10,000 is taken when no video grid is given.
     """
-    x = np.asarray(x, np.float64)
-    d = x.shape[-1]
-    half = d // 2
-    c = np.arange(half, dtype=np.float64)
+    d = np.shape(x)[-1]
+    c = np.arange(d // 2, dtype=np.float64)
     inv_freq = theta ** (-2.0 * c / d)
     ang = np.asarray(positions, np.float64)[:, None] * inv_freq[None, :]  # [N, half]
-    cos, sin = np.cos(ang), np.sin(ang)
-    x0, x1 = x[..., :half], x[..., half:]
-    out = np.empty_like(x)
-    out[..., :half] = x0 * cos - x1 * sin
-    out[..., half:] = x1 * cos + x0 * sin
+    return _rotate_half(x, ang)
+
+
+def rope_axis_split(d: int):
+    """Rotary pairs per axis (time, height, width) for head width d.
+
+    Reading: the pages speak of spatial and temporal rotary coordinates (the h3.c
+    README halves the spatial ones at 256 square) without the split; the common
+    video-DiT split gives height and width floor(d/6) pairs each and time the rest.
+    """
+    half = d // 2
+    ms = half // 3
+    return half - 2 * ms, ms, ms
+
+
+def rope_3d(x, coords, theta: float = 10000.0) -> np.ndarray:
+    """3-D rotary: pair c of axis a (local index j of m_a pairs) turns by
+    coords[row, a] * theta^(-j / m_a); axes in the order time, height, width over
+    consecutive pair ranges."""
+    d = np.shape(x)[-1]
+    coords = np.asarray(coords, np.float64)
+    ang = np.empty((coords.shape[0], d // 2))
+    c0 = 0
+    for a, m in enumerate(rope_axis_split(d)):
+        j = np.arange(m, dtype=np.float64)
+        ang[:, c0:c0 + m] = coords[:, a:a + 1] * theta ** (-j / m)[None, :]
+        c0 += m
+    return _rotate_half(x, ang)
+
+
+def rope_coords(n_prefix: int, n_video: int, grid) -> np.ndarray:
+    """Per packed row (t, h, w) for the 3-D rotary: text/audio row p -> (p, p, p)
+    (reading: the pages give the prefix rows no grid), video row in raster order
+    v = (t * H + h) * W + w -> (t, h, w)."""
+    T, Hg, Wg = grid
+    out = np.empty((n_prefix + n_video, 3), np.int64)
+    p = np.arange(n_prefix)
+    out[:n_prefix] = p[:, None]
+    v = np.arange(n_video)
+    out[n_prefix:, 0] = v // (Hg * Wg)
+    out[n_prefix:, 1] = (v // Wg) % Hg
+    out[n_prefix:, 2] = v % Wg
     return out
 
 
@@ -198,13 +245,48 @@ def video_tiles(n_prefix: int, n_video: int, tile: int = 64):
             for t in range((n_video + tile - 1) // tile)]
 
 
-def tile_means(X, n_prefix: int, n_video: int, tile: int = 64) -> np.ndarray:
-    """Mean over the valid rows of each video tile: [H, N, d] -> [H, Tv, d] (float64)."""
+def cube_tiles(n_prefix: int, grid, cube=(4, 4, 4)) -> list:
+    """Packed row indices of each video tile when the video rows are the latent grid
+    T x H x W in raster order, cut into ct x ch x cw cubes (edge cubes clipped).
+
+    TensorFold #949 "Receipts": 4 x 4 x 4 cubes give 280 video tiles at 864 x 480 x 124
+    (a 37 x 15 x 27 grid).  Reading: cubes numbered in raster (cube t, h, w) order;
+    the rows of a cube listed in raster (t, h, w) order.
+    """
+    T, Hg, Wg = grid
+    ct, ch, cw = cube
+    tiles = []
+    for a in range(0, T, ct):
+        for b in range(0, Hg, ch):
+            for c in range(0, Wg, cw):
+                rows = [n_prefix + (t * Hg + h) * Wg + w
+                        for t in range(a, min(T, a + ct))
+                        for h in range(b, min(Hg, b + ch))
+                        for w in range(c, min(Wg, c + cw))]
+                tiles.append(np.array(rows, dtype=np.int64))
+    return tiles
+
+
+def tile_sets(n_prefix: int, n_video: int, tile: int = 64, grid=None, cube=(4, 4, 4)) -> list:
+    """Packed row indices of each video tile: contiguous slices, or cubes of ``grid``."""
+    if grid is None:
+        return [np.arange(r0, r0 + nv) for r0, nv in video_tiles(n_prefix, n_video, tile)]
+    return cube_tiles(n_prefix, grid, cube)
+
+
+def shape_tiles(shape) -> list:
+    return tile_sets(shape.n_prefix, shape.n_video, shape.tile,
+                     getattr(shape, "video_grid", None), getattr(shape, "cube", (4, 4, 4)))
+
+
+def tile_means(X, n_prefix: int, n_video: int, tile: int = 64, sets=None) -> np.ndarray:
+    """Mean over the rows of each video tile: [H, N, d] -> [H, Tv, d] (float64).
+    ``sets``: the tiles' row indices (default: contiguous 64-row slices)."""
     X = np.asarray(X, np.float64)
-    tiles = video_tiles(n_prefix, n_video, tile)
-    out = np.empty((X.shape[0], len(tiles), X.shape[2]))
-    for t, (r0, nv) in enumerate(tiles):
-        out[:, t, :] = X[:, r0:r0 + nv, :].sum(axis=1) / nv
+    sets = tile_sets(n_prefix, n_video, tile) if sets is None else sets
+    out = np.empty((X.shape[0], len(sets), X.shape[2]))
+    for t, rows in enumerate(sets):
+        out[:, t, :] = X[:, rows, :].sum(axis=1) / len(rows)
     return out
 
 
@@ -292,7 +374,7 @@ def attend(q, k, v, scale: float, p_bf16: bool = False) -> np.ndarray:
 
 
 def routed_attention(Q, K, V, n_prefix: int, n_video: int, idx, tile: int = 64,
-                     p_bf16: bool = False, tiles=None) -> np.ndarray:
+                     p_bf16: bool = False, tiles=None, sets=None) -> np.ndarray:
     """Tile-routed attention, [H, N, d] each -> O [H, N, d] (float64).
 
     TensorFold #949 "What it adds" (h3_attention.metal: tile-routed attention
@@ -303,7 +385,8 @@ def routed_attention(Q, K, V, n_prefix: int, n_video: int, idx, tile: int = 64,
     * a video query row in tile i attends to every prefix row plus the valid
       rows of the tiles idx[h, i].
     Scale 1/sqrt(d).  ``tiles`` optionally restricts the work to a list of
-    (h, i) video query tiles (rows elsewhere are left zero).
+    (h, i) video query tiles (rows elsewhere are left zero); ``sets`` are the
+    tiles' row indices (default: contiguous 64-row slices).
     """
     Q = np.asarray(Q, np.float64)
     K = np.asarray(K, np.float64)
@@ -311,7 +394,7 @@ def routed_attention(Q, K, V, n_prefix: int, n_video: int, idx, tile: int = 64,
     H, N, d = Q.shape
     scale = 1.0 / math.sqrt(d)
     O = np.zeros_like(Q)
-    vt = video_tiles(n_prefix, n_video, tile)
+    vt = tile_sets(n_prefix, n_video, tile) if sets is None else sets
     if tiles is None:
         for h in range(H):
             if n_prefix:
@@ -319,10 +402,9 @@ def routed_attention(Q, K, V, n_prefix: int, n_video: int, idx, tile: int = 64,
         tiles = [(h, i) for h in range(H) for i in range(len(vt))]
     pre = np.arange(n_prefix)
     for h, i in tiles:
-        r0, nv = vt[i]
-        keys = [pre] + [np.arange(vt[j][0], vt[j][0] + vt[j][1]) for j in idx[h, i]]
-        kr = np.concatenate(keys)
-        O[h, r0:r0 + nv] = attend(Q[h, r0:r0 + nv], K[h, kr], V[h, kr], scale, p_bf16)
+        qr = vt[i]
+        kr = np.concatenate([pre] + [vt[j] for j in idx[h, i]])
+        O[h, qr] = attend(Q[h, qr], K[h, kr], V[h, kr], scale, p_bf16)
     return O
 
 
@@ -341,7 +423,7 @@ def pooled_branch(S, mv, head_dim: int) -> np.ndarray:
     return w @ np.asarray(mv, np.float64)
 
 
-def gate_mix(O, G, pooled, n_prefix: int, n_video: int, tile: int = 64) -> np.ndarray:
+def gate_mix(O, G, pooled, n_prefix: int, n_video: int, tile: int = 64, sets=None) -> np.ndarray:
     """o[r, h*d:(h+1)*d] = O[h, r] + G[r, h*d:(h+1)*d] * pooled[h, tile(r)] for video rows.
 
     TensorFold #949 "What it adds" ("the routing gate", h3_gate_mix).
@@ -354,15 +436,15 @@ def gate_mix(O, G, pooled, n_prefix: int, n_video: int, tile: int = 64) -> np.nd
     if pooled is None or G is None or n_video == 0:
         return out
     G = np.asarray(G, np.float64)
-    t_of = (np.arange(n_video) // tile)
-    pb = np.asarray(pooled, np.float64)[:, t_of, :]          # [H, V, d]
-    pb = pb.transpose(1, 0, 2).reshape(n_video, H * d)
-    out[n_prefix:] += G[n_prefix:] * pb
+    sets = tile_sets(n_prefix, n_video, tile) if sets is None else sets
+    pb = np.asarray(pooled, np.float64)
+    for i, rows in enumerate(sets):
+        out[rows] += G[rows] * pb[:, i, :].reshape(H * d)[None, :]
     return out
 
 
 def attention_layer(Q, K, V, G, n_prefix: int, n_video: int, topk: int, tile: int = 64,
-                    pooled: bool = True, p_bf16: bool = False) -> dict:
+                    pooled: bool = True, p_bf16: bool = False, sets=None) -> dict:
     """Router + routed/dense attention + pooled branch + gate mix.
 
     Inputs are the bf16 values of Q, K, V [H, N, d] and G [N, H*d] (or None).
@@ -370,15 +452,16 @@ def attention_layer(Q, K, V, G, n_prefix: int, n_video: int, topk: int, tile: in
     """
     Q = np.asarray(Q, np.float64)
     d = Q.shape[2]
-    mq = tile_means(Q, n_prefix, n_video, tile)
-    mk = tile_means(K, n_prefix, n_video, tile)
-    mv = tile_means(V, n_prefix, n_video, tile)
+    sets = tile_sets(n_prefix, n_video, tile) if sets is None else sets
+    mq = tile_means(Q, n_prefix, n_video, tile, sets)
+    mk = tile_means(K, n_prefix, n_video, tile, sets)
+    mv = tile_means(V, n_prefix, n_video, tile, sets)
     S = tile_scores(mq, mk)
     idx = topk_select(S, topk)
     gap = topk_gap(S, topk)
-    O = routed_attention(Q, K, V, n_prefix, n_video, idx, tile, p_bf16)
+    O = routed_attention(Q, K, V, n_prefix, n_video, idx, tile, p_bf16, sets=sets)
     pb = pooled_branch(S, mv, d) if pooled else None
-    mixed = gate_mix(O, G, pb, n_prefix, n_video, tile)
+    mixed = gate_mix(O, G, pb, n_prefix, n_video, tile, sets)
     return {"mq": mq, "mk": mk, "mv": mv, "scores": S, "idx": idx, "gap": gap,
             "O": O, "pooled": pb, "o_f64": mixed, "o": bf16(mixed)}
 
@@ -388,11 +471,12 @@ def attention_layer(Q, K, V, G, n_prefix: int, n_video: int, topk: int, tile: in
 # ---------------------------------------------------------------------------
 
 def qkv_heads(qkvg, heads: int, head_dim: int, qnorm_w=None, knorm_w=None,
-              eps: float = 1e-6, theta: float = 10000.0, use_rope: bool = True):
+              eps: float = 1e-6, theta: float = 10000.0, use_rope: bool = True, coords=None):
     """Split [N, 4A] projection rows into head-major Q, K, V [H, N, d] and G [N, A].
 
     q and k get the per-head RMS norm (learned weight) and the rotary, then are
-    rounded to bf16; v and g are the projection's bf16 values.  Column order of
+    rounded to bf16; v and g are the projection's bf16 values.  ``coords`` [N, 3]
+    selects the 3-D rotary.  Column order of
     the projection: [Q | K | V | G], each A = H*d wide, head-major inside.
     TensorFold #949 "What it adds" (block.zig "q/k/v and the routing gate,
     head layout"); h3.c README Q/K RMS + RoPE paragraph.
@@ -408,7 +492,10 @@ def qkv_heads(qkvg, heads: int, head_dim: int, qnorm_w=None, knorm_w=None,
         q = head_rms_norm(q, qnorm_w, eps)
     if knorm_w is not None:
         k = head_rms_norm(k, knorm_w, eps)
-    if use_rope:
+    if use_rope and coords is not None:  # 3-D rotary over (t, h, w)
+        q = rope_3d(q, coords, theta)
+        k = rope_3d(k, coords, theta)
+    elif use_rope:
         q = rope(q, pos, theta)
         k = rope(k, pos, theta)
     return bf16(q), bf16(k), v.copy(), qkvg[:, 3 * A:4 * A].copy()
@@ -442,6 +529,11 @@ def gate_rows(mod, mod_prefix, n_prefix: int, k: int, rows) -> np.ndarray:
     return np.where(pre, np.asarray(mod_prefix, np.float64)[k], mod[k])
 
 
+def _coords(shape):
+    grid = getattr(shape, "video_grid", None)
+    return None if grid is None else rope_coords(shape.n_prefix, shape.n_video, grid)
+
+
 def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
     """One DiT block on the packed rows x (bf16 values, [N, D]).
 
@@ -464,9 +556,9 @@ def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
     q, k, v, g = qkv_heads(qkvg, s.heads, s.head_dim,
                            wts.get("qnorm_w") if s.qk_norm else None,
                            wts.get("knorm_w") if s.qk_norm else None,
-                           s.rms_eps, s.rope_theta, s.rope)
+                           s.rms_eps, s.rope_theta, s.rope, _coords(s))
     att = attention_layer(q, k, v, g if s.pooled else None, s.n_prefix, s.n_video,
-                          s.topk, s.tile, s.pooled, p_bf16)
+                          s.topk, s.tile, s.pooled, p_bf16, shape_tiles(s))
     x1 = bf16(x + gate_rows(mod, modp, P, 2, allr) * linear(att["o"], wts["w_o"], wts["b_o"]))
     h2 = modulate_rows(x1, mod, modp, P, 3, 4, s.rms_eps)
     u = mlp_inner(h2, wts, getattr(s, "mlp", "gelu"))
@@ -496,34 +588,34 @@ def block_forward_rows(x, wts: dict, shape, rows) -> dict:
     q, k, v, g = qkv_heads(qkvg, s.heads, s.head_dim,
                            wts.get("qnorm_w") if s.qk_norm else None,
                            wts.get("knorm_w") if s.qk_norm else None,
-                           s.rms_eps, s.rope_theta, s.rope)
+                           s.rms_eps, s.rope_theta, s.rope, _coords(s))
     del qkvg
     P, Vn, tile, d = s.n_prefix, s.n_video, s.tile, s.head_dim
-    mq = tile_means(q, P, Vn, tile)
-    mk = tile_means(k, P, Vn, tile)
-    mv = tile_means(v, P, Vn, tile)
+    vt = shape_tiles(s)
+    tile_of = np.empty(s.n_rows, np.int64)
+    for i, tr in enumerate(vt):
+        tile_of[tr] = i
+    mq = tile_means(q, P, Vn, tile, vt)
+    mk = tile_means(k, P, Vn, tile, vt)
+    mv = tile_means(v, P, Vn, tile, vt)
     S = tile_scores(mq, mk)
     idx = topk_select(S, s.topk)
     H = s.heads
     O = np.zeros((H, len(rows), d))
     scale = 1.0 / math.sqrt(d)
-    vt = video_tiles(P, Vn, tile)
     for n, r in enumerate(rows):
         for hh in range(H):
             if r < P:
                 keys = np.arange(s.n_rows)
             else:
-                i = (r - P) // tile
-                keys = np.concatenate([np.arange(P)] + [np.arange(vt[j][0], vt[j][0] + vt[j][1])
-                                                        for j in idx[hh, i]])
+                keys = np.concatenate([np.arange(P)] + [vt[j] for j in idx[hh, tile_of[r]]])
             O[hh, n] = attend(q[hh, [r]], k[hh, keys], v[hh, keys], scale)[0]
     o = O.transpose(1, 0, 2).reshape(len(rows), H * d)
     if s.pooled:
         pb = pooled_branch(S, mv, d)
         for n, r in enumerate(rows):
             if r >= P:
-                i = (r - P) // tile
-                o[n] += g[r] * pb[:, i, :].reshape(H * d)
+                o[n] += g[r] * pb[:, tile_of[r], :].reshape(H * d)
     o = bf16(o)
     x1 = bf16(x[rows] + gate_rows(mod, modp, s.n_prefix, 2, rows) *
               linear(o, wts["w_o"], wts["b_o"]))

@@ -141,9 +141,10 @@ def attention_inputs(shape: BlockShape, seed: int, structured: float = 0.0,
                      with_gate: bool = True) -> dict:
     """Q, K, V bf16 [H, N, d] ~ N(0,1); gate bf16 [N, H*d] ~ N(0,1).
 
-    ``structured`` > 0 adds a per-(head, video tile) offset vector ~ N(0, s^2)
-    to every row of that tile in Q and K, so that tile means separate and
-    routing is decisive; 0 gives the flat i.i.d. regime.
+    ``structured`` > 0 adds a per-(head, video block) offset vector ~ N(0, s^2)
+    to every row of that block in Q and K (blocks: 64-row slices, or cubes of the
+    latent grid with the video rows in raster order), so that tile means separate
+    and routing is decisive; 0 gives the flat i.i.d. regime.
     """
     H, N, d = shape.heads, shape.n_rows, shape.head_dim
     q = normal(seed, "q", (H, N, d))
@@ -151,11 +152,18 @@ def attention_inputs(shape: BlockShape, seed: int, structured: float = 0.0,
     v = normal(seed, "v", (H, N, d))
     if structured > 0.0:
         P, tile = shape.n_prefix, shape.tile
-        tv = shape.n_video_tiles
+        rows = np.arange(shape.n_video)
+        if shape.video_grid is None:
+            t_of = rows // tile  # one offset per 64-row slice
+        else:  # one offset per block of the latent grid, rows in raster (t, h, w) order
+            T, Hg, Wg = shape.video_grid
+            ct, ch, cw = shape.cube
+            nh, nw = -(-Hg // ch), -(-Wg // cw)
+            t_of = ((rows // (Hg * Wg)) // ct * nh + (rows // Wg % Hg) // ch) * nw \
+                + (rows % Wg) // cw
+        tv = int(t_of.max()) + 1
         cq = normal(seed, "q.tile_offset", (H, tv, d), std=structured)
         ck = normal(seed, "k.tile_offset", (H, tv, d), std=structured)
-        rows = np.arange(shape.n_video)
-        t_of = rows // tile
         q[:, P:, :] += cq[:, t_of, :]
         k[:, P:, :] += ck[:, t_of, :]
     out = {"q": to_bf16_bits(q), "k": to_bf16_bits(k), "v": to_bf16_bits(v)}

@@ -1,8 +1,10 @@
 """Workload shapes.
 
 The packed sequence holds text rows first, then audio rows, then video rows.
-Text and audio rows form the prefix; video rows are cut into 64-row tiles that
-the router selects among.
+Text and audio rows form the prefix; video rows are cut into tiles of at most 64
+rows that the router selects among: contiguous 64-row slices, or, with a video
+grid, 4 x 4 x 4 cubes of the latent grid (edge cubes clipped).  Row order here is
+raster (t, h, w) for video rows.
 """
 from __future__ import annotations
 
@@ -28,6 +30,9 @@ class BlockShape:
     attn_width_override: int = 0
     mlp: str = "gelu"  # "gelu": fc1 [F, D]; "swiglu": fc1 [2F, D] gate/up interleaved by 128 rows
     prefix_mod: bool = False  # text/audio rows modulated by their own [6, D] table
+    # video latent grid (T, H, W) cut into cubes; None = contiguous 64-row tiles
+    video_grid: tuple | None = None
+    cube: tuple = (4, 4, 4)
 
     @property
     def n_rows(self) -> int:
@@ -43,7 +48,12 @@ class BlockShape:
 
     @property
     def n_video_tiles(self) -> int:
-        return (self.n_video + self.tile - 1) // self.tile
+        if self.video_grid is None:
+            return (self.n_video + self.tile - 1) // self.tile
+        n = 1
+        for g, c in zip(self.video_grid, self.cube):
+            n *= (g + c - 1) // c
+        return n
 
     def with_(self, **kw) -> "BlockShape":
         return replace(self, **kw)
@@ -118,7 +128,25 @@ FORWARD_PAGES = Workload(
     n_blocks=50, extra={"dt": -0.125, "forward": True},
 )
 
-CONFIGS = [ATTN_TINY, BLOCK_4K, BLOCK_15K, FORWARD_50, LOOP_4K, BLOCK_PAGES, FORWARD_PAGES]
+# The pages' receipt sequence: 864 x 480, 124 frames -> 15,435 rows (36 text, 414 audio,
+# 14,985 video = a 37 x 15 x 27 latent grid), 4 x 4 x 4 cubes -> 280 video tiles beside
+# 8 prefix tiles, 56 video tiles kept per query tile, on the pages' block shape.
+RECEIPT_SHAPE = PAGES_SHAPE.with_(n_text=36, n_audio=414, n_video=14985, topk=56,
+                                  video_grid=(37, 15, 27))
+BLOCK_RECEIPT = Workload(
+    "block_15435_cubes_d5376_swiglu", 8, RECEIPT_SHAPE,
+    "one block of the pages' shape on the receipt sequence: 15,435 rows (36 text, 414 audio, "
+    "14,985 video on a 37 x 15 x 27 grid), 280 4x4x4 video tiles, top-k 56 + pooled, 3-D rotary",
+)
+FORWARD_RECEIPT = Workload(
+    "forward50_15435_cubes_d5376_swiglu", 9, RECEIPT_SHAPE,
+    "50-block denoising forward of the pages' shape on the receipt sequence (280 cube tiles, "
+    "top-k 56), then z <- z + dt v with dt = -1/8",
+    n_blocks=50, extra={"dt": -0.125, "forward": True},
+)
+
+CONFIGS = [ATTN_TINY, BLOCK_4K, BLOCK_15K, FORWARD_50, LOOP_4K, BLOCK_PAGES, FORWARD_PAGES,
+           BLOCK_RECEIPT, FORWARD_RECEIPT]
 
 
 def config_by_name(name: str) -> Workload:

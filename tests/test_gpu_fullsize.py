@@ -181,3 +181,36 @@ def test_pages_shape_block_sampled(h3):
     assert_close(got[rows], ref["x2"], "pages-shape x2 (sampled rows)")
     assert_close(got[rows] - x0, ref["x2"] - x0, "pages-shape update (sampled rows)", rel=5e-2,
                  cos=0.998)
+
+
+def test_receipt_cubes_block_sampled(h3):
+    """The pages' receipt sequence on the pages' block shape: 36 text + 414 audio rows
+    (a prefix of 450, not a multiple of 64) and 14,985 video rows on a 37 x 15 x 27 grid
+    in 280 clipped 4x4x4 cubes, top-k 56, 3-D rotary; sampled rows against the oracle
+    (video rows in raster order there, cube order on the device)."""
+    wl = S.config_by_name("block_15435_cubes_d5376_swiglu")
+    shp = wl.shape
+    assert shp.n_video_tiles == 280
+    t0 = time.time()
+    w = S.block_weights(shp, wl.seed)
+    xb = S.hidden_rows(shp, wl.seed)
+    perm = np.concatenate([np.arange(shp.n_prefix)] + oracle.shape_tiles(shp))
+    cs = h3.make_shape(shp)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    x = dev_bf16(xb[perm])
+    h3.block_forward(cs, weights_to_device(w), x, ws)
+    torch.cuda.synchronize()
+    assert h3.sync_status(ws) == 0
+    got = np.empty((shp.n_rows, shp.hidden))
+    got[perm] = host_f64(x)
+    P, N = shp.n_prefix, shp.n_rows
+    T, Hg, Wg = shp.video_grid
+    rr = lambda t, h, w: P + (t * Hg + h) * Wg + w  # noqa: E731  raster row of a token
+    rows = [0, 35, 36, 448, 449, rr(0, 0, 0), rr(0, 3, 3), rr(3, 3, 4), rr(17, 7, 13),
+            rr(36, 14, 26), rr(36, 0, 0), rr(35, 12, 24), N - 1]
+    ref = oracle.block_forward_rows(S.bf16_bits_to_f64(xb), weights_to_f64(w), shp, rows)
+    _log(f"receipt cube block sampled oracle {time.time() - t0:.1f}s")
+    x0 = S.bf16_bits_to_f64(xb)[ref["rows"]]
+    assert_close(got[ref["rows"]], ref["x2"], "receipt x2 (sampled rows)")
+    assert_close(got[ref["rows"]] - x0, ref["x2"] - x0, "receipt update (sampled rows)",
+                 rel=5e-2, cos=0.998)

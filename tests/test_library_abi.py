@@ -41,11 +41,20 @@ def test_library_exports_every_declared_symbol(h3):
 def test_shape_checks_on_host(h3):
     good = S.CONFIGS[1].shape
     assert h3.check_shape(h3.make_shape(good)) == 0
-    bad = [good.with_(tile=32), good.with_(n_text=100), good.with_(head_dim=96),
+    bad = [good.with_(tile=32), good.with_(head_dim=96),
            good.with_(hidden=3000), good.with_(mlp_width=1000), good.with_(n_video=0),
-           good.with_(attn_width_override=2048)]
-    for b in bad:
+           good.with_(attn_width_override=2048),
+           good.with_(video_grid=(7, 16, 32)),                  # 3,584 rows, grid holds 3,584?
+           good.with_(video_grid=(7, 16, 32), cube=(4, 4, 2)),  # cube of 32 tokens
+           good.with_(video_grid=(7, 16, 31))]                  # grid != n_video
+    assert 7 * 16 * 32 == good.n_video
+    for b in bad[-2:]:
+        assert h3.check_shape(h3.make_shape(b)) == 2, b
+    for b in bad[:-3]:
         assert h3.check_shape(h3.make_shape(b)) != 0, b
+    assert h3.check_shape(h3.make_shape(bad[-3])) == 0  # a consistent grid is accepted
+    # a prefix that is not a multiple of 64 rows (the receipt's 36 + 414) is accepted
+    assert h3.check_shape(h3.make_shape(good.with_(n_text=36, n_audio=414))) == 0
     assert h3.check_shape(h3.make_shape(good.with_(topk=0))) == 1
 
 
@@ -75,7 +84,7 @@ def test_entry_points_reject_bad_arguments_without_gpu(h3):
     assert lib.h3dit_linear(None, None, None, None, 1, 256, 64, None) == 1
     assert lib.h3dit_linear(16, 16, None, 16, 1, 255, 64, None) == 2   # N not a multiple of 256
     assert lib.h3dit_linear(17, 16, None, 16, 1, 256, 64, None) == 3   # misaligned
-    bad = h3.make_shape(S.CONFIGS[1].shape.with_(n_audio=100))
+    bad = h3.make_shape(S.CONFIGS[1].shape.with_(video_grid=(7, 16, 31)))  # grid != n_video
     assert lib.h3dit_block_forward(ctypes.byref(bad), None, None, None, 0, None) == 2
 
 
@@ -120,3 +129,24 @@ def test_workspace_too_small_and_bad_weights_refused_on_host(h3):
     bad = h3.Schedule(0.5, 0.6, 0.6, -0.1)  # sigma_a == sigma_b: no extrapolation slope
     assert lib.h3dit_denoise_step(ctypes.byref(s), None, None, 0, 4096, 4096, 0, ctypes.byref(bad),
                                   None, 2, 4096, need, None) == 1
+
+
+@pytest.mark.parametrize("grid", [None, (37, 15, 27), (5, 6, 7), (1, 3, 2), (8, 8, 8),
+                                  (9, 1, 17)])
+def test_tile_spans_and_video_order_match_oracle_tiles(h3, grid):
+    """The library's contiguous tiles, mapped through its video order, are exactly the
+    oracle's tiles of raster rows (same tile numbering, same order inside a tile)."""
+    nv = 14985 if grid is None else int(np.prod(grid))
+    shp = S.BlockShape(36, 414, nv, hidden=256, heads=2, head_dim=128, mlp_width=1024, topk=4,
+                       video_grid=grid)
+    cs = h3.make_shape(shp)
+    first, nrows = h3.tile_spans(cs)
+    order = h3.video_order(cs)
+    P = shp.n_prefix
+    assert np.array_equal(np.sort(order), np.arange(nv))
+    want = oracle.shape_tiles(shp)
+    assert len(first) == len(want) == shp.n_video_tiles
+    assert first[0] == P and np.array_equal(first[1:], (first + nrows)[:-1])
+    for i, rows in enumerate(want):
+        lib_rows = P + order[first[i] - P:first[i] - P + nrows[i]]
+        assert np.array_equal(lib_rows, rows), i

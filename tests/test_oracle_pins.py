@@ -308,6 +308,102 @@ def test_gate_mix_brute_force():
                 assert abs(out[r, h * d + c] - want) < 1e-14
 
 
+# --------------------------------------------------------------------------- cubes, 3-D rotary
+def test_cube_tiles_receipt_golden():
+    with open(os.path.join(GOLDEN, "receipt_tiles.txt")) as f:
+        rows = [list(map(int, ln.split())) for ln in f if ln.strip() and not ln.startswith("#")]
+    for nt, na, nv, T, Hg, Wg, total, pre, kept in rows:
+        assert T * Hg * Wg == nv and nt + na + nv == 15435
+        tiles = O.cube_tiles(nt + na, (T, Hg, Wg))
+        assert -(-(nt + na) // 64) == pre
+        assert len(tiles) + pre == total
+        assert kept < len(tiles)
+
+
+@pytest.mark.parametrize("grid,cube", [((37, 15, 27), (4, 4, 4)), ((5, 6, 7), (4, 4, 4)),
+                                       ((1, 1, 1), (4, 4, 4)), ((8, 8, 8), (4, 4, 4)),
+                                       ((3, 9, 10), (2, 8, 4))])
+def test_cube_tiles_partition_by_membership(grid, cube):
+    # every video row lies in exactly one tile, namely the cube containing its (t, h, w),
+    # and each tile lists its rows in raster order
+    P = 7
+    T, Hg, Wg = grid
+    tiles = O.cube_tiles(P, grid, cube)
+    allrows = np.concatenate(tiles)
+    assert np.array_equal(np.sort(allrows), P + np.arange(T * Hg * Wg))
+    nh, nw = -(-Hg // cube[1]), -(-Wg // cube[2])
+    for i, tr in enumerate(tiles):
+        assert np.all(np.diff(tr) > 0) and 1 <= len(tr) <= cube[0] * cube[1] * cube[2]
+        for r in tr:
+            t, h, w = (r - P) // (Hg * Wg), (r - P) // Wg % Hg, (r - P) % Wg
+            assert ((t // cube[0]) * nh + h // cube[1]) * nw + w // cube[2] == i
+
+
+def test_rope_axis_split_values():
+    # the common video-DiT split: 44 / 42 / 42 dims at d = 128, 24 / 20 / 20 at d = 64
+    assert O.rope_axis_split(128) == (22, 21, 21)
+    assert O.rope_axis_split(64) == (12, 10, 10)
+
+
+def test_rope_3d_brute_force_complex():
+    d, N = 64, 9
+    x = rng.standard_normal((2, N, d))
+    coords = rng.integers(0, 40, (N, 3))
+    got = O.rope_3d(x, coords, 10000.0)
+    mt, mh, mw = 12, 10, 10
+    for h in range(2):
+        for n in range(N):
+            for c in range(d // 2):
+                if c < mt:
+                    a, j, m = 0, c, mt
+                elif c < mt + mh:
+                    a, j, m = 1, c - mt, mh
+                else:
+                    a, j, m = 2, c - mt - mh, mw
+                z = complex(x[h, n, c], x[h, n, c + d // 2]) * \
+                    np.exp(1j * coords[n, a] * 10000.0 ** (-j / m))
+                assert abs(got[h, n, c] - z.real) < 1e-12
+                assert abs(got[h, n, c + d // 2] - z.imag) < 1e-12
+
+
+def test_rope_3d_relative_per_axis_and_isolation():
+    d = 128
+    q, k = rng.standard_normal((1, 1, d)), rng.standard_normal((1, 1, d))
+    a, b = np.array([[3, 5, 7]]), np.array([[11, 2, 9]])
+    base = float(O.rope_3d(q, a)[0, 0] @ O.rope_3d(k, b)[0, 0])
+    for delta in ([4, 0, 0], [0, 6, 0], [0, 0, 13], [2, 3, 5]):
+        dd = np.array([delta])
+        moved = float(O.rope_3d(q, a + dd)[0, 0] @ O.rope_3d(k, b + dd)[0, 0])
+        assert abs(moved - base) < 1e-10
+    # a width-only move turns only the width pairs (the last 21 of 64)
+    r0 = O.rope_3d(q, a)[0, 0]
+    r1 = O.rope_3d(q, a + np.array([[0, 0, 1]]))[0, 0]
+    same = np.isclose(r0, r1, rtol=0, atol=1e-15)
+    pair_same = same[:64] & same[64:]
+    assert pair_same[:43].all() and not pair_same[43:].any()
+    assert np.allclose(O.rope_3d(q, np.zeros((1, 3))), q)
+
+
+def test_rope_coords_raster():
+    c = O.rope_coords(5, 3 * 4 * 6, (3, 4, 6))
+    assert np.array_equal(c[:5], np.repeat(np.arange(5)[:, None], 3, axis=1))
+    assert np.array_equal(c[5 + (2 * 4 + 1) * 6 + 5], [2, 1, 5])
+
+
+def test_cube_block_equals_permuted_slices_when_dense():
+    # with every tile selected and no pooled term the tiling does not matter: the cube
+    # shape equals the 1-D shape on the same rows (up to the rotary, disabled here)
+    base = dict(n_text=36, n_audio=64, n_video=5 * 6 * 7, hidden=64, heads=2, head_dim=32,
+                mlp_width=256, topk=64, rope=False, pooled=False)
+    s1 = S.BlockShape(**base)
+    s3 = S.BlockShape(**base, video_grid=(5, 6, 7))
+    w = _weights(s1)
+    x = S.bf16_bits_to_f64(S.hidden_rows(s1, 8))
+    a = O.block_forward(x, w, s1)["x2"]
+    b = O.block_forward(x, w, s3)["x2"]
+    assert np.array_equal(a, b)
+
+
 # --------------------------------------------------------------------------- block
 def _tiny_shape(**kw):
     base = dict(n_text=64, n_audio=64, n_video=150, hidden=64, heads=2, head_dim=32,
