@@ -53,6 +53,15 @@ class Schedule(ctypes.Structure):
                 ("sigma_b", ctypes.c_float), ("dt", ctypes.c_float)]
 
 
+class Ends(ctypes.Structure):
+    _fields_ = [("c_video", ctypes.c_int), ("c_audio", ctypes.c_int)] + [
+        (n, ctypes.c_void_p) for n in
+        ("w_in_video", "b_in_video", "w_in_audio", "b_in_audio", "w_out_video", "b_out_video",
+         "w_out_audio", "b_out_audio", "mod_out_video", "mod_out_audio", "text")]
+
+
+H3DIT_PASS_FRESH, H3DIT_PASS_EXTRAPOLATE, H3DIT_PASS_CORE_REUSE = 0, 1, 2
+
 _lib = None
 
 # (name, restype, argtypes)
@@ -72,6 +81,11 @@ _SIGS = [
       ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(Schedule),
       ctypes.POINTER(Schedule), ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
       ctypes.c_void_p]),
+    ("h3dit_sample_step", ctypes.c_int,
+     [ctypes.POINTER(Shape), ctypes.POINTER(Ends), ctypes.POINTER(BlockWeights),
+      ctypes.POINTER(ctypes.c_int), ctypes.c_int] + [ctypes.c_void_p] * 5
+     + [ctypes.c_int, ctypes.POINTER(Schedule), ctypes.POINTER(Schedule), ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     ("h3dit_select_blocks", ctypes.c_int,
      [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     ("h3dit_tile_spans", ctypes.c_int,
@@ -224,6 +238,30 @@ def video_order(shape: Shape) -> np.ndarray:
     out = np.zeros(shape.n_video, np.int32)
     _check("h3dit_video_order", lib().h3dit_video_order(ctypes.byref(shape), out.ctypes.data))
     return out
+
+
+def make_ends(ends: dict) -> Ends:
+    """ctypes ends struct from a dict of device tensors (plus "c_video", "c_audio")."""
+    return Ends(int(ends["c_video"]), int(ends.get("c_audio", 0)),
+                *[_ptr(ends.get(n)) for n, _ in Ends._fields_[2:]])
+
+
+def sample_step(shape: Shape, ends: dict, blocks: list, block_ids, z_video, z_audio,
+                v_ring_video, v_ring_audio, core_residual, pass_kind: int, video, audio,
+                n_fresh_so_far: int, workspace, stream=None):
+    """One sampler step on the modality latents (both ends included).  ``video`` and
+    ``audio`` are (sigma_i, sigma_a, sigma_b, dt) tuples; ``pass_kind`` one of
+    H3DIT_PASS_FRESH / _EXTRAPOLATE / _CORE_REUSE."""
+    arr = (BlockWeights * max(1, len(blocks)))(*[block_weights(b) for b in blocks])
+    ids = (ctypes.c_int * max(1, len(block_ids)))(*[int(i) for i in block_ids])
+    e = make_ends(ends)
+    sv = Schedule(*[float(x) for x in video])
+    sa = Schedule(*[float(x) for x in (audio if audio is not None else video)])
+    _check("h3dit_sample_step", lib().h3dit_sample_step(
+        ctypes.byref(shape), ctypes.byref(e), arr, ids, len(block_ids), _ptr(z_video),
+        _ptr(z_audio), _ptr(v_ring_video), _ptr(v_ring_audio), _ptr(core_residual),
+        int(pass_kind), ctypes.byref(sv), ctypes.byref(sa), int(n_fresh_so_far),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def select_blocks(mods: np.ndarray, keep: int) -> list:

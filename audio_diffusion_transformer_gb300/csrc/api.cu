@@ -422,6 +422,72 @@ h3dit_status check_weights(const h3dit_shape* s, const h3dit_block_weights* w) {
   return H3DIT_OK;
 }
 
+// Checks the ends struct against a shape (host only).
+h3dit_status check_ends(const h3dit_shape* s, const h3dit_ends* e) {
+  if (!e) return H3DIT_ERR_ARG;
+  auto ok_c = [](int c) { return c >= 32 && c <= 128 && c % 32 == 0; };
+  if (!ok_c(e->c_video) || (s->n_audio > 0 && !ok_c(e->c_audio))) return H3DIT_ERR_SHAPE;
+  const void* vid[] = {e->w_in_video, e->b_in_video, e->w_out_video, e->b_out_video,
+                       e->mod_out_video};
+  for (const void* p : vid) {
+    if (!p) return H3DIT_ERR_ARG;
+    if (!aligned16(p)) return H3DIT_ERR_ALIGN;
+  }
+  if (s->n_audio > 0) {
+    const void* aud[] = {e->w_in_audio, e->b_in_audio, e->w_out_audio, e->b_out_audio,
+                         e->mod_out_audio};
+    for (const void* p : aud) {
+      if (!p) return H3DIT_ERR_ARG;
+      if (!aligned16(p)) return H3DIT_ERR_ALIGN;
+    }
+  }
+  if (s->n_text > 0) {
+    if (!e->text) return H3DIT_ERR_ARG;
+    if (!aligned16(e->text)) return H3DIT_ERR_ALIGN;
+  }
+  return H3DIT_OK;
+}
+
+// x_0 rows from the text rows and the two modalities' patch projections.
+h3dit_status build_x0(const h3dit_shape* s, const Dims& m, const h3dit_ends* e,
+                      const float* z_video, const float* z_audio, __nv_bfloat16* x,
+                      cudaStream_t st) {
+  const int T = s->n_text, Aud = s->n_audio, D = m.D;
+  if (T > 0 && cudaMemcpyAsync(x, e->text, (size_t)T * D * 2, cudaMemcpyDeviceToDevice, st) !=
+                   cudaSuccess)
+    return H3DIT_ERR_CUDA;
+  if (Aud > 0)
+    H3_TRY(cu(counted(launch_patch_in(z_audio, e->w_in_audio, e->b_in_audio, x + (size_t)T * D,
+                                      Aud, e->c_audio, D, st), 1)));
+  return cu(counted(launch_patch_in(z_video, e->w_in_video, e->b_in_video, x + (size_t)m.P * D,
+                                    m.V, e->c_video, D, st), 1));
+}
+
+// Final AdaLN of one modality's rows [r0, r0 + rows) of x, then its output head with the
+// Euler update fused: v = h W_out^T + b; v_out (if set) = v; z += dt v.
+h3dit_status head_pass(const Dims& m, const Ws& w, void* ws, const __nv_bfloat16* x, int r0,
+                       int rows, int c, const float* mod2, const void* w_out, const void* b_out,
+                       float* z, float* v_out, float dt, float eps, cudaStream_t st) {
+  if (rows <= 0) return H3DIT_OK;
+  const int D = m.D;
+  __nv_bfloat16* h = at<__nv_bfloat16>(ws, w.h) + (size_t)r0 * D;
+  H3_TRY(cu(counted(launch_rms_modulate(x + (size_t)r0 * D, mod2, mod2 + D, nullptr, nullptr, 0,
+                                        h, rows, D, eps, st), 1)));
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.a = h;
+  g.w = static_cast<const __nv_bfloat16*>(w_out);
+  g.M = rows;
+  g.N = c;
+  g.K = D;
+  g.bias = static_cast<const __nv_bfloat16*>(b_out);
+  g.z = z;
+  g.v_out = v_out;
+  g.dt = dt;
+  g.status = at<int>(ws, w.status);
+  return cu(counted(launch_gemm(kEpiHeadEuler, g, st), 1));
+}
+
 }  // namespace
 }  // namespace h3
 
@@ -551,6 +617,102 @@ h3dit_status h3dit_denoise_step(const h3dit_shape* shape, const h3dit_block_weig
   StageScope sc(H3DIT_STAGE_SAMPLER, st);
   return cu(counted(launch_euler_extrap(z_inout, va, vb, coef_v, video->dt, coef_p, pre->dt, n_pre,
                                         n, st), 1));
+}
+
+h3dit_status h3dit_sample_step(const h3dit_shape* shape, const h3dit_ends* ends,
+                               const h3dit_block_weights* blocks, const int* block_ids,
+                               int n_blocks, float* z_video, float* z_audio,
+                               float* v_ring_video, float* v_ring_audio, float* core_residual,
+                               int pass, const h3dit_schedule* video,
+                               const h3dit_schedule* audio, int n_fresh_so_far,
+                               void* workspace, size_t ws_bytes, void* stream) {
+  Dims m;
+  H3_TRY(check_block(shape, &m));
+  H3_TRY(check_ends(shape, ends));
+  const bool has_audio = shape->n_audio > 0;
+  if (!video || (has_audio && !audio) || !workspace || !z_video) return H3DIT_ERR_ARG;
+  if (has_audio && !z_audio) return H3DIT_ERR_ARG;
+  if (pass != H3DIT_PASS_FRESH && pass != H3DIT_PASS_EXTRAPOLATE &&
+      pass != H3DIT_PASS_CORE_REUSE)
+    return H3DIT_ERR_ARG;
+  if (n_fresh_so_far < 0) return H3DIT_ERR_ARG;
+  const void* ptrs[] = {z_video, z_audio, v_ring_video, v_ring_audio, core_residual, workspace};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return H3DIT_ERR_ALIGN;
+  if (pass != H3DIT_PASS_CORE_REUSE && (!v_ring_video || (has_audio && !v_ring_audio)))
+    return H3DIT_ERR_ARG;
+  if (pass == H3DIT_PASS_CORE_REUSE && !core_residual) return H3DIT_ERR_ARG;
+  const Ws ws = plan(m);
+  if (ws_bytes < ws.total) return H3DIT_ERR_WORKSPACE;
+  const int cv = ends->c_video, ca = has_audio ? ends->c_audio : 0;
+  const size_t nv = (size_t)m.V * cv, na = (size_t)shape->n_audio * ca;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  if (pass == H3DIT_PASS_EXTRAPOLATE) {
+    if (n_fresh_so_far < 1) return H3DIT_ERR_ARG;  // nothing to extrapolate from
+    const bool two = n_fresh_so_far >= 2;
+    if (two && (video->sigma_a == video->sigma_b ||
+                (has_audio && audio->sigma_a == audio->sigma_b)))
+      return H3DIT_ERR_ARG;
+    H3_TRY(device_ok());
+    auto coef = [](const h3dit_schedule* sc) {
+      return (float)(((double)sc->sigma_i - sc->sigma_a) / ((double)sc->sigma_a - sc->sigma_b));
+    };
+    const size_t sa = (size_t)((n_fresh_so_far - 1) % 2), sb = (size_t)(n_fresh_so_far % 2);
+    StageScope sc(H3DIT_STAGE_SAMPLER, st);
+    H3_TRY(cu(counted(launch_euler_extrap(z_video, v_ring_video + sa * nv,
+                                          two ? v_ring_video + sb * nv : nullptr,
+                                          two ? coef(video) : 0.f, video->dt, 0.f, 0.f, 0, nv,
+                                          st), 1)));
+    if (has_audio)
+      H3_TRY(cu(counted(launch_euler_extrap(z_audio, v_ring_audio + sa * na,
+                                            two ? v_ring_audio + sb * na : nullptr,
+                                            two ? coef(audio) : 0.f, audio->dt, 0.f, 0.f, 0, na,
+                                            st), 1)));
+    return H3DIT_OK;
+  }
+
+  if (pass == H3DIT_PASS_FRESH) {
+    if (!blocks || (n_blocks > 0 && !block_ids) || n_blocks < 0) return H3DIT_ERR_ARG;
+    for (int i = 0; i < n_blocks; ++i) {
+      if (block_ids[i] < 0) return H3DIT_ERR_ARG;
+      H3_TRY(check_weights(shape, &blocks[block_ids[i]]));
+    }
+  }
+  H3_TRY(device_ok());
+  __nv_bfloat16* x = at<__nv_bfloat16>(workspace, ws.x);
+  const size_t nd = (size_t)m.N * m.D;
+  {
+    StageScope sc(H3DIT_STAGE_SAMPLER, st);
+    H3_TRY(build_x0(shape, m, ends, z_video, z_audio, x, st));
+    if (pass == H3DIT_PASS_CORE_REUSE)
+      H3_TRY(cu(counted(launch_core_residual(x, core_residual, nd, 2, st), 1)));
+    if (pass == H3DIT_PASS_FRESH) {
+      if (core_residual) H3_TRY(cu(counted(launch_core_residual(x, core_residual, nd, 0, st), 1)));
+      if ((shape->flags & H3DIT_ROPE) && n_blocks > 0)
+        H3_TRY(cu(counted(launch_rope_table(at<float2>(workspace, ws.rope), m.N, m.d,
+                                            shape->rope_theta, m.geom, st), 1)));
+    }
+  }
+  if (pass == H3DIT_PASS_FRESH) {
+    for (int i = 0; i < n_blocks; ++i)
+      H3_TRY(run_block(shape, m, ws, workspace, &blocks[block_ids[i]], x, true, st));
+    if (core_residual) {
+      StageScope sc(H3DIT_STAGE_SAMPLER, st);
+      H3_TRY(cu(counted(launch_core_residual(x, core_residual, nd, 1, st), 1)));
+    }
+  }
+  const bool fresh = pass == H3DIT_PASS_FRESH;
+  const size_t slot = (size_t)(n_fresh_so_far % 2);
+  StageScope sc(H3DIT_STAGE_SAMPLER, st);
+  H3_TRY(head_pass(m, ws, workspace, x, m.P, m.V, cv, ends->mod_out_video, ends->w_out_video,
+                   ends->b_out_video, z_video, fresh ? v_ring_video + slot * nv : nullptr,
+                   video->dt, shape->rms_eps, st));
+  if (has_audio)
+    H3_TRY(head_pass(m, ws, workspace, x, shape->n_text, shape->n_audio, ca, ends->mod_out_audio,
+                     ends->w_out_audio, ends->b_out_audio, z_audio,
+                     fresh ? v_ring_audio + slot * na : nullptr, audio->dt, shape->rms_eps, st));
+  return H3DIT_OK;
 }
 
 h3dit_status h3dit_select_blocks(const float* mods, int n_blocks, int hidden, int keep,

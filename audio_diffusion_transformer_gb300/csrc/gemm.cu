@@ -25,13 +25,24 @@ namespace {
 #define H3_GEMM_STAGES 4
 #endif
 
-constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int BM = 128, BK = 64;
+constexpr int BN_WIDE = 256;  // output tile width of the projections
 constexpr int STAGES = H3_GEMM_STAGES;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+
+// Per tile width BN: shared-memory ring and TMEM accumulator sizes.
+template <int BN>
+struct Tile {
+  static constexpr int B_BYTES = BN * BK * 2;  // 32 KB at BN = 256
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  // two accumulators of BN columns, allocated as a power of two >= 32
+  static constexpr uint32_t TMEM_COLS =
+      2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512));
+  // accumulator b starts at column b * ACC_STRIDE (a power of two)
+  static constexpr uint32_t ACC_STRIDE = TMEM_COLS / 2;
+};
 
 struct Params {
   int M, N, K;
@@ -46,6 +57,9 @@ struct Params {
   const __nv_bfloat16 *qnorm_w, *knorm_w;
   const float2* rope_cs;
   float eps;
+  float* v_out;  // head epilogue: fp32 velocity [M, N] or null
+  float* z;      // head epilogue: fp32 latents [M, N], z += dt * v
+  float dt;
   int* status;
 };
 
@@ -109,8 +123,38 @@ __device__ __forceinline__ float gelu_erf(float x) {
   return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
 }
 
-// Epilogue of a plain / GELU / residual tile: 8 chunks of 32 columns.
-template <int EPI>
+// Epilogue of an output head: v = acc + b (fp32); v -> the velocity ring, z += dt * v.
+template <int BN>
+__device__ __forceinline__ void epilogue_head(const Params& p, uint32_t t_row, int row, int n0) {
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float v[32];
+    tmem_ld32(t_row + c * 32, v);
+    if (row < p.M) {
+      const int col0 = n0 + c * 32;
+      float b[32];
+      load_bf16x32(p.bias + col0, b);
+      const size_t off = (size_t)row * p.N + col0;
+      float4* z4 = reinterpret_cast<float4*>(p.z + off);
+      float4* v4 = p.v_out ? reinterpret_cast<float4*>(p.v_out + off) : nullptr;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 vv = make_float4(v[4 * j] + b[4 * j], v[4 * j + 1] + b[4 * j + 1],
+                                      v[4 * j + 2] + b[4 * j + 2], v[4 * j + 3] + b[4 * j + 3]);
+        float4 zz = z4[j];
+        zz.x = fmaf(p.dt, vv.x, zz.x);
+        zz.y = fmaf(p.dt, vv.y, zz.y);
+        zz.z = fmaf(p.dt, vv.z, zz.z);
+        zz.w = fmaf(p.dt, vv.w, zz.w);
+        z4[j] = zz;
+        if (v4) v4[j] = vv;
+      }
+    }
+  }
+}
+
+// Epilogue of a plain / GELU / residual tile: BN / 32 chunks of 32 columns.
+template <int EPI, int BN>
 __device__ __forceinline__ void epilogue_rows(const Params& p, uint32_t t_row, int row, int n0) {
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
@@ -171,7 +215,7 @@ __device__ __forceinline__ void epilogue_swiglu(const Params& p, uint32_t t_row,
 }
 
 // Epilogue of the fused q/k/v/gate projection: one head (HD columns) at a time.
-template <int HD>
+template <int HD, int BN>
 __device__ __forceinline__ void epilogue_qkvg(const Params& p, uint32_t t_row, int row, int n0) {
   const int A = p.attn_width;
   const int slab = n0 / A;  // 0 q, 1 k, 2 v, 3 g  (A is a multiple of BN)
@@ -232,10 +276,13 @@ __device__ __forceinline__ void epilogue_qkvg(const Params& p, uint32_t t_row, i
   }
 }
 
-template <int EPI, int HD>
+template <int EPI, int HD, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const Params p) {
+  using T = Tile<BN>;
+  constexpr int B_BYTES = T::B_BYTES;
+  constexpr int STAGE_BYTES = T::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -271,7 +318,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
+    tmem_alloc(tmem_slot, T::TMEM_COLS);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -317,7 +364,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * BN;
+        const uint32_t d_tmem = tmem + acc * T::ACC_STRIDE;
         for (int kb = 0; kb < num_k; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
             ok = false;
@@ -359,13 +406,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
       const int row = m_blk * BM + quad * 32 + lane;
-      const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16) + acc * BN;
+      const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16) + acc * T::ACC_STRIDE;
       if (EPI == kEpiQkvg)
-        epilogue_qkvg<HD>(p, t_row, row, n_blk * BN);
+        epilogue_qkvg<HD, BN>(p, t_row, row, n_blk * BN);
       else if (EPI == kEpiSwiglu)
         epilogue_swiglu(p, t_row, row, n_blk * BN);
+      else if (EPI == kEpiHeadEuler)
+        epilogue_head<BN>(p, t_row, row, n_blk * BN);
       else
-        epilogue_rows<EPI>(p, t_row, row, n_blk * BN);
+        epilogue_rows<EPI, BN>(p, t_row, row, n_blk * BN);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -380,32 +429,36 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, T::TMEM_COLS);
   }
 }
 
-template <int EPI, int HD>
+template <int EPI, int HD, int BN = BN_WIDE>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
                        cudaStream_t stream) {
-  auto kern = gemm_kernel<EPI, HD>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMEM_BYTES);
+  auto kern = gemm_kernel<EPI, HD, BN>;
+  constexpr int smem = Tile<BN>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int tiles = ((p.M + BM - 1) / BM) * (p.N / BN);
   const int sms = num_sms();
   const int grid = tiles < sms ? tiles : sms;
-  kern<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  kern<<<grid, THREADS, smem, stream>>>(ta, tb, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
-  if (g.M <= 0 || g.N % BN != 0 || g.N <= 0 || g.K % BK != 0 || g.K <= 0)
+  // the output heads use one tile of exactly N columns; everything else 256-wide tiles
+  const bool head = epi == kEpiHeadEuler;
+  const int bn = head ? g.N : BN_WIDE;
+  if (head && (g.N % 32 != 0 || g.N > 128 || !g.z || !g.bias)) return cudaErrorInvalidValue;
+  if (g.M <= 0 || g.N <= 0 || g.N % bn != 0 || g.K % BK != 0 || g.K <= 0)
     return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
   if (!make_tmap_2d(&ta, g.a, g.M, g.K, BM)) return cudaErrorInvalidValue;
-  if (!make_tmap_2d(&tb, g.w, g.N, g.K, BN)) return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&tb, g.w, g.N, g.K, bn)) return cudaErrorInvalidValue;
   Params p;
   // raster group: 16 row-blocks when N or K is long (the measured best at 15,435 rows:
   // N = 20,480 and K = 20,480), else 8 (N = K = 5,120)
@@ -429,6 +482,9 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   p.knorm_w = g.knorm_w;
   p.rope_cs = g.rope_cs;
   p.eps = g.eps;
+  p.v_out = g.v_out;
+  p.z = g.z;
+  p.dt = g.dt;
   p.status = g.status;
   switch (epi) {
     case kEpiStore:
@@ -443,6 +499,12 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
     case kEpiQkvg:
       if (g.head_dim == 128) return launch_one<kEpiQkvg, 128>(ta, tb, p, stream);
       if (g.head_dim == 64) return launch_one<kEpiQkvg, 64>(ta, tb, p, stream);
+      return cudaErrorInvalidValue;
+    case kEpiHeadEuler:
+      if (g.N == 32) return launch_one<kEpiHeadEuler, 128, 32>(ta, tb, p, stream);
+      if (g.N == 64) return launch_one<kEpiHeadEuler, 128, 64>(ta, tb, p, stream);
+      if (g.N == 96) return launch_one<kEpiHeadEuler, 128, 96>(ta, tb, p, stream);
+      if (g.N == 128) return launch_one<kEpiHeadEuler, 128, 128>(ta, tb, p, stream);
       return cudaErrorInvalidValue;
     default:
       return cudaErrorInvalidValue;

@@ -18,7 +18,8 @@ enum Epilogue : int {
   kEpiGelu = 1,   // y = bf16(gelu(acc + bias))
   kEpiResid = 2,  // y = bf16(y + gate * (acc + bias))   (y is the residual, in place)
   kEpiQkvg = 3,   // split into head-major q/k/v with q/k norm + rotary, and row-major g
-  kEpiSwiglu = 4  // y[:, 128j + c] = bf16(silu(acc_g + b_g) * (acc_u + b_u)), y is [M, N/2]
+  kEpiSwiglu = 4,   // y[:, 128j + c] = bf16(silu(acc_g + b_g) * (acc_u + b_u)), y is [M, N/2]
+  kEpiHeadEuler = 5 // v = acc + bias (fp32) -> v_out; z += dt * v  (N in {32, 64, 96, 128})
 };
 
 struct GemmArgs {
@@ -36,6 +37,10 @@ struct GemmArgs {
   const __nv_bfloat16 *qnorm_w, *knorm_w;  // [d] or null
   const float2* rope_cs;                   // [M, d/2] (cos, sin) or null
   float eps;
+  // head epilogue
+  float* v_out;  // fp32 [M, N] or null
+  float* z;      // fp32 [M, N]
+  float dt;
   int* status;
 };
 
@@ -78,6 +83,11 @@ cudaError_t launch_rms_modulate(const __nv_bfloat16* x, const float* shift, cons
 cudaError_t launch_rope_table(float2* cs, int rows, int d, float theta, const TileGeom& g,
                               cudaStream_t s);
 cudaError_t launch_f32_to_bf16(const float* z, __nv_bfloat16* x, size_t n, cudaStream_t s);
+// x[r, :] = bf16(z[r, :] w + b), z fp32 [rows, c], w fp32 [c, D] (input-major), b fp32 [D]
+cudaError_t launch_patch_in(const float* z, const float* w, const float* b, __nv_bfloat16* x,
+                            int rows, int c, int D, cudaStream_t s);
+// mode 0: r = x; 1: r = x - r; 2: x = bf16(x + r)   (n elements, x bf16, r fp32)
+cudaError_t launch_core_residual(__nv_bfloat16* x, float* r, size_t n, int mode, cudaStream_t s);
 // elements [0, n_pre) follow the prefix step dt_p (coef_p), the rest dt (coef)
 cudaError_t launch_euler_fresh(const __nv_bfloat16* x, float* z, float* v_slot, float dt,
                                float dt_p, size_t n_pre, size_t n, cudaStream_t s);

@@ -11,6 +11,10 @@
 //    split into time, height and width groups, each with its own frequency
 //    ladder, at the row's latent (t, h, w) (text and audio rows: (p, p, p)).
 //  * f32_to_bf16: the sampler's latents -> the bf16 residual stream.
+//  * patch_in: a modality's fp32 patch projection into its bf16 hidden rows (h3.c
+//    README: fp32 weights, inputs and sums, the result rounded to bf16).
+//  * core_residual: the blocks' residual x_L - x_0 kept in fp32, and x_L =
+//    bf16(x_0 + residual) on a core-reuse pass.
 //  * euler_fresh / euler_extrap: v = fp32(x_L), ring store, z += dt * v; or the
 //    linear extrapolation of the last two fresh velocities (h3.c README sampler
 //    paragraph); prefix rows and video rows each on their own schedule.
@@ -167,6 +171,75 @@ __global__ void euler_extrap_kernel(float4* __restrict__ z, const float4* __rest
   }
 }
 
+// Patch projection of one modality: x[r, :] = bf16(sum_j z[r, j] w[j, :] + b) with fp32
+// weights, inputs and sums (j ascending), one CTA per 32 rows x 256 columns; thread
+// (column group g, row group q) owns 8 rows x 4 columns.
+__global__ void __launch_bounds__(256)
+    patch_in_kernel(const float* __restrict__ z, const float* __restrict__ w,
+                    const float* __restrict__ b, __nv_bfloat16* __restrict__ x, int R, int c,
+                    int D) {
+  __shared__ float4 ws4[32][64];  // 32 input channels x 256 columns of w
+  __shared__ float zs[32][33];    // 32 rows x 32 input channels of z (padded)
+  const int g = threadIdx.x & 63, q = threadIdx.x >> 6;
+  const int row0 = blockIdx.x * 32, col0 = blockIdx.y * 256;
+  float acc[8][4];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
+  for (int k0 = 0; k0 < c; k0 += 32) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < 32 * 64; i += 256) {
+      const int kk = i >> 6, gg = i & 63;
+      ws4[kk][gg] = __ldg(reinterpret_cast<const float4*>(w + (size_t)(k0 + kk) * D + col0) + gg);
+    }
+    for (int i = threadIdx.x; i < 32 * 32; i += 256) {
+      const int r = i >> 5, kk = i & 31;
+      zs[r][kk] = row0 + r < R ? __ldg(z + (size_t)(row0 + r) * c + k0 + kk) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = 0; kk < 32; ++kk) {
+      const float4 wv = ws4[kk][g];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float zv = zs[q * 8 + r][kk];
+        acc[r][0] = fmaf(zv, wv.x, acc[r][0]);
+        acc[r][1] = fmaf(zv, wv.y, acc[r][1]);
+        acc[r][2] = fmaf(zv, wv.z, acc[r][2]);
+        acc[r][3] = fmaf(zv, wv.w, acc[r][3]);
+      }
+    }
+  }
+  const float4 bv = __ldg(reinterpret_cast<const float4*>(b + col0) + g);
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const int row = row0 + q * 8 + r;
+    if (row < R) {
+      *reinterpret_cast<uint2*>(x + (size_t)row * D + col0 + 4 * g) =
+          make_uint2(pack_bf16x2(acc[r][0] + bv.x, acc[r][1] + bv.y),
+                     pack_bf16x2(acc[r][2] + bv.z, acc[r][3] + bv.w));
+    }
+  }
+}
+
+// Core residual: mode 0 r = x; mode 1 r = x - r; mode 2 x = bf16(x + r)  (x bf16, r fp32)
+__global__ void core_residual_kernel(uint2* __restrict__ x, float4* __restrict__ r, size_t n4,
+                                     int mode) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const uint2 u = x[i];
+    const float4 a = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+    if (mode == 0) {
+      r[i] = a;
+    } else if (mode == 1) {
+      const float4 b = r[i];
+      r[i] = make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w);
+    } else {
+      const float4 b = r[i];
+      x[i] = make_uint2(pack_bf16x2(a.x + b.x, a.y + b.y), pack_bf16x2(a.z + b.z, a.w + b.w));
+    }
+  }
+}
+
 int grid_for(size_t n, int threads) {
   size_t b = (n + threads - 1) / threads;
   const size_t cap = (size_t)num_sms() * 16;
@@ -198,6 +271,21 @@ cudaError_t launch_f32_to_bf16(const float* z, __nv_bfloat16* x, size_t n, cudaS
   if (n % 4) return cudaErrorInvalidValue;
   f32_to_bf16_kernel<<<grid_for(n / 4, 256), 256, 0, s>>>(
       reinterpret_cast<const float4*>(z), reinterpret_cast<uint2*>(x), n / 4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_patch_in(const float* z, const float* w, const float* b, __nv_bfloat16* x,
+                            int rows, int c, int D, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (c <= 0 || c % 32 || D % 256) return cudaErrorInvalidValue;
+  patch_in_kernel<<<dim3((rows + 31) / 32, D / 256), 256, 0, s>>>(z, w, b, x, rows, c, D);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_core_residual(__nv_bfloat16* x, float* r, size_t n, int mode, cudaStream_t s) {
+  if (n % 4 || mode < 0 || mode > 2) return cudaErrorInvalidValue;
+  core_residual_kernel<<<grid_for(n / 4, 256), 256, 0, s>>>(
+      reinterpret_cast<uint2*>(x), reinterpret_cast<float4*>(r), n / 4, mode);
   return cudaGetLastError();
 }
 

@@ -13,7 +13,13 @@ the whole job (rows x blocks x steps x ranks / max-over-ranks time).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload forward50_15435_d5120|block_15435_d5120|block_4096_d3072|
                               loop20_4096_d3072|block_15435_d5376_swiglu|
-                              forward50_15435_d5376_swiglu]
+                              forward50_15435_d5376_swiglu|block_15435_cubes_d5376_swiglu|
+                              forward50_15435_cubes_d5376_swiglu|
+                              sample50_15435_cubes_d5376_swiglu]
+
+The sample50 workload runs one fresh pass of h3dit_sample_step instead: fp32 patch
+projections of the video (96 channels) and audio (32) latents, the 50 blocks, the
+final AdaLN and output heads with the Euler update fused.
 
 The loop workload (20 Euler steps, 45 of 50 blocks, reuse 2) also prints a
 top-k density sweep {4, 8, 16, 32, all 56 tiles} of one block.
@@ -292,6 +298,26 @@ def make_blocks(torch, shape, n_blocks, seed, dev):
     return blocks
 
 
+def make_ends(torch, shape, cv, ca, seed, dev):
+    """Both ends on the device, same distributions as synthetic.ends_weights."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    D = shape.hidden
+
+    def rn(*sz, std=1.0, dtype=torch.float32):
+        return (torch.randn(*sz, generator=g, device=dev, dtype=torch.float32) * std).to(
+            dtype).contiguous()
+
+    e = {"c_video": cv, "c_audio": ca, "text": rn(max(shape.n_text, 1), D, dtype=torch.bfloat16)}
+    for m, c in (("video", cv), ("audio", ca)):
+        e[f"w_in_{m}"] = rn(c, D, std=0.1)
+        e[f"b_in_{m}"] = rn(D, std=0.02)
+        e[f"w_out_{m}"] = rn(c, D, std=0.02, dtype=torch.bfloat16)
+        e[f"b_out_{m}"] = rn(c, std=0.02, dtype=torch.bfloat16)
+        e[f"mod_out_{m}"] = rn(2, D, std=0.1)
+    return e
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -309,15 +335,32 @@ def run_ours(args, rank, world, local_rank):
     ids = list(range(n_blocks))
     gz = torch.Generator(device=dev)
     gz.manual_seed(wl.seed + 7 + 1000 * rank)
-    z0 = torch.randn(N, D, generator=gz, device=dev, dtype=torch.float32)
-    z = z0.clone()
-    ring = torch.zeros(2, N, D, dtype=torch.float32, device=dev)
     dt = -0.125
     stream = torch.cuda.current_stream()
+    if wl.extra.get("ends"):
+        # both ends: latents of the two modalities, patch projections and output heads
+        cv, ca = wl.extra["c_video"], wl.extra["c_audio"]
+        ends = make_ends(torch, shape, cv, ca, wl.seed + 2000 + 1000 * rank, dev)
+        z0 = torch.randn(shape.n_video * cv + shape.n_audio * ca, generator=gz, device=dev,
+                         dtype=torch.float32)
+        z = z0.clone()
+        zv = z[:shape.n_video * cv].view(shape.n_video, cv)
+        za = z[shape.n_video * cv:].view(shape.n_audio, ca)
+        rv = torch.zeros(2, shape.n_video, cv, dtype=torch.float32, device=dev)
+        ra = torch.zeros(2, shape.n_audio, ca, dtype=torch.float32, device=dev)
 
-    def step():
-        h3.denoise_step(cs, blocks, ids, z, ring, True, (1.0, 0.0, 0.0, dt), 0, ws,
-                        stream=stream.cuda_stream)
+        def step():
+            h3.sample_step(cs, ends, blocks, ids, zv, za, rv, ra, None, h3.H3DIT_PASS_FRESH,
+                           (1.0, 0.0, 0.0, dt), (1.0, 0.0, 0.0, dt), 0, ws,
+                           stream=stream.cuda_stream)
+    else:
+        z0 = torch.randn(N, D, generator=gz, device=dev, dtype=torch.float32)
+        z = z0.clone()
+        ring = torch.zeros(2, N, D, dtype=torch.float32, device=dev)
+
+        def step():
+            h3.denoise_step(cs, blocks, ids, z, ring, True, (1.0, 0.0, 0.0, dt), 0, ws,
+                            stream=stream.cuda_stream)
 
     def barrier():
         if world > 1:
@@ -422,6 +465,11 @@ def run_ours(args, rank, world, local_rank):
                                    if shape.video_grid else
                                    f"{shape.n_video_tiles} slices of 64 rows"),
                    "dt": dt, "parallelism": f"replicas x{world}",
+                   "step": ("sampler step on the modality latents: fp32 patch projections, "
+                            "blocks, final AdaLN + output heads with the Euler update"
+                            if wl.extra.get("ends") else
+                            "denoiser step on hidden-width latents: bf16(z), blocks, "
+                            "z += dt x_L"),
                    "l2": f"inputs larger than L2 (each block reads its own "
                          f"{block_weight_bytes(shape) / 1e6:.0f} MB of weights)"},
         "s_per_forward": ms_max / K / 1e3 * (50 / n_blocks),
@@ -435,7 +483,7 @@ def run_ours(args, rank, world, local_rank):
     }
     if e2e_ms is not None:
         out["e2e"] = {"value": rows_blocks / (e2e_ms / 1e3), "unit": UNIT,
-                      "h2d_bytes_per_step": N * D * 4, "d2h_bytes_per_step": N * D * 4}
+                      "h2d_bytes_per_step": z.numel() * 4, "d2h_bytes_per_step": z.numel() * 4}
     if not args.no_cpu_baseline and world == 1:
         out["cpu_baseline"] = cpu_baseline(shape)
         out["cpu_baseline"].pop("s_per_block")

@@ -224,6 +224,69 @@ h3dit_status h3dit_denoise_step(const h3dit_shape* shape, const h3dit_block_weig
                                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Both ends of the denoiser: the modality patch projections into the packed
+ * hidden rows and the final per-modality AdaLN + narrow output heads (h3.c
+ * README: fp32 96 -> 5,376 video and 32 -> 5,376 audio patch projections with
+ * fp32 sums rounded to bf16; final audio / video AdaLN on their slices of the
+ * residual stream; narrow bf16 output heads).  D = shape->hidden.
+ *   c_video, c_audio: latent channels per video / audio row (each a multiple of
+ *     32, at most 128; the pages' model: 96 and 32)
+ *   w_in_video fp32 [c_video, D] INPUT-major (row j: the weights of input
+ *     channel j for every hidden column), b_in_video fp32 [D]; same for audio
+ *   w_out_video bf16 [c_video, D] (output-major), b_out_video bf16 [c_video];
+ *     same for audio
+ *   mod_out_video, mod_out_audio fp32 [2, D]: shift, scale of the final AdaLN
+ *   text bf16 [n_text, D]: the text rows (encoder output; constant over steps)
+ * All device pointers, 16-byte aligned; audio pointers may be NULL when
+ * n_audio == 0 and text when n_text == 0.
+ */
+typedef struct {
+  int c_video, c_audio;
+  const float *w_in_video, *b_in_video;
+  const float *w_in_audio, *b_in_audio;
+  const void *w_out_video, *b_out_video;
+  const void *w_out_audio, *b_out_audio;
+  const float *mod_out_video, *mod_out_audio;
+  const void *text;
+} h3dit_ends;
+
+#define H3DIT_PASS_FRESH       0  /* run the blocks                                   */
+#define H3DIT_PASS_EXTRAPOLATE 1  /* whole-velocity reuse: extrapolate, no model work */
+#define H3DIT_PASS_CORE_REUSE  2  /* patch-in and heads fresh, the blocks' residual   */
+                                  /* held from the last fresh pass                    */
+
+/*
+ * h3dit_sample_step -- one sampler step on the modality latents, both ends
+ * included (h3.c README: sampler paragraph -- video and audio on independent
+ * schedules, whole-velocity reuse; core reuse -- the transformer residual held
+ * while the patch projection and the timestep-aware head are refreshed; the
+ * two reuse modes exclude each other).
+ *   z_video fp32 [n_video, c_video], z_audio fp32 [n_audio, c_audio]: latents,
+ *     updated in place; video rows in the library's row order (see
+ *     h3dit_video_order)
+ *   v_ring_video fp32 [2, n_video, c_video], v_ring_audio fp32 [2, n_audio,
+ *     c_audio]: the last two fresh velocities (ring slot n_fresh_so_far % 2)
+ *   core_residual fp32 [N, D] or NULL: written by a FRESH pass (x_L - x_0),
+ *     read by a CORE_REUSE pass
+ *   pass FRESH / CORE_REUSE:
+ *     x_0 = [text; bf16(z_audio W_in_a + b); bf16(z_video W_in_v + b)]
+ *     FRESH: x_L = blocks(x_0); residual <- x_L - x_0 when given
+ *     CORE_REUSE: x_L = bf16(x_0 + residual)
+ *     per modality m: h = bf16(rms(x_L rows of m)(1 + scale_m) + shift_m),
+ *     v = h W_out_m^T + b (fp32 sums), z += dt_m v; FRESH also stores v in
+ *     the ring
+ *   pass EXTRAPOLATE: per modality as in h3dit_denoise_step (fresh == 0)
+ *   video, audio: the two modalities' schedules (HOST structs).
+ */
+h3dit_status h3dit_sample_step(const h3dit_shape* shape, const h3dit_ends* ends,
+                               const h3dit_block_weights* blocks, const int* block_ids,
+                               int n_blocks, float* z_video, float* z_audio,
+                               float* v_ring_video, float* v_ring_audio, float* core_residual,
+                               int pass, const h3dit_schedule* video,
+                               const h3dit_schedule* audio, int n_fresh_so_far,
+                               void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * h3dit_select_blocks -- layer thinning (host only, no GPU).
  * h3.c README layer-thinning paragraph: rank the blocks' AdaLN gates and keep
  * the first and last blocks.  score_b = ||gate1_b||_2 + ||gate2_b||_2 in

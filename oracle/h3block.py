@@ -34,6 +34,7 @@ __all__ = [
     "attention_layer", "qkv_heads", "block_forward", "block_forward_rows", "euler_update",
     "extrapolate",
     "fresh_steps", "sigma_schedule", "denoise_forward", "denoise_loop", "thin_layers",
+    "patch_in", "output_head", "sample_x0", "sample_heads", "sample_step", "sample_loop",
 ]
 
 
@@ -724,6 +725,111 @@ def denoise_loop(z, blocks: list, shape, n_steps: int, reuse: int, block_ids=Non
                 v = va
             z = euler_update(z, v, dtv, dtp, P)
     return {"z": z, "fresh": sorted(fresh)}
+
+
+# ---------------------------------------------------------------------------
+# Both ends of the denoiser (h3.c README: fp32 96 -> 5,376 video and 32 -> 5,376
+# audio patch projections rounded to bf16; final audio / video AdaLN on their
+# slices of the residual stream; narrow bf16 output heads; core reuse holds the
+# transformer residual while the patch projection and the head are refreshed)
+# ---------------------------------------------------------------------------
+
+def patch_in(z, w_in, b_in) -> np.ndarray:
+    """x = bf16(z w_in + b_in): w_in input-major [c, D] (fp32 on the pages; exact sums
+    here), the result rounded to bf16 as it enters the hidden rows."""
+    return bf16(np.asarray(z, np.float64) @ np.asarray(w_in, np.float64)
+                + np.asarray(b_in, np.float64))
+
+
+def output_head(x_rows, mod2, w_out, b_out, eps: float = 1e-6) -> np.ndarray:
+    """Final AdaLN then the narrow head: v = bf16(rms(x)(1 + scale) + shift) W_out^T + b,
+    returned as fp32 (the latents' type).  Reading: the final AdaLN has the block
+    norms' form with its own (shift, scale) table per modality."""
+    mod2 = np.asarray(mod2, np.float64)
+    h = rms_modulate(x_rows, mod2[0], mod2[1], eps)
+    return f32(linear(h, w_out, b_out))
+
+
+def sample_x0(z_video, z_audio, ends: dict, shape) -> np.ndarray:
+    """Packed rows x_0 = [text; patch_in(audio); patch_in(video)] (video rows in the
+    order of z_video)."""
+    parts = [np.asarray(ends["text"], np.float64).reshape(shape.n_text, shape.hidden)]
+    if shape.n_audio:
+        parts.append(patch_in(z_audio, ends["w_in_audio"], ends["b_in_audio"]))
+    parts.append(patch_in(z_video, ends["w_in_video"], ends["b_in_video"]))
+    return np.concatenate(parts, axis=0)
+
+
+def sample_heads(xL, ends: dict, shape) -> tuple:
+    """(v_video, v_audio) from the last hidden rows."""
+    P, T = shape.n_prefix, shape.n_text
+    vv = output_head(xL[P:], ends["mod_out_video"], ends["w_out_video"], ends["b_out_video"],
+                     shape.rms_eps)
+    va = (output_head(xL[T:P], ends["mod_out_audio"], ends["w_out_audio"], ends["b_out_audio"],
+                      shape.rms_eps) if shape.n_audio else np.zeros((0, 0)))
+    return vv, va
+
+
+def sample_step(z_video, z_audio, ends: dict, blocks: list, shape, kind: str, dt_video: float,
+                dt_audio: float, block_ids=None, residual=None) -> dict:
+    """One sampler step on the modality latents.  kind "fresh": x_L = blocks(x_0) and the
+    residual x_L - x_0 (fp32) is returned; kind "core": x_L = bf16(x_0 + residual).
+    Then per modality v = head(x_L rows), z' = fp32(z + dt v)."""
+    x0 = sample_x0(z_video, z_audio, ends, shape)
+    if kind == "fresh":
+        ids = list(range(len(blocks))) if block_ids is None else list(block_ids)
+        x = x0
+        for b in ids:
+            x = block_forward(x, blocks[b], shape)["x2"]
+        res = f32(x - x0)
+    elif kind == "core":
+        res = residual
+        x = bf16(f32(x0 + np.asarray(residual, np.float64)))
+    else:
+        raise ValueError(kind)
+    vv, va = sample_heads(x, ends, shape)
+    zv = f32(np.asarray(z_video, np.float64) + dt_video * vv)
+    za = f32(np.asarray(z_audio, np.float64) + dt_audio * va) if shape.n_audio else z_audio
+    return {"z_video": zv, "z_audio": za, "v_video": vv, "v_audio": va, "residual": res,
+            "x0": x0, "xL": x}
+
+
+def sample_loop(z_video, z_audio, ends: dict, blocks: list, shape, n_steps: int,
+                reuse: int = 1, core_reuse: int = 1, block_ids=None, sig_video=None,
+                sig_audio=None) -> dict:
+    """A sampler run on the modality latents.  Passes that run the blocks follow
+    ``fresh_steps`` of whichever reuse is on; between them whole-velocity reuse
+    extrapolates each modality on its own schedule, and core reuse applies the held
+    residual with fresh patch projections and heads.  The two reuse modes exclude each
+    other (h3.c README)."""
+    assert reuse == 1 or core_reuse == 1, "whole-velocity and core reuse exclude each other"
+    sv = sigma_schedule(n_steps) if sig_video is None else np.asarray(sig_video, np.float64)
+    sa = sv if sig_audio is None else np.asarray(sig_audio, np.float64)
+    fresh = set(fresh_steps(n_steps, max(reuse, core_reuse)))
+    zv, za = np.asarray(z_video, np.float64), np.asarray(z_audio, np.float64)
+    hist, res = [], None
+    for i in range(n_steps):
+        dv, da = sv[i + 1] - sv[i], sa[i + 1] - sa[i]
+        if i in fresh:
+            r = sample_step(zv, za, ends, blocks, shape, "fresh", dv, da, block_ids)
+            hist.append((i, r["v_video"], r["v_audio"]))
+            res = r["residual"]
+            zv, za = r["z_video"], r["z_audio"]
+        elif core_reuse > 1:
+            r = sample_step(zv, za, ends, blocks, shape, "core", dv, da, block_ids, res)
+            zv, za = r["z_video"], r["z_audio"]
+        else:
+            ia, vva, vaa = hist[-1]
+            if len(hist) > 1:
+                ib, vvb, vab = hist[-2]
+                vv = extrapolate(vva, vvb, sv[i], sv[ia], sv[ib])
+                va = extrapolate(vaa, vab, sa[i], sa[ia], sa[ib]) if shape.n_audio else vaa
+            else:
+                vv, va = vva, vaa
+            zv = f32(zv + dv * np.asarray(vv, np.float64))
+            if shape.n_audio:
+                za = f32(za + da * np.asarray(va, np.float64))
+    return {"z_video": zv, "z_audio": za, "fresh": sorted(fresh)}
 
 
 def thin_layers(mods, keep: int) -> list:

@@ -212,3 +212,29 @@ def hidden_rows(shape: BlockShape, seed: int) -> np.ndarray:
 def latents(shape: BlockShape, seed: int) -> np.ndarray:
     """Denoiser latents z, fp32 [N, D] ~ N(0, 1)."""
     return normal(seed, "z", (shape.n_rows, shape.hidden)).astype(np.float32)
+
+
+def ends_weights(shape: BlockShape, seed: int, c_video: int = 96, c_audio: int = 32) -> dict:
+    """Both ends of the denoiser for ``shape``: patch projections (fp32, input-major
+    [c, D], weights ~ N(0, 0.1^2), biases ~ N(0, 0.02^2)), final AdaLN tables (fp32
+    [2, D] ~ N(0, 0.1^2): shift, scale), output heads (bf16 [c, D] and [c], ~ N(0, 0.02^2))
+    and the text rows (bf16 [n_text, D] ~ N(0, 1)).  96 and 32 are the pages' video and
+    audio latent widths."""
+    D = shape.hidden
+    out = {"c_video": c_video, "c_audio": c_audio}
+    for m, c in (("video", c_video), ("audio", c_audio)):
+        out[f"w_in_{m}"] = normal(seed, f"ends.w_in_{m}", (c, D), std=0.1).astype(np.float32)
+        out[f"b_in_{m}"] = normal(seed, f"ends.b_in_{m}", (D,), std=0.02).astype(np.float32)
+        out[f"w_out_{m}"] = normal_bf16(seed, f"ends.w_out_{m}", (c, D), std=0.02)
+        out[f"b_out_{m}"] = normal_bf16(seed, f"ends.b_out_{m}", (c,), std=0.02)
+        out[f"mod_out_{m}"] = normal(seed, f"ends.mod_out_{m}", (2, D), std=0.1).astype(np.float32)
+    out["text"] = normal_bf16(seed, "ends.text", (shape.n_text, D))
+    return out
+
+
+def modality_latents(shape: BlockShape, seed: int, c_video: int = 96, c_audio: int = 32):
+    """Latents of the two modalities, fp32 ~ N(0, 1): video [n_video, c_video] (raster
+    row order), audio [n_audio, c_audio]."""
+    zv = normal(seed, "z.video", (shape.n_video, c_video)).astype(np.float32)
+    za = normal(seed, "z.audio", (shape.n_audio, c_audio)).astype(np.float32)
+    return zv, za

@@ -145,8 +145,17 @@ FORWARD_RECEIPT = Workload(
     n_blocks=50, extra={"dt": -0.125, "forward": True},
 )
 
+SAMPLE_RECEIPT = Workload(
+    "sample50_15435_cubes_d5376_swiglu", 10, RECEIPT_SHAPE,
+    "one fresh sampler step on the modality latents of the receipt sequence: fp32 patch "
+    "projections (96 -> 5,376 video, 32 -> 5,376 audio), 50 blocks of the pages' shape, "
+    "final AdaLN and output heads with the Euler update, dt = -1/8",
+    n_blocks=50, extra={"dt": -0.125, "forward": True, "ends": True, "c_video": 96,
+                        "c_audio": 32},
+)
+
 CONFIGS = [ATTN_TINY, BLOCK_4K, BLOCK_15K, FORWARD_50, LOOP_4K, BLOCK_PAGES, FORWARD_PAGES,
-           BLOCK_RECEIPT, FORWARD_RECEIPT]
+           BLOCK_RECEIPT, FORWARD_RECEIPT, SAMPLE_RECEIPT]
 
 
 def config_by_name(name: str) -> Workload:

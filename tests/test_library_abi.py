@@ -150,3 +150,32 @@ def test_tile_spans_and_video_order_match_oracle_tiles(h3, grid):
     for i, rows in enumerate(want):
         lib_rows = P + order[first[i] - P:first[i] - P + nrows[i]]
         assert np.array_equal(lib_rows, rows), i
+
+
+def test_sample_step_refuses_bad_arguments_on_host(h3):
+    import ctypes
+    lib = h3.lib()
+    s = h3.make_shape(S.CONFIGS[1].shape)
+    need = h3.workspace_bytes(s)
+    fake = 4096  # aligned, never dereferenced: every case fails before a launch
+    good = dict(c_video=96, c_audio=32, **{n: fake for n, _ in h3.Ends._fields_[2:]})
+    sv = h3.Schedule(1.0, 0.0, 0.0, -0.125)
+
+    def call(ends, pass_kind=0, z=fake, ws_bytes=need, nf=0, res=fake, sched=sv):
+        e = h3.make_ends(ends)
+        return lib.h3dit_sample_step(ctypes.byref(s), ctypes.byref(e), None, None, 0, z, fake,
+                                     fake, fake, res, pass_kind,
+                                     ctypes.byref(sched) if sched is not None else None,
+                                     ctypes.byref(sv), nf, fake, ws_bytes, None)
+
+    assert call(dict(good, c_video=100)) == 2             # latent width not a multiple of 32
+    assert call(dict(good, c_audio=160)) == 2             # wider than 128
+    assert call(dict(good, w_out_video=None)) == 1        # missing head
+    assert call(dict(good, b_in_audio=fake + 4)) == 3     # misaligned
+    assert call(good, pass_kind=7) == 1                   # unknown pass
+    assert call(good, z=None) == 1
+    assert call(good, ws_bytes=need - 256) == 4
+    assert call(good, pass_kind=2, res=None) == 1         # core reuse needs the residual
+    assert call(good, pass_kind=1, nf=0) == 1             # nothing to extrapolate from
+    assert call(good, pass_kind=0) == 1                   # fresh pass without blocks array
+    assert call(good, sched=None) == 1

@@ -640,6 +640,74 @@ def test_denoise_loop_orchestration_without_blocks():
     assert abs((sig[3] - sig[2]) / (sig[2] - sig[0]) - 0.5) < 1e-15  # v = v2 + 0.5 (v2 - v0)
 
 
+# --------------------------------------------------------------------------- both ends
+def test_patch_in_small_integers_brute_force():
+    z = rng.integers(-4, 5, (5, 32)).astype(np.float64)
+    w = rng.integers(-4, 5, (32, 16)).astype(np.float64)
+    b = rng.integers(-4, 5, 16).astype(np.float64)
+    got = O.patch_in(z, w, b)
+    for r in range(5):
+        for c in range(16):
+            acc = b[c]
+            for j in range(32):
+                acc += z[r, j] * w[j, c]  # input-major weights: w[j, c]
+            assert got[r, c] == O.bf16(acc)
+
+
+def test_output_head_constant_rows():
+    # scale = -1 turns every normalised row into the shift, so every velocity row is
+    # W_out bf16(shift) + b
+    x = rng.standard_normal((6, 16))
+    mod2 = np.stack([rng.standard_normal(16), -np.ones(16)])
+    w = O.bf16(rng.standard_normal((4, 16)))
+    b = O.bf16(rng.standard_normal(4))
+    v = O.output_head(x, mod2, w, b)
+    want = O.f32(w @ O.bf16(mod2[0]) + b)
+    assert np.array_equal(v, np.tile(want, (6, 1)))
+
+
+def _ends_case(blocks=2):
+    shape = _tiny_shape(n_text=8, n_audio=56, hidden=64, prefix_mod=True)
+    ends = S.ends_weights(shape, 5, c_video=32, c_audio=32)
+    ends = {k: (S.bf16_bits_to_f64(v) if isinstance(v, np.ndarray) and v.dtype == np.uint16
+                else v) for k, v in ends.items()}
+    zv, za = S.modality_latents(shape, 6, 32, 32)
+    return shape, ends, [_weights(shape, 10 + i) for i in range(blocks)], zv, za
+
+
+def test_core_reuse_reproduces_the_fresh_velocity():
+    # the held residual applied to the same x_0 gives back x_L exactly, so the velocity
+    # and the step are the fresh pass's
+    shape, ends, blocks, zv, za = _ends_case()
+    f = O.sample_step(zv, za, ends, blocks, shape, "fresh", -0.125, -0.25)
+    c = O.sample_step(zv, za, ends, blocks, shape, "core", -0.125, -0.25, residual=f["residual"])
+    assert np.array_equal(c["xL"], f["xL"])
+    for k in ("v_video", "v_audio", "z_video", "z_audio"):
+        assert np.array_equal(c[k], f[k])
+    assert not np.array_equal(f["xL"], f["x0"])
+
+
+def test_sample_loop_core_reuse_without_blocks_equals_every_pass_fresh():
+    shape, ends, _, zv, za = _ends_case()
+    a = O.sample_loop(zv, za, ends, [], shape, 6, core_reuse=3)
+    b = O.sample_loop(zv, za, ends, [], shape, 6)
+    assert a["fresh"] == [0, 3, 5]
+    assert np.array_equal(a["z_video"], b["z_video"]) and np.array_equal(a["z_audio"], b["z_audio"])
+
+
+def test_sample_step_without_blocks_is_the_heads_of_the_patches():
+    # no blocks: x_L = x_0, so each modality's velocity is its head over its own patch rows
+    shape, ends, _, zv, za = _ends_case()
+    r = O.sample_step(zv, za, ends, [], shape, "fresh", -0.125, -0.25)
+    xv = O.patch_in(zv, ends["w_in_video"], ends["b_in_video"])
+    xa = O.patch_in(za, ends["w_in_audio"], ends["b_in_audio"])
+    assert np.array_equal(r["v_video"], O.output_head(xv, ends["mod_out_video"],
+                                                      ends["w_out_video"], ends["b_out_video"]))
+    assert np.array_equal(r["v_audio"], O.output_head(xa, ends["mod_out_audio"],
+                                                      ends["w_out_audio"], ends["b_out_audio"]))
+    assert np.array_equal(r["z_video"], (zv + np.float32(-0.125) * r["v_video"].astype(np.float32)))
+
+
 def test_silu_closed_forms():
     assert O.silu(0.0) == 0.0
     x = rng.standard_normal(1000) * 4
