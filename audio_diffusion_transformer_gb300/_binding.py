@@ -19,6 +19,7 @@ H3DIT_QK_NORM = 0x1
 H3DIT_ROPE = 0x2
 H3DIT_POOLED = 0x4
 H3DIT_SWIGLU = 0x8
+H3DIT_TOKEN_REDUCTION = 0x10
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported or inconsistent shape",
           3: "pointer not 16-byte aligned", 4: "workspace missing or too small",
@@ -60,6 +61,10 @@ class Ends(ctypes.Structure):
          "w_out_audio", "b_out_audio", "mod_out_video", "mod_out_audio", "text")]
 
 
+class Reduction(ctypes.Structure):
+    _fields_ = [("first", ctypes.c_int), ("last", ctypes.c_int)]
+
+
 H3DIT_PASS_FRESH, H3DIT_PASS_EXTRAPOLATE, H3DIT_PASS_CORE_REUSE = 0, 1, 2
 
 _lib = None
@@ -84,8 +89,9 @@ _SIGS = [
     ("h3dit_sample_step", ctypes.c_int,
      [ctypes.POINTER(Shape), ctypes.POINTER(Ends), ctypes.POINTER(BlockWeights),
       ctypes.POINTER(ctypes.c_int), ctypes.c_int] + [ctypes.c_void_p] * 5
-     + [ctypes.c_int, ctypes.POINTER(Schedule), ctypes.POINTER(Schedule), ctypes.c_int,
-        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+     + [ctypes.POINTER(Reduction), ctypes.c_int, ctypes.POINTER(Schedule),
+        ctypes.POINTER(Schedule), ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+        ctypes.c_void_p]),
     ("h3dit_select_blocks", ctypes.c_int,
      [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     ("h3dit_tile_spans", ctypes.c_int,
@@ -135,7 +141,8 @@ def make_shape(s, flags=None) -> Shape:
         flags = ((H3DIT_QK_NORM if getattr(s, "qk_norm", False) else 0)
                  | (H3DIT_ROPE if getattr(s, "rope", False) else 0)
                  | (H3DIT_POOLED if getattr(s, "pooled", False) else 0)
-                 | (H3DIT_SWIGLU if getattr(s, "mlp", "gelu") == "swiglu" else 0))
+                 | (H3DIT_SWIGLU if getattr(s, "mlp", "gelu") == "swiglu" else 0)
+                 | (H3DIT_TOKEN_REDUCTION if getattr(s, "token_reduction", False) else 0))
     grid = getattr(s, "video_grid", None) or (0, 0, 0)
     cube = getattr(s, "cube", None) if getattr(s, "video_grid", None) else None
     cube = cube or (0, 0, 0)
@@ -248,18 +255,21 @@ def make_ends(ends: dict) -> Ends:
 
 def sample_step(shape: Shape, ends: dict, blocks: list, block_ids, z_video, z_audio,
                 v_ring_video, v_ring_audio, core_residual, pass_kind: int, video, audio,
-                n_fresh_so_far: int, workspace, stream=None):
+                n_fresh_so_far: int, workspace, stream=None, reduction=None):
     """One sampler step on the modality latents (both ends included).  ``video`` and
     ``audio`` are (sigma_i, sigma_a, sigma_b, dt) tuples; ``pass_kind`` one of
-    H3DIT_PASS_FRESH / _EXTRAPOLATE / _CORE_REUSE."""
+    H3DIT_PASS_FRESH / _EXTRAPOLATE / _CORE_REUSE; ``reduction`` = (first, last) block
+    positions of token reduction, or None."""
     arr = (BlockWeights * max(1, len(blocks)))(*[block_weights(b) for b in blocks])
     ids = (ctypes.c_int * max(1, len(block_ids)))(*[int(i) for i in block_ids])
     e = make_ends(ends)
     sv = Schedule(*[float(x) for x in video])
     sa = Schedule(*[float(x) for x in (audio if audio is not None else video)])
+    red = Reduction(*[int(x) for x in reduction]) if reduction is not None else None
     _check("h3dit_sample_step", lib().h3dit_sample_step(
         ctypes.byref(shape), ctypes.byref(e), arr, ids, len(block_ids), _ptr(z_video),
         _ptr(z_audio), _ptr(v_ring_video), _ptr(v_ring_audio), _ptr(core_residual),
+        ctypes.byref(red) if red is not None else None,
         int(pass_kind), ctypes.byref(sv), ctypes.byref(sa), int(n_fresh_so_far),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 

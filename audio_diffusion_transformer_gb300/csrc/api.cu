@@ -108,8 +108,15 @@ inline size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 struct Dims {
   int N, P, V, Tv, ksel, D, H, d, A, F;
   TileGeom geom;
-  bool block;  // hidden / mlp widths given
+  bool block;   // hidden / mlp widths given
+  bool reduce;  // token-reduction buffers reserved
 };
+
+#define H3_TRY_SHAPE(expr)                    \
+  do {                                        \
+    h3dit_status _st = (expr);                \
+    if (_st != H3DIT_OK) return _st;          \
+  } while (0)
 
 // The video tile geometry of a shape; false if the grid or cube fields are inconsistent.
 bool make_geom(const h3dit_shape* s, TileGeom* g) {
@@ -163,6 +170,7 @@ h3dit_status check_attn(const h3dit_shape* s, Dims* o) {
   o->D = s->hidden;
   o->F = s->mlp_width;
   o->block = false;
+  o->reduce = false;
   return H3DIT_OK;
 }
 
@@ -179,12 +187,25 @@ h3dit_status check_block(const h3dit_shape* s, Dims* o) {
   }
   if ((s->flags & H3DIT_ROPE) && (s->rope_theta <= 1.0f)) return H3DIT_ERR_ARG;
   o->block = true;
+  o->reduce = (s->flags & H3DIT_TOKEN_REDUCTION) != 0;
+  if (o->reduce && (o->geom.gt == 0 || o->geom.gw < 2)) return H3DIT_ERR_SHAPE;
+  return H3DIT_OK;
+}
+
+// The shape of the token-reduced section: the same rows but video t x h x ceil(w/2).
+h3dit_status reduced_dims(const h3dit_shape* s, h3dit_shape* rs, Dims* rm) {
+  *rs = *s;
+  rs->video_w = (s->video_w + 1) / 2;
+  rs->n_video = s->video_t * s->video_h * rs->video_w;
+  rs->flags &= ~H3DIT_TOKEN_REDUCTION;
+  H3_TRY_SHAPE(check_block(rs, rm));
+  rm->geom.gw_full = s->video_w;
   return H3DIT_OK;
 }
 
 // Workspace layout (all offsets 256-byte aligned).
 struct Ws {
-  size_t status, q, k, v, g, o, u, h, x, rope, means, scores, idx, pooled, total;
+  size_t status, q, k, v, g, o, u, h, x, rope, means, scores, idx, pooled, bypass, base, total;
 };
 
 Ws plan(const Dims& m) {
@@ -215,6 +236,11 @@ Ws plan(const Dims& m) {
     w.rope = take((size_t)m.N * (m.d / 2) * 8);
   } else {
     w.u = w.h = w.x = w.rope = 0;
+  }
+  w.bypass = w.base = 0;
+  if (m.reduce) {  // full-resolution bypass and the pooled rows' baselines
+    w.bypass = take((size_t)m.N * m.D * 2);
+    w.base = take((size_t)m.geom.gt * m.geom.gh * ((m.geom.gw + 1) / 2) * m.D * 2);
   }
   w.total = off;
   return w;
@@ -623,9 +649,10 @@ h3dit_status h3dit_sample_step(const h3dit_shape* shape, const h3dit_ends* ends,
                                const h3dit_block_weights* blocks, const int* block_ids,
                                int n_blocks, float* z_video, float* z_audio,
                                float* v_ring_video, float* v_ring_audio, float* core_residual,
-                               int pass, const h3dit_schedule* video,
-                               const h3dit_schedule* audio, int n_fresh_so_far,
-                               void* workspace, size_t ws_bytes, void* stream) {
+                               const h3dit_reduction* reduction, int pass,
+                               const h3dit_schedule* video, const h3dit_schedule* audio,
+                               int n_fresh_so_far, void* workspace, size_t ws_bytes,
+                               void* stream) {
   Dims m;
   H3_TRY(check_block(shape, &m));
   H3_TRY(check_ends(shape, ends));
@@ -672,6 +699,17 @@ h3dit_status h3dit_sample_step(const h3dit_shape* shape, const h3dit_ends* ends,
     return H3DIT_OK;
   }
 
+  // token reduction over block positions [red_first, red_last)
+  int red_first = -1, red_last = -1;
+  h3dit_shape rshape;
+  Dims rm;
+  if (pass == H3DIT_PASS_FRESH && reduction && reduction->first >= 0 &&
+      reduction->first < reduction->last && reduction->first < n_blocks) {
+    if (!m.reduce) return H3DIT_ERR_SHAPE;  // buffers not reserved (H3DIT_TOKEN_REDUCTION)
+    H3_TRY(reduced_dims(shape, &rshape, &rm));
+    red_first = reduction->first;
+    red_last = reduction->last < n_blocks ? reduction->last : n_blocks;
+  }
   if (pass == H3DIT_PASS_FRESH) {
     if (!blocks || (n_blocks > 0 && !block_ids) || n_blocks < 0) return H3DIT_ERR_ARG;
     for (int i = 0; i < n_blocks; ++i) {
@@ -694,22 +732,60 @@ h3dit_status h3dit_sample_step(const h3dit_shape* shape, const h3dit_ends* ends,
                                             shape->rope_theta, m.geom, st), 1)));
     }
   }
+  __nv_bfloat16* cur = x;  // the full-resolution rows (the bypass after a restore)
   if (pass == H3DIT_PASS_FRESH) {
-    for (int i = 0; i < n_blocks; ++i)
-      H3_TRY(run_block(shape, m, ws, workspace, &blocks[block_ids[i]], x, true, st));
+    __nv_bfloat16* bypass = m.reduce ? at<__nv_bfloat16>(workspace, ws.bypass) : nullptr;
+    __nv_bfloat16* base = m.reduce ? at<__nv_bfloat16>(workspace, ws.base) : nullptr;
+    float2* rope = at<float2>(workspace, ws.rope);
+    const bool use_rope = (shape->flags & H3DIT_ROPE) != 0;
+    for (int i = 0; i < n_blocks; ++i) {
+      if (i == red_first) {  // pool: bypass <- x; x <- [prefix rows; pooled video rows]
+        StageScope sc(H3DIT_STAGE_SAMPLER, st);
+        if (cudaMemcpyAsync(bypass, x, nd * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+          return H3DIT_ERR_CUDA;
+        H3_TRY(cu(counted(launch_token_pool(bypass, x, base, m.geom, rm.geom, m.D, st), 1)));
+        if (use_rope)
+          H3_TRY(cu(counted(launch_rope_table(rope, rm.N, rm.d, shape->rope_theta, rm.geom, st),
+                            1)));
+      }
+      if (i == red_last) {  // restore into the bypass, which holds the full rows from here
+        StageScope sc(H3DIT_STAGE_SAMPLER, st);
+        if (cudaMemcpyAsync(bypass, x, (size_t)m.P * m.D * 2, cudaMemcpyDeviceToDevice, st) !=
+            cudaSuccess)
+          return H3DIT_ERR_CUDA;
+        H3_TRY(cu(counted(launch_token_restore(bypass, x, base, m.geom, rm.geom, m.D, st), 1)));
+        if (use_rope)
+          H3_TRY(cu(counted(launch_rope_table(rope, m.N, m.d, shape->rope_theta, m.geom, st),
+                            1)));
+        cur = bypass;
+      }
+      const bool reduced = red_first >= 0 && i >= red_first && i < red_last;
+      if (reduced)
+        H3_TRY(run_block(&rshape, rm, ws, workspace, &blocks[block_ids[i]], x, true, st));
+      else
+        H3_TRY(run_block(shape, m, ws, workspace, &blocks[block_ids[i]], cur, true, st));
+    }
+    if (red_first >= 0 && red_last == n_blocks) {  // restore after the last block
+      StageScope sc(H3DIT_STAGE_SAMPLER, st);
+      if (cudaMemcpyAsync(bypass, x, (size_t)m.P * m.D * 2, cudaMemcpyDeviceToDevice, st) !=
+          cudaSuccess)
+        return H3DIT_ERR_CUDA;
+      H3_TRY(cu(counted(launch_token_restore(bypass, x, base, m.geom, rm.geom, m.D, st), 1)));
+      cur = bypass;
+    }
     if (core_residual) {
       StageScope sc(H3DIT_STAGE_SAMPLER, st);
-      H3_TRY(cu(counted(launch_core_residual(x, core_residual, nd, 1, st), 1)));
+      H3_TRY(cu(counted(launch_core_residual(cur, core_residual, nd, 1, st), 1)));
     }
   }
   const bool fresh = pass == H3DIT_PASS_FRESH;
   const size_t slot = (size_t)(n_fresh_so_far % 2);
   StageScope sc(H3DIT_STAGE_SAMPLER, st);
-  H3_TRY(head_pass(m, ws, workspace, x, m.P, m.V, cv, ends->mod_out_video, ends->w_out_video,
+  H3_TRY(head_pass(m, ws, workspace, cur, m.P, m.V, cv, ends->mod_out_video, ends->w_out_video,
                    ends->b_out_video, z_video, fresh ? v_ring_video + slot * nv : nullptr,
                    video->dt, shape->rms_eps, st));
   if (has_audio)
-    H3_TRY(head_pass(m, ws, workspace, x, shape->n_text, shape->n_audio, ca, ends->mod_out_audio,
+    H3_TRY(head_pass(m, ws, workspace, cur, shape->n_text, shape->n_audio, ca, ends->mod_out_audio,
                      ends->w_out_audio, ends->b_out_audio, z_audio,
                      fresh ? v_ring_audio + slot * na : nullptr, audio->dt, shape->rms_eps, st));
   return H3DIT_OK;

@@ -86,6 +86,13 @@ cudaError_t launch_f32_to_bf16(const float* z, __nv_bfloat16* x, size_t n, cudaS
 // x[r, :] = bf16(z[r, :] w + b), z fp32 [rows, c], w fp32 [c, D] (input-major), b fp32 [D]
 cudaError_t launch_patch_in(const float* z, const float* w, const float* b, __nv_bfloat16* x,
                             int rows, int c, int D, cudaStream_t s);
+// token reduction: pooled rows of the reduced grid gr from the full rows (grid gf) into
+// xr (rows P..) and base; restore: full video rows += xr - base of their pair (in place)
+cudaError_t launch_token_pool(const __nv_bfloat16* full, __nv_bfloat16* xr, __nv_bfloat16* base,
+                              const TileGeom& gf, const TileGeom& gr, int D, cudaStream_t s);
+cudaError_t launch_token_restore(__nv_bfloat16* full, const __nv_bfloat16* xr,
+                                 const __nv_bfloat16* base, const TileGeom& gf,
+                                 const TileGeom& gr, int D, cudaStream_t s);
 // mode 0: r = x; 1: r = x - r; 2: x = bf16(x + r)   (n elements, x bf16, r fp32)
 cudaError_t launch_core_residual(__nv_bfloat16* x, float* r, size_t n, int mode, cudaStream_t s);
 // elements [0, n_pre) follow the prefix step dt_p (coef_p), the rest dt (coef)

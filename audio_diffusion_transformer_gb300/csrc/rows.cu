@@ -13,6 +13,9 @@
 //  * f32_to_bf16: the sampler's latents -> the bf16 residual stream.
 //  * patch_in: a modality's fp32 patch projection into its bf16 hidden rows (h3.c
 //    README: fp32 weights, inputs and sums, the result rounded to bf16).
+//  * token_pool / token_restore: token reduction (h3.c README): adjacent horizontal
+//    video tokens pooled into one row with a full-resolution bypass, and each token
+//    restored as its bypass value plus the update its pair received.
 //  * core_residual: the blocks' residual x_L - x_0 kept in fp32, and x_L =
 //    bf16(x_0 + residual) on a core-reuse pass.
 //  * euler_fresh / euler_extrap: v = fp32(x_L), ring store, z += dt * v; or the
@@ -102,16 +105,21 @@ __global__ void rope_table_kernel(float2* cs, int rows, int half, int d, double 
   } else {  // 3-D: pairs [0, mt) time, [mt, mt + ms) height, the rest width
     const int ms = half / 3, mt = half - 2 * ms;
     int tt = p, hh = p, ww = p;  // text and audio rows: the packed index on every axis
-    if (p >= g.P) video_coord(g, p - g.P, &tt, &hh, &ww);
-    int axis_pos, j, m;
-    if (c < mt) {
-      axis_pos = tt, j = c, m = mt;
-    } else if (c < mt + ms) {
-      axis_pos = hh, j = c - mt, m = ms;
-    } else {
-      axis_pos = ww, j = c - mt - ms, m = ms;
+    double wpos = (double)p;
+    if (p >= g.P) {
+      video_coord(g, p - g.P, &tt, &hh, &ww);
+      wpos = (double)ww;
+      // a pooled pair of full-width tokens sits at their mean column
+      if (g.gw_full > 0) wpos = 2 * ww + 1 < g.gw_full ? 2.0 * ww + 0.5 : 2.0 * ww;
     }
-    pos = (double)axis_pos;
+    int j, m;
+    if (c < mt) {
+      pos = (double)tt, j = c, m = mt;
+    } else if (c < mt + ms) {
+      pos = (double)hh, j = c - mt, m = ms;
+    } else {
+      pos = wpos, j = c - mt - ms, m = ms;
+    }
     expo = (double)j / (double)m;
   }
   double sn, cn;
@@ -240,6 +248,64 @@ __global__ void core_residual_kernel(uint2* __restrict__ x, float4* __restrict__
   }
 }
 
+// Token reduction entry: reduced video row i (cube order of the reduced grid gr) is the
+// mean of the full tokens (t, h, 2j) and (t, h, 2j + 1), or the lone last token of an odd
+// row; written to xr row P + i and to the baseline row i.  One CTA per reduced row.
+__global__ void __launch_bounds__(ROW_THREADS)
+    token_pool_kernel(const __nv_bfloat16* __restrict__ full, __nv_bfloat16* __restrict__ xr,
+                      __nv_bfloat16* __restrict__ base, const TileGeom gf, const TileGeom gr,
+                      int D) {
+  const int i = blockIdx.x;
+  int t, h, j;
+  video_coord(gr, i, &t, &h, &j);
+  const bool pair = 2 * j + 1 < gf.gw;
+  const int s0 = video_row_of(gf, t, h, 2 * j);
+  const int s1 = pair ? video_row_of(gf, t, h, 2 * j + 1) : s0;
+  const uint4* a = reinterpret_cast<const uint4*>(full + (size_t)(gf.P + s0) * D);
+  const uint4* b = reinterpret_cast<const uint4*>(full + (size_t)(gf.P + s1) * D);
+  uint4* o = reinterpret_cast<uint4*>(xr + (size_t)(gr.P + i) * D);
+  uint4* q = reinterpret_cast<uint4*>(base + (size_t)i * D);
+  for (int v = threadIdx.x; v < D / 8; v += ROW_THREADS) {
+    const uint4 ua = a[v], ub = b[v];
+    const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+    uint32_t r[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      r[e] = pack_bf16x2((bf16_lo(wa[e]) + bf16_lo(wb[e])) * 0.5f,
+                         (bf16_hi(wa[e]) + bf16_hi(wb[e])) * 0.5f);
+    const uint4 out = make_uint4(r[0], r[1], r[2], r[3]);
+    o[v] = out;
+    q[v] = out;
+  }
+}
+
+// Token reduction exit: full video row k (cube order of gf) becomes
+// bf16(bypass_k + (xr_i - baseline_i)) with i its pair's reduced row.  In place on the
+// bypass.  One CTA per full video row.
+__global__ void __launch_bounds__(ROW_THREADS)
+    token_restore_kernel(__nv_bfloat16* __restrict__ full, const __nv_bfloat16* __restrict__ xr,
+                         const __nv_bfloat16* __restrict__ base, const TileGeom gf,
+                         const TileGeom gr, int D) {
+  const int k = blockIdx.x;
+  int t, h, w;
+  video_coord(gf, k, &t, &h, &w);
+  const int i = video_row_of(gr, t, h, w / 2);
+  uint4* f = reinterpret_cast<uint4*>(full + (size_t)(gf.P + k) * D);
+  const uint4* y = reinterpret_cast<const uint4*>(xr + (size_t)(gr.P + i) * D);
+  const uint4* b0 = reinterpret_cast<const uint4*>(base + (size_t)i * D);
+  for (int v = threadIdx.x; v < D / 8; v += ROW_THREADS) {
+    const uint4 uf = f[v], uy = y[v], ub = b0[v];
+    const uint32_t wf[4] = {uf.x, uf.y, uf.z, uf.w}, wy[4] = {uy.x, uy.y, uy.z, uy.w},
+                   wb[4] = {ub.x, ub.y, ub.z, ub.w};
+    uint32_t r[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      r[e] = pack_bf16x2(bf16_lo(wf[e]) + (bf16_lo(wy[e]) - bf16_lo(wb[e])),
+                         bf16_hi(wf[e]) + (bf16_hi(wy[e]) - bf16_hi(wb[e])));
+    f[v] = make_uint4(r[0], r[1], r[2], r[3]);
+  }
+}
+
 int grid_for(size_t n, int threads) {
   size_t b = (n + threads - 1) / threads;
   const size_t cap = (size_t)num_sms() * 16;
@@ -286,6 +352,21 @@ cudaError_t launch_core_residual(__nv_bfloat16* x, float* r, size_t n, int mode,
   if (n % 4 || mode < 0 || mode > 2) return cudaErrorInvalidValue;
   core_residual_kernel<<<grid_for(n / 4, 256), 256, 0, s>>>(
       reinterpret_cast<uint2*>(x), reinterpret_cast<float4*>(r), n / 4, mode);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_token_pool(const __nv_bfloat16* full, __nv_bfloat16* xr, __nv_bfloat16* base,
+                              const TileGeom& gf, const TileGeom& gr, int D, cudaStream_t s) {
+  if (gr.V <= 0 || D % 8 || gf.gt == 0 || gr.gt == 0) return cudaErrorInvalidValue;
+  token_pool_kernel<<<gr.V, ROW_THREADS, 0, s>>>(full, xr, base, gf, gr, D);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_token_restore(__nv_bfloat16* full, const __nv_bfloat16* xr,
+                                 const __nv_bfloat16* base, const TileGeom& gf,
+                                 const TileGeom& gr, int D, cudaStream_t s) {
+  if (gf.V <= 0 || D % 8 || gf.gt == 0 || gr.gt == 0) return cudaErrorInvalidValue;
+  token_restore_kernel<<<gf.V, ROW_THREADS, 0, s>>>(full, xr, base, gf, gr, D);
   return cudaGetLastError();
 }
 

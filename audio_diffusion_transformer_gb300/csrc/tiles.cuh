@@ -19,6 +19,8 @@ struct TileGeom {
   int gt, gh, gw;  // latent grid; gt == 0 selects the 1-D layout
   int ct, ch, cw;  // cube extents (product = 64)
   int nt, nh, nw;  // cubes along t, h, w
+  int gw_full;     // token reduction: the full width whose horizontal pairs form this
+                   // grid's columns (rotary w = 2j + 0.5, or 2j for a lone last token); 0 = none
 };
 
 __host__ __device__ __forceinline__ int tg_min(int a, int b) { return a < b ? a : b; }
@@ -62,6 +64,16 @@ __host__ __device__ __forceinline__ void video_coord(const TileGeom& g, int v, i
   *tt = a * g.ct + rem / (eh * ew);
   *hh = b * g.ch + (rem / ew) % eh;
   *ww = c * g.cw + rem % ew;
+}
+
+// Row (0 <= row < V, cube order) of the video token at latent (t, h, w).
+__host__ __device__ __forceinline__ int video_row_of(const TileGeom& g, int tt, int hh, int ww) {
+  const int a = tt / g.ct, b = hh / g.ch, c = ww / g.cw;
+  int first, count;
+  tile_span(g, (a * g.nh + b) * g.nw + c, &first, &count);
+  const int eh = tg_min(g.ch, g.gh - b * g.ch);
+  const int ew = tg_min(g.cw, g.gw - c * g.cw);
+  return first - g.P + ((tt - a * g.ct) * eh + (hh - b * g.ch)) * ew + (ww - c * g.cw);
 }
 
 }  // namespace h3

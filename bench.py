@@ -84,6 +84,21 @@ def block_flops(s):
     return gemm, attn
 
 
+def reduced_shape(s):
+    """The token-reduced section's shape: video grid T x H x ceil(W/2)."""
+    T, Hg, Wg = s.video_grid
+    Wr = (Wg + 1) // 2
+    return s.with_(n_video=T * Hg * Wr, video_grid=(T, Hg, Wr), pair_w=Wg, token_reduction=False)
+
+
+def block_shapes(s, n_blocks, reduction):
+    """The shape of every block position of one step."""
+    if not reduction or not (0 <= reduction[0] < reduction[1]) or reduction[0] >= n_blocks:
+        return [s] * n_blocks
+    rs = reduced_shape(s)
+    return [rs if reduction[0] <= b < reduction[1] else s for b in range(n_blocks)]
+
+
 def stage_flops(s):
     N, D, A, F = s.n_rows, s.hidden, s.attn_width, s.mlp_width
     _, attn = block_flops(s)
@@ -349,10 +364,12 @@ def run_ours(args, rank, world, local_rank):
         rv = torch.zeros(2, shape.n_video, cv, dtype=torch.float32, device=dev)
         ra = torch.zeros(2, shape.n_audio, ca, dtype=torch.float32, device=dev)
 
+        red = wl.extra.get("reduction")
+
         def step():
             h3.sample_step(cs, ends, blocks, ids, zv, za, rv, ra, None, h3.H3DIT_PASS_FRESH,
                            (1.0, 0.0, 0.0, dt), (1.0, 0.0, 0.0, dt), 0, ws,
-                           stream=stream.cuda_stream)
+                           stream=stream.cuda_stream, reduction=red)
     else:
         z0 = torch.randn(N, D, generator=gz, device=dev, dtype=torch.float32)
         z = z0.clone()
@@ -420,12 +437,15 @@ def run_ours(args, rank, world, local_rank):
     K = args.steps
     rows_blocks = N * n_blocks * K * world
     value = job_rows_per_s(N * n_blocks * K, world, ms_max)
-    gemm_f, attn_f = block_flops(shape)
-    step_flops = n_blocks * (gemm_f + attn_f)
+    # the shape each block position runs at (token reduction shrinks the video rows)
+    shapes = block_shapes(shape, n_blocks, wl.extra.get("reduction"))
+    step_flops = sum(sum(block_flops(sb)) for sb in shapes)
     pk, pk_kind = peaks()
     peak_tc = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     achieved_total = step_flops * K / (ms_max / 1e3) / 1e12
-    sf = stage_flops(shape)
+    # per-launch flops of each stage, averaged over the block positions
+    sf = {k: sum(stage_flops(sb)[k] for sb in shapes) / len(shapes)
+          for k in stage_flops(shape)}
     # dominant kernel: group the stages by the kernel function that runs them and take the
     # one with the largest total time; achieved = its algorithmic flops / its time
     groups = {"gemm<qkvg>": ["qkvg"], "gemm<gelu>": ["fc1"], "gemm<resid>": ["out_proj", "fc2"],
@@ -465,8 +485,14 @@ def run_ours(args, rank, world, local_rank):
                                    if shape.video_grid else
                                    f"{shape.n_video_tiles} slices of 64 rows"),
                    "dt": dt, "parallelism": f"replicas x{world}",
+                   "rows_per_block": ({"full": N, "reduced": min(sb.n_rows for sb in shapes),
+                                       "reduced_blocks": list(wl.extra["reduction"])}
+                                      if len(set(sb.n_rows for sb in shapes)) > 1 else N),
                    "step": ("sampler step on the modality latents: fp32 patch projections, "
                             "blocks, final AdaLN + output heads with the Euler update"
+                            + (f", token reduction over blocks [{wl.extra['reduction'][0]}, "
+                               f"{wl.extra['reduction'][1]})" if wl.extra.get("reduction")
+                               else "")
                             if wl.extra.get("ends") else
                             "denoiser step on hidden-width latents: bf16(z), blocks, "
                             "z += dt x_L"),

@@ -55,6 +55,8 @@ typedef enum {
 #define H3DIT_POOLED  0x4u   /* pooled branch + gate mix for video rows            */
 #define H3DIT_SWIGLU  0x8u   /* MLP u = silu(h W_gate^T + b_g) * (h W_up^T + b_u)   */
                              /* (else u = gelu(h W1^T + b1)); see w1 below          */
+#define H3DIT_TOKEN_REDUCTION 0x10u /* reserve workspace for token reduction (needs a  */
+                                    /* video grid at least 2 wide); see h3dit_sample_step */
 
 typedef struct {
   int n_text, n_audio, n_video; /* packed row counts, in this order               */
@@ -250,6 +252,23 @@ typedef struct {
   const void *text;
 } h3dit_ends;
 
+/*
+ * Token reduction (h3.c README, token-reduction paragraph): from the block at
+ * position `first` of block_ids up to the one before position `last`, each pair
+ * of horizontally adjacent video tokens (t, h, 2j), (t, h, 2j + 1) runs as one
+ * row, their mean (an odd row's last token runs alone); text and audio rows are
+ * untouched.  The full-resolution rows are kept as a bypass, and before position
+ * `last` every video token returns as its bypass value plus the update its pair's
+ * row received since pooling.  The reduced rows use the grid t x h x ceil(w/2) in
+ * cube order, with rotary width coordinate 2j + 0.5 (2j for a lone token).  The
+ * pages pool after block 3 and restore before block 40 for the first ten noisy
+ * evaluations, before block 30 after that.  Requires H3DIT_TOKEN_REDUCTION in the
+ * shape's flags.
+ */
+typedef struct {
+  int first, last;  /* block_ids positions; no reduction unless first < last, first < n */
+} h3dit_reduction;
+
 #define H3DIT_PASS_FRESH       0  /* run the blocks                                   */
 #define H3DIT_PASS_EXTRAPOLATE 1  /* whole-velocity reuse: extrapolate, no model work */
 #define H3DIT_PASS_CORE_REUSE  2  /* patch-in and heads fresh, the blocks' residual   */
@@ -268,6 +287,7 @@ typedef struct {
  *     c_audio]: the last two fresh velocities (ring slot n_fresh_so_far % 2)
  *   core_residual fp32 [N, D] or NULL: written by a FRESH pass (x_L - x_0),
  *     read by a CORE_REUSE pass
+ *   reduction_or_null: token reduction of a FRESH pass (see h3dit_reduction)
  *   pass FRESH / CORE_REUSE:
  *     x_0 = [text; bf16(z_audio W_in_a + b); bf16(z_video W_in_v + b)]
  *     FRESH: x_L = blocks(x_0); residual <- x_L - x_0 when given
@@ -282,9 +302,10 @@ h3dit_status h3dit_sample_step(const h3dit_shape* shape, const h3dit_ends* ends,
                                const h3dit_block_weights* blocks, const int* block_ids,
                                int n_blocks, float* z_video, float* z_audio,
                                float* v_ring_video, float* v_ring_audio, float* core_residual,
-                               int pass, const h3dit_schedule* video,
-                               const h3dit_schedule* audio, int n_fresh_so_far,
-                               void* workspace, size_t ws_bytes, void* stream);
+                               const h3dit_reduction* reduction_or_null, int pass,
+                               const h3dit_schedule* video, const h3dit_schedule* audio,
+                               int n_fresh_so_far, void* workspace, size_t ws_bytes,
+                               void* stream);
 
 /*
  * h3dit_select_blocks -- layer thinning (host only, no GPU).

@@ -35,6 +35,7 @@ __all__ = [
     "extrapolate",
     "fresh_steps", "sigma_schedule", "denoise_forward", "denoise_loop", "thin_layers",
     "patch_in", "output_head", "sample_x0", "sample_heads", "sample_step", "sample_loop",
+    "rope_coords_pooled", "reduced_shape", "token_pool", "token_restore", "run_blocks",
 ]
 
 
@@ -225,6 +226,17 @@ def rope_coords(n_prefix: int, n_video: int, grid) -> np.ndarray:
     out[n_prefix:, 0] = v // (Hg * Wg)
     out[n_prefix:, 1] = (v // Wg) % Hg
     out[n_prefix:, 2] = v % Wg
+    return out
+
+
+def rope_coords_pooled(n_prefix: int, grid, pair_w: int) -> np.ndarray:
+    """``rope_coords`` of a token-reduced grid (T, H, ceil(W/2)): the row for column j
+    pools full columns 2j and 2j + 1 and sits at their mean, 2j + 0.5; a lone last
+    column of an odd width stays at 2j.  Reading: the pages do not give the pooled
+    rows' rotary positions."""
+    out = rope_coords(n_prefix, int(np.prod(grid)), grid).astype(np.float64)
+    j = out[n_prefix:, 2]
+    out[n_prefix:, 2] = np.where(2 * j + 1 < pair_w, 2 * j + 0.5, 2 * j)
     return out
 
 
@@ -532,7 +544,78 @@ def gate_rows(mod, mod_prefix, n_prefix: int, k: int, rows) -> np.ndarray:
 
 def _coords(shape):
     grid = getattr(shape, "video_grid", None)
-    return None if grid is None else rope_coords(shape.n_prefix, shape.n_video, grid)
+    if grid is None:
+        return None
+    if getattr(shape, "pair_w", 0):
+        return rope_coords_pooled(shape.n_prefix, grid, shape.pair_w)
+    return rope_coords(shape.n_prefix, shape.n_video, grid)
+
+
+# ---------------------------------------------------------------------------
+# Token reduction (h3.c README, token-reduction paragraph: horizontally adjacent
+# video tokens run as one row through the middle blocks, text and audio exact, a
+# full-resolution bypass kept, each token restored as its original value plus the
+# update its pair received)
+# ---------------------------------------------------------------------------
+
+def reduced_shape(shape):
+    """The reduced section's shape: video grid T x H x ceil(W/2), rotary at pair means."""
+    T, Hg, Wg = shape.video_grid
+    Wr = (Wg + 1) // 2
+    return shape.with_(n_video=T * Hg * Wr, video_grid=(T, Hg, Wr), pair_w=Wg,
+                       token_reduction=False)
+
+
+def token_pool(x, shape):
+    """(x_r, baseline): prefix rows as they are, then per (t, h, j) the mean of video
+    tokens (t, h, 2j) and (t, h, 2j + 1) (fp32 sum, halved, rounded to bf16; a lone last
+    token of an odd row passes as it is), rows in raster order of the reduced grid.
+    Reading: "pairs" is taken as the mean."""
+    T, Hg, Wg = shape.video_grid
+    P = shape.n_prefix
+    x = np.asarray(x, np.float64)
+    v = x[P:].reshape(T, Hg, Wg, -1)
+    pooled = v[:, :, 0::2].copy()
+    npair = Wg // 2
+    pooled[:, :, :npair] = bf16(f32(v[:, :, 0:2 * npair:2] + v[:, :, 1:2 * npair:2]) * 0.5)
+    base = pooled.reshape(-1, x.shape[1])
+    return np.concatenate([x[:P], base], axis=0), base
+
+
+def token_restore(bypass, x_r, base, shape) -> np.ndarray:
+    """Full rows again: prefix rows from x_r; video token (t, h, w) =
+    bf16(bypass + (x_r - base) of its pair (t, h, w // 2)), in fp32 arithmetic."""
+    T, Hg, Wg = shape.video_grid
+    P = shape.n_prefix
+    Wr = (Wg + 1) // 2
+    D = np.shape(bypass)[1]
+    d = f32(np.asarray(x_r, np.float64)[P:] - np.asarray(base, np.float64)).reshape(T, Hg, Wr, D)
+    dfull = np.repeat(d, 2, axis=2)[:, :, :Wg].reshape(-1, D)
+    out = np.array(bypass, np.float64)
+    out[:P] = np.asarray(x_r, np.float64)[:P]
+    out[P:] = bf16(f32(out[P:] + dfull))
+    return out
+
+
+def run_blocks(x, blocks: list, shape, block_ids=None, reduction=None) -> np.ndarray:
+    """Run the blocks ``block_ids`` on x, with token reduction over the block positions
+    [first, last) when ``reduction`` = (first, last) is given (first < last)."""
+    ids = list(range(len(blocks))) if block_ids is None else list(block_ids)
+    first, last = reduction if reduction is not None else (-1, -1)
+    on = reduction is not None and 0 <= first < last and first < len(ids)
+    rs = reduced_shape(shape) if on else None
+    bypass = base = None
+    for pos, b in enumerate(ids):
+        if on and pos == first:
+            bypass = x
+            x, base = token_pool(x, shape)
+        if on and pos == last:
+            x = token_restore(bypass, x, base, shape)
+        s = rs if on and first <= pos < last else shape
+        x = block_forward(x, blocks[b], s)["x2"]
+    if on and last >= len(ids):
+        x = token_restore(bypass, x, base, shape)
+    return x
 
 
 def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
@@ -771,16 +854,13 @@ def sample_heads(xL, ends: dict, shape) -> tuple:
 
 
 def sample_step(z_video, z_audio, ends: dict, blocks: list, shape, kind: str, dt_video: float,
-                dt_audio: float, block_ids=None, residual=None) -> dict:
+                dt_audio: float, block_ids=None, residual=None, reduction=None) -> dict:
     """One sampler step on the modality latents.  kind "fresh": x_L = blocks(x_0) and the
     residual x_L - x_0 (fp32) is returned; kind "core": x_L = bf16(x_0 + residual).
     Then per modality v = head(x_L rows), z' = fp32(z + dt v)."""
     x0 = sample_x0(z_video, z_audio, ends, shape)
     if kind == "fresh":
-        ids = list(range(len(blocks))) if block_ids is None else list(block_ids)
-        x = x0
-        for b in ids:
-            x = block_forward(x, blocks[b], shape)["x2"]
+        x = run_blocks(x0, blocks, shape, block_ids, reduction)
         res = f32(x - x0)
     elif kind == "core":
         res = residual

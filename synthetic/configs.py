@@ -33,6 +33,10 @@ class BlockShape:
     # video latent grid (T, H, W) cut into cubes; None = contiguous 64-row tiles
     video_grid: tuple | None = None
     cube: tuple = (4, 4, 4)
+    # token reduction: reserve its buffers (the pass chooses the blocks it spans)
+    token_reduction: bool = False
+    # set on the reduced section's shape: the full width whose column pairs were pooled
+    pair_w: int = 0
 
     @property
     def n_rows(self) -> int:
@@ -154,8 +158,16 @@ SAMPLE_RECEIPT = Workload(
                         "c_audio": 32},
 )
 
+SAMPLE_RECEIPT_TR = Workload(
+    "sample50_15435_cubes_d5376_swiglu_tokred", 11, RECEIPT_SHAPE.with_(token_reduction=True),
+    "the sampler step of the receipt sequence with token reduction: horizontal video token "
+    "pairs pooled after block 3 and restored before block 40 (an early, noisy evaluation)",
+    n_blocks=50, extra={"dt": -0.125, "forward": True, "ends": True, "c_video": 96,
+                        "c_audio": 32, "reduction": (3, 40)},
+)
+
 CONFIGS = [ATTN_TINY, BLOCK_4K, BLOCK_15K, FORWARD_50, LOOP_4K, BLOCK_PAGES, FORWARD_PAGES,
-           BLOCK_RECEIPT, FORWARD_RECEIPT, SAMPLE_RECEIPT]
+           BLOCK_RECEIPT, FORWARD_RECEIPT, SAMPLE_RECEIPT, SAMPLE_RECEIPT_TR]
 
 
 def config_by_name(name: str) -> Workload:

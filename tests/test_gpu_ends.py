@@ -63,9 +63,9 @@ class Run:
         self.ra = torch.zeros(2, shp.n_audio, ca, dtype=torch.float32, device="cuda")
         self.res = torch.zeros(shp.n_rows, shp.hidden, dtype=torch.float32, device="cuda")
 
-    def step(self, blocks, ids, kind, video, audio, nf):
+    def step(self, blocks, ids, kind, video, audio, nf, reduction=None):
         self.h3.sample_step(self.cs, self.ends, blocks, ids, self.zv, self.za, self.rv, self.ra,
-                            self.res, kind, video, audio, nf, self.ws)
+                            self.res, kind, video, audio, nf, self.ws, reduction=reduction)
 
     def z(self):
         torch.cuda.synchronize()
@@ -179,3 +179,50 @@ def test_sample_loop_matches_oracle(h3, mode):
                              block_ids=[0, 1], sig_video=sv, sig_audio=sa, **kw)
     assert_close(gv - zv, ref["z_video"] - zv, f"{mode}: video change", rel=2e-2, cos=0.998)
     assert_close(ga - za, ref["z_audio"] - za, f"{mode}: audio change", rel=2e-2, cos=0.998)
+
+
+# ----------------------------------------------------------------------------- token reduction
+TR = CUBES.with_(token_reduction=True)  # 5 x 6 x 7 grid: the odd width leaves lone tokens
+
+
+def test_token_reduction_around_an_identity_block_is_exact(h3):
+    """Pool before block 1, restore before block 2, block 1 with zero gates: each token
+    comes back as its bypass value plus a zero update, so the run equals blocks 0 and 2
+    without reduction, bit for bit."""
+    e = S.ends_weights(TR, 13)
+    bw = [S.block_weights(TR, 900 + b) for b in range(3)]
+    bw[1]["mod"][2] = 0.0
+    bw[1]["mod"][5] = 0.0
+    bw[1]["mod_prefix"][2] = 0.0
+    bw[1]["mod_prefix"][5] = 0.0
+    blocks = [weights_to_device(b) for b in bw]
+    zv, za = S.modality_latents(TR, 14)
+    a = Run(h3, TR, e, zv, za)
+    a.step(blocks, [0, 1, 2], FRESH, (1.0, 0, 0, -0.125), (1.0, 0, 0, -0.25), 0, reduction=(1, 2))
+    b = Run(h3, TR, e, zv, za)
+    b.step(blocks, [0, 2], FRESH, (1.0, 0, 0, -0.125), (1.0, 0, 0, -0.25), 0)
+    av, aa = a.z()
+    bv, ba = b.z()
+    assert np.array_equal(av, bv) and np.array_equal(aa, ba)
+
+
+@pytest.mark.parametrize("reduction", [(1, 2), (1, 3), (0, 2)])
+def test_token_reduction_matches_oracle(h3, reduction):
+    e = S.ends_weights(TR, 15)
+    bw = [S.block_weights(TR, 950 + b) for b in range(3)]
+    zv, za = S.modality_latents(TR, 16)
+    r = Run(h3, TR, e, zv, za)
+    r.step([weights_to_device(b) for b in bw], [0, 1, 2], FRESH, (1.0, 0, 0, -0.125),
+           (1.0, 0, 0, -0.25), 0, reduction=reduction)
+    gv, ga = r.z()
+    ref = oracle.sample_step(zv, za, ends_f64(e), [weights_to_f64(b) for b in bw], TR, "fresh",
+                             -0.125, -0.25, reduction=reduction)
+    plain = oracle.sample_step(zv, za, ends_f64(e), [weights_to_f64(b) for b in bw], TR,
+                               "fresh", -0.125, -0.25)
+    vv = np.empty_like(ref["v_video"])
+    vv[r.perm] = r.rv[0].cpu().double().numpy()
+    assert_close(vv, ref["v_video"], f"video velocity {reduction}")
+    assert_close(r.ra[0].cpu().double().numpy(), ref["v_audio"], f"audio velocity {reduction}")
+    from helpers import rel_l2
+    # the reduction changes the result (it is an approximation); the GPU follows the oracle's
+    assert rel_l2(vv, ref["v_video"]) < 0.25 * rel_l2(plain["v_video"], ref["v_video"])

@@ -164,7 +164,7 @@ def test_sample_step_refuses_bad_arguments_on_host(h3):
     def call(ends, pass_kind=0, z=fake, ws_bytes=need, nf=0, res=fake, sched=sv):
         e = h3.make_ends(ends)
         return lib.h3dit_sample_step(ctypes.byref(s), ctypes.byref(e), None, None, 0, z, fake,
-                                     fake, fake, res, pass_kind,
+                                     fake, fake, res, None, pass_kind,
                                      ctypes.byref(sched) if sched is not None else None,
                                      ctypes.byref(sv), nf, fake, ws_bytes, None)
 
@@ -179,3 +179,32 @@ def test_sample_step_refuses_bad_arguments_on_host(h3):
     assert call(good, pass_kind=1, nf=0) == 1             # nothing to extrapolate from
     assert call(good, pass_kind=0) == 1                   # fresh pass without blocks array
     assert call(good, sched=None) == 1
+
+
+def test_token_reduction_needs_its_buffers(h3):
+    import ctypes
+    lib = h3.lib()
+    base = S.BlockShape(36, 92, 5 * 6 * 7, hidden=256, heads=2, head_dim=128, mlp_width=512,
+                        topk=3, video_grid=(5, 6, 7))
+    s_plain = h3.make_shape(base)
+    s_red = h3.make_shape(base.with_(token_reduction=True))
+    # the flag reserves a bypass of N x D bf16 and the pooled rows' baselines
+    extra = h3.workspace_bytes(s_red) - h3.workspace_bytes(s_plain)
+    assert extra >= (base.n_rows + 5 * 6 * 4) * 256 * 2
+    # a grid is required; a 1-wide grid has nothing to pair
+    assert h3.check_shape(h3.make_shape(base.with_(video_grid=None, token_reduction=True))) == 2
+    one = S.BlockShape(36, 92, 5 * 6, hidden=256, heads=2, head_dim=128, mlp_width=512, topk=3,
+                       video_grid=(5, 6, 1), token_reduction=True)
+    assert h3.check_shape(h3.make_shape(one)) == 2
+    # a reduction asked of a shape without the buffers is refused before any launch
+    fake = 4096
+    e = h3.make_ends(dict(c_video=96, c_audio=32, **{n: fake for n, _ in h3.Ends._fields_[2:]}))
+    bw = h3.BlockWeights(*[fake] * len(h3.BlockWeights._fields_))
+    ids = (ctypes.c_int * 1)(0)
+    red = h3.Reduction(0, 1)
+    sv = h3.Schedule(1.0, 0.0, 0.0, -0.125)
+    st = lib.h3dit_sample_step(ctypes.byref(s_plain), ctypes.byref(e), ctypes.byref(bw), ids, 1,
+                               fake, fake, fake, fake, None, ctypes.byref(red), 0,
+                               ctypes.byref(sv), ctypes.byref(sv), 0, fake,
+                               h3.workspace_bytes(s_plain), None)
+    assert st == 2

@@ -708,6 +708,74 @@ def test_sample_step_without_blocks_is_the_heads_of_the_patches():
     assert np.array_equal(r["z_video"], (zv + np.float32(-0.125) * r["v_video"].astype(np.float32)))
 
 
+# --------------------------------------------------------------------------- token reduction
+def _tr_shape(grid=(3, 4, 7)):
+    return S.BlockShape(8, 24, int(np.prod(grid)), hidden=16, heads=2, head_dim=8,
+                        mlp_width=64, topk=2, video_grid=grid, token_reduction=True)
+
+
+@pytest.mark.parametrize("grid", [(3, 4, 7), (2, 3, 8), (1, 1, 1), (2, 2, 3)])
+def test_token_pool_brute_force_pairs(grid):
+    shape = _tr_shape(grid)
+    T, Hg, Wg = grid
+    P = shape.n_prefix
+    x = O.bf16(rng.standard_normal((shape.n_rows, 16)))
+    xr, base = O.token_pool(x, shape)
+    Wr = (Wg + 1) // 2
+    assert xr.shape[0] == P + T * Hg * Wr and np.array_equal(xr[:P], x[:P])
+    for t in range(T):
+        for h in range(Hg):
+            for j in range(Wr):
+                a = x[P + (t * Hg + h) * Wg + 2 * j]
+                want = a if 2 * j + 1 == Wg else O.bf16(
+                    O.f32(a + x[P + (t * Hg + h) * Wg + 2 * j + 1]) * 0.5)
+                assert np.array_equal(xr[P + (t * Hg + h) * Wr + j], want)
+    assert np.array_equal(base, xr[P:])
+
+
+def test_token_restore_identity_and_pair_update():
+    shape = _tr_shape()
+    P = shape.n_prefix
+    x = O.bf16(rng.standard_normal((shape.n_rows, 16)))
+    xr, base = O.token_pool(x, shape)
+    assert np.array_equal(O.token_restore(x, xr, base, shape), x)  # nothing learned
+    # a pair's update reaches both of its tokens; text/audio rows come from the reduced rows
+    y = xr.copy()
+    y[:P] += 1.0
+    y[P + 5] += 0.25  # reduced row 5 = (t 0, h 1, j 1): full columns 2 and 3 of row (0, 1)
+    out = O.token_restore(x, y, base, shape)
+    assert np.array_equal(out[:P], y[:P])
+    changed = np.nonzero(np.any(out[P:] != x[P:], axis=1))[0]
+    assert changed.tolist() == [7 + 2, 7 + 3]
+    assert np.allclose(out[P + 9], O.bf16(x[P + 9] + 0.25), atol=0)
+
+
+def test_rope_coords_pooled_positions():
+    c = O.rope_coords_pooled(4, (2, 3, 4), 7)
+    assert np.array_equal(c[4:8, 2], [0.5, 2.5, 4.5, 6.0])  # last column of width 7 is alone
+    assert np.array_equal(c[4 + 12 + 4 * 2 + 1], [1, 2, 2.5])
+
+
+def test_run_blocks_reduction_boundaries():
+    # first == last is no reduction; an identity block (zero gates) between pool and
+    # restore gives back the unreduced run exactly
+    shape = _tr_shape()
+    blocks = [_weights(shape, 20 + i) for i in range(3)]
+    x = S.bf16_bits_to_f64(S.hidden_rows(shape, 3))
+    plain = O.run_blocks(x, blocks, shape)
+    assert np.array_equal(O.run_blocks(x, blocks, shape, reduction=(1, 1)), plain)
+    ident = dict(blocks[1])
+    ident["mod"] = ident["mod"].copy()
+    ident["mod"][2] = 0.0
+    ident["mod"][5] = 0.0
+    three = [blocks[0], ident, blocks[2]]
+    a = O.run_blocks(x, three, shape, reduction=(1, 2))
+    b = O.run_blocks(x, [blocks[0], blocks[2]], shape)
+    assert np.array_equal(a, b)
+    c = O.run_blocks(x, blocks, shape, reduction=(1, 2))
+    assert not np.array_equal(c, plain)
+
+
 def test_silu_closed_forms():
     assert O.silu(0.0) == 0.0
     x = rng.standard_normal(1000) * 4
