@@ -448,7 +448,8 @@ def run_ours(args, rank, world, local_rank):
           for k in stage_flops(shape)}
     # dominant kernel: group the stages by the kernel function that runs them and take the
     # one with the largest total time; achieved = its algorithmic flops / its time
-    groups = {"gemm<qkvg>": ["qkvg"], "gemm<gelu>": ["fc1"], "gemm<resid>": ["out_proj", "fc2"],
+    fc1_name = "gemm<swiglu>" if shape.mlp == "swiglu" else "gemm<gelu>"
+    groups = {"gemm<qkvg>": ["qkvg"], fc1_name: ["fc1"], "gemm<resid>": ["out_proj", "fc2"],
               "attention": ["attention"]}
     g_ms = {g: sum(stages[s_][0] for s_ in st) for g, st in groups.items()}
     dom = max(g_ms, key=g_ms.get)
