@@ -164,6 +164,9 @@ h3dit_status check_attn(const h3dit_shape* s, Dims* o) {
   o->V = s->n_video;
   o->Tv = Tv;
   o->ksel = s->topk < Tv ? s->topk : Tv;
+  // a video unit's key list (prefix chunks + both query tiles' selections) must fit the
+  // attention kernels' 1,024-entry lists
+  if ((P + 63) / 64 + 2 * o->ksel > 1024) return H3DIT_ERR_SHAPE;
   o->H = s->heads;
   o->d = s->head_dim;
   o->A = s->attn_width;

@@ -32,7 +32,9 @@
 //               of S per step, row max on the raw scores, P = exp2(s*scale*log2e
 //               - m) rounded to bf16 and stored back over the step's S columns
 //               (two bf16 per 32-bit column), l summing the unrounded weights;
-//               O is rescaled in TMEM only when the max grows by more than 2^8.
+//               O is rescaled in TMEM only when the max grows by more than 2^8, and
+//               only then does a step wait for the previous step's PV to finish, so
+//               the softmax of step t overlaps the PV of step t - 1.
 //               Epilogue: O / l, + gate * pooled for video rows, bf16 store.
 #include <math.h>
 
@@ -345,14 +347,14 @@ __global__ void __launch_bounds__(THREADS, 2)
                          ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       // P over the first 32 columns of this step's S buffer (already read above)
       tmem_st32_u(s_addr, pk);
-      if (t > 0) {
+      if (t > 0 && __any_sync(0xffffffffu, need)) {
         // O must not change under a rescale while the previous step's PV runs
         if (!mbar_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) rescale_rows<HD>(t_lane + L::O_COL, alpha);
+        rescale_rows<HD>(t_lane + L::O_COL, alpha);
       }
       l_run = fmaf(l_run, alpha, lsum);
       m_run = m_new;
