@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   // so its V stage is free and O is stable (waited by the V producer and the softmax)
   uint64_t* s_done = bars + 5;    // [2]
   uint64_t* pv_done = bars + 7;   // [2]
-  uint64_t* p_full = bars + 11;
+  uint64_t* p_full = bars + 11;   // [2] by step parity: no waiter can fall two phases behind
   uint64_t* drain = bars + 13;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   int* n_steps_s = reinterpret_cast<int*>(tmem_slot + 1);
@@ -180,7 +180,8 @@ __global__ void __launch_bounds__(THREADS, 2)
       mbar_init(&s_done[s], 1);
       mbar_init(&pv_done[s], 1);
     }
-    mbar_init(p_full, 4);
+    mbar_init(&p_full[0], 4);
+    mbar_init(&p_full[1], 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(THREADS, 2)
           tc_fence_after();
           issue_s(t + 1);
         }
-        if (!mbar_wait(p_full, t & 1, abort_flag, p.status)) break;
+        if (!mbar_wait(&p_full[st], (t >> 1) & 1, abort_flag, p.status)) break;
         if (!mbar_wait(&v_full[st], (t >> 1) & 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t v0 = smem_u32(smem + L::V_OFF0 + st * L::KV_BYTES);
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       m_run = m_new;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[sb]);
     }
     if (ok && n_steps > 0 &&
         mbar_wait(&pv_done[(n_steps - 1) & 1], ((n_steps - 1) >> 1) & 1, abort_flag, p.status)) {
