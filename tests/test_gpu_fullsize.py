@@ -214,3 +214,50 @@ def test_receipt_cubes_block_sampled(h3):
     assert_close(got[ref["rows"]], ref["x2"], "receipt x2 (sampled rows)")
     assert_close(got[ref["rows"]] - x0, ref["x2"] - x0, "receipt update (sampled rows)",
                  rel=5e-2, cos=0.998)
+
+
+def test_receipt_attention_repeat_identical_and_sampled(h3):
+    """Routed attention alone on the receipt sequence (56 heads, 280 cubes, k = 56: long key
+    lists, 64+ steps per unit) three times: byte-identical outputs (a race between the
+    softmax warps and the MMA issuer would show here), and sampled query tiles and
+    prefix rows against the oracle."""
+    wl = S.config_by_name("block_15435_cubes_d5376_swiglu")
+    shp = wl.shape
+    t0 = time.time()
+    inp = S.attention_inputs(shp, wl.seed + 3, structured=0.3)
+    perm = np.concatenate([np.arange(shp.n_prefix)] + oracle.shape_tiles(shp))
+    _log(f"receipt attention inputs {time.time() - t0:.1f}s")
+    cs = h3.attn_shape(shp)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    q, k, v = (dev_bf16(inp[n][:, perm]) for n in ("q", "k", "v"))
+    g = dev_bf16(inp["gate"][perm])
+    tv = shp.n_video_tiles
+    idx = torch.empty(shp.heads, tv, shp.topk, dtype=torch.int32, device="cuda")
+    pooled = torch.empty(shp.heads, tv, shp.head_dim, dtype=torch.float32, device="cuda")
+    outs = []
+    for _ in range(3):
+        out = torch.empty(shp.n_rows, shp.attn_width, dtype=torch.bfloat16, device="cuda")
+        h3.routed_attention(cs, q, k, v, g, out, ws, pooled=pooled, idx=idx)
+        torch.cuda.synchronize()
+        assert h3.sync_status(ws) == 0
+        outs.append(out.view(torch.int16).clone())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    got = np.empty((shp.n_rows, shp.attn_width))
+    got[perm] = outs[0].view(torch.bfloat16).float().cpu().double().numpy()
+    q64, k64, v64, g64 = (S.bf16_bits_to_f64(inp[n]) for n in ("q", "k", "v", "gate"))
+    sets = oracle.shape_tiles(shp)
+    gi = idx.cpu().numpy()
+    pb = pooled.cpu().double().numpy()
+    tiles = [(0, 0), (13, 139), (55, tv - 1), (27, 101)]
+    O = oracle.routed_attention(q64, k64, v64, shp.n_prefix, shp.n_video, gi, tiles=tiles,
+                                sets=sets)
+    d = shp.head_dim
+    for h, i in tiles:
+        rows = sets[i]
+        want = O[h, rows] + g64[rows, h * d:(h + 1) * d] * pb[h, i]
+        assert_close(got[rows, h * d:(h + 1) * d], want, f"receipt video tile ({h},{i})")
+    for r in (0, 35, 36, shp.n_prefix - 1):
+        for h in (0, 30, 55):
+            want = oracle.attend(q64[h, [r]], k64[h], v64[h], 1 / np.sqrt(d))[0]
+            assert_close(got[r, h * d:(h + 1) * d], want, f"receipt prefix row {r} head {h}")
+    _log(f"receipt attention repeat + sampled oracle {time.time() - t0:.1f}s")
