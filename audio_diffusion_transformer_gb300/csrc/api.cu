@@ -157,6 +157,7 @@ h3dit_status check_attn(const h3dit_shape* s, Dims* o) {
   if (s->topk < 1) return H3DIT_ERR_ARG;
   if (!make_geom(s, &o->geom)) return H3DIT_ERR_SHAPE;
   const int Tv = tile_count_of(o->geom);
+  if (Tv > 1024) return H3DIT_ERR_SHAPE;  // the router's top-k tracks at most 1,024 tiles
   if ((size_t)(s->head_dim + 3 * Tv) * 4 > 200 * 1024) return H3DIT_ERR_SHAPE;
   if (!(s->rms_eps >= 0.f)) return H3DIT_ERR_ARG;
   o->N = (int)N;

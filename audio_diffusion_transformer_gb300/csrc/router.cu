@@ -14,10 +14,12 @@
 //   tile; the head's key / value tile means pass through shared memory once
 //   per CTA in chunks of 32 tiles:
 //   S[h,i,j] = sum_c mq[h,i,c] mk[h,j,c]: one lane per key tile, four
-//   interleaved partial sums over c (c mod 4) added as ((p0 + p1) + (p2 + p3));
-//   top-k by k rounds of warp-wide arg-max under the total order (score
-//   descending, tile index ascending), NaN ranking as -inf -- the same set as
-//   "rank_j < k" with rank_j = #{j' : s_j' > s_j or (s_j' == s_j and j' < j)};
+//   interleaved partial sums over c (c mod 4) added as ((p0 + p1) + (p2 + p3)),
+//   operands read from shared memory 16 bytes at a time;
+//   top-k under the total order (score descending, tile index ascending), NaN
+//   ranking as -inf: the k-th largest order key found bit by bit with warp
+//   reductions, then every larger key and the lowest-index equal keys -- the same
+//   set as "rank_j < k" with rank_j = #{j' : s_j' > s_j or (s_j' == s_j and j' < j)};
 //   kept tiles are written ascending (ballots);
 //   pooled[h,i,:] = sum_j softmax_j(S[h,i,j] / sqrt(d)) mv[h,j,:]: max and
 //   denominator by fixed warp reductions, the weighted sum in j order.
@@ -88,10 +90,9 @@ __global__ void __launch_bounds__(128)
   }
 }
 
-__device__ __forceinline__ float rank_key(float s) { return isnan(s) ? -INFINITY : s; }
-
 constexpr int TILES_PER_CTA = ROUTE_THREADS / 32;  // one warp per query tile
 constexpr int KCHUNK = 32;                          // key-tile means staged per round
+constexpr int SPAD = 4;  // staged row padding (floats): conflict-free 16-byte column reads
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -104,45 +105,104 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Order key of a score for the top-k: a larger key ranks first; NaN ranks as -inf and
+// -0 equals +0 (the float comparison's view), so equal keys are exactly the ties.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  float v = isnan(x) ? -INFINITY : x;
+  if (v == 0.f) v = 0.f;
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Top-k of one query tile's scores s[0, Tv) by one warp; lane l owns tiles l + 32m, m < NM,
+// and gets bit m of `taken` set for each of its selected tiles.  T = the ksel-th largest
+// order key, found bit by bit (the largest T with #{key >= T} >= ksel); every tile with a
+// key above T is selected, then those equal to T in ascending tile order until ksel --
+// the ksel first tiles of the total order (score descending, tile ascending).
+template <int NM>
+__device__ __forceinline__ unsigned select_topk(const float* s, int Tv, int ksel, int lane) {
+  uint32_t u[NM];
+  unsigned valid = 0u;
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+    const int j = lane + 32 * m;
+    u[m] = j < Tv ? order_key(s[j]) : 0u;
+    if (j < Tv) valid |= 1u << m;
+  }
+  uint32_t T = 0u;
+#pragma unroll 1
+  for (int b = 31; b >= 0; --b) {
+    const uint32_t cand = T | (1u << b);
+    int c = 0;
+#pragma unroll
+    for (int m = 0; m < NM; ++m) c += (((valid >> m) & 1u) && u[m] >= cand) ? 1 : 0;
+    if (__reduce_add_sync(0xffffffffu, c) >= ksel) T = cand;
+  }
+  unsigned taken = 0u;
+  int gt = 0;
+#pragma unroll
+  for (int m = 0; m < NM; ++m)
+    if (((valid >> m) & 1u) && u[m] > T) {
+      taken |= 1u << m;
+      ++gt;
+    }
+  int need = ksel - __reduce_add_sync(0xffffffffu, gt);
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+    if (need <= 0) break;  // warp-uniform
+    const bool eq = ((valid >> m) & 1u) && u[m] == T;
+    const unsigned bal = __ballot_sync(0xffffffffu, eq);
+    if (eq && __popc(bal & ((1u << lane) - 1u)) < need) taken |= 1u << m;
+    need -= __popc(bal);
+  }
+  return taken;
+}
+
 // One CTA per (head h, block of 8 query tiles); warp w owns query tile i = 8 * blockIdx.x + w.
 // The head's key and value tile means are staged through shared memory once per CTA.
-template <int D>
+// NM: 32-tile groups per lane in the top-k (Tv <= 32 * NM).
+template <int D, int NM>
 __global__ void __launch_bounds__(ROUTE_THREADS)
     route_kernel(const float* __restrict__ means, float* __restrict__ scores,
                  int* __restrict__ idx, float* __restrict__ pooled, int H, int Tv, int ksel) {
-  extern __shared__ float sh[];
-  float* stage = sh;                                  // [KCHUNK][D + 1] staged means
-  float* qrow = stage + KCHUNK * (D + 1);             // [8][D] query means, one row per warp
-  float* srow = qrow + TILES_PER_CTA * D;             // [8][Tv] scores, then pooled weights
+  extern __shared__ __align__(16) float sh[];
+  float* stage = sh;                                  // [KCHUNK][D + SPAD] staged means
+  float* qrow = stage + KCHUNK * (D + SPAD);          // [8][D] query means, one row per warp
+  float* srow = qrow + TILES_PER_CTA * D;             // [8][Tv4] scores, then pooled weights
+  const int Tv4 = (Tv + 3) & ~3;                      // row stride: 16-byte aligned rows
   const int h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * TILES_PER_CTA + warp;
   const bool active = i < Tv;
-  float* s = srow + warp * Tv;
+  float* s = srow + warp * Tv4;
   float* mq = qrow + warp * D;
   const float* mQ = means + ((size_t)0 * H + h) * Tv * D;
   const float* mK = means + ((size_t)1 * H + h) * Tv * D;
   const float* mV = means + ((size_t)2 * H + h) * Tv * D;
   constexpr int D4 = D / 4;  // float4 lanes per row (<= 32)
   for (int c = lane; c < D; c += 32) mq[c] = active ? mQ[(size_t)i * D + c] : 0.f;
-  // scores: stage 32 key means (row stride D + 1: conflict-free column reads), then lane l
-  // of each warp computes the whole dot product for key tile j0 + l with four interleaved
-  // partial sums over the dimensions (c mod 4), added as ((p0 + p1) + (p2 + p3))
+  // scores: stage 32 key means (row stride D + 4 floats: 16-byte column reads are
+  // conflict-free), then lane l of each warp computes the whole dot product for key tile
+  // j0 + l with four interleaved partial sums over the dimensions (c mod 4), added as
+  // ((p0 + p1) + (p2 + p3)); query and key means are read four floats at a time
   for (int j0 = 0; j0 < Tv; j0 += KCHUNK) {
     const int nj = min(KCHUNK, Tv - j0);
     __syncthreads();
-    for (int e = threadIdx.x; e < nj * D; e += ROUTE_THREADS)
-      stage[(e / D) * (D + 1) + (e % D)] = __ldg(mK + (size_t)j0 * D + e);
+    for (int e = threadIdx.x; e < nj * D4; e += ROUTE_THREADS)
+      reinterpret_cast<float4*>(stage + (e / D4) * (D + SPAD))[e % D4] =
+          __ldg(reinterpret_cast<const float4*>(mK + (size_t)j0 * D) + e);
     __syncthreads();
     if (active && lane < nj) {
-      const float* kr = stage + lane * (D + 1);
+      const float4* kr = reinterpret_cast<const float4*>(stage + lane * (D + SPAD));
+      const float4* q4 = reinterpret_cast<const float4*>(mq);
       float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll 8
-      for (int c = 0; c < D; c += 4) {
-        a0 = fmaf(mq[c], kr[c], a0);
-        a1 = fmaf(mq[c + 1], kr[c + 1], a1);
-        a2 = fmaf(mq[c + 2], kr[c + 2], a2);
-        a3 = fmaf(mq[c + 3], kr[c + 3], a3);
+      for (int c = 0; c < D4; ++c) {
+        const float4 x = q4[c], y = kr[c];
+        a0 = fmaf(x.x, y.x, a0);
+        a1 = fmaf(x.y, y.y, a1);
+        a2 = fmaf(x.z, y.z, a2);
+        a3 = fmaf(x.w, y.w, a3);
       }
       s[j0 + lane] = (a0 + a1) + (a2 + a3);
     }
@@ -151,39 +211,14 @@ __global__ void __launch_bounds__(ROUTE_THREADS)
   if (active) {
     float* srow_out = scores + ((size_t)h * Tv + i) * Tv;
     for (int j = lane; j < Tv; j += 32) srow_out[j] = s[j];
-    // top-k: k rounds of a warp-wide arg-max under the total order (score desc, index asc),
-    // NaN ranking as -inf; lane l owns tiles l, l + 32, ... (bit m of `taken` = tile l + 32m).
-    // Selected tiles are then written in ascending order via ballots.
+    // top-k under the total order (score desc, index asc), NaN ranking as -inf; selected
+    // tiles are then written in ascending order via ballots
     int* out = idx + ((size_t)h * Tv + i) * ksel;
     unsigned taken = 0u;
     if (ksel >= Tv) {
       for (int m = 0; lane + 32 * m < Tv; ++m) taken |= 1u << m;
     } else {
-      for (int r = 0; r < ksel; ++r) {
-        float bs = -INFINITY;
-        int bj = 0x7fffffff;
-        for (int m = 0; lane + 32 * m < Tv; ++m) {
-          const int j = lane + 32 * m;
-          if ((taken >> m) & 1u) continue;
-          const float v = rank_key(s[j]);
-          if (bj == 0x7fffffff || v > bs || (v == bs && j < bj)) {
-            bs = v;
-            bj = j;
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-          const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
-          const bool better = oj != 0x7fffffff &&
-                              (bj == 0x7fffffff || os > bs || (os == bs && oj < bj));
-          if (better) {
-            bs = os;
-            bj = oj;
-          }
-        }
-        if (bj != 0x7fffffff && (bj & 31) == lane) taken |= 1u << (bj >> 5);
-      }
+      taken = select_topk<NM>(s, Tv, ksel, lane);
     }
     int base = 0;
     for (int m = 0; 32 * m < Tv; ++m) {
@@ -219,7 +254,20 @@ __global__ void __launch_bounds__(ROUTE_THREADS)
       reinterpret_cast<float4*>(stage)[e] = __ldg(reinterpret_cast<const float4*>(mV + (size_t)j0 * D) + e);
     __syncthreads();
     if (active && lane < D4) {
-      for (int jj = 0; jj < nj; ++jj) {  // j order
+      int jj = 0;
+      for (; jj + 4 <= nj; jj += 4) {  // j order; four weights per 16-byte read
+        const float4 w4 = *reinterpret_cast<const float4*>(s + j0 + jj);
+        const float w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float4 v = reinterpret_cast<const float4*>(stage + (jj + u) * D)[lane];
+          acc.x = fmaf(w[u], v.x, acc.x);
+          acc.y = fmaf(w[u], v.y, acc.y);
+          acc.z = fmaf(w[u], v.z, acc.z);
+          acc.w = fmaf(w[u], v.w, acc.w);
+        }
+      }
+      for (; jj < nj; ++jj) {
         const float w = s[j0 + jj];
         const float4 v = reinterpret_cast<const float4*>(stage + jj * D)[lane];
         acc.x = fmaf(w, v.x, acc.x);
@@ -250,9 +298,14 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream) {
                                                   a.Tv);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t shm = (size_t)(KCHUNK * (a.d + 1) + TILES_PER_CTA * (a.d + a.Tv)) * 4;
+  const size_t shm =
+      (size_t)(KCHUNK * (a.d + SPAD) + TILES_PER_CTA * (a.d + ((a.Tv + 3) & ~3))) * 4;
   if (shm > 200 * 1024) return cudaErrorInvalidValue;
-  auto kern = a.d == 128 ? route_kernel<128> : route_kernel<64>;
+  const int nm = (a.Tv + 31) / 32;
+  auto kern = a.d == 128 ? (nm <= 8 ? route_kernel<128, 8>
+                                    : (nm <= 16 ? route_kernel<128, 16> : route_kernel<128, 32>))
+                         : (nm <= 8 ? route_kernel<64, 8>
+                                    : (nm <= 16 ? route_kernel<64, 16> : route_kernel<64, 32>));
   if (shm > 48 * 1024) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm);
     if (e != cudaSuccess) return e;
