@@ -261,3 +261,72 @@ def test_receipt_attention_repeat_identical_and_sampled(h3):
             want = oracle.attend(q64[h, [r]], k64[h], v64[h], 1 / np.sqrt(d))[0]
             assert_close(got[r, h * d:(h + 1) * d], want, f"receipt prefix row {r} head {h}")
     _log(f"receipt attention repeat + sampled oracle {time.time() - t0:.1f}s")
+
+
+def _device_block(shp, g, zero_gates=False):
+    """One block of random weights of ``shp`` made on the device (no host generation)."""
+    D, A, F, d = shp.hidden, shp.attn_width, shp.mlp_width, shp.head_dim
+    F1 = 2 * F if shp.mlp == "swiglu" else F
+
+    def rn(*sz, std=0.02, mean=0.0, dtype=torch.bfloat16):
+        return (torch.randn(*sz, generator=g, device="cuda") * std + mean).to(dtype)
+
+    w = {"w_qkvg": rn(4 * A, D), "b_qkvg": rn(4 * A), "w_o": rn(D, A), "b_o": rn(D),
+         "w1": rn(F1, D), "b1": rn(F1), "w2": rn(D, F), "b2": rn(D),
+         "mod": rn(6, D, std=0.1, dtype=torch.float32), "qnorm_w": rn(d, mean=1.0),
+         "knorm_w": rn(d, mean=1.0), "mod_prefix": rn(6, D, std=0.1, dtype=torch.float32)}
+    if zero_gates:
+        for t in ("mod", "mod_prefix"):
+            w[t][2].zero_()
+            w[t][5].zero_()
+    return w
+
+
+def _device_ends(shp, g, cv=96, ca=32):
+    D = shp.hidden
+
+    def rn(*sz, std=1.0, dtype=torch.float32):
+        return (torch.randn(*sz, generator=g, device="cuda") * std).to(dtype)
+
+    e = {"c_video": cv, "c_audio": ca, "text": rn(shp.n_text, D, dtype=torch.bfloat16)}
+    for m, c in (("video", cv), ("audio", ca)):
+        e.update({f"w_in_{m}": rn(c, D, std=0.1), f"b_in_{m}": rn(D, std=0.02),
+                  f"w_out_{m}": rn(c, D, std=0.02, dtype=torch.bfloat16),
+                  f"b_out_{m}": rn(c, std=0.02, dtype=torch.bfloat16),
+                  f"mod_out_{m}": rn(2, D, std=0.1)})
+    return e
+
+
+def test_receipt_sampler_exact_properties_fullsize(h3):
+    """The sampler at the receipt size (pages' shape, 280 cubes, k = 56), exact properties
+    that hold at any size: (1) a core-reuse pass at the same latents gives the fresh
+    pass's latents bit for bit; (2) token reduction around a block with zero gates gives
+    the run without that block bit for bit (each token = bypass + a zero update)."""
+    shp = S.config_by_name("sample50_15435_cubes_d5376_swiglu_tokred").shape
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2024)
+    blocks = [_device_block(shp, g), _device_block(shp, g, zero_gates=True), _device_block(shp, g)]
+    ends = _device_ends(shp, g)
+    zv0 = torch.randn(shp.n_video, 96, generator=g, device="cuda")
+    za0 = torch.randn(shp.n_audio, 32, generator=g, device="cuda")
+    cs = h3.make_shape(shp)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
+    rv = torch.zeros(2, shp.n_video, 96, device="cuda")
+    ra = torch.zeros(2, shp.n_audio, 32, device="cuda")
+    res = torch.zeros(shp.n_rows, shp.hidden, device="cuda")
+    sched = (1.0, 0.0, 0.0, -0.125)
+
+    def run(ids, kind, reduction=None, residual=None):
+        zv, za = zv0.clone(), za0.clone()
+        h3.sample_step(cs, ends, blocks, ids, zv, za, rv, ra, residual, kind, sched, sched, 1,
+                       ws, reduction=reduction)
+        torch.cuda.synchronize()
+        assert h3.sync_status(ws) == 0
+        return zv, za
+
+    fresh = run([0, 2], h3.H3DIT_PASS_FRESH, residual=res)
+    core = run([], h3.H3DIT_PASS_CORE_REUSE, residual=res)
+    assert torch.equal(fresh[0], core[0]) and torch.equal(fresh[1], core[1])
+    assert not torch.equal(fresh[0], zv0)
+    reduced = run([0, 1, 2], h3.H3DIT_PASS_FRESH, reduction=(1, 2))
+    assert torch.equal(fresh[0], reduced[0]) and torch.equal(fresh[1], reduced[1])
