@@ -333,6 +333,36 @@ def make_ends(torch, shape, cv, ca, seed, dev):
     return e
 
 
+def dominant_kernel(shape, shapes, stages, K, workload_name):
+    """Roofline of the kernel with the largest stage time, from the live stage records
+    (ms, launches); achieved = its algorithmic flops / its time.  Also per-kernel rates."""
+    pk, pk_kind = peaks()
+    peak_tc = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    # per-launch flops of each stage, averaged over the block positions
+    sf = {k: sum(stage_flops(sb)[k] for sb in shapes) / len(shapes)
+          for k in stage_flops(shape)}
+    fc1_name = "gemm<swiglu>" if shape.mlp == "swiglu" else "gemm<gelu>"
+    groups = {"gemm<qkvg>": ["qkvg"], fc1_name: ["fc1"], "gemm<resid>": ["out_proj", "fc2"],
+              "attention": ["attention"]}
+    g_ms = {g: sum(stages[s_][0] for s_ in st) for g, st in groups.items()}
+    dom = max(g_ms, key=g_ms.get)
+    n_launch = sum(stages[s_][1] for s_ in groups[dom])
+    flops = sum(sf[s_] * stages[s_][1] for s_ in groups[dom])
+    kernel = "attention" if dom == "attention" else "gemm"
+    roofline = {"bound": "tensor", "kernel": dom,
+                "achieved": flops / (g_ms[dom] / 1e3) / 1e12, "peak": peak_tc,
+                "peak_kind": f"bf16 sustained, {pk_kind}", "unit": "TFLOP/s",
+                "traffic": recorded_traffic(kernel, dom, workload_name),
+                "launch_ms": g_ms[dom] / max(n_launch, 1), "launches": n_launch}
+    roofline["frac"] = roofline["achieved"] / peak_tc
+    kernels = {}
+    for g, st in groups.items():
+        fl = sum(sf[s_] * stages[s_][1] for s_ in st)
+        kernels[g] = {"ms_per_step": g_ms[g] / K,
+                      "tflops": fl / (g_ms[g] / 1e3) / 1e12 if g_ms[g] > 0 else None}
+    return roofline, kernels
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -443,30 +473,7 @@ def run_ours(args, rank, world, local_rank):
     pk, pk_kind = peaks()
     peak_tc = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     achieved_total = step_flops * K / (ms_max / 1e3) / 1e12
-    # per-launch flops of each stage, averaged over the block positions
-    sf = {k: sum(stage_flops(sb)[k] for sb in shapes) / len(shapes)
-          for k in stage_flops(shape)}
-    # dominant kernel: group the stages by the kernel function that runs them and take the
-    # one with the largest total time; achieved = its algorithmic flops / its time
-    fc1_name = "gemm<swiglu>" if shape.mlp == "swiglu" else "gemm<gelu>"
-    groups = {"gemm<qkvg>": ["qkvg"], fc1_name: ["fc1"], "gemm<resid>": ["out_proj", "fc2"],
-              "attention": ["attention"]}
-    g_ms = {g: sum(stages[s_][0] for s_ in st) for g, st in groups.items()}
-    dom = max(g_ms, key=g_ms.get)
-    n_launch = sum(stages[s_][1] for s_ in groups[dom])
-    flops = sum(sf[s_] * stages[s_][1] for s_ in groups[dom])
-    kernel = "attention" if dom == "attention" else "gemm"
-    roofline = {"bound": "tensor", "kernel": dom,
-                "achieved": flops / (g_ms[dom] / 1e3) / 1e12, "peak": peak_tc,
-                "peak_kind": f"bf16 sustained, {pk_kind}", "unit": "TFLOP/s",
-                "traffic": recorded_traffic(kernel, dom, wl.name),
-                "launch_ms": g_ms[dom] / max(n_launch, 1), "launches": n_launch}
-    roofline["frac"] = roofline["achieved"] / peak_tc
-    kernels = {}
-    for g, st in groups.items():
-        fl = sum(sf[s_] * stages[s_][1] for s_ in st)
-        kernels[g] = {"ms_per_step": g_ms[g] / K,
-                      "tflops": fl / (g_ms[g] / 1e3) / 1e12 if g_ms[g] > 0 else None}
+    roofline, kernels = dominant_kernel(shape, shapes, stages, K, wl.name)
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_max / K, "higher_is_better": True,
@@ -574,6 +581,7 @@ def run_loop(args, rank, world, local_rank):
     sampler = ClockSampler()
     sampler.start()
     time.sleep(0.3)
+    h3.profile_begin(16 * n_steps * len(ids) * args.steps + 64 * n_steps * args.steps)
     l0 = h3.launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -581,12 +589,26 @@ def run_loop(args, rank, world, local_rank):
         loop()
     e1.record(stream)
     torch.cuda.synchronize()
+    stages = h3.profile_end()
     launches = h3.launch_count() - l0
     clocks = sampler.stop()
     ms = e0.elapsed_time(e1)
     if h3.sync_status(ws) != 0:
         raise SystemExit("device status error in the timed region")
     ms = max_over_ranks(ms, world, dev)
+    # end to end: H2D of the latents, the loop, D2H of the result, every timed step
+    e2e_ms = None
+    if not args.no_e2e:
+        z_host = z0.cpu().pin_memory()
+        z_back = torch.empty_like(z_host).pin_memory()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            z0.copy_(z_host, non_blocking=True)
+            loop()
+            z_back.copy_(z, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world, dev)
     n_fresh = sum(fresh)
     block_evals = n_fresh * len(ids)
     # top-k density sweep: one block of this shape per k, rows/s per block
@@ -612,7 +634,14 @@ def run_loop(args, rank, world, local_rank):
     pk, pk_kind = peaks()
     gf, af = block_flops(shape)
     achieved = block_evals * (gf + af) * args.steps / (ms / 1e3) / 1e12
-    return {
+    roofline, kernels = dominant_kernel(shape, [shape], stages, args.steps, wl.name)
+    extra = {"roofline": roofline, "kernels": kernels,
+             "stages_ms_per_step": {k: v[0] / args.steps for k, v in stages.items()}}
+    if e2e_ms is not None:
+        extra["e2e"] = {"value": job_rows_per_s(N * block_evals * args.steps, world, e2e_ms),
+                        "unit": UNIT, "h2d_bytes_per_step": N * D * 4,
+                        "d2h_bytes_per_step": N * D * 4}
+    return dict(extra, **{
         "metric": METRIC, "value": job_rows_per_s(N * block_evals * args.steps, world, ms),
         "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -626,7 +655,7 @@ def run_loop(args, rank, world, local_rank):
         "tc_frac_of_peak": achieved / pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
         "achieved_tflops": achieved, "topk_sweep": sweep, "gpu_launches": int(launches),
         "clocks": clocks,
-    }
+    })
 
 
 def run_reference(args, rank, world):

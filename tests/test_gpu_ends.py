@@ -226,3 +226,27 @@ def test_token_reduction_matches_oracle(h3, reduction):
     from helpers import rel_l2
     # the reduction changes the result (it is an approximation); the GPU follows the oracle's
     assert rel_l2(vv, ref["v_video"]) < 0.25 * rel_l2(plain["v_video"], ref["v_video"])
+
+
+def test_sample_step_video_only_without_text_or_audio(h3):
+    """No text and no audio rows (prefix of 0): the audio latents, heads and schedule are
+    absent (null pointers) and the video path alone runs, against the oracle."""
+    shp = S.BlockShape(0, 0, 6 * 5 * 7, hidden=256, heads=2, head_dim=128, mlp_width=1024,
+                       topk=3, video_grid=(6, 5, 7))
+    e = S.ends_weights(shp, 21, 96, 32)
+    for n in ("w_in_audio", "b_in_audio", "w_out_audio", "b_out_audio", "mod_out_audio", "text"):
+        e.pop(n)
+    e["c_audio"] = 0
+    bw = [S.block_weights(shp, 1000 + b) for b in range(2)]
+    zv, _ = S.modality_latents(shp, 22, 96, 32)
+    za = np.zeros((0, 32), np.float32)
+    r = Run(h3, shp, dict(e, c_audio=32), zv, za)
+    r.ends = ends_device(e)
+    r.step([weights_to_device(b) for b in bw], [0, 1], FRESH, (1.0, 0, 0, -0.125),
+           (1.0, 0, 0, -0.125), 0)
+    gv, _ = r.z()
+    ref = oracle.sample_step(zv, za, ends_f64(dict(e, text=np.zeros((0, shp.hidden)))),
+                             [weights_to_f64(b) for b in bw], shp, "fresh", -0.125, -0.125)
+    vv = np.empty_like(ref["v_video"])
+    vv[r.perm] = r.rv[0].cpu().double().numpy()
+    assert_close(vv, ref["v_video"], "video velocity (no prefix)")
