@@ -559,19 +559,37 @@ def run_loop(args, rank, world, local_rank):
     fresh = fresh_schedule(n_steps, reuse)
     stream = torch.cuda.current_stream()
 
-    def loop():
+    def eager_loop(st=None):
+        st = stream.cuda_stream if st is None else st
         z.copy_(z0)
         nf, fs = 0, []
         for i in range(n_steps):
             if fresh[i]:
                 h3.denoise_step(cs, blocks, ids, z, ring, True, (sig[i], 0.0, 0.0, dt), nf, ws,
-                                stream=stream.cuda_stream)
+                                stream=st)
                 nf += 1
                 fs.append(sig[i])
             else:
                 sb = fs[-2] if len(fs) > 1 else fs[-1]
                 h3.denoise_step(cs, blocks, ids, z, ring, False, (sig[i], fs[-1], sb, dt), nf,
-                                ws, stream=stream.cuda_stream)
+                                ws, stream=st)
+
+    loop = eager_loop
+    graph_launches = None
+    if args.graph:
+        # the whole loop (~4,500 launches) captured once into a CUDA graph and replayed
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            eager_loop(side.cuda_stream)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        c0 = h3.launch_count()
+        with torch.cuda.graph(graph):
+            eager_loop(torch.cuda.current_stream().cuda_stream)
+        graph_launches = h3.launch_count() - c0
+        loop = graph.replay
 
     for _ in range(args.warmup):
         loop()
@@ -589,6 +607,8 @@ def run_loop(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     launches = h3.launch_count() - l0
+    if graph_launches is not None:  # replays launch the captured kernels without the host
+        launches = graph_launches * args.steps
     clocks = sampler.stop()
     ms = e0.elapsed_time(e1)
     if h3.sync_status(ws) != 0:
@@ -597,7 +617,7 @@ def run_loop(args, rank, world, local_rank):
     # stage times from one separately profiled pass: at 4,096 rows the loop is
     # launch-heavy and per-stage events in the timed region would slow it by ~3%
     h3.profile_begin(16 * n_steps * len(ids) + 64 * n_steps)
-    loop()
+    eager_loop()
     torch.cuda.synchronize()
     stages = h3.profile_end()
     # end to end: H2D of the latents, the loop, D2H of the result, every timed step
@@ -656,6 +676,7 @@ def run_loop(args, rank, world, local_rank):
                    "reuse": reuse, "fresh_passes": n_fresh, "blocks_kept": len(ids),
                    "blocks_total": wl.n_blocks, "kept_ids": ids,
                    "parallelism": f"replicas x{world}",
+                   "launch": "one CUDA graph per loop" if args.graph else "eager",
                    "l2": "inputs larger than L2 (45 blocks x 113 MB of weights per pass)"},
         "tc_frac_of_peak": achieved / pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
         "achieved_tflops": achieved, "topk_sweep": sweep, "gpu_launches": int(launches),
@@ -696,6 +717,8 @@ def main():
     ap.add_argument("--workload", default="forward50_15435_d5120")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="loop workload: capture the loop into a CUDA graph and replay it")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
