@@ -81,6 +81,13 @@ struct Params {
   int* status;
 };
 
+// max of three fp32 values in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <int HD>
 __device__ __forceinline__ void rescale_rows(uint32_t taddr, float alpha) {
 #pragma unroll 1
@@ -312,40 +319,37 @@ __global__ void __launch_bounds__(THREADS, 2)
       const uint32_t s_addr = t_lane + L::S_COL + sb * 64;
       float sv[64];
       tmem_ld64(s_addr, sv);
-      float mx8[8];
+      // row max, two new scores per three-input max
+      float mx4[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
-      if (nv == 64) {  // warp-uniform: every key of the tile is visible to these rows
+      for (int u = 0; u < 4; ++u) mx4[u] = -INFINITY;
+      if (nv < 64) {  // warp-uniform: mask the keys of this tile that the row does not see
 #pragma unroll
-        for (int j = 0; j < 64; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], sv[j]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          sv[j] = j < nv ? sv[j] : -INFINITY;
-          mx8[j & 7] = fmaxf(mx8[j & 7], sv[j]);
-        }
+        for (int j = 0; j < 64; ++j) sv[j] = j < nv ? sv[j] : -INFINITY;
       }
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
+#pragma unroll
+      for (int j = 0; j < 64; j += 2) mx4[(j >> 1) & 3] = fmax3(mx4[(j >> 1) & 3], sv[j], sv[j + 1]);
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
       const bool need = mx > m_run + kRescaleLog2;
       const float m_new = need ? mx : m_run;
       const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      // P = exp2(s * scale - m) rounded to bf16; l sums the unrounded weights
+      // P = exp2(s * scale - m) rounded to bf16; l sums the unrounded weights.  The
+      // scale-and-shift and the sums run two lanes of fp32 per instruction.
       uint32_t pk[32];
-      float ls8[8];
+      const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
+      float2 ls2[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) ls8[u] = 0.f;
+      for (int u = 0; u < 4; ++u) ls2[u] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < 64; j += 2) {
-        const float e0 = ex2_approx(fmaf(sv[j], sl2, -m_use));
-        const float e1 = ex2_approx(fmaf(sv[j + 1], sl2, -m_use));
-        ls8[(j >> 1) & 7] += e0;
-        ls8[(j >> 1) & 7] += e1;
-        pk[j >> 1] = pack_bf16x2(e0, e1);
+        const float2 x = __ffma2_rn(make_float2(sv[j], sv[j + 1]), sc2, nm2);
+        const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        ls2[(j >> 1) & 3] = __fadd2_rn(ls2[(j >> 1) & 3], e);
+        pk[j >> 1] = pack_bf16x2(e.x, e.y);
       }
-      const float lsum = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) +
-                         ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      const float lsum = ((ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y)) +
+                         ((ls2[2].x + ls2[2].y) + (ls2[3].x + ls2[3].y));
       // P over the first 32 columns of this step's S buffer (already read above)
       tmem_st32_u(s_addr, pk);
       if (t > 0 && __any_sync(0xffffffffu, need)) {
