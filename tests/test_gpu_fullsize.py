@@ -31,9 +31,13 @@ def h3():
 
 
 def _log(msg):
-    os.makedirs("gpurun_out", exist_ok=True)
-    with open(os.path.join("gpurun_out", "fullsize_timing.log"), "a") as f:
-        f.write(msg + "\n")
+    """Oracle timings: printed (pytest -s shows them) and appended to the file named by
+    H3DIT_TEST_LOG when that is set."""
+    print(msg)
+    path = os.environ.get("H3DIT_TEST_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(msg + "\n")
 
 
 def sample_rows(shp):
