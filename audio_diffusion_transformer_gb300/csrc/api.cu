@@ -101,7 +101,7 @@ inline cudaError_t counted(cudaError_t e, int n) {
 }
 
 constexpr size_t kAlign = 256;
-constexpr int kMaxRows = 1022 * 64;  // attention key-tile list limit
+constexpr int kMaxRows = 1022 * 64;  // a prefix attention unit walks N / 128 <= 512 steps
 
 inline size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
@@ -165,9 +165,9 @@ h3dit_status check_attn(const h3dit_shape* s, Dims* o) {
   o->V = s->n_video;
   o->Tv = Tv;
   o->ksel = s->topk < Tv ? s->topk : Tv;
-  // a video unit's key list (prefix chunks + both query tiles' selections) must fit the
-  // attention kernels' 1,024-entry lists
-  if ((P + 63) / 64 + 2 * o->ksel > 1024) return H3DIT_ERR_SHAPE;
+  // a video unit's steps (128-row prefix chunks + one per selected tile) must fit the
+  // attention kernel's 512-entry step lists
+  if ((P + 127) / 128 + o->ksel > 512) return H3DIT_ERR_SHAPE;
   o->H = s->heads;
   o->d = s->head_dim;
   o->A = s->attn_width;
@@ -295,6 +295,8 @@ h3dit_status run_attention(const h3dit_shape* s, const Dims& m, const Ws& w, voi
   r.scores = scores ? scores : at<float>(ws, w.scores);
   r.idx = idx ? idx : at<int>(ws, w.idx);
   r.pooled = use_pool || pooled ? (pooled ? pooled : at<float>(ws, w.pooled)) : nullptr;
+  // the attention kernel's unit counter shares the status block (a separate 128-byte line)
+  r.counter = at<int>(ws, w.status) + 32;
   {
     StageScope sc(H3DIT_STAGE_ROUTER, st);
     H3_TRY(cu(counted(launch_router(r, st), 2)));
@@ -316,6 +318,7 @@ h3dit_status run_attention(const h3dit_shape* s, const Dims& m, const Ws& w, voi
   a.pooled = use_pool ? r.pooled : nullptr;
   a.out = out;
   a.status = at<int>(ws, w.status);
+  a.counter = r.counter;
   StageScope sc(H3DIT_STAGE_ATTN, st);
   return cu(counted(launch_attention(a, st), 1));
 }

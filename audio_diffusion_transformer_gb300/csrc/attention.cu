@@ -4,38 +4,48 @@
 // with fp32 scores and an online softmax) and "Precision" (softmax weights
 // rounded to bf16 before the value product).
 //
-// One CTA owns 128 query rows of one head:
+// Work unit: 128 query rows of one head.
 //   * a prefix unit: 128 text/audio rows, attending to all N rows;
-//   * a video unit: two video query tiles (2u, 2u+1) of up to 64 rows each (a
-//     64-row slice or a clipped 4x4x4 cube, contiguous in the library's row
-//     order), attending to all prefix rows plus the union of the two tiles'
-//     selected key tiles; a key tile with fewer than 64 rows masks the rest.  Each
-//     key tile carries a 2-bit mask saying which of the two query tiles chose
-//     it; scores of the other half are masked to -inf, so every row sees
-//     exactly its own key set.
-// CTAs run the long prefix units first (all heads), then the video units
-// head-major, so a wave of video CTAs shares one or two heads' K/V in L2 and no
-// long unit starts at the end of the grid.  The KV loop walks the key-tile
-// list one 64-row tile per step.  K and V tiles arrive by TMA (one box per
-// 64 x 64 piece, 128-byte swizzle, no multicast) into 2-stage K and V rings; a
-// K stage is released as soon as its S MMA completes, a V stage as soon as its
-// PV MMA completes, and each ring has its own producer warp, so a key tile is
-// requested two steps before its S MMA.  A CTA needs ~101 KB of shared memory
-// and 256 TMEM columns, so two CTAs share an SM and each hides the other's
-// latencies.
-//   warp 0      TMA producer: Q once, then the K ring
-//   warp 6      TMA producer: the V ring
-//   warp 1      MMA issuer: S = Q K^T (M=128, N=64, fp32 in TMEM, double
-//               buffered) and O += P V (M=128, N=d, K=64) with P read from TMEM
-//               and V from shared memory as an MN-major operand
-//   warps 2..5  softmax, thread = query row (TMEM lane): one 64-column TMEM read
-//               of S per step, row max on the raw scores, P = exp2(s*scale*log2e
-//               - m) rounded to bf16 and stored back over the step's S columns
-//               (two bf16 per 32-bit column), l summing the unrounded weights;
-//               O is rescaled in TMEM only when the max grows by more than 2^8, and
-//               only then does a step wait for the previous step's PV to finish, so
-//               the softmax of step t overlaps the PV of step t - 1.
-//               Epilogue: O / l, + gate * pooled for video rows, bf16 store.
+//   * a video unit: two video query tiles a = 2u and b = 2u + 1 (up to 64 rows each, a
+//     64-row slice or a clipped 4x4x4 cube, contiguous in the library's row order) as
+//     rows 0-63 and 64-127, attending to all prefix rows plus each tile's own k
+//     selected key tiles.
+// A step feeds 128 keys to the tensor cores as two 64-row key blocks, X and Y:
+//   * dense step (the prefix keys of a video unit, every key of a prefix unit): X and
+//     Y are consecutive 64-row chunks and every query row uses both;
+//   * routed step i (video units): X is the i-th key tile selected by tile a, Y the
+//     i-th selected by tile b.  The score MMA computes all four 64 x 64 products
+//     (N = 128); rows of a read only the X columns, rows of b only the Y columns, and
+//     the softmax writes P block-diagonally (zeros in the other block), so the PV MMA
+//     (K = 128) adds each row's own keys and nothing else.
+//   A video unit takes ceil(P / 128) + k steps however much the two selections
+//   overlap, and a row's softmax sees 64 scores per routed step.  A key block with
+//   fewer than 64 rows (a clipped cube, the end of a range) masks the rest.
+//
+// Persistent: one CTA per SM.  A CTA takes units blockIdx.x and gridDim.x + blockIdx.x,
+// then fetches further units from a counter in the workspace (zeroed by the router,
+// which runs first), so that the long prefix units spread evenly; units are numbered
+// prefix units first (head-major), then video units head-major, so the CTAs in flight
+// share one or two heads' K/V in L2.  The pipelines run across unit boundaries.
+// Tensor memory (512 columns): two 128-column score buffers, the O accumulator, and
+// two Q buffers -- Q is the score MMA's A operand straight from tensor memory, which
+// leaves shared memory to three-stage K and V rings (192 KB): the kernel is bound by the
+// bytes it keeps in flight against the L2 latency under load.
+//   warp 0       TMA: the K ring (a stage = X + Y, 128 keys)
+//   warp 1       S issuer: S = Q [K_X; K_Y]^T (M = 128, N = 128, fp32) into the step's
+//                score buffer once the PV two steps back has read it
+//   warp 11      PV issuer: O += P [V_X; V_Y] (K = 128, P from tensor memory, V
+//                MN-major).  Two issuing threads keep the tensor pipe fed: the S
+//                MMAs of later steps queue while the PV issuer waits for a softmax.
+//   warps 2..5   softmax, thread = query row (TMEM lane): P = exp2(s * scale * log2e
+//                - m) rounded to bf16 over the step's S columns (two per 32-bit
+//                column), l summing the unrounded weights; O is rescaled in TMEM only
+//                when the row max grows by more than 2^8, and only then does a step
+//                wait for the previous PV
+//   warp 6       TMA: the V ring
+//   warps 7..10  per unit: O / l, + gate * pooled for video rows, bf16 store; then Q of
+//                the unit two ahead into tensor memory; warp 7 also fetches units and
+//                writes their step lists
 #include <math.h>
 
 #include "internal.h"
@@ -45,47 +55,111 @@ namespace h3 {
 
 namespace {
 
-constexpr int THREADS = 224;  // 7 warps: K/Q producer, MMA, 4 softmax, V producer
-constexpr int MAX_TILES = 1024;  // key tiles per unit: N <= 65,536 rows
+constexpr int THREADS = 384;     // 12 warps
+constexpr int MAX_STEPS = 512;   // steps per unit (a prefix unit walks N / 128 steps)
+constexpr int NST = 3;           // stages of the K ring and of the V ring
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int HD>
 struct Layout {
-  static constexpr int QCHUNK = 128 * 128;       // 128 query rows x 64 dims (bf16)
-  static constexpr int KCHUNK = 64 * 128;        // 64 keys x 64 dims (bf16)
-  static constexpr int Q_BYTES = 128 * HD * 2;
-  static constexpr int KV_BYTES = 64 * HD * 2;   // one 64-row key tile
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF0 = Q_OFF + Q_BYTES;          // K stage s at K_OFF0 + s * KV_BYTES
-  static constexpr int V_OFF0 = K_OFF0 + 2 * KV_BYTES;    // V stage s at V_OFF0 + s * KV_BYTES
-  static constexpr int TILES_OFF = V_OFF0 + 2 * KV_BYTES;
-  static constexpr int BAR_OFF = TILES_OFF + MAX_TILES * 4;
+  static constexpr int KCHUNK = 64 * 128;  // 64 keys x 64 dims (bf16, 128-byte rows)
+  static constexpr int BLK = 64 * HD * 2;  // one 64-row key block
+  // A K or V stage holds X and Y interleaved per 64-dim chunk: chunk c of X at
+  // 2c * KCHUNK, chunk c of Y right after it, so each chunk is one 128-row operand.
+  static constexpr int STAGE = 2 * BLK;
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + NST * STAGE;
+  static constexpr int LIST_OFF = V_OFF + NST * STAGE;          // two step lists (int2)
+  static constexpr int LBUF_OFF = LIST_OFF + 2 * MAX_STEPS * 8;  // 128 row sums
+  static constexpr int UNIT_OFF = LBUF_OFF + 128 * 4;            // two unit numbers
+  static constexpr int BAR_OFF = UNIT_OFF + 16;
   static constexpr int USED = BAR_OFF + 256;
-  // + alignment slack; at least 80 KB so that no more than two CTAs (the TMEM
-  // budget: 2 x 256 columns) are resident on an SM
-  static constexpr int SMEM = (USED + 1024) > 80 * 1024 ? (USED + 1024) : 80 * 1024;
-  static constexpr uint32_t S_COL = 0;                    // two 64-column score buffers
-  static constexpr uint32_t O_COL = 128;                  // HD-column accumulator
-  static constexpr uint32_t TMEM_COLS = 256;
+  static constexpr int SMEM = USED + 1024;                       // + alignment slack
+  static constexpr uint32_t S_COL = 0;    // two 128-column score buffers
+  static constexpr uint32_t O_COL = 256;  // the accumulator, HD columns
+  static constexpr uint32_t Q_COL = 384;  // two Q buffers, HD / 2 columns each (bf16 pairs)
+  static constexpr uint32_t TMEM_COLS = 512;
 };
 
 struct Params {
-  int N, H, n_prefix, n_video, Tv, ksel;
-  int n_pre_units;
+  int N, H, n_prefix, Tv, ksel;
+  int n_pre_units, n_vid_units, total;  // units per head (prefix, video); all units
+  int steps_all, steps_pre;             // ceil(N / 128), ceil(n_prefix / 128)
   TileGeom geom;
+  const __nv_bfloat16* q;
   const int* idx;
   const __nv_bfloat16* gate;
   const float* pooled;
   __nv_bfloat16* out;
   float scale_log2;
   int* status;
+  int* counter;
 };
+
+struct Unit {
+  int h, unit, ta, tb, n;
+  bool prefix;
+};
+
+__device__ __forceinline__ Unit unit_of(const Params& p, int w) {
+  Unit u;
+  const int n_pre = p.n_pre_units * p.H;
+  if (w < n_pre) {
+    u.h = w / p.n_pre_units;
+    u.unit = w % p.n_pre_units;
+  } else {
+    const int b = w - n_pre;
+    u.h = b / p.n_vid_units;
+    u.unit = p.n_pre_units + b % p.n_vid_units;
+  }
+  u.prefix = u.unit < p.n_pre_units;
+  u.ta = 2 * (u.unit - p.n_pre_units);
+  u.tb = u.ta + 1;
+  u.n = u.prefix ? p.steps_all : p.steps_pre + p.ksel;
+  return u;
+}
+
+// key block entry: first_row << 9 | rows << 2 | dense (rows 0..64 from first_row)
+__device__ __forceinline__ int chunk_entry(int r0, int limit) {
+  return (r0 << 9) | (max(0, min(64, limit - r0)) << 2) | 1;
+}
+
+// Step list of unit u, written by one warp.
+__device__ void build_list(const Params& p, const Unit& u, int2* list, int lane) {
+  const int limit = u.prefix ? p.N : p.n_prefix;
+  const int n_dense = u.prefix ? p.steps_all : p.steps_pre;
+  for (int s = lane; s < n_dense; s += 32)
+    list[s] = make_int2(chunk_entry(128 * s, limit), chunk_entry(128 * s + 64, limit));
+  if (u.prefix) return;
+  const int* ia = p.idx + ((size_t)u.h * p.Tv + u.ta) * p.ksel;
+  // an odd tile count leaves the last unit's second half without a tile: it repeats a
+  const int* ib = u.tb < p.Tv ? p.idx + ((size_t)u.h * p.Tv + u.tb) * p.ksel : ia;
+  for (int i = lane; i < p.ksel; i += 32) {
+    // indices come from the router; clamp defensively
+    const int a = min(max(__ldg(ia + i), 0), p.Tv - 1);
+    const int b = min(max(__ldg(ib + i), 0), p.Tv - 1);
+    int fa, ca, fb, cb;
+    tile_span(p.geom, a, &fa, &ca);
+    tile_span(p.geom, b, &fb, &cb);
+    list[n_dense + i] = make_int2((fa << 9) | (ca << 2), (fb << 9) | (cb << 2));
+  }
+}
 
 // max of three fp32 values in one instruction
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+
+// 32 lanes x 32 columns of TMEM <- 0 (no wait; the P store that follows waits for both)
+__device__ __forceinline__ void tmem_zero32(uint32_t taddr) {
+  const uint32_t z = 0;
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,"
+      "%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};" ::"r"(taddr),
+      "r"(z)
+      : "memory");
 }
 
 template <int HD>
@@ -100,96 +174,88 @@ __device__ __forceinline__ void rescale_rows(uint32_t taddr, float alpha) {
   }
 }
 
+// Masks scores j >= c (warp-uniform c) and returns the max of the 64 values.
+__device__ __forceinline__ float masked_max64(float* sv, int c) {
+  if (c < 64) {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) sv[j] = j < c ? sv[j] : -INFINITY;
+  }
+  float mx4[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) mx4[u] = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 64; j += 2) mx4[(j >> 1) & 3] = fmax3(mx4[(j >> 1) & 3], sv[j], sv[j + 1]);
+  return fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+}
+
+// P = exp2(s * scale - m) for 64 scores: bf16 pairs into pk, returns the unrounded sum.
+// The scale-and-shift and the sums run two lanes of fp32 per instruction.
+__device__ __forceinline__ float exp_pack64(const float* sv, float sl2, float m_use,
+                                            uint32_t* pk) {
+  const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
+  float2 ls2[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) ls2[u] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 64; j += 2) {
+    const float2 x = __ffma2_rn(make_float2(sv[j], sv[j + 1]), sc2, nm2);
+    const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    ls2[(j >> 1) & 3] = __fadd2_rn(ls2[(j >> 1) & 3], e);
+    pk[j >> 1] = pack_bf16x2(e.x, e.y);
+  }
+  return ((ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y)) +
+         ((ls2[2].x + ls2[2].y) + (ls2[3].x + ls2[3].y));
+}
+
 template <int HD>
-__global__ void __launch_bounds__(THREADS, 2)
-    attention_kernel(const __grid_constant__ CUtensorMap tmQ,
-                     const __grid_constant__ CUtensorMap tmK,
+__global__ void __launch_bounds__(THREADS, 1)
+    attention_kernel(const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const Params p) {
   using L = Layout<HD>;
-  static_assert(L::SMEM <= 113 * 1024, "two CTAs must fit on one SM");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem + L::Q_OFF;
-  int* tiles = reinterpret_cast<int*>(smem + L::TILES_OFF);
+  int2* lists = reinterpret_cast<int2*>(smem + L::LIST_OFF);
+  float* lbuf = reinterpret_cast<float*>(smem + L::LBUF_OFF);
+  volatile int* unit_w = reinterpret_cast<volatile int*>(smem + L::UNIT_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-  uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;    // [2]
-  uint64_t* v_full = bars + 3;    // [2]
-  // s_done[st]: S of the step in stage st is in TMEM and its K stage is free (one commit,
-  // waited by the softmax warps and the K producer); pv_done[st]: the step's PV completed,
-  // so its V stage is free and O is stable (waited by the V producer and the softmax)
-  uint64_t* s_done = bars + 5;    // [2]
-  uint64_t* pv_done = bars + 7;   // [2]
-  uint64_t* p_full = bars + 11;   // [2] by step parity: no waiter can fall two phases behind
-  uint64_t* drain = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
-  int* n_steps_s = reinterpret_cast<int*>(tmem_slot + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  uint64_t* k_full = bars + 0;      // [NST] K stage landed
+  uint64_t* k_free = bars + 3;      // [NST] the stage's S MMAs completed
+  uint64_t* v_full = bars + 6;      // [NST] V stage landed
+  uint64_t* v_free = bars + 9;      // [NST] the stage's PV MMAs completed (O stable)
+  uint64_t* s_done = bars + 12;     // [2] S of the step is in its buffer (step parity)
+  uint64_t* p_full = bars + 14;     // [2] P of the step written (four softmax warps)
+  uint64_t* q_full = bars + 16;     // [2] Q of the unit on this buffer written (four warps)
+  uint64_t* list_full = bars + 18;  // [2] unit number and step list written
+  uint64_t* o_full = bars + 20;     // the unit's last PV completed
+  uint64_t* o_free = bars + 21;     // O and the row sums read (four epilogue warps)
+  uint64_t* l_ready = bars + 22;    // the row sums are in lbuf (four softmax warps)
+  uint64_t* s_free = bars + 23;     // [2] the step's PV completed: its score buffer is free
+  uint64_t* drain = bars + 25;      // [2] per issuing thread
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 27);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // longest work first: all prefix units (each walks every key tile), head-major, then all
-  // video units, head-major (a wave of video CTAs shares one or two heads' K/V in L2)
-  const int n_vid_units = (p.Tv + 1) / 2;
-  const int n_pre_ctas = p.n_pre_units * p.H;
-  int h, unit;
-  if ((int)blockIdx.x < n_pre_ctas) {
-    h = blockIdx.x / p.n_pre_units;
-    unit = blockIdx.x % p.n_pre_units;
-  } else {
-    const int b = blockIdx.x - n_pre_ctas;
-    h = b / n_vid_units;
-    unit = p.n_pre_units + b % n_vid_units;
-  }
-  const bool is_prefix = unit < p.n_pre_units;
-  const int vu = unit - p.n_pre_units;
-  const int ta = 2 * vu, tb = 2 * vu + 1;  // video query tiles of a video unit
 
   if (threadIdx.x == 0) {
-    // key-tile list: entry = first_row << 9 | rows << 2 | mask (rows: 1..64 keys from
-    // first_row; mask bit 0: query rows 0-63 use it, bit 1: query rows 64-127)
-    int nt = 0;
-    if (is_prefix) {
-      for (int r0 = 0; r0 < p.N && nt < MAX_TILES; r0 += 64)
-        tiles[nt++] = (r0 << 9) | (min(64, p.N - r0) << 2) | 3;
-    } else {
-      for (int r0 = 0; r0 < p.n_prefix && nt < MAX_TILES; r0 += 64)
-        tiles[nt++] = (r0 << 9) | (min(64, p.n_prefix - r0) << 2) | 3;
-      const int* ia = p.idx + ((size_t)h * p.Tv + ta) * p.ksel;
-      const int* ib = p.idx + ((size_t)h * p.Tv + tb) * p.ksel;
-      const int na = p.ksel, nb = tb < p.Tv ? p.ksel : 0;
-      int i = 0, j = 0;
-      while ((i < na || j < nb) && nt < MAX_TILES) {
-        int t, m;
-        if (j >= nb || (i < na && ia[i] < ib[j])) {
-          t = ia[i++];
-          m = 1;
-        } else if (i >= na || ib[j] < ia[i]) {
-          t = ib[j++];
-          m = 2;
-        } else {
-          t = ia[i++];
-          ++j;
-          m = 3;
-        }
-        t = min(max(t, 0), p.Tv - 1);  // indices come from the router; clamp defensively
-        int f, c;
-        tile_span(p.geom, t, &f, &c);
-        tiles[nt++] = (f << 9) | (c << 2) | m;
-      }
+    for (int b = 0; b < NST; ++b) {
+      mbar_init(&k_full[b], 1);
+      mbar_init(&k_free[b], 1);
+      mbar_init(&v_full[b], 1);
+      mbar_init(&v_free[b], 1);
     }
-    *n_steps_s = nt;
-    mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&s_done[s], 1);
-      mbar_init(&pv_done[s], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_free[b], 1);
+      mbar_init(&drain[b], 1);
+      mbar_init(&s_done[b], 1);
+      mbar_init(&p_full[b], 4);
+      mbar_init(&q_full[b], 4);
+      mbar_init(&list_full[b], 1);
     }
-    mbar_init(&p_full[0], 4);
-    mbar_init(&p_full[1], 4);
-    mbar_init(drain, 1);
+    mbar_init(o_full, 1);
+    mbar_init(o_free, 4);
+    mbar_init(l_ready, 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -201,225 +267,378 @@ __global__ void __launch_bounds__(THREADS, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n_steps = *n_steps_s;
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 6) {
+    // ------------------------------------------------------------ TMA producers
     if (lane == 0) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      int qrow0, qrow1;
-      if (is_prefix) {
-        qrow0 = unit * 128;
-        qrow1 = unit * 128 + 64;
-      } else {
-        int c;
-        tile_span(p.geom, ta, &qrow0, &c);
-        qrow1 = qrow0;  // an odd tile count leaves the second half without a tile
-        if (tb < p.Tv) tile_span(p.geom, tb, &qrow1, &c);
-      }
-      mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+      const bool is_k = warp == 0;
+      const CUtensorMap* tm = is_k ? &tmK : &tmV;
+      prefetch_tmap(tm);
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* freed = is_k ? k_free : v_free;
+      uint8_t* ring = smem + (is_k ? L::K_OFF : L::V_OFF);
+      int st = 0;        // ring stage and phase of the next load
+      uint32_t ph = 0;
+      int issued = 0;
+      for (int lj = 0;; ++lj) {
+        const int lb = lj & 1;
+        if (!mbar_wait(&list_full[lb], (lj >> 1) & 1, abort_flag, p.status)) break;
+        const int w = unit_w[lb];
+        if (w >= p.total) break;
+        const Unit u = unit_of(p, w);
+        const int2* list = lists + lb * MAX_STEPS;
+        bool ok = true;
+        for (int t = 0; t < u.n; ++t) {
+          if (!mbar_wait(&freed[st], ph ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const int2 e = list[t];
+          uint8_t* s = ring + st * L::STAGE;
+          mbar_arrive_expect_tx(&full[st], L::STAGE);
 #pragma unroll
-      for (int c = 0; c < HD / 64; ++c) {
-        tma_load_3d(sQ + c * L::QCHUNK, &tmQ, q_full, 64 * c, qrow0, h);
-        tma_load_3d(sQ + c * L::QCHUNK + 8192, &tmQ, q_full, 64 * c, qrow1, h);
+          for (int ch = 0; ch < HD / 64; ++ch) {
+            tma_load_3d(s + 2 * ch * L::KCHUNK, tm, &full[st], 64 * ch, e.x >> 9, u.h);
+            tma_load_3d(s + (2 * ch + 1) * L::KCHUNK, tm, &full[st], 64 * ch, e.y >> 9, u.h);
+          }
+          ++issued;
+          if (++st == NST) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
       }
-      // K ring: a stage is refilled as soon as its S MMA completes (V has its own producer)
-      for (int t = 0; t < n_steps; ++t) {
-        const int st = t & 1;
-        if (!mbar_wait(&s_done[st], ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
-        uint8_t* sK = smem + L::K_OFF0 + st * L::KV_BYTES;
-        const int r0 = tiles[t] >> 9;
-        mbar_arrive_expect_tx(&k_full[st], L::KV_BYTES);
-#pragma unroll
-        for (int c = 0; c < HD / 64; ++c)
-          tma_load_3d(sK + c * L::KCHUNK, &tmK, &k_full[st], 64 * c, r0, h);
-      }
+      // wait (bounded) for the last load into each stage before the CTA exits (already
+      // complete unless the CTA is aborting)
+      for (int i = issued > NST ? issued - NST : 0; i < issued; ++i)
+        mbar_drain(&full[i % NST], (i / NST) & 1);
     }
-  } else if (warp == 6) {
+  } else if (warp == 1 || warp == 11) {
+    // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
-      // V ring: a stage is refilled as soon as its PV MMA completes
-      for (int t = 0; t < n_steps; ++t) {
-        const int st = t & 1;
-        if (!mbar_wait(&pv_done[st], ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
-        uint8_t* sV = smem + L::V_OFF0 + st * L::KV_BYTES;
-        const int r0 = tiles[t] >> 9;
-        mbar_arrive_expect_tx(&v_full[st], L::KV_BYTES);
+      const bool is_s = warp == 1;
+      uint32_t g = 0;  // steps issued, across units
+      int st = 0;      // K (S issuer) or V (PV issuer) ring stage and phase
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int lj = 0; ok; ++lj) {
+        const int lb = lj & 1;
+        if (!mbar_wait(&list_full[lb], (lj >> 1) & 1, abort_flag, p.status)) break;
+        const int w = unit_w[lb];
+        if (w >= p.total) break;
+        const int n = unit_of(p, w).n;
+        for (int t = 0; t < n; ++t, ++g) {
+          const int sb = g & 1;
+          if (is_s) {
+            // S of step g: Q of the unit, K of the step, and a score buffer the PV of step
+            // g - 2 has finished reading
+            if (t == 0 && !mbar_wait(&q_full[lb], (lj >> 1) & 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            if (!mbar_wait(&k_full[st], ph, abort_flag, p.status) ||
+                !mbar_wait(&s_free[sb], ((g >> 1) & 1) ^ 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+            const uint64_t kd =
+                sdesc_sw128(smem_u32(smem + L::K_OFF + st * L::STAGE), 16, 1024);
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c)
-          tma_load_3d(sV + c * L::KCHUNK, &tmV, &v_full[st], 64 * c, r0, h);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, 64, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(128, HD, false, true);
-      const uint32_t q0 = smem_u32(sQ);
-      auto issue_s = [&](int t) {
-        const int st = t & 1;
-        const uint32_t k0 = smem_u32(smem + L::K_OFF0 + st * L::KV_BYTES);
+            for (int ks = 0; ks < HD / 16; ++ks) {
+              // Q: dims 16ks..16ks+15 are columns 8ks..8ks+7 of the unit's Q buffer
+              const uint32_t koff = (ks >> 2) * 2 * L::KCHUNK + (ks & 3) * 32;
+              umma_bf16_ts(tmem + L::S_COL + sb * 128, tmem + L::Q_COL + lb * 64 + ks * 8,
+                           kd + (koff >> 4), idesc_s, ks > 0 ? 1u : 0u);
+            }
+            umma_commit(&s_done[sb]);
+            umma_commit(&k_free[st]);
+          } else {
+            // PV of step g: O read out of the previous unit, P of the step, V of the step
+            if (t == 0 && !mbar_wait(o_free, (lj & 1) ^ 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            if (!mbar_wait(&p_full[sb], (g >> 1) & 1, abort_flag, p.status) ||
+                !mbar_wait(&v_full[st], ph, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            constexpr uint32_t idesc_pv = idesc_bf16(128, HD, false, true);
+            const uint64_t vd =
+                sdesc_sw128(smem_u32(smem + L::V_OFF + st * L::STAGE), 2 * L::KCHUNK, 1024);
 #pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
-          const uint32_t qoff = (ks >> 2) * L::QCHUNK + (ks & 3) * 32;
-          const uint32_t koff = (ks >> 2) * L::KCHUNK + (ks & 3) * 32;
-          umma_bf16(tmem + L::S_COL + st * 64, sdesc_sw128(q0 + qoff, 16, 1024),
-                    sdesc_sw128(k0 + koff, 16, 1024), idesc_s, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < 8; ++ks) {
+              // P: keys 16ks..16ks+15 of the step are columns 8ks..8ks+7 of its S buffer;
+              // V: block ks / 4 (X or Y), MN-major, LBO = next 64-dim chunk, SBO = next 8 keys
+              const uint32_t voff = (ks >> 2) * L::KCHUNK + (ks & 3) * 2048;
+              umma_bf16_ts(tmem + L::O_COL, tmem + L::S_COL + sb * 128 + ks * 8, vd + (voff >> 4),
+                           idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
+            }
+            umma_commit(&s_free[sb]);
+            umma_commit(&v_free[st]);
+            if (t == n - 1) umma_commit(o_full);
+          }
+          if (++st == NST) {
+            st = 0;
+            ph ^= 1;
+          }
         }
-        umma_commit(&s_done[st]);
-      };
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
-      if (ok && n_steps > 0) ok = mbar_wait(&k_full[0], 0, abort_flag, p.status);
-      if (ok && n_steps > 0) {
-        tc_fence_after();
-        issue_s(0);
       }
-      for (int t = 0; ok && t < n_steps; ++t) {
-        const int st = t & 1;
-        if (t + 1 < n_steps) {
-          if (!mbar_wait(&k_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort_flag, p.status)) break;
-          tc_fence_after();
-          issue_s(t + 1);
-        }
-        if (!mbar_wait(&p_full[st], (t >> 1) & 1, abort_flag, p.status)) break;
-        if (!mbar_wait(&v_full[st], (t >> 1) & 1, abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t v0 = smem_u32(smem + L::V_OFF0 + st * L::KV_BYTES);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          // P: keys 16ks..16ks+15 are TMEM columns 8ks..8ks+7 of the step's S buffer;
-          // V: MN-major, LBO = next 64-dim column block, SBO = next 8 keys
-          umma_bf16_ts(tmem + L::O_COL, tmem + L::S_COL + st * 64 + ks * 8,
-                       sdesc_sw128(v0 + ks * 2048, L::KCHUNK, 1024), idesc_pv,
-                       (t > 0 || ks > 0) ? 1u : 0u);
-        }
-        umma_commit(&pv_done[st]);
-      }
-      umma_commit(drain);
-      mbar_drain(drain, 0);
+      umma_commit(&drain[is_s ? 0 : 1]);
+      mbar_drain(&drain[is_s ? 0 : 1], 0);
     }
   } else if (warp >= 2 && warp <= 5) {
-    // ---------------------------------------------------------------- softmax
+    // ------------------------------------------------------------ softmax
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const int half = row >> 6;
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t o_addr = t_lane + L::O_COL;
     const float sl2 = p.scale_log2;
-    float m_run = -INFINITY;
-    float l_run = 0.f;
+    uint32_t g = 0;
+    int v_st = 0;  // V stage and phase of step g (the rescale waits on step g - 1's PV)
+    uint32_t v_ph = 0;
+    int pv_st = 0;
+    uint32_t pv_ph = 0;
     bool ok = true;
-    for (int t = 0; t < n_steps; ++t) {
-      const int sb = t & 1;
-      if (!mbar_wait(&s_done[sb], (t >> 1) & 1, abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int e = tiles[t];
-      const int nv = ((e >> half) & 1) ? ((e >> 2) & 127) : 0;
-      const uint32_t s_addr = t_lane + L::S_COL + sb * 64;
-      float sv[64];
-      tmem_ld64(s_addr, sv);
-      // row max, two new scores per three-input max
-      float mx4[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) mx4[u] = -INFINITY;
-      if (nv < 64) {  // warp-uniform: mask the keys of this tile that the row does not see
-#pragma unroll
-        for (int j = 0; j < 64; ++j) sv[j] = j < nv ? sv[j] : -INFINITY;
-      }
-#pragma unroll
-      for (int j = 0; j < 64; j += 2) mx4[(j >> 1) & 3] = fmax3(mx4[(j >> 1) & 3], sv[j], sv[j + 1]);
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
-      const bool need = mx > m_run + kRescaleLog2;
-      const float m_new = need ? mx : m_run;
-      const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      // P = exp2(s * scale - m) rounded to bf16; l sums the unrounded weights.  The
-      // scale-and-shift and the sums run two lanes of fp32 per instruction.
-      uint32_t pk[32];
-      const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
-      float2 ls2[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) ls2[u] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < 64; j += 2) {
-        const float2 x = __ffma2_rn(make_float2(sv[j], sv[j + 1]), sc2, nm2);
-        const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-        ls2[(j >> 1) & 3] = __fadd2_rn(ls2[(j >> 1) & 3], e);
-        pk[j >> 1] = pack_bf16x2(e.x, e.y);
-      }
-      const float lsum = ((ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y)) +
-                         ((ls2[2].x + ls2[2].y) + (ls2[3].x + ls2[3].y));
-      // P over the first 32 columns of this step's S buffer (already read above)
-      tmem_st32_u(s_addr, pk);
-      if (t > 0 && __any_sync(0xffffffffu, need)) {
-        // O must not change under a rescale while the previous step's PV runs
-        if (!mbar_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, p.status)) {
+    for (int lj = 0; ok; ++lj) {
+      const int lb = lj & 1;
+      if (!mbar_wait(&list_full[lb], (lj >> 1) & 1, abort_flag, p.status)) break;
+      const int w = unit_w[lb];
+      if (w >= p.total) break;
+      const int n = unit_of(p, w).n;
+      const int2* list = lists + lb * MAX_STEPS;
+      float m_run = -INFINITY;
+      float l_run = 0.f;
+      for (int t = 0; t < n; ++t, ++g) {
+        const int sb = g & 1;
+        if (!mbar_wait(&s_done[sb], (g >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        rescale_rows<HD>(t_lane + L::O_COL, alpha);
+        const int2 e = list[t];
+        const uint32_t s_addr = t_lane + L::S_COL + sb * 128;
+        float sv[64];
+        uint32_t pk[32];
+        float mx, lsum, alpha;
+        bool need;
+        if (e.x & 1) {
+          // dense: every row uses X (columns 0-63) and Y (64-127)
+          const int cx = (e.x >> 2) & 127, cy = (e.y >> 2) & 127;
+          float my = -INFINITY;
+          if (cy > 0) {
+            tmem_ld64(s_addr + 64, sv);
+            my = masked_max64(sv, cy);
+          }
+          tmem_ld64(s_addr, sv);
+          mx = fmaxf(masked_max64(sv, cx), my) * sl2;
+          need = mx > m_run + kRescaleLog2;
+          const float m_new = need ? mx : m_run;
+          alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          m_run = m_new;
+          lsum = exp_pack64(sv, sl2, m_use, pk);
+          if (cy == 0) tmem_zero32(s_addr + 32);  // no Y keys
+          tmem_st32_u(s_addr, pk);  // P_X over S columns 0-31 (already read)
+          if (cy > 0) {
+            tmem_ld64(s_addr + 64, sv);
+            masked_max64(sv, cy);  // re-apply the mask
+            lsum += exp_pack64(sv, sl2, m_use, pk);
+            tmem_st32_u(s_addr + 32, pk);  // P_Y over S columns 32-63 (already read)
+          }
+        } else {
+          // routed: rows 0-63 use X (columns 0-63), rows 64-127 use Y (64-127)
+          const int c = ((half ? e.y : e.x) >> 2) & 127;
+          tmem_ld64(s_addr + half * 64, sv);
+          mx = masked_max64(sv, c) * sl2;
+          need = mx > m_run + kRescaleLog2;
+          const float m_new = need ? mx : m_run;
+          alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          m_run = m_new;
+          lsum = exp_pack64(sv, sl2, m_use, pk);
+          tmem_zero32(s_addr + (half ^ 1) * 32);  // the other block's keys
+          tmem_st32_u(s_addr + half * 32, pk);
+        }
+        if (t > 0 && __any_sync(0xffffffffu, need)) {
+          // O must not change under a rescale while the previous step's PV runs
+          if (!mbar_wait(&v_free[pv_st], pv_ph, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          rescale_rows<HD>(o_addr, alpha);
+        }
+        l_run = fmaf(l_run, alpha, lsum);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[sb]);
+        pv_st = v_st;
+        pv_ph = v_ph;
+        if (++v_st == NST) {
+          v_st = 0;
+          v_ph ^= 1;
+        }
       }
-      l_run = fmaf(l_run, alpha, lsum);
-      m_run = m_new;
+      if (!ok) break;
+      // hand the row sums over once the epilogue has read the previous unit's
+      if (!mbar_wait(o_free, (lj & 1) ^ 1, abort_flag, p.status)) break;
+      lbuf[row] = l_run;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(l_ready);
+    }
+  } else if (warp >= 7 && warp <= 10) {
+    // ------------------------------------------------------------ epilogue, Q, scheduler
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int half = row >> 6;
+    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+    const bool sched = warp == 7;
+    bool ended = false;  // (warp 7) the end of the unit sequence has been published
+    auto publish = [&](int buf, int w) {
+      if (lane == 0) unit_w[buf] = w;
+      if (w < p.total) build_list(p, unit_of(p, w), lists + buf * MAX_STEPS, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&list_full[buf]);
+      if (w >= p.total) ended = true;
+    };
+    // Q rows of unit u (this thread's row) into tensor-memory Q buffer buf
+    auto load_q = [&](int buf, const Unit& u) {
+      int grow;
+      if (u.prefix) {
+        grow = u.unit * 128 + row;
+      } else {
+        // an odd tile count leaves the last unit's second half without a tile: it repeats a
+        const int tile = (half && u.tb < p.Tv) ? u.tb : u.ta;
+        int f, c;
+        tile_span(p.geom, tile, &f, &c);
+        grow = f + (row & 63);
+      }
+      const bool valid = grow < p.N;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + ((size_t)u.h * p.N + (valid ? grow : 0)) * HD);
+      uint32_t wq[HD / 2];
+#pragma unroll
+      for (int i = 0; i < HD / 8; ++i) {
+        const uint4 v = valid ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+        wq[4 * i + 0] = v.x;
+        wq[4 * i + 1] = v.y;
+        wq[4 * i + 2] = v.z;
+        wq[4 * i + 3] = v.w;
+      }
+#pragma unroll
+      for (int c = 0; c < HD / 64; ++c)
+        tmem_st32_u(t_lane + L::Q_COL + buf * 64 + c * 32, wq + 32 * c);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[sb]);
+      if (lane == 0) mbar_arrive(&q_full[buf]);
+    };
+    int end_at = 1 << 30;  // first unit index known to be past the end
+    int wc0 = 0, wc1 = 0;  // units on list buffers 0 and 1
+    bool ok = true;
+    if (sched) {
+      publish(0, blockIdx.x);
+      if (!ended) publish(1, gridDim.x + blockIdx.x);
     }
-    if (ok && n_steps > 0 &&
-        mbar_wait(&pv_done[(n_steps - 1) & 1], ((n_steps - 1) >> 1) & 1, abort_flag, p.status)) {
+    for (int b = 0; b < 2 && ok; ++b) {
+      if (!mbar_wait(&list_full[b], 0, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      const int w = unit_w[b];
+      if (b) wc1 = w; else wc0 = w;
+      if (w >= p.total) {
+        end_at = b;
+        break;
+      }
+      load_q(b, unit_of(p, w));
+    }
+    const int A = p.H * HD;
+    for (int lj = 0; ok && lj < end_at; ++lj) {
+      const int ob = lj & 1;
+      const Unit u = unit_of(p, ob ? wc1 : wc0);
+      if (!mbar_wait(o_full, lj & 1, abort_flag, p.status)) break;
+      if (!mbar_wait(l_ready, lj & 1, abort_flag, p.status)) break;
       tc_fence_after();
+      const float l = lbuf[row];
+      float o[HD];
+      if constexpr (HD == 128)
+        tmem_ld128(t_lane + L::O_COL, o);
+      else
+        tmem_ld64(t_lane + L::O_COL, o);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);  // O and lbuf may take the next unit
       int grow, tile = -1;
       bool store;
-      if (is_prefix) {
-        grow = unit * 128 + row;
+      if (u.prefix) {
+        grow = u.unit * 128 + row;
         store = grow < p.n_prefix;
       } else {
-        tile = half ? tb : ta;
+        tile = half ? u.tb : u.ta;
         int f = 0, c = 0;
         if (tile < p.Tv) tile_span(p.geom, tile, &f, &c);
         grow = f + (row & 63);
         store = (row & 63) < c;
       }
-      const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
-      const int A = p.H * HD;
-      const bool mix = !is_prefix && p.gate != nullptr && p.pooled != nullptr;
-#pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
-        float o[32];
-        tmem_ld32(t_lane + L::O_COL + c * 32, o);
-        if (store) {
+      const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+      const bool mix = !u.prefix && p.gate != nullptr && p.pooled != nullptr;
+      if (store) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] *= inv_l;
+        for (int c = 0; c < HD / 32; ++c) {
+          float* oc = o + 32 * c;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) oc[j] *= inv_l;
           if (mix) {
             const uint4* g4 =
-                reinterpret_cast<const uint4*>(p.gate + (size_t)grow * A + h * HD + c * 32);
+                reinterpret_cast<const uint4*>(p.gate + (size_t)grow * A + u.h * HD + c * 32);
             const float4* pb4 = reinterpret_cast<const float4*>(
-                p.pooled + ((size_t)h * p.Tv + tile) * HD + c * 32);
+                p.pooled + ((size_t)u.h * p.Tv + tile) * HD + c * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const uint4 g = __ldg(g4 + i);
+              const uint4 gv = __ldg(g4 + i);
               const float4 b0 = __ldg(pb4 + 2 * i), b1 = __ldg(pb4 + 2 * i + 1);
-              o[8 * i + 0] = fmaf(bf16_lo(g.x), b0.x, o[8 * i + 0]);
-              o[8 * i + 1] = fmaf(bf16_hi(g.x), b0.y, o[8 * i + 1]);
-              o[8 * i + 2] = fmaf(bf16_lo(g.y), b0.z, o[8 * i + 2]);
-              o[8 * i + 3] = fmaf(bf16_hi(g.y), b0.w, o[8 * i + 3]);
-              o[8 * i + 4] = fmaf(bf16_lo(g.z), b1.x, o[8 * i + 4]);
-              o[8 * i + 5] = fmaf(bf16_hi(g.z), b1.y, o[8 * i + 5]);
-              o[8 * i + 6] = fmaf(bf16_lo(g.w), b1.z, o[8 * i + 6]);
-              o[8 * i + 7] = fmaf(bf16_hi(g.w), b1.w, o[8 * i + 7]);
+              oc[8 * i + 0] = fmaf(bf16_lo(gv.x), b0.x, oc[8 * i + 0]);
+              oc[8 * i + 1] = fmaf(bf16_hi(gv.x), b0.y, oc[8 * i + 1]);
+              oc[8 * i + 2] = fmaf(bf16_lo(gv.y), b0.z, oc[8 * i + 2]);
+              oc[8 * i + 3] = fmaf(bf16_hi(gv.y), b0.w, oc[8 * i + 3]);
+              oc[8 * i + 4] = fmaf(bf16_lo(gv.z), b1.x, oc[8 * i + 4]);
+              oc[8 * i + 5] = fmaf(bf16_hi(gv.z), b1.y, oc[8 * i + 5]);
+              oc[8 * i + 6] = fmaf(bf16_lo(gv.w), b1.z, oc[8 * i + 6]);
+              oc[8 * i + 7] = fmaf(bf16_hi(gv.w), b1.w, oc[8 * i + 7]);
             }
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t)grow * A + h * HD + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t)grow * A + u.h * HD + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            dst[i] = make_uint4(pack_bf16x2(o[8 * i + 0], o[8 * i + 1]),
-                                pack_bf16x2(o[8 * i + 2], o[8 * i + 3]),
-                                pack_bf16x2(o[8 * i + 4], o[8 * i + 5]),
-                                pack_bf16x2(o[8 * i + 6], o[8 * i + 7]));
+            dst[i] = make_uint4(pack_bf16x2(oc[8 * i + 0], oc[8 * i + 1]),
+                                pack_bf16x2(oc[8 * i + 2], oc[8 * i + 3]),
+                                pack_bf16x2(oc[8 * i + 4], oc[8 * i + 5]),
+                                pack_bf16x2(oc[8 * i + 6], oc[8 * i + 7]));
           }
         }
+      }
+      // unit lj + 2 takes this list and Q buffer once all four warps are done with unit lj
+      // (its S MMAs completed before o_full)
+      if (sched && !ended) {
+        if (!mbar_wait(o_free, lj & 1, abort_flag, p.status)) break;
+        int w2 = 0;
+        if (lane == 0) w2 = 2 * (int)gridDim.x + atomicAdd(p.counter, 1);
+        publish(ob, __shfl_sync(0xffffffffu, w2, 0));
+      }
+      if (lj + 1 < end_at) {  // unit lj + 1 exists, so unit lj + 2 (or the end) is published
+        if (!mbar_wait(&list_full[ob], ((lj + 2) >> 1) & 1, abort_flag, p.status)) break;
+        const int w2 = unit_w[ob];
+        if (ob) wc1 = w2; else wc0 = w2;
+        if (w2 >= p.total)
+          end_at = lj + 2;
+        else
+          load_q(ob, unit_of(p, w2));
       }
     }
   }
@@ -435,38 +654,44 @@ __global__ void __launch_bounds__(THREADS, 2)
 template <int HD>
 cudaError_t launch_hd(const AttnArgs& a, cudaStream_t stream) {
   using L = Layout<HD>;
-  CUtensorMap tq, tk, tv;
-  if (!make_tmap_3d(&tq, a.q, a.H, a.N, HD) || !make_tmap_3d(&tk, a.k, a.H, a.N, HD) ||
-      !make_tmap_3d(&tv, a.v, a.H, a.N, HD))
+  CUtensorMap tk, tv;
+  if (!make_tmap_3d(&tk, a.k, a.H, a.N, HD) || !make_tmap_3d(&tv, a.v, a.H, a.N, HD))
     return cudaErrorInvalidValue;
   Params p;
   p.N = a.N;
   p.H = a.H;
   p.n_prefix = a.n_prefix;
-  p.n_video = a.n_video;
   p.Tv = a.Tv;
   p.ksel = a.ksel;
   p.n_pre_units = (a.n_prefix + 127) / 128;
+  p.n_vid_units = (a.Tv + 1) / 2;
+  p.total = (p.n_pre_units + p.n_vid_units) * a.H;
+  p.steps_all = (a.N + 127) / 128;
+  p.steps_pre = (a.n_prefix + 127) / 128;
+  if (p.steps_all > MAX_STEPS || p.steps_pre + a.ksel > MAX_STEPS) return cudaErrorInvalidValue;
   p.geom = a.geom;
+  p.q = a.q;
   p.idx = a.idx;
   p.gate = a.gate;
   p.pooled = a.pooled;
   p.out = a.out;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
   p.status = a.status;
-  const int n_units = p.n_pre_units + (a.Tv + 1) / 2;
+  p.counter = a.counter;
   auto kern = attention_kernel<HD>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<n_units * a.H, THREADS, L::SMEM, stream>>>(tq, tk, tv, p);
+  const int grid = p.total < num_sms() ? p.total : num_sms();
+  kern<<<grid, THREADS, L::SMEM, stream>>>(tk, tv, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
-  if (a.N <= 0 || a.H <= 0 || a.N > MAX_TILES * 64) return cudaErrorInvalidValue;
+  if (a.N <= 0 || a.H <= 0 || a.N > MAX_STEPS * 128 || a.counter == nullptr)
+    return cudaErrorInvalidValue;
   if (a.d == 128) return launch_hd<128>(a, stream);
   if (a.d == 64) return launch_hd<64>(a, stream);
   return cudaErrorInvalidValue;

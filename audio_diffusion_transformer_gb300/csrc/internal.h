@@ -56,6 +56,7 @@ struct AttnArgs {
   const float* pooled;        // [H, Tv, d] or null
   __nv_bfloat16* out;         // [N, A]
   int* status;
+  int* counter;  // unit counter of the persistent kernel; zero on entry (the router clears it)
 };
 
 cudaError_t launch_attention(const AttnArgs& args, cudaStream_t stream);
@@ -69,6 +70,7 @@ struct RouterArgs {
   float* scores;  // [H, Tv, Tv]
   int* idx;       // [H, Tv, ksel]
   float* pooled;  // [H, Tv, d] or null (skip)
+  int* counter;   // set to zero for the attention kernel that follows
 };
 
 cudaError_t launch_router(const RouterArgs& args, cudaStream_t stream);

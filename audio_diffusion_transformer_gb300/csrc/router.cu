@@ -42,10 +42,12 @@ template <int D>
 __global__ void __launch_bounds__(128)
     tile_means_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                       const __nv_bfloat16* __restrict__ v, float* __restrict__ means, int N, int H,
-                      const TileGeom geom, int Tv) {
+                      const TileGeom geom, int Tv, int* __restrict__ counter) {
   constexpr int CPL = D / 32;  // columns per lane: 4 (d = 128) or 2 (d = 64)
   __shared__ float part[4][D];
   const int t = blockIdx.x, h = blockIdx.y, which = blockIdx.z;
+  // the attention kernel, which runs after the router, fetches work units from this counter
+  if ((t | h | which | threadIdx.x) == 0 && counter != nullptr) *counter = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const __nv_bfloat16* X = which == 0 ? q : (which == 1 ? k : v);
   int r0, nv;
@@ -292,10 +294,10 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream) {
   dim3 g1(a.Tv, a.H, 3);
   if (a.d == 128)
     tile_means_kernel<128><<<g1, 128, 0, stream>>>(a.q, a.k, a.v, a.means, a.N, a.H, a.geom,
-                                                   a.Tv);
+                                                   a.Tv, a.counter);
   else
     tile_means_kernel<64><<<g1, 128, 0, stream>>>(a.q, a.k, a.v, a.means, a.N, a.H, a.geom,
-                                                  a.Tv);
+                                                  a.Tv, a.counter);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t shm =

@@ -165,9 +165,9 @@ h3dit_status h3dit_block_forward(const h3dit_shape* shape, const h3dit_block_wei
  * attends to all prefix rows plus the rows of its selected tiles.  Scale 1/sqrt(d).
  * Tiles are 64-row slices or clipped cubes of the video grid (see h3dit_shape;
  * with a grid, every buffer holds the video rows in cube order); Tv is the number
- * of video tiles (h3dit_tile_spans), at most 1,024, and the prefix chunks plus two
- * query tiles' selections (ceil(P / 64) + 2 min(k, Tv)) at most 1,024 entries --
- * larger shapes return H3DIT_ERR_SHAPE.
+ * of video tiles (h3dit_tile_spans), at most 1,024, and the attention steps of a
+ * video query tile, ceil(P / 128) + min(k, Tv), at most 512 -- larger shapes return
+ * H3DIT_ERR_SHAPE.
  * The pooled branch and mix run when H3DIT_POOLED is set and gate is given.
  */
 h3dit_status h3dit_routed_attention(const h3dit_shape* shape, const void* q, const void* k,

@@ -84,7 +84,7 @@ def test_all_scores_equal_tie_rule(h3):
 
 
 def test_maximum_rows(h3):
-    # the attention's key-tile list holds at most 1,024 tiles: 65,408 rows (1,022 tiles)
+    # the largest accepted sequence: 65,408 rows (1,022 tiles)
     shp = S.BlockShape(0, 0, 1022 * 64, hidden=256, heads=1, head_dim=64, mlp_width=1024,
                        topk=8)
     inp = S.attention_inputs(shp, 53, structured=0.3, with_gate=False)
