@@ -18,8 +18,10 @@
 //     (N = 128); rows of a read only the X columns, rows of b only the Y columns, and
 //     the softmax writes P block-diagonally (zeros in the other block), so the PV MMA
 //     (K = 128) adds each row's own keys and nothing else.
-//   A video unit takes ceil(P / 128) + k steps however much the two selections
-//   overlap, and a row's softmax sees 64 scores per routed step.  A key block with
+//   Key tiles that both query tiles selected go two to a dense step (no discarded
+//   blocks), and the routed steps pair the tiles only a selected with those only b
+//   selected: a video unit with s tiles in common takes ceil(P / 128) + ceil(s / 2) +
+//   (k - s) steps, and a row's softmax sees 64 scores per routed step.  A key block with
 //   fewer than 64 rows (a clipped cube, the end of a range) masks the rest.
 //
 // Persistent: one CTA per SM.  A CTA takes units blockIdx.x and gridDim.x + blockIdx.x,
@@ -71,8 +73,9 @@ struct Layout {
   static constexpr int V_OFF = K_OFF + NST * STAGE;
   static constexpr int LIST_OFF = V_OFF + NST * STAGE;          // two step lists (int2)
   static constexpr int LBUF_OFF = LIST_OFF + 2 * MAX_STEPS * 8;  // 128 row sums
-  static constexpr int UNIT_OFF = LBUF_OFF + 128 * 4;            // two unit numbers
-  static constexpr int BAR_OFF = UNIT_OFF + 16;
+  static constexpr int UNIT_OFF = LBUF_OFF + 128 * 4;            // unit numbers, step counts
+  static constexpr int MASK_OFF = UNIT_OFF + 16;                 // list builder's tile masks
+  static constexpr int BAR_OFF = MASK_OFF + 2 * 32 * 4;
   static constexpr int USED = BAR_OFF + 256;
   static constexpr int SMEM = USED + 1024;                       // + alignment slack
   static constexpr uint32_t S_COL = 0;    // two 128-column score buffers
@@ -97,7 +100,7 @@ struct Params {
 };
 
 struct Unit {
-  int h, unit, ta, tb, n;
+  int h, unit, ta, tb;
   bool prefix;
 };
 
@@ -115,7 +118,6 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int w) {
   u.prefix = u.unit < p.n_pre_units;
   u.ta = 2 * (u.unit - p.n_pre_units);
   u.tb = u.ta + 1;
-  u.n = u.prefix ? p.steps_all : p.steps_pre + p.ksel;
   return u;
 }
 
@@ -124,13 +126,25 @@ __device__ __forceinline__ int chunk_entry(int r0, int limit) {
   return (r0 << 9) | (max(0, min(64, limit - r0)) << 2) | 1;
 }
 
-// Step list of unit u, written by one warp.
-__device__ void build_list(const Params& p, const Unit& u, int2* list, int lane) {
+// Step list of unit u, written by one warp; returns the unit's step count.
+//   prefix unit: ceil(N / 128) dense steps over consecutive 128-row chunks;
+//   video unit: ceil(P / 128) dense steps over the prefix rows, then the key tiles both
+//   query tiles selected, two to a dense step, then routed steps pairing the tiles only
+//   tile a selected with those only tile b selected (ascending tile order throughout).
+// The selections become bitmasks over the (at most 1,024) video tiles in masks[0..63]:
+// lane i owns the words for tiles 32i..32i+31, so ascending order is lane order.
+__device__ int build_list(const Params& p, const Unit& u, int2* list, uint32_t* masks,
+                          int lane) {
   const int limit = u.prefix ? p.N : p.n_prefix;
   const int n_dense = u.prefix ? p.steps_all : p.steps_pre;
   for (int s = lane; s < n_dense; s += 32)
     list[s] = make_int2(chunk_entry(128 * s, limit), chunk_entry(128 * s + 64, limit));
-  if (u.prefix) return;
+  if (u.prefix) return n_dense;
+  uint32_t* ma = masks;
+  uint32_t* mb = masks + 32;
+  ma[lane] = 0u;
+  mb[lane] = 0u;
+  __syncwarp();
   const int* ia = p.idx + ((size_t)u.h * p.Tv + u.ta) * p.ksel;
   // an odd tile count leaves the last unit's second half without a tile: it repeats a
   const int* ib = u.tb < p.Tv ? p.idx + ((size_t)u.h * p.Tv + u.tb) * p.ksel : ia;
@@ -138,11 +152,54 @@ __device__ void build_list(const Params& p, const Unit& u, int2* list, int lane)
     // indices come from the router; clamp defensively
     const int a = min(max(__ldg(ia + i), 0), p.Tv - 1);
     const int b = min(max(__ldg(ib + i), 0), p.Tv - 1);
-    int fa, ca, fb, cb;
-    tile_span(p.geom, a, &fa, &ca);
-    tile_span(p.geom, b, &fb, &cb);
-    list[n_dense + i] = make_int2((fa << 9) | (ca << 2), (fb << 9) | (cb << 2));
+    atomicOr(&ma[a >> 5], 1u << (a & 31));
+    atomicOr(&mb[b >> 5], 1u << (b & 31));
   }
+  __syncwarp();
+  const uint32_t A = ma[lane], B = mb[lane];
+  const uint32_t m_sh = A & B, m_ao = A & ~B, m_bo = B & ~A;
+  // exclusive prefix counts over the lanes (tiles below this lane's 32)
+  int e_sh = __popc(m_sh), e_ao = __popc(m_ao), e_bo = __popc(m_bo);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, e_sh, o);
+    const int y = __shfl_up_sync(0xffffffffu, e_ao, o);
+    const int z = __shfl_up_sync(0xffffffffu, e_bo, o);
+    if (lane >= o) {
+      e_sh += x;
+      e_ao += y;
+      e_bo += z;
+    }
+  }
+  const int n_sh = __shfl_sync(0xffffffffu, e_sh, 31);
+  const int n_ao = __shfl_sync(0xffffffffu, e_ao, 31);
+  const int n_bo = __shfl_sync(0xffffffffu, e_bo, 31);
+  e_sh -= __popc(m_sh);
+  e_ao -= __popc(m_ao);
+  e_bo -= __popc(m_bo);
+  const int n_shared = (n_sh + 1) / 2;
+  const int n_routed = max(n_ao, n_bo);  // equal unless the router repeated an index
+  const int base_r = n_dense + n_shared;
+  // empty halves (entry 0: row 0, no keys): the Y of an odd last shared step, and routed
+  // halves without a partner
+  if (lane == 0 && (n_sh & 1)) list[base_r - 1].y = 0;
+  for (int i = lane; i < n_routed; i += 32) list[base_r + i] = make_int2(0, 0);
+  __syncwarp();
+  int* words = reinterpret_cast<int*>(list);
+  auto put = [&](uint32_t m, int k, int at, int stride, int flag) {
+    while (m) {
+      const int t = lane * 32 + __ffs(m) - 1;
+      m &= m - 1;
+      int f, c;
+      tile_span(p.geom, t, &f, &c);
+      words[at + k * stride] = (f << 9) | (c << 2) | flag;
+      ++k;
+    }
+  };
+  put(m_sh, e_sh, 2 * n_dense, 1, 1);     // shared k -> step n_dense + k/2, X or Y
+  put(m_ao, e_ao, 2 * base_r, 2, 0);      // only a: X of routed step k
+  put(m_bo, e_bo, 2 * base_r + 1, 2, 0);  // only b: Y of routed step k
+  return base_r + n_routed;
 }
 
 // max of three fp32 values in one instruction
@@ -218,6 +275,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   int2* lists = reinterpret_cast<int2*>(smem + L::LIST_OFF);
   float* lbuf = reinterpret_cast<float*>(smem + L::LBUF_OFF);
   volatile int* unit_w = reinterpret_cast<volatile int*>(smem + L::UNIT_OFF);
+  volatile int* unit_n = unit_w + 2;  // step counts of the units on list buffers 0 and 1
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* k_full = bars + 0;      // [NST] K stage landed
   uint64_t* k_free = bars + 3;      // [NST] the stage's S MMAs completed
@@ -287,8 +345,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (w >= p.total) break;
         const Unit u = unit_of(p, w);
         const int2* list = lists + lb * MAX_STEPS;
+        const int n = unit_n[lb];
         bool ok = true;
-        for (int t = 0; t < u.n; ++t) {
+        for (int t = 0; t < n; ++t) {
           if (!mbar_wait(&freed[st], ph ^ 1, abort_flag, p.status)) {
             ok = false;
             break;
@@ -327,7 +386,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(&list_full[lb], (lj >> 1) & 1, abort_flag, p.status)) break;
         const int w = unit_w[lb];
         if (w >= p.total) break;
-        const int n = unit_of(p, w).n;
+        const int n = unit_n[lb];
         for (int t = 0; t < n; ++t, ++g) {
           const int sb = g & 1;
           if (is_s) {
@@ -410,7 +469,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!mbar_wait(&list_full[lb], (lj >> 1) & 1, abort_flag, p.status)) break;
       const int w = unit_w[lb];
       if (w >= p.total) break;
-      const int n = unit_of(p, w).n;
+      const int n = unit_n[lb];
       const int2* list = lists + lb * MAX_STEPS;
       float m_run = -INFINITY;
       float l_run = 0.f;
@@ -500,9 +559,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
     const bool sched = warp == 7;
     bool ended = false;  // (warp 7) the end of the unit sequence has been published
+    uint32_t* masks = reinterpret_cast<uint32_t*>(smem + L::MASK_OFF);
     auto publish = [&](int buf, int w) {
-      if (lane == 0) unit_w[buf] = w;
-      if (w < p.total) build_list(p, unit_of(p, w), lists + buf * MAX_STEPS, lane);
+      const int n =
+          w < p.total ? build_list(p, unit_of(p, w), lists + buf * MAX_STEPS, masks, lane) : 0;
+      if (lane == 0) {
+        unit_w[buf] = w;
+        unit_n[buf] = n;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&list_full[buf]);
       if (w >= p.total) ended = true;
