@@ -2,16 +2,25 @@
 //
 // y[M, N] = a[M, K] * w[N, K]^T with fp32 accumulation in TMEM (TensorFold
 // #949 "Precision": bf16 weights and activations, fp32 sums).  One persistent
-// CTA per SM walks 128 x 256 output tiles in a grouped order (8 or 16 row-blocks
-// per group, so a wave of tiles shares A and B panels in L2).  Warp roles:
-//   warp 0      TMA producer: 64-wide K slices of A (128 rows) and W (256 rows)
-//               into a 4-stage shared-memory ring (128-byte swizzle)
-//   warp 1      tcgen05.mma issuer (one thread), M=128 N=256 K=16 per op, into
-//               one of two 256-column TMEM accumulators
-//   warps 2..5  epilogue: TMEM -> registers (warp w reads lanes 32*(w%4)..),
-//               bias / GELU / SwiGLU / gated residual / q-k norm + rotary, bf16 stores
-// The double accumulator lets the epilogue of tile i overlap the K loop of
-// tile i+1.  No split-K and no atomics: results are deterministic.
+// CTA per SM walks the output tiles in a grouped order (8 or 16 row-blocks per
+// group, so a wave of tiles shares A and B panels in L2).  Two tilings:
+//   128 x 256 tiles (every epilogue of the block: GELU, SwiGLU, q/k norm + rotary,
+//   gated residual; the output heads):
+//     warp 0      TMA producer: 64-wide K slices of A (128 rows) and W (256 rows)
+//                 into a 4-stage shared-memory ring (128-byte swizzle)
+//     warp 1      tcgen05.mma issuer (one thread), M=128 N=256 K=16 per op, into
+//                 one of two 256-column TMEM accumulators, so the epilogue of tile i
+//                 overlaps the K loop of tile i+1
+//     warps 2..5  epilogue: TMEM -> registers (warp w reads lanes 32*(w%4)..)
+//   256 x 256 tiles ("pair" tiles: plain stores, h3dit_linear): two M=128 MMAs per K
+//   step share the W slice, so each stage's 64 KB (3 stages) feeds twice the tensor
+//   work of a 128-row stage; the two 256-column accumulators fill TMEM, so the epilogue
+//   (warps 2..9, one half each) runs between tiles while the producer prefills the ring.
+//   The first bands of 256 rows are pair tiles and the remaining rows 128 x 256 tiles on
+//   the same accumulator, in a number that balances the last wave across the SMs.  An
+//   epilogue that reads memory (the gated residual) stays on the double accumulator:
+//   between pair tiles it cannot hide behind the next K loop.
+// No split-K and no atomics: results are deterministic.
 #include <math.h>
 
 #include "internal.h"
@@ -22,31 +31,34 @@ namespace h3 {
 namespace {
 
 #ifndef H3_GEMM_STAGES
-#define H3_GEMM_STAGES 4
+#define H3_GEMM_STAGES 4  // 128 x 256 tiles: a 4-stage ring of 48 KB stages
 #endif
 
 constexpr int BM = 128, BK = 64;
 constexpr int BN_WIDE = 256;  // output tile width of the projections
-constexpr int STAGES = H3_GEMM_STAGES;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int THREADS = 192;
 
-// Per tile width BN: shared-memory ring and TMEM accumulator sizes.
-template <int BN>
+// Per tile width BN and tiling: shared-memory ring, threads and TMEM accumulators.
+template <int BN, bool PAIR>
 struct Tile {
-  static constexpr int B_BYTES = BN * BK * 2;  // 32 KB at BN = 256
+  static constexpr int A_ROWS = PAIR ? 2 * BM : BM;  // A rows per stage
+  static constexpr int A_BYTES = A_ROWS * BK * 2;    // 16 KB, or 32 KB for pair tiles
+  static constexpr int B_BYTES = BN * BK * 2;        // 32 KB at BN = 256
+  static constexpr int STAGES = PAIR ? 3 : H3_GEMM_STAGES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
-  // two accumulators of BN columns, allocated as a power of two >= 32
+  static constexpr int EPI_WARPS = PAIR ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int NACC = PAIR ? 1 : 2;  // accumulators (a pair tile's two halves fill TMEM)
   static constexpr uint32_t TMEM_COLS =
-      2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512));
-  // accumulator b starts at column b * ACC_STRIDE (a power of two)
-  static constexpr uint32_t ACC_STRIDE = TMEM_COLS / 2;
+      PAIR ? 512 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+  // accumulator b (or, for pair tiles, row half b) starts at column b * ACC_STRIDE
+  static constexpr uint32_t ACC_STRIDE = PAIR ? 256 : TMEM_COLS / 2;
 };
 
 struct Params {
   int M, N, K;
   int group;  // row-blocks per raster group
+  int pairs;  // pair tiling: bands of 256 rows taken as pair tiles (rows beyond: 128-row tiles)
   const __nv_bfloat16* bias;
   __nv_bfloat16* y;
   const float* gate;
@@ -116,6 +128,24 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const float* v) 
     u.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
     u.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
     d[i] = u;
+  }
+}
+
+// Tile t of the pair tiling: first pairs x num_n tiles of 256 rows, then 128-row tiles for
+// the rest; each region in grouped raster order.  two = true for a 256-row tile.
+__device__ __forceinline__ void pair_tile(const Params& p, int tile, int num_n, int& m0,
+                                          bool& two, int& n_blk) {
+  const int big = p.pairs * num_n;
+  int mb;
+  if (tile < big) {
+    tile_coords(tile, p.pairs, num_n, p.group > 1 ? p.group / 2 : 1, mb, n_blk);
+    m0 = mb * 2 * BM;
+    two = true;
+  } else {
+    const int rest = (p.M + BM - 1) / BM - 2 * p.pairs;
+    tile_coords(tile - big, rest, num_n, p.group, mb, n_blk);
+    m0 = (2 * p.pairs + mb) * BM;
+    two = false;
   }
 }
 
@@ -276,12 +306,15 @@ __device__ __forceinline__ void epilogue_qkvg(const Params& p, uint32_t t_row, i
   }
 }
 
-template <int EPI, int HD, int BN>
-__global__ void __launch_bounds__(THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const Params p) {
-  using T = Tile<BN>;
+template <int EPI, int HD, int BN, bool PAIR>
+__global__ void __launch_bounds__(Tile<BN, PAIR>::THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA1,
+                const __grid_constant__ CUtensorMap tmB, const Params p) {
+  // tmA: A with boxes of A_ROWS rows; tmA1 (pair tiling): boxes of 128 rows
+  using T = Tile<BN, PAIR>;
+  constexpr int A_BYTES = T::A_BYTES;
   constexpr int B_BYTES = T::B_BYTES;
+  constexpr int STAGES = T::STAGES;
   constexpr int STAGE_BYTES = T::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -301,8 +334,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int lane = threadIdx.x & 31;
   const int num_m = (p.M + BM - 1) / BM;
   const int num_n = p.N / BN;
-  const int num_tiles = num_m * num_n;
+  const int num_tiles = PAIR ? (num_m - p.pairs) * num_n : num_m * num_n;
   const int num_k = p.K / BK;
+  // tile -> first row, whether it is a 256-row pair tile, column block
+  auto coords = [&](int tile, int& m0, bool& two, int& n_blk) {
+    if constexpr (PAIR) {
+      pair_tile(p, tile, num_n, m0, two, n_blk);
+    } else {
+      int m_blk;
+      tile_coords(tile, num_m, num_n, p.group, m_blk, n_blk);
+      m0 = m_blk * BM;
+      two = false;
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -311,7 +355,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], T::EPI_WARPS);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -323,6 +367,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
+    if (PAIR) prefetch_tmap(&tmA1);
     prefetch_tmap(&tmB);
   }
   tc_fence_before();
@@ -336,15 +381,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        int m_blk, n_blk;
-        tile_coords(tile, num_m, num_n, p.group, m_blk, n_blk);
+        int m0, n_blk;
+        bool two;
+        coords(tile, m0, two, n_blk);
+        // a 128-row tile of the pair tiling loads half an A stage
+        const uint32_t bytes = (PAIR && !two) ? STAGE_BYTES - A_BYTES / 2 : STAGE_BYTES;
         for (int kb = 0; kb < num_k; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, m_blk * BM);
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          tma_load_2d(sA + stage * A_BYTES, (PAIR && !two) ? &tmA1 : &tmA, &full[stage], kb * BK,
+                      m0);
           tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, n_blk * BN);
           if (++stage == STAGES) {
             stage = 0;
@@ -362,6 +411,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        int m0, n_blk;
+        bool two;
+        coords(tile, m0, two, n_blk);
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * T::ACC_STRIDE;
@@ -375,9 +427,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(b0 + k * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+            umma_bf16(d_tmem, sdesc_sw128(a0 + k * 32, 16, 1024), bd, idesc, accum);
+            // rows 128..255 of a pair tile (16 KB into the stage) into the second half
+            if (PAIR && two)
+              umma_bf16(d_tmem + T::ACC_STRIDE, sdesc_sw128(a0 + BM * 128 + k * 32, 16, 1024), bd,
+                        idesc, accum);
           }
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -387,7 +443,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (!ok) break;
         umma_commit(&acc_full[acc]);
-        if (++acc == 2) {
+        if (++acc == T::NACC) {
           acc = 0;
           acc_phase ^= 1;
         }
@@ -398,27 +454,32 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     const int quad = warp & 3;
+    const int half = PAIR ? (warp - 2) / 4 : 0;  // pair tiling: warps 6..9 take rows 128..255
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      int m_blk, n_blk;
-      tile_coords(tile, num_m, num_n, p.group, m_blk, n_blk);
+      int m0, n_blk;
+      bool two;
+      coords(tile, m0, two, n_blk);
       if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
-      const int row = m_blk * BM + quad * 32 + lane;
-      const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16) + acc * T::ACC_STRIDE;
-      if (EPI == kEpiQkvg)
-        epilogue_qkvg<HD, BN>(p, t_row, row, n_blk * BN);
-      else if (EPI == kEpiSwiglu)
-        epilogue_swiglu(p, t_row, row, n_blk * BN);
-      else if (EPI == kEpiHeadEuler)
-        epilogue_head<BN>(p, t_row, row, n_blk * BN);
-      else
-        epilogue_rows<EPI, BN>(p, t_row, row, n_blk * BN);
+      if (half == 0 || two) {
+        const int row = m0 + half * BM + quad * 32 + lane;
+        const uint32_t t_row =
+            tmem + ((uint32_t)(quad * 32) << 16) + (acc + half) * T::ACC_STRIDE;
+        if (EPI == kEpiQkvg)
+          epilogue_qkvg<HD, BN>(p, t_row, row, n_blk * BN);
+        else if (EPI == kEpiSwiglu)
+          epilogue_swiglu(p, t_row, row, n_blk * BN);
+        else if (EPI == kEpiHeadEuler)
+          epilogue_head<BN>(p, t_row, row, n_blk * BN);
+        else
+          epilogue_rows<EPI, BN>(p, t_row, row, n_blk * BN);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
-      if (++acc == 2) {
+      if (++acc == T::NACC) {
         acc = 0;
         acc_phase ^= 1;
       }
@@ -433,17 +494,30 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int EPI, int HD, int BN = BN_WIDE>
-cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
-                       cudaStream_t stream) {
-  auto kern = gemm_kernel<EPI, HD, BN>;
-  constexpr int smem = Tile<BN>::SMEM_BYTES;
+template <int EPI, int HD, int BN = BN_WIDE, bool PAIR = false>
+cudaError_t launch_one(const GemmArgs& g, const CUtensorMap& tb, Params p, cudaStream_t stream) {
+  using T = Tile<BN, PAIR>;
+  CUtensorMap ta, ta1;
+  if (!make_tmap_2d(&ta, g.a, g.M, g.K, T::A_ROWS)) return cudaErrorInvalidValue;
+  ta1 = ta;
+  if (PAIR && !make_tmap_2d(&ta1, g.a, g.M, g.K, BM)) return cudaErrorInvalidValue;
+  auto kern = gemm_kernel<EPI, HD, BN, PAIR>;
+  constexpr int smem = T::SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int tiles = ((p.M + BM - 1) / BM) * (p.N / BN);
   const int sms = num_sms();
+  const int num_m = (p.M + BM - 1) / BM, num_n = p.N / BN;
+  p.pairs = 0;
+  if (PAIR) {
+    // as many bands of 256 rows as fill whole waves while leaving about two 128-row tiles
+    // per SM for the last wave, which the round-robin then balances to within one tile
+    const double per_sm = (double)num_m * num_n / sms;
+    const int big = per_sm > 1.0 ? sms * (int)((per_sm - 1.0) / 2.0) : 0;
+    p.pairs = big / num_n < num_m / 2 ? big / num_n : num_m / 2;
+  }
+  const int tiles = (num_m - p.pairs) * num_n;
   const int grid = tiles < sms ? tiles : sms;
-  kern<<<grid, THREADS, smem, stream>>>(ta, tb, p);
+  kern<<<grid, T::THREADS, smem, stream>>>(ta, ta1, tb, p);
   return cudaGetLastError();
 }
 
@@ -456,8 +530,7 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   if (head && (g.N % 32 != 0 || g.N > 128 || !g.z || !g.bias)) return cudaErrorInvalidValue;
   if (g.M <= 0 || g.N <= 0 || g.N % bn != 0 || g.K % BK != 0 || g.K <= 0)
     return cudaErrorInvalidValue;
-  CUtensorMap ta, tb;
-  if (!make_tmap_2d(&ta, g.a, g.M, g.K, BM)) return cudaErrorInvalidValue;
+  CUtensorMap tb;
   if (!make_tmap_2d(&tb, g.w, g.N, g.K, bn)) return cudaErrorInvalidValue;
   Params p;
   // raster group: 16 row-blocks when N or K is long (the measured best at 15,435 rows:
@@ -487,24 +560,25 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   p.dt = g.dt;
   p.status = g.status;
   switch (epi) {
+    // plain stores: pair tiles; the rest 128 x 256
     case kEpiStore:
-      return launch_one<kEpiStore, 128>(ta, tb, p, stream);
+      return launch_one<kEpiStore, 128, BN_WIDE, true>(g, tb, p, stream);
     case kEpiGelu:
-      return launch_one<kEpiGelu, 128>(ta, tb, p, stream);
+      return launch_one<kEpiGelu, 128>(g, tb, p, stream);
     case kEpiResid:
-      return launch_one<kEpiResid, 128>(ta, tb, p, stream);
+      return launch_one<kEpiResid, 128>(g, tb, p, stream);
     case kEpiSwiglu:
       if (!g.bias) return cudaErrorInvalidValue;
-      return launch_one<kEpiSwiglu, 128>(ta, tb, p, stream);
+      return launch_one<kEpiSwiglu, 128>(g, tb, p, stream);
     case kEpiQkvg:
-      if (g.head_dim == 128) return launch_one<kEpiQkvg, 128>(ta, tb, p, stream);
-      if (g.head_dim == 64) return launch_one<kEpiQkvg, 64>(ta, tb, p, stream);
+      if (g.head_dim == 128) return launch_one<kEpiQkvg, 128>(g, tb, p, stream);
+      if (g.head_dim == 64) return launch_one<kEpiQkvg, 64>(g, tb, p, stream);
       return cudaErrorInvalidValue;
     case kEpiHeadEuler:
-      if (g.N == 32) return launch_one<kEpiHeadEuler, 128, 32>(ta, tb, p, stream);
-      if (g.N == 64) return launch_one<kEpiHeadEuler, 128, 64>(ta, tb, p, stream);
-      if (g.N == 96) return launch_one<kEpiHeadEuler, 128, 96>(ta, tb, p, stream);
-      if (g.N == 128) return launch_one<kEpiHeadEuler, 128, 128>(ta, tb, p, stream);
+      if (g.N == 32) return launch_one<kEpiHeadEuler, 128, 32>(g, tb, p, stream);
+      if (g.N == 64) return launch_one<kEpiHeadEuler, 128, 64>(g, tb, p, stream);
+      if (g.N == 96) return launch_one<kEpiHeadEuler, 128, 96>(g, tb, p, stream);
+      if (g.N == 128) return launch_one<kEpiHeadEuler, 128, 128>(g, tb, p, stream);
       return cudaErrorInvalidValue;
     default:
       return cudaErrorInvalidValue;

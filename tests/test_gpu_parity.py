@@ -49,6 +49,20 @@ def test_linear_small_integers_bit_exact(h3, M, N, K):
     assert np.array_equal(host_f64(y2), oracle.bf16(oracle.linear(a, w)))
 
 
+def test_linear_pair_tiles_bit_exact(h3):
+    """Rows enough for 256-row pair tiles (38 bands at 152 SMs), the 128-row tiles after
+    them and a ragged last block: exact on small integers."""
+    M, N, K = 15360 + 37, 1024, 192
+    rng = np.random.default_rng(7)
+    a = rng.integers(-8, 9, (M, K)).astype(np.float32)
+    w = rng.integers(-8, 9, (N, K)).astype(np.float32)
+    ad, wd = (dev_bf16(S.to_bf16_bits(x)) for x in (a, w))
+    y = empty_bf16(M, N)
+    h3.linear(ad, wd, None, y)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_f64(y), oracle.bf16(oracle.linear(a, w)))
+
+
 def test_linear_random_close(h3):
     M, N, K = 1000, 1024, 3072
     a = S.normal_bf16(5, "a", (M, K))
