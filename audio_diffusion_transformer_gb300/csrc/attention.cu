@@ -31,8 +31,8 @@
 // share one or two heads' K/V in L2.  The pipelines run across unit boundaries.
 // Tensor memory (512 columns): two 128-column score buffers, the O accumulator, and
 // two Q buffers -- Q is the score MMA's A operand straight from tensor memory, which
-// leaves shared memory to three-stage K and V rings (192 KB): the kernel is bound by the
-// bytes it keeps in flight against the L2 latency under load.
+// leaves shared memory to three-stage K and V rings (192 KB).  The kernel's time is set
+// by the latency of each step's S -> softmax -> PV chain, not by memory bandwidth.
 //   warp 0       TMA: the K ring (a stage = X + Y, 128 keys)
 //   warp 1       S issuer: S = Q [K_X; K_Y]^T (M = 128, N = 128, fp32) into the step's
 //                score buffer once the PV two steps back has read it
