@@ -55,7 +55,7 @@ KERNEL_SOURCES = {"gemm": ["gemm.cu", "ptx.cuh"], "attention": ["attention.cu", 
 
 # ----------------------------------------------------------------------------- helpers
 def workload(name):
-    wl = S.config_by_name(name)
+    wl = S.workload_by_name(name)
     n_blocks = wl.n_blocks if wl.extra.get("forward") else 1
     return wl, n_blocks
 
@@ -538,7 +538,7 @@ def run_loop(args, rank, world, local_rank):
     import audio_diffusion_transformer_gb300 as h3
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    wl = S.config_by_name(args.workload)
+    wl = S.workload_by_name(args.workload)
     shape = wl.shape
     N, D = shape.n_rows, shape.hidden
     n_steps, reuse, keep = wl.extra["steps"], wl.extra["reuse"], wl.extra["keep"]
@@ -732,7 +732,7 @@ def main():
             import torch
             torch.cuda.set_device(local_rank)
             torch.distributed.init_process_group("nccl")
-        if S.config_by_name(args.workload).config_id == 5:
+        if S.workload_by_name(args.workload) is S.LOOP_4K:
             out = run_loop(args, rank, world, local_rank)
         else:
             out = run_ours(args, rank, world, local_rank)

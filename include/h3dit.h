@@ -22,8 +22,11 @@
  *   - bf16 tensors are IEEE bfloat16 bit patterns (uint16).  Linear weights
  *     are stored [out, in] row-major (input features contiguous).
  *   - Row order of the packed sequence: text rows, then audio rows, then video
- *     rows.  The prefix (text + audio) must be a multiple of the tile (64).
- *     Video rows are cut into contiguous 64-row tiles; the last may be partial.
+ *     rows.  The prefix (text + audio) may have any length (the pages' receipt
+ *     has 36 + 414 rows); its keys are walked in 64-row chunks, the last one
+ *     partial.  Video rows are cut into routing tiles of at most 64 rows:
+ *     contiguous 64-row slices (the last may be partial), or clipped cubes of a
+ *     latent grid (see h3dit_shape).
  *   - Results are deterministic: the same inputs give the same bytes.
  *   - Pointers must be 16-byte aligned; row pitches are dense.
  */

@@ -12,9 +12,10 @@ projection outputs, head layout, attention output, residual stream) are
 rounded to bf16 exactly where the method stores bf16, and the top-k decision
 is taken on fp32 scores, the precision the FastH3 pages fix for routing.
 
-Parity status of each function is stated in its docstring; every function is
-pinned by a test in ``tests/test_oracle_pins.py`` except the composed block
-and denoiser, whose parity rests on the pinned parts (no weights, fixtures or
-worked examples exist on the pages).
+Every public function is pinned by tests in ``tests/test_oracle_pins.py``;
+the pin table in the header of ``h3block.py`` names them.  The pages print no
+worked example of a whole block or denoiser step (no weights or fixtures), so
+the composed block and denoiser are pinned through closed-form special cases
+of each of their stages, not by value on general inputs.
 """
 from .h3block import *  # noqa: F401,F403

@@ -18,6 +18,70 @@ Sources, cited by page title and section:
 Readings taken where the pages leave a step open are marked "Reading:".
 Array conventions: activations are [rows, features]; head-major tensors are
 [H, N, d]; linear weights are [out, in] and ``linear`` computes h @ W^T + b.
+
+Pins.  Every public function below is tied, by the tests named beside it in
+tests/test_oracle_pins.py, to something other than itself: a closed form, an
+invariant, a brute force on a tiny input, an independent library routine or a
+value printed on the pages (tests/golden/).  The pages print no worked example
+of a whole block or denoiser step, so the composed functions (block_forward,
+denoise_forward, sample_step and the loops) are pinned through closed-form
+special cases of each of their stages rather than by value on general inputs.
+
+PIN TABLE (function: pin tests, without their "test_" prefix)
+  bf16: bf16_against_torch_conversion, bf16_hand_values
+  f32: output_head_constant_rows, token_pool_brute_force_pairs
+  rms_modulate: rms_modulate_closed_forms
+  linear: linear_small_integers_exact
+  gelu_erf: gelu_closed_forms
+  silu: silu_closed_forms
+  swiglu_split: swiglu_split_layout_and_block
+  mlp_inner: swiglu_split_layout_and_block, block_mlp_half_closed_form
+  head_rms_norm: head_rms_norm_unit_rms
+  rope: rope_closed_form_and_relative_position
+  rope_axis_split: rope_axis_split_values
+  rope_3d: rope_3d_brute_force_complex, rope_3d_relative_per_axis_and_isolation
+  rope_coords: rope_coords_raster
+  rope_coords_pooled: rope_coords_pooled_positions
+  video_tiles: tile_means_brute_force_and_partial_tile, tile_sets_slices_and_cubes
+  cube_tiles: cube_tiles_receipt_golden, cube_tiles_partition_by_membership
+  tile_sets: tile_sets_slices_and_cubes
+  shape_tiles: tile_sets_slices_and_cubes
+  tile_means: tile_means_brute_force_and_partial_tile
+  tile_scores: tile_scores_brute_force
+  topk_select: topk_brute_force_with_ties_and_nans, topk_nan_regression_exact_k
+  topk_gap: topk_all_and_gap
+  topk_set_valid: topk_all_and_gap
+  attend: routed_all_tiles_equals_dense_brute_force, block_all_tiles_equals_dense
+  routed_attention: routed_all_tiles_equals_dense_brute_force, routed_keyset_brute_force,
+    attention_row_stochastic_and_zero_query
+  pooled_branch: pooled_closed_forms
+  gate_mix: gate_mix_brute_force
+  attention_layer: router_tile_permutation_equivariance, block_closed_form_constant_rows
+  qkv_heads: qkv_heads_layout_by_loops
+  block_forward: block_closed_form_constant_rows, block_mlp_half_closed_form,
+    block_zero_gates_pass_residual, block_all_tiles_equals_dense,
+    block_prefix_table_zero_gates_split_by_modality
+  block_forward_rows: block_rows_equals_full_block
+  euler_update: euler_power_of_two_exact, euler_and_extrapolation_per_modality_rows
+  extrapolate: extrapolation_exact_for_linear_velocity
+  fresh_steps: fresh_step_counts_golden
+  sigma_schedule: sigma_schedule_shift_endpoints_and_composition
+  denoise_forward: denoise_forward_closed_forms
+  denoise_loop: denoise_loop_orchestration_without_blocks,
+    denoise_loop_per_modality_without_blocks
+  thin_layers: thin_layers_hand_example
+  patch_in: patch_in_small_integers_brute_force
+  output_head: output_head_constant_rows
+  sample_x0: sample_step_without_blocks_is_the_heads_of_the_patches
+  sample_heads: sample_step_without_blocks_is_the_heads_of_the_patches
+  sample_step: sample_step_without_blocks_is_the_heads_of_the_patches,
+    core_reuse_reproduces_the_fresh_velocity
+  sample_loop: sample_loop_core_reuse_without_blocks_equals_every_pass_fresh
+  reduced_shape: reduced_shape_hand_values
+  token_pool: token_pool_brute_force_pairs
+  token_restore: token_restore_identity_and_pair_update
+  run_blocks: run_blocks_reduction_boundaries
+END PIN TABLE
 """
 from __future__ import annotations
 

@@ -23,7 +23,10 @@ from __future__ import annotations
 
 import numpy as np
 
-from .configs import CONFIGS, BlockShape, config_by_name  # noqa: F401
+from .configs import (  # noqa: F401
+    ATTN_TINY, BLOCK_4K, BLOCK_15K, BLOCK_PAGES, BLOCK_RECEIPT, FORWARD_50, FORWARD_PAGES,
+    FORWARD_RECEIPT, LOOP_4K, SAMPLE_RECEIPT, SAMPLE_RECEIPT_TR, WORKLOADS, BlockShape,
+    Workload, workload_by_name)
 
 _GOLDEN = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)

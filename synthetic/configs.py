@@ -66,7 +66,7 @@ class BlockShape:
 @dataclass(frozen=True)
 class Workload:
     name: str
-    config_id: int
+    seed_id: int  # seed = 0x48334454 + seed_id
     shape: BlockShape
     description: str
     n_blocks: int = 1
@@ -74,10 +74,10 @@ class Workload:
 
     @property
     def seed(self) -> int:
-        return 0x48334454 + self.config_id
+        return 0x48334454 + self.seed_id
 
 
-# 1: routed attention alone, 1,024 video rows, 4 heads x 64, top-k 4 of 16.
+# routed attention alone, 1,024 video rows, 4 heads x 64, top-k 4 of 16.
 ATTN_TINY = Workload(
     "attn_tiny_1024", 1,
     BlockShape(0, 0, 1024, hidden=256, heads=4, head_dim=64, mlp_width=1024, topk=4,
@@ -85,7 +85,7 @@ ATTN_TINY = Workload(
     "routed attention only: 1,024 rows, 4 heads x 64, 16 tiles of 64, top-k 4 + pooled",
 )
 
-# 2: one block shaped like a 512x512 video: 4,096 rows, D = 3,072, 24 x 128.
+# one block shaped like a 512x512 video: 4,096 rows, D = 3,072, 24 x 128.
 BLOCK_4K = Workload(
     "block_4096_d3072", 2,
     BlockShape(256, 256, 3584, hidden=3072, heads=24, head_dim=128, mlp_width=4 * 3072, topk=8),
@@ -93,7 +93,7 @@ BLOCK_4K = Workload(
     "MLP 4x GELU, top-k 8 of 56",
 )
 
-# 3: one block at the long-sequence shape: 15,435 rows, D = 5,120, 40 x 128.
+# one block at the long-sequence shape: 15,435 rows, D = 5,120, 40 x 128.
 BLOCK_15K = Workload(
     "block_15435_d5120", 3,
     BlockShape(512, 1024, 13899, hidden=5120, heads=40, head_dim=128, mlp_width=4 * 5120, topk=16),
@@ -101,7 +101,7 @@ BLOCK_15K = Workload(
     "MLP 4x GELU, top-k 16 of 218 + pooled",
 )
 
-# 4: 50 blocks of the 15,435-row shape, then one Euler step dt = -1/8.
+# 50 blocks of the 15,435-row shape, then one Euler step dt = -1/8.
 FORWARD_50 = Workload(
     "forward50_15435_d5120", 4, BLOCK_15K.shape,
     "50-block denoising forward at 15,435 rows (hidden 5,120 block shape), "
@@ -109,7 +109,7 @@ FORWARD_50 = Workload(
     n_blocks=50, extra={"dt": -0.125, "forward": True},
 )
 
-# 5: 20-step denoising loop at 4,096 rows, 45 of 50 blocks, reuse 2.
+# 20-step denoising loop at 4,096 rows, 45 of 50 blocks, reuse 2.
 LOOP_4K = Workload(
     "loop20_4096_d3072", 5, BLOCK_4K.shape,
     "20 Euler steps, 45 of 50 blocks, velocity reuse 2 (11 fresh), top-k sweep {4,8,16,32,56}",
@@ -166,12 +166,12 @@ SAMPLE_RECEIPT_TR = Workload(
                         "c_audio": 32, "reduction": (3, 40)},
 )
 
-CONFIGS = [ATTN_TINY, BLOCK_4K, BLOCK_15K, FORWARD_50, LOOP_4K, BLOCK_PAGES, FORWARD_PAGES,
-           BLOCK_RECEIPT, FORWARD_RECEIPT, SAMPLE_RECEIPT, SAMPLE_RECEIPT_TR]
+WORKLOADS = [ATTN_TINY, BLOCK_4K, BLOCK_15K, FORWARD_50, LOOP_4K, BLOCK_PAGES, FORWARD_PAGES,
+             BLOCK_RECEIPT, FORWARD_RECEIPT, SAMPLE_RECEIPT, SAMPLE_RECEIPT_TR]
 
 
-def config_by_name(name: str) -> Workload:
-    for w in CONFIGS:
+def workload_by_name(name: str) -> Workload:
+    for w in WORKLOADS:
         if w.name == name:
             return w
     raise KeyError(name)

@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
-WL = S.config_by_name("block_15435_d5120")
+WL = S.workload_by_name("block_15435_d5120")
 SHAPE = WL.shape
 
 
@@ -166,7 +166,7 @@ def test_denoise_two_blocks_fullsize(h3):
 def test_pages_shape_block_sampled(h3):
     """The pages' own block shape at 15,435 rows: hidden 5,376, attention width 7,168
     (56 x 128), SwiGLU 14,336, checked on sampled rows."""
-    wl = S.config_by_name("block_15435_d5376_swiglu")
+    wl = S.workload_by_name("block_15435_d5376_swiglu")
     shp = wl.shape
     t0 = time.time()
     w = S.block_weights(shp, wl.seed)
@@ -192,7 +192,7 @@ def test_receipt_cubes_block_sampled(h3):
     (a prefix of 450, not a multiple of 64) and 14,985 video rows on a 37 x 15 x 27 grid
     in 280 clipped 4x4x4 cubes, top-k 56, 3-D rotary; sampled rows against the oracle
     (video rows in raster order there, cube order on the device)."""
-    wl = S.config_by_name("block_15435_cubes_d5376_swiglu")
+    wl = S.workload_by_name("block_15435_cubes_d5376_swiglu")
     shp = wl.shape
     assert shp.n_video_tiles == 280
     t0 = time.time()
@@ -225,7 +225,7 @@ def test_receipt_attention_repeat_identical_and_sampled(h3):
     lists, 64+ steps per unit) three times: byte-identical outputs (a race between the
     softmax warps and the MMA issuer would show here), and sampled query tiles and
     prefix rows against the oracle."""
-    wl = S.config_by_name("block_15435_cubes_d5376_swiglu")
+    wl = S.workload_by_name("block_15435_cubes_d5376_swiglu")
     shp = wl.shape
     t0 = time.time()
     inp = S.attention_inputs(shp, wl.seed + 3, structured=0.3)
@@ -306,7 +306,7 @@ def test_receipt_sampler_exact_properties_fullsize(h3):
     that hold at any size: (1) a core-reuse pass at the same latents gives the fresh
     pass's latents bit for bit; (2) token reduction around a block with zero gates gives
     the run without that block bit for bit (each token = bypass + a zero update)."""
-    shp = S.config_by_name("sample50_15435_cubes_d5376_swiglu_tokred").shape
+    shp = S.workload_by_name("sample50_15435_cubes_d5376_swiglu_tokred").shape
     g = torch.Generator(device="cuda")
     g.manual_seed(2024)
     blocks = [_device_block(shp, g), _device_block(shp, g, zero_gates=True), _device_block(shp, g)]

@@ -105,9 +105,9 @@ def oracle_attention(shp, inp, with_gate=True, pooled=True, p_bf16=False):
 
 ATTN_CASES = [
     # (name, shape, structured)
-    ("tiny_k4", S.CONFIGS[0].shape, 0.0),
-    ("tiny_k4_structured", S.CONFIGS[0].shape, 0.5),
-    ("tiny_k16_dense", S.CONFIGS[0].shape.with_(topk=16), 0.0),
+    ("tiny_k4", S.ATTN_TINY.shape, 0.0),
+    ("tiny_k4_structured", S.ATTN_TINY.shape, 0.5),
+    ("tiny_k16_dense", S.ATTN_TINY.shape.with_(topk=16), 0.0),
     ("prefix_ragged_d128", S.BlockShape(64, 64, 300, hidden=256, heads=2, head_dim=128,
                                         mlp_width=1024, topk=2), 0.3),
     ("prefix_odd_tiles_d64", S.BlockShape(128, 64, 5 * 64 + 1, hidden=256, heads=3, head_dim=64,
@@ -137,7 +137,7 @@ def test_routed_attention_matches_oracle(h3, name, shp, structured):
 
 
 def test_routed_all_tiles_equals_dense_attention(h3):
-    shp = S.CONFIGS[0].shape.with_(topk=16)
+    shp = S.ATTN_TINY.shape.with_(topk=16)
     inp = S.attention_inputs(shp, 77)
     got = run_attention(h3, shp, inp, with_gate=False)
     q, k, v = (S.bf16_bits_to_f64(inp[n]) for n in ("q", "k", "v"))
@@ -221,7 +221,7 @@ def test_block_forward_small(h3, name, shp):
 
 
 def test_block_forward_4096_rows(h3):
-    wl = S.CONFIGS[1]
+    wl = S.BLOCK_4K
     shp = wl.shape
     x, w, xb = run_block(h3, shp, wl.seed)
     ref = oracle.block_forward(S.bf16_bits_to_f64(xb), weights_to_f64(w), shp)

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(h3):
 
 
 def test_shape_checks_on_host(h3):
-    good = S.CONFIGS[1].shape
+    good = S.BLOCK_4K.shape
     assert h3.check_shape(h3.make_shape(good)) == 0
     bad = [good.with_(tile=32), good.with_(head_dim=96),
            good.with_(hidden=3000), good.with_(mlp_width=1000), good.with_(n_video=0),
@@ -59,14 +59,14 @@ def test_shape_checks_on_host(h3):
 
 
 def test_workspace_sizes(h3):
-    for wl in S.CONFIGS:
+    for wl in S.WORKLOADS:
         s = wl.shape
-        if wl.config_id == 1:
+        if wl is S.ATTN_TINY:
             n = h3.workspace_bytes(h3.attn_shape(s))
         else:
             n = h3.workspace_bytes(h3.make_shape(s))
         assert n > 0 and n % 256 == 0
-    s3 = S.CONFIGS[2].shape
+    s3 = S.BLOCK_15K.shape
     n = h3.workspace_bytes(h3.make_shape(s3))
     # q, k, v, g, o, h, x at least: 7 * N * D * 2 bytes
     assert n >= 7 * s3.n_rows * s3.hidden * 2
@@ -77,14 +77,14 @@ def test_workspace_sizes(h3):
 def test_entry_points_reject_bad_arguments_without_gpu(h3):
     import ctypes
     lib = h3.lib()
-    s = h3.make_shape(S.CONFIGS[1].shape)
+    s = h3.make_shape(S.BLOCK_4K.shape)
     # null pointers are refused before any CUDA call
     assert lib.h3dit_block_forward(ctypes.byref(s), None, None, None, 0, None) == 1
     assert lib.h3dit_routed_attention(ctypes.byref(s), *([None] * 8), None, 0, None) == 1
     assert lib.h3dit_linear(None, None, None, None, 1, 256, 64, None) == 1
     assert lib.h3dit_linear(16, 16, None, 16, 1, 255, 64, None) == 2   # N not a multiple of 256
     assert lib.h3dit_linear(17, 16, None, 16, 1, 256, 64, None) == 3   # misaligned
-    bad = h3.make_shape(S.CONFIGS[1].shape.with_(video_grid=(7, 16, 31)))  # grid != n_video
+    bad = h3.make_shape(S.BLOCK_4K.shape.with_(video_grid=(7, 16, 31)))  # grid != n_video
     assert lib.h3dit_block_forward(ctypes.byref(bad), None, None, None, 0, None) == 2
 
 
@@ -108,7 +108,7 @@ def test_select_blocks_ties_drop_higher_index(h3):
 def test_workspace_too_small_and_bad_weights_refused_on_host(h3):
     import ctypes
     lib = h3.lib()
-    s = h3.make_shape(S.CONFIGS[1].shape)
+    s = h3.make_shape(S.BLOCK_4K.shape)
     fake = {n: 4096 for n, _ in h3.BlockWeights._fields_}  # aligned, never dereferenced
     bw = h3.BlockWeights(*[fake[n] for n, _ in h3.BlockWeights._fields_])
     need = h3.workspace_bytes(s)
@@ -155,7 +155,7 @@ def test_tile_spans_and_video_order_match_oracle_tiles(h3, grid):
 def test_sample_step_refuses_bad_arguments_on_host(h3):
     import ctypes
     lib = h3.lib()
-    s = h3.make_shape(S.CONFIGS[1].shape)
+    s = h3.make_shape(S.BLOCK_4K.shape)
     need = h3.workspace_bytes(s)
     fake = 4096  # aligned, never dereferenced: every case fails before a launch
     good = dict(c_video=96, c_audio=32, **{n: fake for n, _ in h3.Ends._fields_[2:]})

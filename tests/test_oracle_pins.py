@@ -805,3 +805,149 @@ def test_swiglu_split_layout_and_block():
             a = h[r] @ gate[c] + bg[c]
             b = h[r] @ up[c] + bu[c]
             assert u[r, c] == O.bf16(a / (1 + math.exp(-a)) * b)
+
+
+# --------------------------------------------------------------------------- added pins
+def test_qkv_heads_layout_by_loops():
+    # projection columns [Q | K | V | G], each H*d wide and head-major inside: head h of row
+    # n is columns h*d .. h*d+d-1 of its slab; q and k are RMS-normed over d, scaled by the
+    # learned weight, then turned pair (c, c + d/2) by n * theta^(-2c/d) as a complex product
+    H, d, N, eps, theta = 3, 8, 5, 1e-6, 10000.0
+    A = H * d
+    qkvg = O.bf16(rng.standard_normal((N, 4 * A)))
+    wq = 1.0 + 0.1 * rng.standard_normal(d)
+    wk = 1.0 + 0.1 * rng.standard_normal(d)
+    Q, K, V, G = O.qkv_heads(qkvg, H, d, wq, wk, eps, theta)
+    assert Q.shape == K.shape == V.shape == (H, N, d) and G.shape == (N, A)
+    for h in range(H):
+        for n in range(N):
+            for slab, w, got in ((0, wq, Q), (1, wk, K)):
+                x = [float(t) for t in qkvg[n, slab * A + h * d:slab * A + (h + 1) * d]]
+                inv = 1.0 / math.sqrt(sum(t * t for t in x) / d + eps)
+                y = [t * inv * float(wi) for t, wi in zip(x, w)]
+                zs = [complex(y[c], y[c + d // 2]) * complex(math.cos(n * theta ** (-2 * c / d)),
+                                                             math.sin(n * theta ** (-2 * c / d)))
+                      for c in range(d // 2)]
+                want = O.bf16(np.array([z.real for z in zs] + [z.imag for z in zs]))
+                assert np.allclose(got[h, n], want, rtol=2.0 ** -8, atol=0)
+            for c in range(d):
+                assert V[h, n, c] == qkvg[n, 2 * A + h * d + c]
+                assert G[n, h * d + c] == qkvg[n, 3 * A + h * d + c]
+    # no norm weights and no rotary: plain head-major slices
+    Q0, K0, _, _ = O.qkv_heads(qkvg, H, d, None, None, eps, theta, use_rope=False)
+    for h in range(H):
+        assert np.array_equal(Q0[h], qkvg[:, h * d:(h + 1) * d])
+        assert np.array_equal(K0[h], qkvg[:, A + h * d:A + (h + 1) * d])
+
+
+def _mlp_row_by_loops(h2row, w, mlp):
+    # the MLP of one row written out: fc1 (+ bias), activation, bf16 mid, fc2 (+ bias)
+    D = len(h2row)
+    w1, b1, w2, b2 = w["w1"], w["b1"], w["w2"], w["b2"]
+    F = w2.shape[1]
+
+    def fc1(r):
+        return float(b1[r]) + sum(float(w1[r, c]) * float(h2row[c]) for c in range(D))
+    u = []
+    for j in range(F):
+        if mlp == "swiglu":  # gate row 256*(j//128) + j%128, its up row 128 further on
+            rg = 256 * (j // 128) + j % 128
+            a, b = fc1(rg), fc1(rg + 128)
+            u.append(a / (1.0 + math.exp(-a)) * b)
+        else:
+            a = fc1(j)
+            u.append(0.5 * a * (1.0 + math.erf(a / math.sqrt(2.0))))
+    u = O.bf16(np.array(u))
+    return np.array([float(b2[o]) + sum(float(w2[o, j]) * float(u[j]) for j in range(F))
+                     for o in range(w2.shape[0])])
+
+
+@pytest.mark.parametrize("mlp", ["gelu", "swiglu"])
+def test_block_mlp_half_closed_form(mlp):
+    # gate1 = 0 leaves x1 = x; scale2 = -1 makes every h2 row bf16(shift2), so every row
+    # gets the same MLP output m and x2 = bf16(x + gate2 * m): pins the second norm's table
+    # rows, the MLP's biases, activation and bf16 mid, and the second gated residual
+    shape = _tiny_shape(hidden=64, mlp_width=128, mlp=mlp)
+    w = _weights(shape, 21)
+    w["mod"][2] = 0.0
+    w["mod"][4] = -1.0
+    x = S.bf16_bits_to_f64(S.hidden_rows(shape, 9))
+    out = O.block_forward(x, w, shape)
+    assert np.array_equal(out["x1"], x)
+    m = _mlp_row_by_loops(O.bf16(w["mod"][3]), w, mlp)
+    want = O.bf16(x + w["mod"][5] * m[None, :])
+    got = out["x2"]
+    assert np.all(np.abs(got - want) <= np.abs(want) * 2.0 ** -8)
+    assert np.mean(got == want) > 0.99
+
+
+def test_denoise_forward_closed_forms():
+    # blocks with zero gates are the identity on bf16 rows, so v = bf16(z) and
+    # z' = fp32(z + dt v); with dt = -1/8 the product is exact
+    shape = _tiny_shape()
+    z = rng.standard_normal((shape.n_rows, shape.hidden)).astype(np.float32).astype(np.float64)
+    blocks = []
+    for i in range(3):
+        w = _weights(shape, 30 + i)
+        w["mod"][2] = 0.0
+        w["mod"][5] = 0.0
+        blocks.append(w)
+    want_v = O.bf16(z)
+    want_z = (z.astype(np.float32) + np.float32(-0.125) * want_v.astype(np.float32))
+    for blks, ids in (([], None), (blocks, None), (blocks, [2, 0])):
+        r = O.denoise_forward(z, blks, shape, -0.125, ids)
+        assert np.array_equal(r["v"], want_v)
+        assert np.array_equal(r["z"], want_z.astype(np.float64))
+    # the text/audio rows step by their own dt
+    r = O.denoise_forward(z, [], shape, -0.125, None, dt_prefix=-0.5)
+    P = shape.n_prefix
+    assert np.array_equal(r["z"][:P], (z[:P].astype(np.float32)
+                                       + np.float32(-0.5) * want_v[:P].astype(np.float32)))
+    assert np.array_equal(r["z"][P:], want_z[P:])
+
+
+def test_tile_sets_slices_and_cubes():
+    # without a grid: consecutive 64-row slices of the video rows, the last one partial
+    sets = O.tile_sets(100, 150, 64)
+    assert [list(s) for s in sets] == [list(range(100, 164)), list(range(164, 228)),
+                                       list(range(228, 250))]
+    # with a grid: the cubes, and shape_tiles picks by the shape's grid field
+    shape = S.BlockShape(4, 0, 2 * 3 * 5, hidden=64, heads=1, head_dim=64, mlp_width=256,
+                         topk=1, video_grid=(2, 3, 5))
+    cubes = O.shape_tiles(shape)
+    assert [list(s) for s in cubes] == [list(s) for s in O.cube_tiles(4, (2, 3, 5))]
+    assert len(cubes) == 2  # 1 x 1 x 2 cubes of 4 x 4 x 4: w splits into 4 + 1
+    assert sorted(np.concatenate(cubes).tolist()) == list(range(4, 34))
+    plain = O.shape_tiles(shape.with_(video_grid=None))
+    assert [list(s) for s in plain] == [list(range(4, 34))]
+
+
+def test_reduced_shape_hand_values():
+    shape = _tr_shape((3, 2, 5))
+    r = O.reduced_shape(shape)
+    assert r.video_grid == (3, 2, 3) and r.n_video == 18 and r.pair_w == 5
+    assert not r.token_reduction and r.n_prefix == shape.n_prefix
+    r2 = O.reduced_shape(_tr_shape((2, 3, 8)))
+    assert r2.video_grid == (2, 3, 4) and r2.n_video == 24 and r2.pair_w == 8
+
+
+def test_pin_table_covers_every_oracle_function():
+    # the oracle's header names the pins of every public function; each must exist here
+    doc = O.h3block.__doc__
+    body = doc[doc.index("PIN TABLE"):doc.index("END PIN TABLE")].splitlines()[1:]
+    table, last = {}, None
+    for line in body:
+        if not line.strip():
+            continue
+        if line.startswith("    "):  # continuation of the previous entry
+            table[last] += [t.strip() for t in line.split(",") if t.strip()]
+            continue
+        name, tests = line.strip().split(":", 1)
+        last = name
+        table[name] = [t.strip() for t in tests.split(",") if t.strip()]
+    assert set(table) == set(O.h3block.__all__)
+    here = globals()
+    for name, tests in table.items():
+        assert tests, name
+        for t in tests:
+            assert callable(here.get("test_" + t)), f"{name}: no pin test_{t}"

@@ -39,7 +39,7 @@ def _outputs(shp):
 
 
 CASES = [
-    ("video_only_d64", S.CONFIGS[0].shape),                       # 1,024 rows, 4 x 64, k 4
+    ("video_only_d64", S.ATTN_TINY.shape),                       # 1,024 rows, 4 x 64, k 4
     ("prefix_ragged_d128", S.BlockShape(128, 64, 300, hidden=256, heads=2, head_dim=128,
                                         mlp_width=1024, topk=2)),  # text + audio + ragged video
 ]
@@ -66,7 +66,7 @@ def test_static_scratch_matches_workspace_entry(h3, name, shp):
 
 
 def test_static_scratch_rejects_oversized_shape(h3):
-    big = S.CONFIGS[1].shape  # 4,096 rows x 24 heads x 128 needs more than the fixed scratch
+    big = S.BLOCK_4K.shape  # 4,096 rows x 24 heads x 128 needs more than the fixed scratch
     cs = h3.attn_shape(big)
     assert h3.workspace_bytes(cs) > 4 << 20
     lib = h3.lib()
