@@ -192,6 +192,42 @@ class ClockSampler:
 _SAMPLE_INPUTS = {}
 
 
+def forward_config(wl, n_blocks, world):
+    """The ``config`` object of a forward or sampler-step line (both arms print it)."""
+    shape = wl.shape
+    N, D = shape.n_rows, shape.hidden
+    dt = -0.125
+    shapes = block_shapes(shape, n_blocks, wl.extra.get("reduction"))
+    return {"workload": wl.name, "n_rows": N, "n_text": shape.n_text,
+            "n_audio": shape.n_audio, "n_video": shape.n_video, "n_blocks": n_blocks,
+            "hidden": D, "heads": shape.heads, "head_dim": shape.head_dim,
+            "attn_width": shape.attn_width,
+            "mlp": (f"SwiGLU {shape.mlp_width}" if shape.mlp == "swiglu"
+                    else f"{shape.mlp_width // D}x GELU"),
+            "params_b": n_blocks * (D * 4 * shape.attn_width + shape.attn_width * D
+                                    + D * fc1_width(shape) + shape.mlp_width * D) / 1e9,
+            "topk": shape.topk, "tile": shape.tile,
+            "video_tiles": (f"{shape.n_video_tiles} cubes "
+                            f"{'x'.join(map(str, shape.cube))} of a "
+                            f"{'x'.join(map(str, shape.video_grid))} grid, 3-D rotary"
+                            if shape.video_grid else
+                            f"{shape.n_video_tiles} slices of 64 rows"),
+            "dt": dt, "parallelism": f"replicas x{world}",
+            "rows_per_block": ({"full": N, "reduced": min(sb.n_rows for sb in shapes),
+                                "reduced_blocks": list(wl.extra["reduction"])}
+                               if len(set(sb.n_rows for sb in shapes)) > 1 else N),
+            "step": ("sampler step on the modality latents: fp32 patch projections, "
+                     "blocks, final AdaLN + output heads with the Euler update"
+                     + (f", token reduction over blocks [{wl.extra['reduction'][0]}, "
+                        f"{wl.extra['reduction'][1]})" if wl.extra.get("reduction")
+                        else "")
+                     if wl.extra.get("ends") else
+                     "denoiser step on hidden-width latents: bf16(z), blocks, "
+                     "z += dt x_L"),
+            "l2": f"inputs larger than L2 (each block reads its own "
+                  f"{block_weight_bytes(shape) / 1e6:.0f} MB of weights)"}
+
+
 def oracle_block_sample(shape, rng_seed=0):
     """Times the oracle on a bounded sample of one block of ``shape`` and scales it
     to the whole block.  Returns (seconds per block, description)."""
@@ -478,34 +514,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_max / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "n_rows": N, "n_text": shape.n_text,
-                   "n_audio": shape.n_audio, "n_video": shape.n_video, "n_blocks": n_blocks,
-                   "hidden": D, "heads": shape.heads, "head_dim": shape.head_dim,
-                   "attn_width": shape.attn_width,
-                   "mlp": (f"SwiGLU {shape.mlp_width}" if shape.mlp == "swiglu"
-                           else f"{shape.mlp_width // D}x GELU"),
-                   "params_b": n_blocks * (D * 4 * shape.attn_width + shape.attn_width * D
-                                           + D * fc1_width(shape) + shape.mlp_width * D) / 1e9,
-                   "topk": shape.topk, "tile": shape.tile,
-                   "video_tiles": (f"{shape.n_video_tiles} cubes "
-                                   f"{'x'.join(map(str, shape.cube))} of a "
-                                   f"{'x'.join(map(str, shape.video_grid))} grid, 3-D rotary"
-                                   if shape.video_grid else
-                                   f"{shape.n_video_tiles} slices of 64 rows"),
-                   "dt": dt, "parallelism": f"replicas x{world}",
-                   "rows_per_block": ({"full": N, "reduced": min(sb.n_rows for sb in shapes),
-                                       "reduced_blocks": list(wl.extra["reduction"])}
-                                      if len(set(sb.n_rows for sb in shapes)) > 1 else N),
-                   "step": ("sampler step on the modality latents: fp32 patch projections, "
-                            "blocks, final AdaLN + output heads with the Euler update"
-                            + (f", token reduction over blocks [{wl.extra['reduction'][0]}, "
-                               f"{wl.extra['reduction'][1]})" if wl.extra.get("reduction")
-                               else "")
-                            if wl.extra.get("ends") else
-                            "denoiser step on hidden-width latents: bf16(z), blocks, "
-                            "z += dt x_L"),
-                   "l2": f"inputs larger than L2 (each block reads its own "
-                         f"{block_weight_bytes(shape) / 1e6:.0f} MB of weights)"},
+        "config": forward_config(wl, n_blocks, world),
         "s_per_forward": ms_max / K / 1e3 * (50 / n_blocks),
         "tc_frac_of_peak": achieved_total / peak_tc,
         "achieved_tflops": achieved_total,
@@ -701,7 +710,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": tot / args.steps * 1e3 * n_blocks, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "n_rows": shape.n_rows, "n_blocks": n_blocks},
+            "config": forward_config(wl, n_blocks, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(),
                              "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
