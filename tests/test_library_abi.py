@@ -86,6 +86,16 @@ def test_entry_points_reject_bad_arguments_without_gpu(h3):
     assert lib.h3dit_linear(17, 16, None, 16, 1, 256, 64, None) == 3   # misaligned
     bad = h3.make_shape(S.BLOCK_4K.shape.with_(video_grid=(7, 16, 31)))  # grid != n_video
     assert lib.h3dit_block_forward(ctypes.byref(bad), None, None, None, 0, None) == 2
+    # the fixed-scratch attention entry point: shape and size are checked, then pointers,
+    # all before any CUDA call
+    fn = lib.h3dit_routed_attention_static
+    assert fn(None, *([None] * 9)) == 1
+    small = h3.attn_shape(S.ATTN_TINY.shape)
+    assert fn(ctypes.byref(small), *([None] * 9)) == 1
+    big = h3.attn_shape(S.BLOCK_4K.shape)  # needs more than the 4 MiB scratch
+    dummy = ctypes.c_void_p(16)
+    assert fn(ctypes.byref(big), dummy, dummy, dummy, None, dummy, None, None, None, None) == 4
+    assert fn(ctypes.byref(bad), dummy, dummy, dummy, None, dummy, None, None, None, None) == 2
 
 
 @pytest.mark.parametrize("L,keep", [(50, 45), (50, 40), (6, 3), (5, 5), (3, 2)])
