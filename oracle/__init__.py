@@ -12,6 +12,9 @@ projection outputs, head layout, attention output, residual stream) are
 rounded to bf16 exactly where the method stores bf16, and the top-k decision
 is taken on fp32 scores, the precision the FastH3 pages fix for routing.
 
+``h3ref.c`` (loaded by ``cref.py``) restates the block once more in plain C
+loops, written apart from the numpy code; the tests require the two to agree.
+
 Every public function is pinned by tests in ``tests/test_oracle_pins.py``;
 the pin table in the header of ``h3block.py`` names them.  The pages print no
 worked example of a whole block or denoiser step (no weights or fixtures), so
