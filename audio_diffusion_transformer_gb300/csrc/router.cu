@@ -10,9 +10,10 @@
 //   rows: a 64-row slice, or a clipped 4x4x4 cube) in row order, the block sums
 //   are added in order and divided by the tile's row count.  Reads each
 //   video row of q, k, v once (HBM-bound).
-// Kernel 2 (route): one CTA per (head h, 8 query tiles), one warp per query
-//   tile; the head's key / value tile means pass through shared memory once
-//   per CTA in chunks of 32 tiles:
+// Kernel 2 (route): one CTA per (head h, 32 query tiles), four query tiles per
+//   warp; the head's key / value tile means pass through shared memory once
+//   per CTA in chunks of 32 tiles, and each staged mean a lane reads serves the
+//   warp's four query tiles (the kernel is bound by shared-memory bandwidth):
 //   S[h,i,j] = sum_c mq[h,i,c] mk[h,j,c]: one lane per key tile, four
 //   interleaved partial sums over c (c mod 4) added as ((p0 + p1) + (p2 + p3)),
 //   operands read from shared memory 16 bytes at a time;
@@ -92,8 +93,9 @@ __global__ void __launch_bounds__(128)
   }
 }
 
-constexpr int TILES_PER_CTA = ROUTE_THREADS / 32;  // one warp per query tile
-constexpr int KCHUNK = 32;                          // key-tile means staged per round
+constexpr int TILES_PER_WARP = 4;  // query tiles per warp: each staged mean read serves 4
+constexpr int TILES_PER_CTA = ROUTE_THREADS / 32 * TILES_PER_WARP;
+constexpr int KCHUNK = 32;  // key-tile means staged per round
 constexpr int SPAD = 4;  // staged row padding (floats): conflict-free 16-byte column reads
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -160,33 +162,38 @@ __device__ __forceinline__ unsigned select_topk(const float* s, int Tv, int ksel
   return taken;
 }
 
-// One CTA per (head h, block of 8 query tiles); warp w owns query tile i = 8 * blockIdx.x + w.
-// The head's key and value tile means are staged through shared memory once per CTA.
+// One CTA per (head h, block of 32 query tiles); warp w owns query tiles
+// i = 32 * blockIdx.x + 4 * w + r, r < 4.  The head's key and value tile means are
+// staged through shared memory once per CTA; every staged mean a lane reads serves the
+// warp's four query tiles (shared-memory bandwidth is what bounds this kernel).
 // NM: 32-tile groups per lane in the top-k (Tv <= 32 * NM).
 template <int D, int NM>
 __global__ void __launch_bounds__(ROUTE_THREADS)
     route_kernel(const float* __restrict__ means, float* __restrict__ scores,
                  int* __restrict__ idx, float* __restrict__ pooled, int H, int Tv, int ksel) {
+  constexpr int R = TILES_PER_WARP;
   extern __shared__ __align__(16) float sh[];
   float* stage = sh;                                  // [KCHUNK][D + SPAD] staged means
-  float* qrow = stage + KCHUNK * (D + SPAD);          // [8][D] query means, one row per warp
-  float* srow = qrow + TILES_PER_CTA * D;             // [8][Tv4] scores, then pooled weights
+  float* qrow = stage + KCHUNK * (D + SPAD);          // [32][D] query means, 4 rows per warp
+  float* srow = qrow + TILES_PER_CTA * D;             // [32][Tv4] scores, then pooled weights
   const int Tv4 = (Tv + 3) & ~3;                      // row stride: 16-byte aligned rows
   const int h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i = blockIdx.x * TILES_PER_CTA + warp;
-  const bool active = i < Tv;
-  float* s = srow + warp * Tv4;
-  float* mq = qrow + warp * D;
+  const int i0 = blockIdx.x * TILES_PER_CTA + warp * R;  // the warp's first query tile
   const float* mQ = means + ((size_t)0 * H + h) * Tv * D;
   const float* mK = means + ((size_t)1 * H + h) * Tv * D;
   const float* mV = means + ((size_t)2 * H + h) * Tv * D;
   constexpr int D4 = D / 4;  // float4 lanes per row (<= 32)
-  for (int c = lane; c < D; c += 32) mq[c] = active ? mQ[(size_t)i * D + c] : 0.f;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    float* mq = qrow + (warp * R + r) * D;
+    for (int c = lane; c < D; c += 32) mq[c] = i0 + r < Tv ? mQ[(size_t)(i0 + r) * D + c] : 0.f;
+  }
   // scores: stage 32 key means (row stride D + 4 floats: 16-byte column reads are
-  // conflict-free), then lane l of each warp computes the whole dot product for key tile
-  // j0 + l with four interleaved partial sums over the dimensions (c mod 4), added as
-  // ((p0 + p1) + (p2 + p3)); query and key means are read four floats at a time
+  // conflict-free), then lane l of each warp computes the whole dot product of key tile
+  // j0 + l with each of its four query tiles, four interleaved partial sums over the
+  // dimensions (c mod 4) per product, added as ((p0 + p1) + (p2 + p3)); the key mean is
+  // read once per 16-byte step for the four products, the query means by broadcast
   for (int j0 = 0; j0 < Tv; j0 += KCHUNK) {
     const int nj = min(KCHUNK, Tv - j0);
     __syncthreads();
@@ -194,27 +201,38 @@ __global__ void __launch_bounds__(ROUTE_THREADS)
       reinterpret_cast<float4*>(stage + (e / D4) * (D + SPAD))[e % D4] =
           __ldg(reinterpret_cast<const float4*>(mK + (size_t)j0 * D) + e);
     __syncthreads();
-    if (active && lane < nj) {
+    if (i0 < Tv && lane < nj) {
       const float4* kr = reinterpret_cast<const float4*>(stage + lane * (D + SPAD));
-      const float4* q4 = reinterpret_cast<const float4*>(mq);
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 8
+      const float4* q4 = reinterpret_cast<const float4*>(qrow + warp * R * D);
+      float a[R][4];
+#pragma unroll
+      for (int r = 0; r < R; ++r) a[r][0] = a[r][1] = a[r][2] = a[r][3] = 0.f;
+#pragma unroll 4
       for (int c = 0; c < D4; ++c) {
-        const float4 x = q4[c], y = kr[c];
-        a0 = fmaf(x.x, y.x, a0);
-        a1 = fmaf(x.y, y.y, a1);
-        a2 = fmaf(x.z, y.z, a2);
-        a3 = fmaf(x.w, y.w, a3);
+        const float4 y = kr[c];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float4 x = q4[r * D4 + c];
+          a[r][0] = fmaf(x.x, y.x, a[r][0]);
+          a[r][1] = fmaf(x.y, y.y, a[r][1]);
+          a[r][2] = fmaf(x.z, y.z, a[r][2]);
+          a[r][3] = fmaf(x.w, y.w, a[r][3]);
+        }
       }
-      s[j0 + lane] = (a0 + a1) + (a2 + a3);
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        srow[(warp * R + r) * Tv4 + j0 + lane] = (a[r][0] + a[r][1]) + (a[r][2] + a[r][3]);
     }
   }
   __syncwarp();
-  if (active) {
+  // top-k of each of the warp's query tiles under the total order (score desc, index asc),
+  // NaN ranking as -inf; selected tiles are then written in ascending order via ballots
+  for (int r = 0; r < R; ++r) {
+    const int i = i0 + r;
+    if (i >= Tv) break;  // warp-uniform
+    const float* s = srow + (warp * R + r) * Tv4;
     float* srow_out = scores + ((size_t)h * Tv + i) * Tv;
     for (int j = lane; j < Tv; j += 32) srow_out[j] = s[j];
-    // top-k under the total order (score desc, index asc), NaN ranking as -inf; selected
-    // tiles are then written in ascending order via ballots
     int* out = idx + ((size_t)h * Tv + i) * ksel;
     unsigned taken = 0u;
     if (ksel >= Tv) {
@@ -233,55 +251,81 @@ __global__ void __launch_bounds__(ROUTE_THREADS)
   }
   if (!pooled) return;
   // pooled branch: softmax over all video tiles of S / sqrt(D), then weights . mean(v)
-  float inv_sum = 0.f;
-  if (active) {
-    const float sc = 1.0f / sqrtf((float)D);
-    float mx = -INFINITY;
-    for (int j = lane; j < Tv; j += 32) mx = fmaxf(mx, s[j] * sc);
-    mx = warp_max(mx);
-    float sum = 0.f;
-    for (int j = lane; j < Tv; j += 32) {
-      const float e = expf(s[j] * sc - mx);
-      s[j] = e;  // the scores row becomes the weights row
-      sum += e;
+  float inv_sum[R];
+  const float sc = 1.0f / sqrtf((float)D);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    inv_sum[r] = 0.f;
+    if (i0 + r < Tv) {
+      float* s = srow + (warp * R + r) * Tv4;
+      float mx = -INFINITY;
+      for (int j = lane; j < Tv; j += 32) mx = fmaxf(mx, s[j] * sc);
+      mx = warp_max(mx);
+      float sum = 0.f;
+      for (int j = lane; j < Tv; j += 32) {
+        const float e = expf(s[j] * sc - mx);
+        s[j] = e;  // the scores row becomes the weights row
+        sum += e;
+      }
+      inv_sum[r] = 1.0f / warp_sum(sum);
     }
-    inv_sum = 1.0f / warp_sum(sum);
   }
   __syncwarp();
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 acc[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float* wrow = srow + warp * R * Tv4;
   for (int j0 = 0; j0 < Tv; j0 += KCHUNK) {
     const int nj = min(KCHUNK, Tv - j0);
     __syncthreads();
     for (int e = threadIdx.x; e < nj * D4; e += ROUTE_THREADS)
       reinterpret_cast<float4*>(stage)[e] = __ldg(reinterpret_cast<const float4*>(mV + (size_t)j0 * D) + e);
     __syncthreads();
-    if (active && lane < D4) {
+    if (i0 < Tv && lane < D4) {
       int jj = 0;
       for (; jj + 4 <= nj; jj += 4) {  // j order; four weights per 16-byte read
-        const float4 w4 = *reinterpret_cast<const float4*>(s + j0 + jj);
-        const float w[4] = {w4.x, w4.y, w4.z, w4.w};
+        float w[R][4];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float4 w4 = *reinterpret_cast<const float4*>(wrow + r * Tv4 + j0 + jj);
+          w[r][0] = w4.x;
+          w[r][1] = w4.y;
+          w[r][2] = w4.z;
+          w[r][3] = w4.w;
+        }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const float4 v = reinterpret_cast<const float4*>(stage + (jj + u) * D)[lane];
-          acc.x = fmaf(w[u], v.x, acc.x);
-          acc.y = fmaf(w[u], v.y, acc.y);
-          acc.z = fmaf(w[u], v.z, acc.z);
-          acc.w = fmaf(w[u], v.w, acc.w);
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            acc[r].x = fmaf(w[r][u], v.x, acc[r].x);
+            acc[r].y = fmaf(w[r][u], v.y, acc[r].y);
+            acc[r].z = fmaf(w[r][u], v.z, acc[r].z);
+            acc[r].w = fmaf(w[r][u], v.w, acc[r].w);
+          }
         }
       }
       for (; jj < nj; ++jj) {
-        const float w = s[j0 + jj];
         const float4 v = reinterpret_cast<const float4*>(stage + jj * D)[lane];
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float w = wrow[r * Tv4 + j0 + jj];
+          acc[r].x = fmaf(w, v.x, acc[r].x);
+          acc[r].y = fmaf(w, v.y, acc[r].y);
+          acc[r].z = fmaf(w, v.z, acc[r].z);
+          acc[r].w = fmaf(w, v.w, acc[r].w);
+        }
       }
     }
   }
-  if (active && lane < D4) {
-    reinterpret_cast<float4*>(pooled + ((size_t)h * Tv + i) * D)[lane] =
-        make_float4(acc.x * inv_sum, acc.y * inv_sum, acc.z * inv_sum, acc.w * inv_sum);
+  if (lane < D4) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (i0 + r < Tv)
+        reinterpret_cast<float4*>(pooled + ((size_t)h * Tv + i0 + r) * D)[lane] =
+            make_float4(acc[r].x * inv_sum[r], acc[r].y * inv_sum[r], acc[r].z * inv_sum[r],
+                        acc[r].w * inv_sum[r]);
+    }
   }
 }
 
