@@ -218,3 +218,38 @@ def test_token_reduction_needs_its_buffers(h3):
                                ctypes.byref(sv), ctypes.byref(sv), 0, fake,
                                h3.workspace_bytes(s_plain), None)
     assert st == 2
+
+
+def test_binding_struct_layouts_match_the_header(h3, tmp_path):
+    """The ctypes structs of the binding have the sizes and field offsets of the C
+    structs in include/h3dit.h, as the host C compiler lays them out."""
+    import ctypes
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    from audio_diffusion_transformer_gb300 import _binding as B
+    structs = {"h3dit_shape": B.Shape, "h3dit_block_weights": B.BlockWeights,
+               "h3dit_schedule": B.Schedule, "h3dit_ends": B.Ends,
+               "h3dit_reduction": B.Reduction}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "h3dit.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'  printf("{cname} sizeof %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'  printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), "-o", str(exe),
+                    str(src)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    got = {}
+    for ln in out.splitlines():
+        cname, field, val = ln.split()
+        got[(cname, field)] = int(val)
+    for cname, py in structs.items():
+        assert got[(cname, "sizeof")] == ctypes.sizeof(py), cname
+        for f, _ in py._fields_:
+            assert got[(cname, f)] == getattr(py, f).offset, f"{cname}.{f}"
