@@ -164,6 +164,10 @@ def _ptr(t):
     if hasattr(t, "data_ptr"):
         if not t.is_contiguous():
             raise ValueError("tensor must be contiguous")
+        if getattr(t, "is_cuda", True) is False:
+            # the kernels read and write these buffers: a host tensor would reach them as
+            # a host address, so it is refused here, before anything is launched
+            raise ValueError("tensor must be in GPU memory")
         return t.data_ptr()
     return t
 

@@ -253,3 +253,16 @@ def test_binding_struct_layouts_match_the_header(h3, tmp_path):
         assert got[(cname, "sizeof")] == ctypes.sizeof(py), cname
         for f, _ in py._fields_:
             assert got[(cname, f)] == getattr(py, f).offset, f"{cname}.{f}"
+
+
+def test_binding_refuses_host_tensors_before_any_launch(h3):
+    torch = pytest.importorskip("torch")
+    shp = S.BlockShape(64, 0, 64, hidden=256, heads=2, head_dim=128, mlp_width=256, topk=1)
+    cs = h3.make_shape(shp)
+    w = {n: torch.zeros(16, dtype=torch.bfloat16) for n in ("w_qkvg", "b_qkvg")}
+    x = torch.zeros(shp.n_rows, shp.hidden, dtype=torch.bfloat16)
+    ws = torch.zeros(256, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="GPU memory"):
+        h3.block_forward(cs, w, x, ws, stream=0)
+    with pytest.raises(ValueError, match="GPU memory"):
+        h3.linear(x, x, None, x, stream=0)
