@@ -168,8 +168,9 @@ h3dit_status h3dit_block_forward(const h3dit_shape* shape, const h3dit_block_wei
  * attends to all prefix rows plus the rows of its selected tiles.  Scale 1/sqrt(d).
  * Tiles are 64-row slices or clipped cubes of the video grid (see h3dit_shape;
  * with a grid, every buffer holds the video rows in cube order); Tv is the number
- * of video tiles (h3dit_tile_spans), at most 1,024, and the attention steps of a
- * video query tile, ceil(P / 128) + min(k, Tv), at most 512 -- larger shapes return
+ * of video tiles (h3dit_tile_spans), at most 1,024, the attention steps of a
+ * video query tile, ceil(P / 128) + min(k, Tv), at most 512, and N at most 65,408
+ * rows (a prefix query walks N / 128 key steps) -- larger shapes return
  * H3DIT_ERR_SHAPE.
  * The pooled branch and mix run when H3DIT_POOLED is set and gate is given.
  */

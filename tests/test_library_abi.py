@@ -266,3 +266,34 @@ def test_binding_refuses_host_tensors_before_any_launch(h3):
         h3.block_forward(cs, w, x, ws, stream=0)
     with pytest.raises(ValueError, match="GPU memory"):
         h3.linear(x, x, None, x, stream=0)
+
+
+def test_documented_size_limits_refused_on_host(h3):
+    """The limits the header documents come back as H3DIT_ERR_SHAPE before any launch."""
+    base = S.BlockShape(0, 0, 64, hidden=256, heads=4, head_dim=64, mlp_width=256, topk=1)
+    assert h3.check_shape(h3.make_shape(base.with_(heads=1))) == 2  # attention width 64
+    ok = lambda s: h3.check_shape(h3.make_shape(s))  # noqa: E731
+    # at most 65,408 packed rows (a prefix query unit walks N / 128 key steps)
+    assert ok(base.with_(n_video=1022 * 64)) == 0
+    assert ok(base.with_(n_video=1022 * 64 + 1)) == 2
+    # at most 1,024 video tiles: a 1 x 1 x W grid cut into clipped 4 x 4 x 4 cubes has
+    # ceil(W / 4) tiles of at most 4 rows
+    assert ok(base.with_(n_video=4096, video_grid=(1, 1, 4096))) == 0
+    assert ok(base.with_(n_video=4097, video_grid=(1, 1, 4097))) == 2
+    # a video query tile's steps, ceil(P / 128) + min(k, Tv), at most 512
+    assert ok(base.with_(n_text=128 * 500, n_video=64 * 12, topk=12)) == 0
+    assert ok(base.with_(n_text=128 * 500, n_video=64 * 13, topk=13)) == 2
+    # head widths 64 and 128 only; hidden and MLP widths in multiples of 256 (SwiGLU 128)
+    assert ok(base.with_(head_dim=32)) == 2
+    assert ok(base.with_(hidden=384)) == 2
+    assert ok(base.with_(mlp_width=384)) == 2
+    assert ok(base.with_(mlp_width=384, mlp="swiglu")) == 0
+    assert ok(base.with_(mlp_width=192, mlp="swiglu")) == 2
+    # token reduction needs a video grid at least two tokens wide
+    assert ok(base.with_(token_reduction=True)) == 2
+    assert ok(base.with_(n_video=2 * 4 * 8, video_grid=(2, 4, 8), token_reduction=True)) == 0
+    assert ok(base.with_(n_video=2 * 4 * 1, video_grid=(2, 4, 1), token_reduction=True)) == 2
+    # the attention-only shape (hidden = mlp_width = 0) sizes its own, smaller workspace
+    full = h3.workspace_bytes(h3.make_shape(base))
+    attn = h3.workspace_bytes(h3.attn_shape(base))
+    assert 0 < attn < full
