@@ -279,18 +279,23 @@ def oracle_block_sample(shape, rng_seed=0):
     O.routed_attention(Q, K, V, s.n_prefix, s.n_video, idx, tiles=vt)
     t_vid = (time.perf_counter() - t0) * (H * tv) / len(vt)
     t_pre = 0.0
+    n_chunks = 0
     if s.n_prefix:
         t0 = time.perf_counter()
-        n_chunks = min(2, s.n_prefix // 64)
+        n_chunks = min(2, (s.n_prefix + 63) // 64)
+        pre_rows = min(s.n_prefix, 64 * n_chunks)  # prefix query rows attended per head
         for h in range(hs):
             for c in range(n_chunks):
-                O.attend(Q[h, 64 * c:64 * c + 64], K[h], V[h], 1.0 / math.sqrt(d))
-        t_pre = (time.perf_counter() - t0) * (H * s.n_prefix / 64) / (hs * n_chunks)
+                O.attend(Q[h, 64 * c:min(64 * c + 64, s.n_prefix)], K[h], V[h],
+                         1.0 / math.sqrt(d))
+        t_pre = (time.perf_counter() - t0) * (H * s.n_prefix) / (hs * pre_rows)
     total = t_rows + t_router + t_vid + t_pre
+    pre = (f" and {hs * n_chunks} prefix chunks of up to 64 rows "
+           f"(x{H * s.n_prefix / (hs * pre_rows):.3g})" if n_chunks else "")
     desc = (f"one block of the {N}-row shape, float64 oracle: row-local stages on {R} rows "
-            f"(x{N / R:.0f}), router on {hs} of {H} heads (x{H / hs:.0f}), attention on "
-            f"{len(vt)} video query tiles (x{H * tv / len(vt):.0f}) and {2 * hs} prefix 64-row "
-            f"chunks (x{H * s.n_prefix / 64 / (2 * hs):.0f}); scaled to the whole block")
+            f"(x{N / R:.3g}), router on {hs} of {H} heads (x{H / hs:.3g}), attention on "
+            f"{len(vt)} video query tiles (x{H * tv / len(vt):.3g}){pre}; scaled to the whole "
+            f"block")
     return total, desc
 
 
