@@ -73,7 +73,8 @@ enum { TILE = 64 };
 
 /* ------------------------------------------------------------------ roundings */
 
-/* Nearest bf16 (8 significant bits, ties to even), returned as a double. */
+/* Nearest bf16 (8 significant bits, ties to even), returned as a double: the storage
+ * type of weights and activations (TensorFold #949 "Precision"). */
 static double bf16r(double x) {
   if (x != x || isinf(x) || x == 0.0) return x;
   const double a = fabs(x);
@@ -132,7 +133,8 @@ int h3ref_tiles(const h3ref_shape* s, int* rows, int* start) {
 
 /* ------------------------------------------------------------------ row steps */
 
-/* h = bf16(x / sqrt(mean(x^2) + eps) * (1 + scale) + shift) for one row. */
+/* h = bf16(x / sqrt(mean(x^2) + eps) * (1 + scale) + shift) for one row (TensorFold #949
+ * "What it adds": modulated norm; h3.c README fused gated-AdaLN paragraph: per-row RMS). */
 static void modulated_norm(const double* x, int D, const double* shift, const double* scale,
                            double eps, double* h) {
   double ss = 0.0;
@@ -141,7 +143,8 @@ static void modulated_norm(const double* x, int D, const double* shift, const do
   for (int c = 0; c < D; ++c) h[c] = bf16r(x[c] * inv * (1.0 + scale[c]) + shift[c]);
 }
 
-/* y[r, o] = sum_i a[r, i] w[o, i] + b[o]  (w stored [out, in]; b may be NULL) */
+/* y[r, o] = sum_i a[r, i] w[o, i] + b[o]  (w stored [out, in]; b may be NULL): the
+ * projections, bf16 operands with wide sums (TensorFold #949 "Precision"). */
 static void linear(const double* a, int M, int K, const double* w, const double* b, int Nout,
                    double* y) {
   for (int r = 0; r < M; ++r)
@@ -160,7 +163,8 @@ static void head_norm(double* v, int d, const double* w, double eps) {
   for (int c = 0; c < d; ++c) v[c] = v[c] * inv * w[c];
 }
 
-/* Rotary angle of pair c (c < d/2) for packed row p. */
+/* Rotary angle of pair c (c < d/2) for packed row p (h3.c README, Q/K RMS + RoPE
+ * paragraph: spatial and temporal rotary coordinates when a latent grid is given). */
 static double rope_angle(const h3ref_shape* s, int p, int c) {
   const int d = s->head_dim, half = d / 2;
   if (!is_grid(s)) return (double)p * pow(s->theta, -2.0 * c / d);
@@ -216,7 +220,8 @@ static void attend_row(const double* q, const double* K, const double* V, const 
   for (int c = 0; c < d; ++c) o[c] /= l;
 }
 
-/* Top-k of one query tile's scores under the total order (score descending, index
+/* TensorFold #949 "Kernel contract" and "Precision" (fp32 routing).
+ * Top-k of one query tile's scores under the total order (score descending, index
  * ascending) with NaN as -inf, decided on fp32 scores: tile j is kept when fewer than
  * k tiles rank ahead of it.  Kept tiles are written ascending. */
 static void topk_row(const double* srow, int Tv, int k, int* out) {
@@ -234,7 +239,9 @@ static void topk_row(const double* srow, int Tv, int k, int* out) {
   }
 }
 
-/* Router + routed / dense attention + pooled branch + gate mix for one layer.
+/* TensorFold #949 "What it adds": h3_routing.metal (tile means, tile scores, top-k,
+ * pooled branch), h3_attention.metal (tile-routed attention), h3_gate_mix.
+ * Router + routed / dense attention + pooled branch + gate mix for one layer.
  * Q, K, V [H, N, d]; G [N, H*d] or NULL.  Outputs: o_mixed [N, H*d] (float64, not
  * rounded), idx [H, Tv, min(k, Tv)], scores [H, Tv, Tv], pooled [H, Tv, d] (any may
  * be NULL except o_mixed).  Returns 0, or -1 on a bad shape or allocation failure. */
@@ -358,7 +365,10 @@ done:
 static double gelu(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
 static double silu(double x) { return x / (1.0 + exp(-x)); }
 
-/* One DiT block on the packed rows x [N, D] (bf16 values).  Writes x1 and x2
+/* TensorFold #949 "What it adds" (block.zig, the block's steps in order); gated
+ * residual adds as in the h3.c README's fused gated-AdaLN paragraph; SwiGLU MLP as in
+ * its FC1 gate/up paragraph.
+ * One DiT block on the packed rows x [N, D] (bf16 values).  Writes x1 and x2
  * (either may be NULL) and, when given, the bf16 attention output o [N, A].
  * Returns 0, or -1 on a bad shape or allocation failure. */
 int h3ref_block_forward(const h3ref_shape* s, const h3ref_weights* w, const double* x,
