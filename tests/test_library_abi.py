@@ -297,3 +297,42 @@ def test_documented_size_limits_refused_on_host(h3):
     full = h3.workspace_bytes(h3.make_shape(base))
     attn = h3.workspace_bytes(h3.attn_shape(base))
     assert 0 < attn < full
+
+
+def test_plain_c_program_links_and_calls_the_library(h3, tmp_path):
+    """A C99 program includes the header, links libh3dit.so and calls its host-only
+    entry points; its answers equal the Python binding's."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    src = tmp_path / "use.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "h3dit.h"
+int main(void) {
+  h3dit_shape s = {.n_text = 512, .n_audio = 1024, .n_video = 13899, .hidden = 5120,
+                   .heads = 40, .head_dim = 128, .attn_width = 5120, .mlp_width = 20480,
+                   .tile = 64, .topk = 16, .rms_eps = 1e-6f, .rope_theta = 10000.f,
+                   .flags = H3DIT_QK_NORM | H3DIT_ROPE | H3DIT_POOLED};
+  int first[256], rows[256], n = 256;
+  h3dit_status st = h3dit_tile_spans(&s, first, rows, &n);
+  printf("%zu %d %d %d %d %d %s\n", h3dit_workspace_bytes(&s), (int)h3dit_check_shape(&s),
+         (int)st, n, first[n - 1], rows[n - 1], h3dit_status_string(H3DIT_ERR_ALIGN));
+  return 0;
+}
+''')
+    from audio_diffusion_transformer_gb300._binding import LIB_PATH
+    pkg = os.path.dirname(LIB_PATH)
+    exe = tmp_path / "use"
+    subprocess.run([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), "-o", str(exe),
+                    str(src), LIB_PATH, f"-Wl,-rpath,{pkg}"], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    shp = S.BLOCK_15K.shape
+    cs = h3.make_shape(shp)
+    first, nrows = h3.tile_spans(cs)
+    assert int(out[0]) == h3.workspace_bytes(cs)
+    assert out[1:4] == ["0", "0", str(shp.n_video_tiles)]
+    assert int(out[4]) == first[-1] and int(out[5]) == nrows[-1] == 13899 - 217 * 64
+    assert " ".join(out[6:]) == "pointer not 16-byte aligned"
