@@ -56,6 +56,20 @@ def lib():
                                              vp, vp, vp, vp]
         _lib.h3ref_bf16.argtypes = [ctypes.c_double]
         _lib.h3ref_bf16.restype = ctypes.c_double
+        i, d = ctypes.c_int, ctypes.c_double
+        _lib.h3ref_euler.argtypes = [vp, vp, i, i, i, d, d, vp]
+        _lib.h3ref_euler.restype = None
+        _lib.h3ref_extrapolate.argtypes = [vp, vp, i, i, i, vp, vp, vp]
+        _lib.h3ref_extrapolate.restype = None
+        _lib.h3ref_patch_in.argtypes = [vp, i, i, vp, vp, i, vp]
+        _lib.h3ref_patch_in.restype = None
+        _lib.h3ref_output_head.argtypes = [vp, i, i, vp, vp, vp, i, d, vp]
+        _lib.h3ref_output_head.restype = None
+        _lib.h3ref_token_pool.argtypes = [vp, i, i, i, i, i, vp, vp]
+        _lib.h3ref_token_pool.restype = None
+        _lib.h3ref_token_restore.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+        _lib.h3ref_token_restore.restype = None
+        _lib.h3ref_thin_layers.argtypes = [vp, i, i, i, vp]
     return _lib
 
 
@@ -131,3 +145,69 @@ def block_forward(x, wts: dict, s, p_bf16: bool = False) -> dict:
 
 def bf16(x: float) -> float:
     return lib().h3ref_bf16(float(x))
+
+
+def euler(z, v, dt, dt_prefix=None, n_prefix=0):
+    z, v = _f64(z), _f64(v)
+    N, D = z.shape
+    out = np.zeros((N, D))
+    lib().h3ref_euler(_p(z), _p(v), N, D, n_prefix, float(dt),
+                      float(dt if dt_prefix is None else dt_prefix), _p(out))
+    return out
+
+
+def extrapolate(va, vb, sig_video, sig_prefix=None, n_prefix=0):
+    va, vb = _f64(va), _f64(vb)
+    N, D = va.shape
+    sv = _f64(np.asarray(sig_video))
+    sp = _f64(np.asarray(sig_video if sig_prefix is None else sig_prefix))
+    out = np.zeros((N, D))
+    lib().h3ref_extrapolate(_p(va), _p(vb), N, D, n_prefix, _p(sv), _p(sp), _p(out))
+    return out
+
+
+def patch_in(z, w_in, b_in):
+    z, w_in, b_in = _f64(z), _f64(w_in), _f64(b_in)
+    rows, c = z.shape
+    D = w_in.shape[1]
+    x = np.zeros((rows, D))
+    lib().h3ref_patch_in(_p(z), rows, c, _p(w_in), _p(b_in), D, _p(x))
+    return x
+
+
+def output_head(x, mod2, w_out, b_out, eps=1e-6):
+    x, mod2, w_out, b_out = _f64(x), _f64(mod2), _f64(w_out), _f64(b_out)
+    rows, D = x.shape
+    c = w_out.shape[0]
+    v = np.zeros((rows, c))
+    lib().h3ref_output_head(_p(x), rows, D, _p(mod2), _p(w_out), _p(b_out), c, float(eps), _p(v))
+    return v
+
+
+def token_pool(x, s):
+    x = _f64(x)
+    T, Hg, W = s.video_grid
+    Wr = (W + 1) // 2
+    D = x.shape[1]
+    xr = np.zeros((s.n_prefix + T * Hg * Wr, D))
+    base = np.zeros((T * Hg * Wr, D))
+    lib().h3ref_token_pool(_p(x), s.n_prefix, T, Hg, W, D, _p(xr), _p(base))
+    return xr, base
+
+
+def token_restore(bypass, x_r, base, s):
+    bypass, x_r, base = _f64(bypass), _f64(x_r), _f64(base)
+    T, Hg, W = s.video_grid
+    out = np.zeros(bypass.shape)
+    lib().h3ref_token_restore(_p(bypass), _p(x_r), _p(base), s.n_prefix, T, Hg, W,
+                              bypass.shape[1], _p(out))
+    return out
+
+
+def thin_layers(mods, keep):
+    m = _f64(np.asarray(mods))
+    L, _, D = m.shape
+    kept = np.zeros(max(L, 1), np.int32)
+    n = lib().h3ref_thin_layers(_p(m), L, D, keep, _p(kept))
+    assert n >= 0
+    return kept[:n].tolist()

@@ -42,7 +42,9 @@
  * sets, top-k selections, scores, pooled branch and attention outputs against the
  * numpy oracle on slices, clipped cubes with the 3-D rotary, a 450-row prefix and a
  * SwiGLU block with a prefix table; every tile selected against dense attention by
- * brute force; planted ties and NaN for the top-k rule.
+ * brute force; planted ties and NaN for the top-k rule; the Euler step, the
+ * extrapolation, the patch projection, the output head, token pooling and restore and
+ * layer thinning against the numpy oracle.
  */
 #include <math.h>
 #include <stdint.h>
@@ -481,6 +483,144 @@ done:
   free(x1);
   free(u);
   return rc;
+}
+
+/* ------------------------------------------------------------------ denoiser and ends */
+
+/* h3.c README sampler paragraph: z' = fp32(z + dt v), the text and audio rows (index < P)
+ * on their own step dt_prefix.  z, v, out [N, D]. */
+void h3ref_euler(const double* z, const double* v, int N, int D, int P, double dt,
+                 double dt_prefix, double* out) {
+  for (int r = 0; r < N; ++r)
+    for (int c = 0; c < D; ++c) {
+      const double step = r < P ? dt_prefix : dt;
+      out[(size_t)r * D + c] = f32r(z[(size_t)r * D + c] + step * v[(size_t)r * D + c]);
+    }
+}
+
+/* h3.c README sampler paragraph: a skipped pass extrapolates linearly in sigma from the
+ * last two fresh velocities, v = v_a + (v_a - v_b) (s_i - s_a) / (s_a - s_b), the text
+ * and audio rows on their own sigmas sp[3] = (s_i, s_a, s_b). */
+void h3ref_extrapolate(const double* va, const double* vb, int N, int D, int P,
+                       const double* sv, const double* sp, double* out) {
+  const double cv = (sv[0] - sv[1]) / (sv[1] - sv[2]);
+  const double cp = (sp[0] - sp[1]) / (sp[1] - sp[2]);
+  for (int r = 0; r < N; ++r)
+    for (int c = 0; c < D; ++c) {
+      const size_t e = (size_t)r * D + c;
+      out[e] = va[e] + (va[e] - vb[e]) * (r < P ? cp : cv);
+    }
+}
+
+/* h3.c README: a modality's patch projection, x = bf16(z w_in + b) with w_in stored
+ * input-major [c, D] (fp32 weights and sums on the pages; float64 here). */
+void h3ref_patch_in(const double* z, int rows, int c, const double* w_in, const double* b_in,
+                    int D, double* x) {
+  for (int r = 0; r < rows; ++r)
+    for (int o = 0; o < D; ++o) {
+      double acc = 0.0;
+      for (int j = 0; j < c; ++j) acc += z[(size_t)r * c + j] * w_in[(size_t)j * D + o];
+      x[(size_t)r * D + o] = bf16r(acc + b_in[o]);
+    }
+}
+
+/* h3.c README: final AdaLN of a modality's rows (the block norms' form with its own
+ * shift, scale [2, D]) and its narrow head: v = fp32(h W_out^T + b), W_out [c, D]. */
+void h3ref_output_head(const double* x, int rows, int D, const double* mod2,
+                       const double* w_out, const double* b_out, int c, double eps,
+                       double* v) {
+  double* h = malloc(sizeof(double) * (size_t)D);
+  if (!h) return;
+  for (int r = 0; r < rows; ++r) {
+    modulated_norm(x + (size_t)r * D, D, mod2, mod2 + D, eps, h);
+    for (int o = 0; o < c; ++o) {
+      double acc = 0.0;
+      for (int i = 0; i < D; ++i) acc += h[i] * w_out[(size_t)o * D + i];
+      v[(size_t)r * c + o] = f32r(acc + b_out[o]);
+    }
+  }
+  free(h);
+}
+
+/* h3.c README token-reduction paragraph: the prefix rows pass unchanged; each pair of
+ * horizontally adjacent video tokens (t, h, 2j), (t, h, 2j + 1) becomes one row, their
+ * mean (fp32 sum halved, rounded to bf16); a lone last token of an odd row passes as it
+ * is.  Video rows of x are in raster order of the T x H x W grid; x_r [P + T H Wr, D] and
+ * base [T H Wr, D] (the pooled rows as they were at pooling time), Wr = ceil(W / 2). */
+void h3ref_token_pool(const double* x, int P, int T, int Hg, int W, int D, double* x_r,
+                      double* base) {
+  const int Wr = (W + 1) / 2;
+  memcpy(x_r, x, sizeof(double) * (size_t)P * D);
+  for (int tt = 0; tt < T; ++tt)
+    for (int hh = 0; hh < Hg; ++hh)
+      for (int j = 0; j < Wr; ++j) {
+        const double* a = x + ((size_t)P + ((size_t)tt * Hg + hh) * W + 2 * j) * D;
+        double* o = base + (((size_t)tt * Hg + hh) * Wr + j) * D;
+        for (int c = 0; c < D; ++c)
+          o[c] = (2 * j + 1 < W) ? bf16r(f32r(a[c] + a[D + c]) * 0.5) : a[c];
+        memcpy(x_r + ((size_t)P + ((size_t)tt * Hg + hh) * Wr + j) * D, o, sizeof(double) * D);
+      }
+}
+
+/* Restore: prefix rows from x_r; video token (t, h, w) = bf16(bypass + fp32(x_r - base)
+ * of its pair row (t, h, w / 2)), in fp32 arithmetic.  out [P + T H W, D]. */
+void h3ref_token_restore(const double* bypass, const double* x_r, const double* base, int P,
+                         int T, int Hg, int W, int D, double* out) {
+  const int Wr = (W + 1) / 2;
+  memcpy(out, x_r, sizeof(double) * (size_t)P * D);
+  for (int tt = 0; tt < T; ++tt)
+    for (int hh = 0; hh < Hg; ++hh)
+      for (int w = 0; w < W; ++w) {
+        const size_t pr = ((size_t)tt * Hg + hh) * Wr + w / 2;
+        const size_t full = (size_t)P + ((size_t)tt * Hg + hh) * W + w;
+        for (int c = 0; c < D; ++c) {
+          const double dlt = f32r(x_r[((size_t)P + pr) * D + c] - base[pr * D + c]);
+          out[full * D + c] = bf16r(f32r(bypass[full * D + c] + dlt));
+        }
+      }
+}
+
+/* h3.c README layer-thinning paragraph: keep the first and last of L blocks, score the
+ * others by ||gate1||_2 + ||gate2||_2 of their [6, D] tables (rows 2 and 5), drop the
+ * lowest scores, ties dropping the higher index.  kept [keep] ascending; returns the
+ * number kept, or -1 when keep < 2. */
+int h3ref_thin_layers(const double* mods, int L, int D, int keep, int* kept) {
+  if (keep >= L) {
+    for (int b = 0; b < L; ++b) kept[b] = b;
+    return L;
+  }
+  if (keep < 2) return -1;
+  double* score = malloc(sizeof(double) * (size_t)L);
+  char* drop = calloc((size_t)L, 1);
+  if (!score || !drop) {
+    free(score);
+    free(drop);
+    return -1;
+  }
+  for (int b = 1; b < L - 1; ++b) {
+    double g1 = 0.0, g2 = 0.0;
+    for (int c = 0; c < D; ++c) {
+      const double a = mods[((size_t)b * 6 + 2) * D + c], e = mods[((size_t)b * 6 + 5) * D + c];
+      g1 += a * a;
+      g2 += e * e;
+    }
+    score[b] = sqrt(g1) + sqrt(g2);
+  }
+  /* drop L - keep blocks one at a time: the lowest score, the higher index among equals */
+  for (int n = 0; n < L - keep; ++n) {
+    int pick = -1;
+    for (int b = 1; b < L - 1; ++b) {
+      if (drop[b]) continue;
+      if (pick < 0 || score[b] < score[pick] || (score[b] == score[pick] && b > pick)) pick = b;
+    }
+    drop[pick] = 1;
+  }
+  int n = 0;
+  for (int b = 0; b < L; ++b)
+    if (!drop[b]) kept[n++] = b;
+  free(score);
+  free(drop);
+  return n;
 }
 
 /* Exported for the tests' rounding checks. */

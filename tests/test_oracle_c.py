@@ -139,3 +139,48 @@ def test_c_topk_rules():
     K[0, 0:64] = np.nan
     assert layer(K, 1) == [[2]] * 4
     assert layer(K, 3) == [[1, 2, 3]] * 4
+
+
+# --------------------------------------------------------------------------- denoiser and ends
+def test_euler_and_extrapolation_match_numpy_oracle():
+    N, D, P = 40, 24, 9
+    z = rng.standard_normal((N, D)).astype(np.float32).astype(np.float64)
+    v = O.bf16(rng.standard_normal((N, D)))
+    for dt, dtp in ((-0.125, None), (-0.05, -0.3)):
+        assert np.array_equal(cref.euler(z, v, dt, dtp, P), O.euler_update(z, v, dt, dtp, P))
+    va, vb = rng.standard_normal((2, N, D))
+    sv, sp = (0.4, 0.5, 0.65), (0.3, 0.45, 0.5)
+    assert np.array_equal(cref.extrapolate(va, vb, sv, sp, P),
+                          O.extrapolate(va, vb, *sv, sp, P))
+
+
+def test_both_ends_match_numpy_oracle():
+    z = rng.standard_normal((37, 96))
+    w_in = rng.standard_normal((96, 256)) * 0.1
+    b_in = rng.standard_normal(256) * 0.02
+    _bf16_close(cref.patch_in(z, w_in, b_in), O.patch_in(z, w_in, b_in), min_equal=0.999)
+    x = O.bf16(rng.standard_normal((37, 256)))
+    mod2 = rng.standard_normal((2, 256)) * 0.1
+    w_out = O.bf16(rng.standard_normal((32, 256)) * 0.02)
+    b_out = O.bf16(rng.standard_normal(32) * 0.02)
+    a, b = cref.output_head(x, mod2, w_out, b_out), O.output_head(x, mod2, w_out, b_out)
+    assert np.all(np.abs(a - b) <= np.abs(b) * 2.0 ** -22 + 1e-30)  # fp32 rounding order
+
+
+@pytest.mark.parametrize("grid", [(3, 4, 7), (2, 3, 8), (1, 1, 1)])
+def test_token_pool_and_restore_match_numpy_oracle(grid):
+    s = S.BlockShape(8, 24, int(np.prod(grid)), hidden=16, heads=2, head_dim=8, mlp_width=64,
+                     topk=2, video_grid=grid, token_reduction=True)
+    x = O.bf16(rng.standard_normal((s.n_rows, 16)))
+    xr_c, base_c = cref.token_pool(x, s)
+    xr_n, base_n = O.token_pool(x, s)
+    assert np.array_equal(xr_c, xr_n) and np.array_equal(base_c, base_n)
+    y = O.bf16(xr_n + rng.standard_normal(xr_n.shape) * 0.1)  # the reduced rows after blocks
+    assert np.array_equal(cref.token_restore(x, y, base_n, s), O.token_restore(x, y, base_n, s))
+
+
+def test_thin_layers_matches_numpy_oracle():
+    mods = rng.standard_normal((12, 6, 32))
+    mods[4] = mods[7]  # a planted tie: the higher index is dropped first
+    for keep in (2, 5, 9, 11, 12):
+        assert cref.thin_layers(mods, keep) == O.thin_layers(mods, keep)
