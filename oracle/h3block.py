@@ -51,7 +51,8 @@ PIN TABLE (function: pin tests, without their "test_" prefix)
   topk_select: topk_brute_force_with_ties_and_nans, topk_nan_regression_exact_k
   topk_gap: topk_all_and_gap
   topk_set_valid: topk_all_and_gap
-  attend: routed_all_tiles_equals_dense_brute_force, block_all_tiles_equals_dense
+  attend: routed_all_tiles_equals_dense_brute_force, block_all_tiles_equals_dense,
+    attend_bf16_weights_streamed_in_octaves
   routed_attention: routed_all_tiles_equals_dense_brute_force, routed_keyset_brute_force,
     attention_row_stochastic_and_zero_query
   pooled_branch: pooled_closed_forms
@@ -436,17 +437,28 @@ def topk_set_valid(scores_row, chosen, tol: float = 1e-5) -> bool:
 def attend(q, k, v, scale: float, p_bf16: bool = False) -> np.ndarray:
     """softmax(q k^T * scale) v for one head; bidirectional, no mask.
 
-    With ``p_bf16`` the unnormalised weights exp(s - max) are rounded to bf16
-    before the value product, as TensorFold #949 "Precision" states for the
-    routed attention; the row sum l uses the unrounded weights (reading: the
-    pages do not say which).  Default: exact float64.
+    With ``p_bf16`` the unnormalised weights are rounded to bf16 before the
+    value product, as TensorFold #949 "Precision" states for the routed
+    attention; the row sum l uses the unrounded weights (reading: the pages do
+    not say which).  The pages do not say against which maximum the
+    unnormalised weights are taken, and a bf16 rounding depends on it.
+    Reading: against a whole power of two, p_j = 2^(z_j - M) with
+    z_j = s_j log2(e) and M = ceil(max_j z_j).  Scaling by a power of two
+    commutes with the rounding, so the result is the same for every integer M
+    (any maximum a streaming softmax meets on the way, if it keeps its maximum
+    in whole octaves); without rounding it is the exact softmax.
+    Default: exact float64.
     """
     s = (np.asarray(q, np.float64) @ np.asarray(k, np.float64).T) * scale
+    if p_bf16:
+        z = s * (1.0 / math.log(2.0))
+        M = np.ceil(z.max(axis=1, keepdims=True))
+        p = np.exp2(z - M)
+        l = p.sum(axis=1, keepdims=True)
+        return (bf16(p) @ np.asarray(v, np.float64)) / l
     m = s.max(axis=1, keepdims=True)
     p = np.exp(s - m)
     l = p.sum(axis=1, keepdims=True)
-    if p_bf16:
-        p = bf16(p)
     return (p @ np.asarray(v, np.float64)) / l
 
 
@@ -717,14 +729,15 @@ def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
     return out
 
 
-def block_forward_rows(x, wts: dict, shape, rows) -> dict:
+def block_forward_rows(x, wts: dict, shape, rows, p_bf16: bool = False) -> dict:
     """``block_forward`` evaluated for a subset of output rows (for full-size checks).
 
     The same steps in the same order as ``block_forward``; only the work that
     the requested rows depend on is done: the projection of every row (keys,
     values and the video query rows that feed the tile means), the router over
     all tiles, attention for the requested rows' query rows / tiles, and the
-    out projection and MLP for the requested rows.
+    out projection and MLP for the requested rows.  ``p_bf16`` as in
+    ``block_forward``.
     """
     s = shape
     mod = np.asarray(wts["mod"], np.float64)
@@ -757,7 +770,7 @@ def block_forward_rows(x, wts: dict, shape, rows) -> dict:
                 keys = np.arange(s.n_rows)
             else:
                 keys = np.concatenate([np.arange(P)] + [vt[j] for j in idx[hh, tile_of[r]]])
-            O[hh, n] = attend(q[hh, [r]], k[hh, keys], v[hh, keys], scale)[0]
+            O[hh, n] = attend(q[hh, [r]], k[hh, keys], v[hh, keys], scale, p_bf16)[0]
     o = O.transpose(1, 0, 2).reshape(len(rows), H * d)
     if s.pooled:
         pb = pooled_branch(S, mv, d)

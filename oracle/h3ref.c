@@ -199,22 +199,28 @@ static void rotate(const h3ref_shape* s, int p, double* v) {
 /* ------------------------------------------------------------------ attention */
 
 /* One query row against a key set: o = sum softmax(q k / sqrt(d)) v; with p_bf16 the
- * weights exp(s - max) are rounded to bf16 before the value product and the row sum
- * uses the unrounded weights. */
+ * weights are rounded to bf16 before the value product and the row sum uses the
+ * unrounded weights.  Reading (the pages do not fix the maximum the rounded weights
+ * are taken against): with p_bf16 a weight is 2^(s log2(e) - M), M the smallest whole
+ * number not below the largest s log2(e) of the row, so that the rounding does not
+ * depend on which maximum a streaming softmax has met (whole octaves commute with it). */
 static void attend_row(const double* q, const double* K, const double* V, const int* keys,
                        int nk, int d, int p_bf16, double* sbuf, double* o) {
   const double scale = 1.0 / sqrt((double)d);
+  const double log2e = 1.0 / log(2.0);
   double m = -INFINITY;
   for (int j = 0; j < nk; ++j) {
     double acc = 0.0;
     for (int c = 0; c < d; ++c) acc += q[c] * K[(size_t)keys[j] * d + c];
     sbuf[j] = acc * scale;
+    if (p_bf16) sbuf[j] *= log2e;
     if (sbuf[j] > m) m = sbuf[j];
   }
+  if (p_bf16) m = ceil(m);
   double l = 0.0;
   for (int c = 0; c < d; ++c) o[c] = 0.0;
   for (int j = 0; j < nk; ++j) {
-    const double p = exp(sbuf[j] - m);
+    const double p = p_bf16 ? exp2(sbuf[j] - m) : exp(sbuf[j] - m);
     l += p;
     const double pv = p_bf16 ? bf16r(p) : p;
     for (int c = 0; c < d; ++c) o[c] += pv * V[(size_t)keys[j] * d + c];

@@ -208,6 +208,41 @@ def test_routed_all_tiles_equals_dense_brute_force(P):
         assert np.allclose(out[h], want, atol=1e-12)
 
 
+def test_attend_bf16_weights_streamed_in_octaves():
+    """The bf16-weight reading: weights rounded against a whole-octave maximum give the
+    same result however the keys are streamed, as long as each running maximum is a
+    whole octave (a power-of-two rescale commutes with the bf16 rounding).  A streaming
+    softmax over random key chunks, written here with its own running maximum, must
+    reproduce the one-shot result; for positive values the rounding moves the output
+    by at most 2^-9 relative."""
+    d, nq, nk = 16, 5, 300
+    q = rng.standard_normal((nq, d)) * 2.0
+    k = rng.standard_normal((nk, d))
+    v = rng.standard_normal((nk, d))
+    scale = 1.0 / math.sqrt(d)
+    want = O.attend(q, k, v, scale, p_bf16=True)
+    for trial in range(4):
+        cuts = np.sort(rng.choice(np.arange(1, nk), size=5 + trial, replace=False))
+        chunks = np.split(np.arange(nk), cuts)
+        for r in range(nq):
+            m, l, acc = -np.inf, 0.0, np.zeros(d)
+            for ch in chunks:
+                z = (k[ch] @ q[r]) * scale / math.log(2.0)
+                if z.max() > m:
+                    m_new = math.ceil(z.max())
+                    f = 0.0 if m == -np.inf else 2.0 ** (m - m_new)
+                    l, acc, m = l * f, acc * f, m_new
+                w = 2.0 ** (z - m)
+                l += w.sum()
+                acc += O.bf16(w) @ v[ch]
+            assert np.allclose(acc / l, want[r], rtol=0, atol=1e-13)
+    vp = np.abs(v) + 0.5
+    exact = O.attend(q, k, vp, scale)
+    rounded = O.attend(q, k, vp, scale, p_bf16=True)
+    assert np.all(np.abs(rounded - exact) <= 2.0 ** -9 * exact + 1e-15)
+    assert not np.array_equal(rounded, exact)
+
+
 def test_routed_keyset_brute_force():
     # every video query row attends to the prefix plus exactly its selected tiles
     H, P, Vn, d, k = 1, 64, 256, 8, 2
@@ -616,6 +651,12 @@ def test_block_rows_equals_full_block():
     assert np.all(np.abs(part["x2"] - ref) <= ulp)
     assert np.mean(part["x2"] == ref) > 0.99
     assert np.array_equal(part["idx"], full["idx"])
+    # the same with the softmax weights rounded to bf16
+    full = O.block_forward(x, w, shape, p_bf16=True)
+    part = O.block_forward_rows(x, w, shape, rows, p_bf16=True)
+    ref = full["x2"][rows]
+    assert np.all(np.abs(part["x2"] - ref) <= np.abs(ref) * 2.0 ** -7)
+    assert np.mean(part["x2"] == ref) > 0.99
 
 
 def test_denoise_loop_orchestration_without_blocks():
