@@ -20,6 +20,8 @@ H3DIT_ROPE = 0x2
 H3DIT_POOLED = 0x4
 H3DIT_SWIGLU = 0x8
 H3DIT_TOKEN_REDUCTION = 0x10
+H3DIT_KEEP_INTERMEDIATES = 0x20
+H3DIT_WS_ABSENT = (1 << (8 * ctypes.sizeof(ctypes.c_size_t))) - 1
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported or inconsistent shape",
           3: "pointer not 16-byte aligned", 4: "workspace missing or too small",
@@ -65,6 +67,12 @@ class Reduction(ctypes.Structure):
     _fields_ = [("first", ctypes.c_int), ("last", ctypes.c_int)]
 
 
+class WorkspaceLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("status", "q", "k", "v", "g", "o", "u", "h", "x1", "means", "scores", "idx",
+                 "pooled", "total")]
+
+
 H3DIT_PASS_FRESH, H3DIT_PASS_EXTRAPOLATE, H3DIT_PASS_CORE_REUSE = 0, 1, 2
 
 _lib = None
@@ -81,6 +89,9 @@ _SIGS = [
                                                         ctypes.c_void_p]),
     ("h3dit_routed_attention_static", ctypes.c_int,
      [ctypes.POINTER(Shape)] + [ctypes.c_void_p] * 8 + [ctypes.c_void_p]),
+    ("h3dit_routed_attention_static_status", ctypes.c_int, [ctypes.c_void_p]),
+    ("h3dit_get_workspace_layout", ctypes.c_int,
+     [ctypes.POINTER(Shape), ctypes.POINTER(WorkspaceLayout)]),
     ("h3dit_denoise_step", ctypes.c_int,
      [ctypes.POINTER(Shape), ctypes.POINTER(BlockWeights), ctypes.POINTER(ctypes.c_int),
       ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(Schedule),
@@ -190,6 +201,15 @@ def check_shape(shape: Shape) -> int:
     return int(lib().h3dit_check_shape(ctypes.byref(shape)))
 
 
+def workspace_layout(shape: Shape) -> dict:
+    """{region: byte offset} of the workspace regions (None where not reserved)."""
+    out = WorkspaceLayout()
+    _check("h3dit_get_workspace_layout",
+           lib().h3dit_get_workspace_layout(ctypes.byref(shape), ctypes.byref(out)))
+    return {n: (None if getattr(out, n) == H3DIT_WS_ABSENT else int(getattr(out, n)))
+            for n, _ in WorkspaceLayout._fields_}
+
+
 def block_weights(w: dict) -> BlockWeights:
     return BlockWeights(*[_ptr(w.get(n)) for n, _ in BlockWeights._fields_])
 
@@ -215,6 +235,11 @@ def routed_attention_static(shape: Shape, q, k, v, gate, out, pooled=None, idx=N
     _check("h3dit_routed_attention_static", lib().h3dit_routed_attention_static(
         ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out), _ptr(pooled),
         _ptr(idx), _ptr(scores), _stream(stream)))
+
+
+def routed_attention_static_status(stream=None) -> int:
+    """Status word of the fixed scratch array (synchronises the stream, then clears it)."""
+    return int(lib().h3dit_routed_attention_static_status(_stream(stream)))
 
 
 def denoise_step(shape: Shape, blocks: list, block_ids, z, v_ring, fresh: bool, video,

@@ -110,6 +110,7 @@ struct Dims {
   TileGeom geom;
   bool block;   // hidden / mlp widths given
   bool reduce;  // token-reduction buffers reserved
+  bool keep;    // intermediates kept apart (H3DIT_KEEP_INTERMEDIATES)
 };
 
 #define H3_TRY_SHAPE(expr)                    \
@@ -175,6 +176,7 @@ h3dit_status check_attn(const h3dit_shape* s, Dims* o) {
   o->F = s->mlp_width;
   o->block = false;
   o->reduce = false;
+  o->keep = false;
   return H3DIT_OK;
 }
 
@@ -192,6 +194,7 @@ h3dit_status check_block(const h3dit_shape* s, Dims* o) {
   if ((s->flags & H3DIT_ROPE) && (s->rope_theta <= 1.0f)) return H3DIT_ERR_ARG;
   o->block = true;
   o->reduce = (s->flags & H3DIT_TOKEN_REDUCTION) != 0;
+  o->keep = (s->flags & H3DIT_KEEP_INTERMEDIATES) != 0;
   if (o->reduce && (o->geom.gt == 0 || o->geom.gw < 2)) return H3DIT_ERR_SHAPE;
   return H3DIT_OK;
 }
@@ -207,9 +210,11 @@ h3dit_status reduced_dims(const h3dit_shape* s, h3dit_shape* rs, Dims* rm) {
   return H3DIT_OK;
 }
 
-// Workspace layout (all offsets 256-byte aligned).
+// Workspace layout (all offsets 256-byte aligned; kAbsent = region not reserved).
+constexpr size_t kAbsent = H3DIT_WS_ABSENT;
 struct Ws {
-  size_t status, q, k, v, g, o, u, h, x, rope, means, scores, idx, pooled, bypass, base, total;
+  size_t status, q, k, v, g, o, u, h, x, x1, rope, means, scores, idx, pooled, bypass, base,
+      total;
 };
 
 Ws plan(const Dims& m) {
@@ -222,24 +227,29 @@ Ws plan(const Dims& m) {
   };
   const size_t NA = (size_t)m.N * m.A * 2;
   w.status = take(kAlign);
-  w.q = take(NA);
-  w.k = take(NA);
-  w.v = take(NA);
-  w.g = take(NA);
-  w.o = take(NA);
+  // attention alone needs only the status word and the router's regions
+  w.q = w.k = w.v = w.g = w.o = kAbsent;
+  if (m.block) {
+    w.q = take(NA);
+    w.k = take(NA);
+    w.v = take(NA);
+    w.g = take(NA);
+    w.o = take(NA);
+  }
   w.means = take((size_t)3 * m.H * m.Tv * m.d * 4);
   w.scores = take((size_t)m.H * m.Tv * m.Tv * 4);
   w.idx = take((size_t)m.H * m.Tv * m.ksel * 4);
   w.pooled = take((size_t)m.H * m.Tv * m.d * 4);
+  w.u = w.h = w.x = w.x1 = w.rope = kAbsent;
   if (m.block) {
     const size_t NF = (size_t)m.N * m.F * 2;
-    // u (the MLP inner activations) reuses q..g, which are dead after attention
-    w.u = NF <= 4 * NA ? w.q : take(NF);
+    // u (the MLP inner activations) reuses q..g, which are dead after attention, unless
+    // the intermediates are kept for inspection
+    w.u = (!m.keep && NF <= 4 * NA) ? w.q : take(NF);
     w.h = take((size_t)m.N * m.D * 2);
     w.x = take((size_t)m.N * m.D * 2);
     w.rope = take((size_t)m.N * (m.d / 2) * 8);
-  } else {
-    w.u = w.h = w.x = w.rope = 0;
+    if (m.keep) w.x1 = take((size_t)m.N * m.D * 2);
   }
   w.bypass = w.base = 0;
   if (m.reduce) {  // full-resolution bypass and the pooled rows' baselines
@@ -399,6 +409,10 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
     StageScope sc(H3DIT_STAGE_OUT, st);
     H3_TRY(cu(counted(launch_gemm(kEpiResid, gb, st), 1)));
   }
+  if (w.x1 != kAbsent &&
+      cudaMemcpyAsync(at<__nv_bfloat16>(ws, w.x1), x, (size_t)N * D * 2,
+                      cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return H3DIT_ERR_CUDA;
   // a11: modulated norm 2
   {
     StageScope sc(H3DIT_STAGE_NORM2, st);
@@ -558,6 +572,31 @@ size_t h3dit_workspace_bytes(const h3dit_shape* shape) {
     return 0;
   }
   return plan(m).total;
+}
+
+h3dit_status h3dit_get_workspace_layout(const h3dit_shape* shape, h3dit_workspace_layout* out) {
+  if (!shape || !out) return H3DIT_ERR_ARG;
+  Dims m;
+  if (shape->hidden == 0 && shape->mlp_width == 0)
+    H3_TRY(check_attn(shape, &m));
+  else
+    H3_TRY(check_block(shape, &m));
+  const Ws w = plan(m);
+  out->status = w.status;
+  out->q = w.q;
+  out->k = w.k;
+  out->v = w.v;
+  out->g = w.g;
+  out->o = w.o;
+  out->u = w.u;
+  out->h = w.h;
+  out->x1 = w.x1;
+  out->means = w.means;
+  out->scores = w.scores;
+  out->idx = w.idx;
+  out->pooled = w.pooled;
+  out->total = w.total;
+  return H3DIT_OK;
 }
 
 h3dit_status h3dit_block_forward(const h3dit_shape* shape, const h3dit_block_weights* w,

@@ -41,9 +41,12 @@
 //                MMAs of later steps queue while the PV issuer waits for a softmax.
 //   warps 2..5   softmax, thread = query row (TMEM lane): P = exp2(s * scale * log2e
 //                - m) rounded to bf16 over the step's S columns (two per 32-bit
-//                column), l summing the unrounded weights; O is rescaled in TMEM only
-//                when the row max grows by more than 2^8, and only then does a step
-//                wait for the previous PV
+//                column), l summing the unrounded weights; the running max m is kept
+//                in whole octaves (rounded up to an integer in the log2 domain), so a
+//                weight's bf16 rounding does not depend on which max the row had met
+//                (a power-of-two scale commutes with it); O is rescaled in TMEM, by an
+//                exact power of two, only when the row max grows by more than 2^8, and
+//                only then does a step wait for the previous PV
 //   warp 6       TMA: the V ring
 //   warps 7..10  per unit: O / l, + gate * pooled for video rows, bf16 store; then Q of
 //                the unit two ahead into tensor memory; warp 7 also fetches units and
@@ -200,6 +203,12 @@ __device__ int build_list(const Params& p, const Unit& u, int2* list, uint32_t* 
   put(m_ao, e_ao, 2 * base_r, 2, 0);      // only a: X of routed step k
   put(m_bo, e_bo, 2 * base_r + 1, 2, 0);  // only b: Y of routed step k
   return base_r + n_routed;
+}
+
+// 2^e for a whole number e <= 0 (or -inf), exactly: the rescale factor between two
+// running maxima that are both whole octaves; 0 below the normal range.
+__device__ __forceinline__ float octave(float e) {
+  return e < -126.0f ? 0.0f : __int_as_float((127 + (int)e) << 23);
 }
 
 // max of three fp32 values in one instruction
@@ -497,8 +506,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld64(s_addr, sv);
           mx = fmaxf(masked_max64(sv, cx), my) * sl2;
           need = mx > m_run + kRescaleLog2;
-          const float m_new = need ? mx : m_run;
-          alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+          const float m_new = need ? ceilf(mx) : m_run;
+          alpha = need ? octave(m_run - m_new) : 1.0f;
           const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
           m_run = m_new;
           lsum = exp_pack64(sv, sl2, m_use, pk);
@@ -516,8 +525,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld64(s_addr + half * 64, sv);
           mx = masked_max64(sv, c) * sl2;
           need = mx > m_run + kRescaleLog2;
-          const float m_new = need ? mx : m_run;
-          alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+          const float m_new = need ? ceilf(mx) : m_run;
+          alpha = need ? octave(m_run - m_new) : 1.0f;
           const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
           m_run = m_new;
           lsum = exp_pack64(sv, sl2, m_use, pk);

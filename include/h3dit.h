@@ -60,6 +60,9 @@ typedef enum {
                              /* (else u = gelu(h W1^T + b1)); see w1 below          */
 #define H3DIT_TOKEN_REDUCTION 0x10u /* reserve workspace for token reduction (needs a  */
                                     /* video grid at least 2 wide); see h3dit_sample_step */
+#define H3DIT_KEEP_INTERMEDIATES 0x20u /* block forward keeps its intermediates in the    */
+                                       /* workspace for inspection: see                   */
+                                       /* h3dit_get_workspace_layout                      */
 
 typedef struct {
   int n_text, n_audio, n_video; /* packed row counts, in this order               */
@@ -128,6 +131,35 @@ size_t h3dit_workspace_bytes(const h3dit_shape* shape);
 h3dit_status h3dit_check_shape(const h3dit_shape* shape);
 
 /*
+ * Byte offsets, from the start of the workspace, of the regions a call with this
+ * shape uses (host only; no counterpart on the pages: a debugging aid).  A region
+ * the shape does not reserve reads H3DIT_WS_ABSENT.
+ *   status   int32 device status word (h3dit_sync_status)
+ *   q, k, v  bf16 [H, N, d] after q/k norm and rotary        (block shapes only)
+ *   g        bf16 [N, A] routing gate                          (block shapes only)
+ *   o        bf16 [N, A] attention output after the gate mix (block shapes only)
+ *   u        bf16 [N, F] MLP activations                       (block shapes only)
+ *   h        bf16 [N, D] modulated-norm output (norm 2 after a block)
+ *   x1       bf16 [N, D] residual rows after the attention half
+ *                        (only with H3DIT_KEEP_INTERMEDIATES)
+ *   means    fp32 [3, H, Tv, d] q, k, v tile means;  scores fp32 [H, Tv, Tv]
+ *   idx      int32 [H, Tv, min(k, Tv)];             pooled fp32 [H, Tv, d]
+ *   total    bytes the shape needs (= h3dit_workspace_bytes)
+ * Without H3DIT_KEEP_INTERMEDIATES the MLP activations u reuse the q..g region (dead
+ * once attention has run) and x1 is not kept, so after h3dit_block_forward only o,
+ * h, u and the router regions hold that block's values.  With the flag u has its own
+ * region and x1 is copied out after the out projection, so every region above holds
+ * the block's values when its stream reaches the end of the call; attention-only
+ * shapes (hidden = mlp_width = 0, h3dit_routed_attention) reserve only status and
+ * the router regions.
+ */
+#define H3DIT_WS_ABSENT ((size_t)-1)
+typedef struct {
+  size_t status, q, k, v, g, o, u, h, x1, means, scores, idx, pooled, total;
+} h3dit_workspace_layout;
+h3dit_status h3dit_get_workspace_layout(const h3dit_shape* shape, h3dit_workspace_layout* out);
+
+/*
  * h3dit_block_forward -- one DiT block, in place on the residual rows.
  *
  * TensorFold #949, "What it adds" (block.zig: modulated norm, q/k/v and the
@@ -190,19 +222,23 @@ h3dit_status h3dit_routed_attention(const h3dit_shape* shape, const void* q, con
  * device.  Same arguments and results as h3dit_routed_attention, minus the
  * workspace: scratch comes from a 4 MiB array compiled into the library, which
  * every GPU that loads the library holds until the process exits.
- *   - Returns H3DIT_ERR_WORKSPACE, before any launch, when the shape needs more
- *     than 4 MiB of scratch (the attention-only h3dit_workspace_bytes of the
- *     shape, i.e. with hidden = mlp_width = 0, must be <= 4 MiB; for example
- *     1,024 rows x 4 heads x 64 fits, 4,096 rows x 24 heads x 128 does not).
- *   - The first call on each device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *   - Every argument is checked before the first CUDA call.  Returns
+ *     H3DIT_ERR_WORKSPACE when the shape needs more than 4 MiB of scratch (the
+ *     attention-only h3dit_workspace_bytes of the shape, i.e. with
+ *     hidden = mlp_width = 0, must be <= 4 MiB: the status word and the router's
+ *     tile means, scores, selections and pooled branch; for example 4,096 rows x
+ *     24 heads x 128 with 56 video tiles needs 3.1 MB and fits, 15,435 rows x 40
+ *     heads x 128 with 218 video tiles needs 26 MB and does not).
+ *   - Each call looks up the array's device address with the caller's device
+ *     current; the first call on a device may load the library's device code
+ *     there, so make it before any stream capture.
  *   - Allocates nothing: no cudaMalloc, no cudaFree.
  *   - All calls share the array and it keeps the previous call's contents; the
  *     call clears the part that must start at zero (the device status word) on
  *     its stream.  Calls whose kernels overlap on the GPU (other streams, other
  *     host threads) race on the array: serialise them.
- *   - Device-side wait timeouts are not reported (h3dit_sync_status needs a
- *     workspace); the status word is cleared by the next call.
+ *   - A device-side wait that runs out is recorded in the array's status word;
+ *     h3dit_routed_attention_static_status reads it (the next call clears it).
  */
 h3dit_status h3dit_routed_attention_static(const h3dit_shape* shape, const void* q,
                                            const void* k, const void* v,
@@ -210,6 +246,12 @@ h3dit_status h3dit_routed_attention_static(const h3dit_shape* shape, const void*
                                            float* pooled_out_or_null,
                                            int* topk_idx_out_or_null,
                                            float* tile_scores_out_or_null, void* stream);
+
+/* Synchronises the stream, then returns and clears the device status word of
+ * h3dit_routed_attention_static's scratch array on the current device (H3DIT_OK
+ * when the calls since the last query ran every wait to its end).  No
+ * counterpart on the pages; allocates nothing. */
+h3dit_status h3dit_routed_attention_static_status(void* stream);
 
 /*
  * h3dit_denoise_step -- one Euler step of the denoiser, with velocity reuse.

@@ -57,7 +57,8 @@ PIN TABLE (function: pin tests, without their "test_" prefix)
     attention_row_stochastic_and_zero_query
   pooled_branch: pooled_closed_forms
   gate_mix: gate_mix_brute_force
-  attention_layer: router_tile_permutation_equivariance, block_closed_form_constant_rows
+  attention_layer: router_tile_permutation_equivariance, block_closed_form_constant_rows,
+    attention_layer_given_selections
   qkv_heads: qkv_heads_layout_by_loops
   block_forward: block_closed_form_constant_rows, block_mlp_half_closed_form,
     block_zero_gates_pass_residual, block_all_tiles_equals_dense,
@@ -533,11 +534,14 @@ def gate_mix(O, G, pooled, n_prefix: int, n_video: int, tile: int = 64, sets=Non
 
 
 def attention_layer(Q, K, V, G, n_prefix: int, n_video: int, topk: int, tile: int = 64,
-                    pooled: bool = True, p_bf16: bool = False, sets=None) -> dict:
+                    pooled: bool = True, p_bf16: bool = False, sets=None, idx=None) -> dict:
     """Router + routed/dense attention + pooled branch + gate mix.
 
     Inputs are the bf16 values of Q, K, V [H, N, d] and G [N, H*d] (or None).
-    Returns the intermediates and ``o`` = bf16(mixed output) [N, H*d].
+    Returns the intermediates and ``o`` = bf16(mixed output) [N, H*d].  ``idx``
+    [H, Tv, k], when given, replaces the router's selections in the attention
+    (the comparison rule for near-tied selections recomputes the outputs with
+    the other implementation's tiles); the returned "idx" stays the router's.
     """
     Q = np.asarray(Q, np.float64)
     d = Q.shape[2]
@@ -546,12 +550,13 @@ def attention_layer(Q, K, V, G, n_prefix: int, n_video: int, topk: int, tile: in
     mk = tile_means(K, n_prefix, n_video, tile, sets)
     mv = tile_means(V, n_prefix, n_video, tile, sets)
     S = tile_scores(mq, mk)
-    idx = topk_select(S, topk)
+    idx_r = topk_select(S, topk)
     gap = topk_gap(S, topk)
+    idx = idx_r if idx is None else np.asarray(idx)
     O = routed_attention(Q, K, V, n_prefix, n_video, idx, tile, p_bf16, sets=sets)
     pb = pooled_branch(S, mv, d) if pooled else None
     mixed = gate_mix(O, G, pb, n_prefix, n_video, tile, sets)
-    return {"mq": mq, "mk": mk, "mv": mv, "scores": S, "idx": idx, "gap": gap,
+    return {"mq": mq, "mk": mk, "mv": mv, "scores": S, "idx": idx_r, "gap": gap,
             "O": O, "pooled": pb, "o_f64": mixed, "o": bf16(mixed)}
 
 
@@ -694,7 +699,7 @@ def run_blocks(x, blocks: list, shape, block_ids=None, reduction=None) -> np.nda
     return x
 
 
-def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
+def block_forward(x, wts: dict, shape, p_bf16: bool = False, idx=None) -> dict:
     """One DiT block on the packed rows x (bf16 values, [N, D]).
 
     TensorFold #949 "What it adds" (block.zig: modulated norm, q/k/v and the
@@ -704,6 +709,7 @@ def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
     pages' own shape; gated residuals are x + gate * branch with shift/scale/gate
     rows of the [6, D] table.
     ``wts`` holds float64 values of the bf16 weights and the fp32 table.
+    ``p_bf16`` and ``idx`` as in ``attention_layer``.
     """
     s = shape
     mod = np.asarray(wts["mod"], np.float64)
@@ -718,7 +724,7 @@ def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
                            wts.get("knorm_w") if s.qk_norm else None,
                            s.rms_eps, s.rope_theta, s.rope, _coords(s))
     att = attention_layer(q, k, v, g if s.pooled else None, s.n_prefix, s.n_video,
-                          s.topk, s.tile, s.pooled, p_bf16, shape_tiles(s))
+                          s.topk, s.tile, s.pooled, p_bf16, shape_tiles(s), idx)
     x1 = bf16(x + gate_rows(mod, modp, P, 2, allr) * linear(att["o"], wts["w_o"], wts["b_o"]))
     h2 = modulate_rows(x1, mod, modp, P, 3, 4, s.rms_eps)
     u = mlp_inner(h2, wts, getattr(s, "mlp", "gelu"))
@@ -729,14 +735,14 @@ def block_forward(x, wts: dict, shape, p_bf16: bool = False) -> dict:
     return out
 
 
-def block_forward_rows(x, wts: dict, shape, rows, p_bf16: bool = False) -> dict:
+def block_forward_rows(x, wts: dict, shape, rows, p_bf16: bool = False, idx=None) -> dict:
     """``block_forward`` evaluated for a subset of output rows (for full-size checks).
 
     The same steps in the same order as ``block_forward``; only the work that
     the requested rows depend on is done: the projection of every row (keys,
     values and the video query rows that feed the tile means), the router over
     all tiles, attention for the requested rows' query rows / tiles, and the
-    out projection and MLP for the requested rows.  ``p_bf16`` as in
+    out projection and MLP for the requested rows.  ``p_bf16`` and ``idx`` as in
     ``block_forward``.
     """
     s = shape
@@ -760,7 +766,8 @@ def block_forward_rows(x, wts: dict, shape, rows, p_bf16: bool = False) -> dict:
     mk = tile_means(k, P, Vn, tile, vt)
     mv = tile_means(v, P, Vn, tile, vt)
     S = tile_scores(mq, mk)
-    idx = topk_select(S, s.topk)
+    idx_r = topk_select(S, s.topk)
+    idx = idx_r if idx is None else np.asarray(idx)
     H = s.heads
     O = np.zeros((H, len(rows), d))
     scale = 1.0 / math.sqrt(d)
@@ -783,7 +790,7 @@ def block_forward_rows(x, wts: dict, shape, rows, p_bf16: bool = False) -> dict:
     h2 = modulate_rows(x1, mod, modp, s.n_prefix, 3, 4, s.rms_eps, rows)
     u = mlp_inner(h2, wts, getattr(s, "mlp", "gelu"))
     x2 = bf16(x1 + gate_rows(mod, modp, s.n_prefix, 5, rows) * linear(u, wts["w2"], wts["b2"]))
-    return {"rows": rows, "x1": x1, "x2": x2, "idx": idx, "scores": S, "o": o}
+    return {"rows": rows, "x1": x1, "x2": x2, "idx": idx_r, "scores": S, "o": o}
 
 
 # ---------------------------------------------------------------------------

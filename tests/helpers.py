@@ -1,6 +1,8 @@
 """Shared test helpers: device upload of seeded inputs and the comparison metrics."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 import synthetic as S
@@ -65,3 +67,52 @@ def compare_topk(gpu_idx, ref_idx, ref_scores, k):
                         float(gap[h, i])))
     assert not bad, f"top-k mismatches beyond near-ties: {bad[:5]} (total {len(bad)})"
     return int(diff.sum())
+
+
+def log(msg: str):
+    """Measured figures of a test (oracle timings, errors against the oracle): printed
+    (pytest -s shows them) and appended to the file named by H3DIT_TEST_LOG when set."""
+    print(msg)
+    path = os.environ.get("H3DIT_TEST_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(msg + "\n")
+
+
+def check_close(got, ref, what="", rel=REL_L2_TOL, cos=COS_TOL):
+    """assert_close that also logs the measured relative L2 error and cosine."""
+    r, c = rel_l2(got, ref), cosine(got, ref)
+    log(f"{what}: rel L2 {r:.3e} (bar {rel:g}), cos {c:.7f} (bar {cos})")
+    assert r <= rel and c >= cos, f"{what}: rel L2 {r:.3e} (<= {rel}), cos {c:.6f} (>= {cos})"
+    return r, c
+
+
+def same_fraction(got, ref) -> float:
+    """Fraction of elements with identical values (bf16 results against bf16 mids)."""
+    return float(np.mean(np.asarray(got) == np.asarray(ref)))
+
+
+def workspace_views(h3, cs, shp, ws) -> dict:
+    """Host float64 copies of a block's intermediates from a workspace laid out with
+    H3DIT_KEEP_INTERMEDIATES (library row order): q, k, v [H, N, d]; g, o [N, A];
+    x1, h2 [N, D]; u [N, F]; idx [H, Tv, k] (int32)."""
+    import torch
+    lay = h3.workspace_layout(cs)
+    N, H, d, A, D, F = (shp.n_rows, shp.heads, shp.head_dim, shp.attn_width, shp.hidden,
+                        shp.mlp_width)
+    tv, ks = shp.n_video_tiles, min(shp.topk, shp.n_video_tiles)
+
+    def view(name, shape, dtype, size):
+        off = lay[name]
+        assert off is not None, name
+        n = int(np.prod(shape)) * size
+        return ws[off:off + n].view(dtype).view(*shape)
+
+    out = {n: host_f64(view(n, (H, N, d), torch.bfloat16, 2)) for n in ("q", "k", "v")}
+    out["g"] = host_f64(view("g", (N, A), torch.bfloat16, 2))
+    out["o"] = host_f64(view("o", (N, A), torch.bfloat16, 2))
+    out["x1"] = host_f64(view("x1", (N, D), torch.bfloat16, 2))
+    out["h2"] = host_f64(view("h", (N, D), torch.bfloat16, 2))
+    out["u"] = host_f64(view("u", (N, F), torch.bfloat16, 2))
+    out["idx"] = view("idx", (H, tv, ks), torch.int32, 4).cpu().numpy()
+    return out

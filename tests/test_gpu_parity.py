@@ -10,8 +10,8 @@ import pytest
 
 import oracle
 import synthetic as S
-from helpers import (assert_close, compare_topk, dev_bf16, dev_f32, host_f64, weights_to_device,
-                     weights_to_f64)
+from helpers import (assert_close, check_close, compare_topk, dev_bf16, dev_f32, host_f64, log,
+                     same_fraction, weights_to_device, weights_to_f64, workspace_views)
 
 pytestmark = pytest.mark.gpu
 
@@ -129,11 +129,13 @@ def test_routed_attention_matches_oracle(h3, name, shp, structured):
         ref["o_f64"] = oracle.gate_mix(O, S.bf16_bits_to_f64(inp["gate"]), ref["pooled"],
                                        shp.n_prefix, shp.n_video, shp.tile)
     assert np.allclose(got["pooled"], ref["pooled"], rtol=1e-4, atol=1e-6)
-    assert_close(got["o"], ref["o_f64"], name)
-    # tighter: against the oracle that also rounds P to bf16
+    check_close(got["o"], ref["o_f64"], name)
+    # tighter: against the oracle that also rounds the softmax weights to bf16 (in whole
+    # octaves, as the kernel does), which leaves only fp32 sums and the output rounding
     refp = oracle_attention(shp, inp, p_bf16=True)
     if not n_tie:
-        assert_close(got["o"], refp["o_f64"], name + " (bf16 P)", rel=5e-3, cos=0.99995)
+        check_close(got["o"], refp["o_f64"], name + " (bf16 P)", rel=2e-3, cos=0.999998)
+        log(f"{name} (bf16 P): identical bf16 outputs {same_fraction(got['o'], refp['o']):.5f}")
 
 
 def test_routed_all_tiles_equals_dense_attention(h3):
@@ -187,16 +189,48 @@ def test_attention_deterministic(h3):
 
 
 # ----------------------------------------------------------------------------- block
-def run_block(h3, shp, seed, x_bits=None, wts=None):
+def run_block(h3, shp, seed, x_bits=None, wts=None, keep=False):
     w = wts if wts is not None else S.block_weights(shp, seed)
     xb = x_bits if x_bits is not None else S.hidden_rows(shp, seed)
     cs = h3.make_shape(shp)
+    if keep:
+        cs = h3.make_shape(shp, cs.flags | h3.H3DIT_KEEP_INTERMEDIATES)
     ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device="cuda")
     x = dev_bf16(xb)
     h3.block_forward(cs, weights_to_device(w), x, ws)
     torch.cuda.synchronize()
     assert h3.sync_status(ws) == 0
+    if keep:
+        return x, w, xb, workspace_views(h3, cs, shp, ws)
     return x, w, xb
+
+
+def check_block(h3, shp, seed, name, intermediates=True):
+    """One block with its intermediates kept, against the oracle that rounds the softmax
+    weights to bf16 (TensorFold #949 "Precision"): x2 overall; the block's own updates
+    x1 - x and x2 - x at the required bar (rel L2 2e-2, cos 0.998); q, k, v after the
+    per-head norm and rotary, the gate, the attention output, h2 and the MLP activations
+    u element by element.  Where a near-tied selection differs, the oracle recomputes
+    the attention with the GPU's tiles.  Keeping the intermediates must not change x2."""
+    x, w, xb, it = run_block(h3, shp, seed, keep=True)
+    x0 = S.bf16_bits_to_f64(xb)
+    wo = weights_to_f64(w)
+    ref = oracle.block_forward(x0, wo, shp, p_bf16=True)
+    n_diff = compare_topk(it["idx"], ref["idx"], ref["scores"], min(shp.topk, shp.n_video_tiles))
+    log(f"{name}: query tiles whose selections differ (near-ties): {n_diff}")
+    if n_diff:
+        ref = oracle.block_forward(x0, wo, shp, p_bf16=True, idx=it["idx"])
+    got = host_f64(x)
+    check_close(got, ref["x2"], name + " x2", rel=2e-3, cos=0.99999)
+    check_close(it["x1"] - x0, ref["x1"] - x0, name + " x1 - x", rel=2e-2, cos=0.998)
+    check_close(got - x0, ref["x2"] - x0, name + " x2 - x", rel=2e-2, cos=0.998)
+    if intermediates:
+        for n in ("q", "k", "v", "g", "o", "h2", "u"):
+            check_close(it[n], ref[n], f"{name} {n}", rel=3e-3, cos=0.99999)
+            log(f"{name} {n}: identical bf16 values {same_fraction(it[n], ref[n]):.5f}")
+    plain = run_block(h3, shp, seed, wts=w)[0]
+    assert torch.equal(plain.view(torch.int16), x.view(torch.int16)), "keep mode changed x2"
+    return got, ref, x0
 
 
 BLOCK_CASES = [
@@ -211,24 +245,15 @@ BLOCK_CASES = [
 
 @pytest.mark.parametrize("name,shp", BLOCK_CASES, ids=[c[0] for c in BLOCK_CASES])
 def test_block_forward_small(h3, name, shp):
-    x, w, xb = run_block(h3, shp, 31)
-    ref = oracle.block_forward(S.bf16_bits_to_f64(xb), weights_to_f64(w), shp)
-    got = host_f64(x)
-    assert_close(got, ref["x2"], name, rel=2e-3, cos=0.99999)
-    # the residual update itself (x2 - x) must match as well
-    x0 = S.bf16_bits_to_f64(xb)
-    assert_close(got - x0, ref["x2"] - x0, name + " update", rel=3e-2, cos=0.999)
+    got, _, x0 = check_block(h3, shp, 31, name)
+    # against the exact-weight oracle the required bar still holds
+    ref = oracle.block_forward(x0, weights_to_f64(S.block_weights(shp, 31)), shp)
+    check_close(got - x0, ref["x2"] - x0, name + " x2 - x (exact weights)", rel=3e-2, cos=0.999)
 
 
 def test_block_forward_4096_rows(h3):
     wl = S.BLOCK_4K
-    shp = wl.shape
-    x, w, xb = run_block(h3, shp, wl.seed)
-    ref = oracle.block_forward(S.bf16_bits_to_f64(xb), weights_to_f64(w), shp)
-    got = host_f64(x)
-    x0 = S.bf16_bits_to_f64(xb)
-    assert_close(got, ref["x2"], "block 4096")
-    assert_close(got - x0, ref["x2"] - x0, "block 4096 update", rel=5e-2, cos=0.998)
+    check_block(h3, wl.shape, wl.seed, "block 4096")
 
 
 def test_block_forward_deterministic(h3):
@@ -336,12 +361,7 @@ SWIGLU_CASES = [
 @pytest.mark.parametrize("name,shp", SWIGLU_CASES, ids=[c[0] for c in SWIGLU_CASES])
 def test_block_forward_swiglu_small(h3, name, shp):
     assert shp.attn_width != shp.hidden or shp.head_dim == 64
-    x, w, xb = run_block(h3, shp, 61)
-    ref = oracle.block_forward(S.bf16_bits_to_f64(xb), weights_to_f64(w), shp)
-    got = host_f64(x)
-    x0 = S.bf16_bits_to_f64(xb)
-    assert_close(got, ref["x2"], name, rel=2e-3, cos=0.99999)
-    assert_close(got - x0, ref["x2"] - x0, name + " update", rel=3e-2, cos=0.999)
+    check_block(h3, shp, 61, name)
 
 
 # ----------------------------------------------------------------------------- per-modality
@@ -354,20 +374,13 @@ PREFIX_MOD_CASES = [
 @pytest.mark.parametrize("name,shp", PREFIX_MOD_CASES, ids=[c[0] for c in PREFIX_MOD_CASES])
 def test_block_forward_prefix_table(h3, name, shp):
     """Text and audio rows on their own modulation table (norm shift/scale and gates)."""
-    x, w, xb = run_block(h3, shp, 71)
-    assert "mod_prefix" in w
-    ref = oracle.block_forward(S.bf16_bits_to_f64(xb), weights_to_f64(w), shp)
-    got = host_f64(x)
-    x0 = S.bf16_bits_to_f64(xb)
+    assert "mod_prefix" in S.block_weights(shp, 71)
+    got, ref, x0 = check_block(h3, shp, 71, name)
     P = shp.n_prefix
-    assert_close(got, ref["x2"], name, rel=2e-3, cos=0.99999)
-    # The oracle keeps the softmax weights exact; rounding them to bf16 (the pages'
-    # precision) alone moves these updates by up to 2.2% (oracle with and without
-    # p_bf16 at this shape and seed), and the kernel rounds against its own running
-    # maxima, so its roundings differ from any fixed reference: 4% rel L2.
     for part, sl in (("prefix", slice(0, P)), ("video", slice(P, None))):
-        assert_close(got[sl] - x0[sl], ref["x2"][sl] - x0[sl], f"{name} {part} update",
-                     rel=4e-2, cos=0.999)
+        check_close(got[sl] - x0[sl], ref["x2"][sl] - x0[sl], f"{name} {part} x2 - x",
+                    rel=2e-2, cos=0.998)
+
 
 
 def test_block_prefix_table_zero_gates_leave_prefix_rows(h3):

@@ -92,10 +92,15 @@ def test_entry_points_reject_bad_arguments_without_gpu(h3):
     assert fn(None, *([None] * 9)) == 1
     small = h3.attn_shape(S.ATTN_TINY.shape)
     assert fn(ctypes.byref(small), *([None] * 9)) == 1
-    big = h3.attn_shape(S.BLOCK_4K.shape)  # needs more than the 4 MiB scratch
+    big = h3.attn_shape(S.BLOCK_15K.shape)  # 26 MB of router scratch: beyond the 4 MiB
     dummy = ctypes.c_void_p(16)
     assert fn(ctypes.byref(big), dummy, dummy, dummy, None, dummy, None, None, None, None) == 4
     assert fn(ctypes.byref(bad), dummy, dummy, dummy, None, dummy, None, None, None, None) == 2
+    # 4,096 rows x 24 heads x 128 needs 3.1 MB of router scratch and passes the size check;
+    # a misaligned pointer is then refused, still before any CUDA call
+    mid = h3.attn_shape(S.BLOCK_4K.shape)
+    odd = ctypes.c_void_p(24)
+    assert fn(ctypes.byref(mid), dummy, dummy, odd, None, dummy, None, None, None, None) == 3
 
 
 @pytest.mark.parametrize("L,keep", [(50, 45), (50, 40), (6, 3), (5, 5), (3, 2)])
@@ -232,7 +237,7 @@ def test_binding_struct_layouts_match_the_header(h3, tmp_path):
     from audio_diffusion_transformer_gb300 import _binding as B
     structs = {"h3dit_shape": B.Shape, "h3dit_block_weights": B.BlockWeights,
                "h3dit_schedule": B.Schedule, "h3dit_ends": B.Ends,
-               "h3dit_reduction": B.Reduction}
+               "h3dit_reduction": B.Reduction, "h3dit_workspace_layout": B.WorkspaceLayout}
     lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "h3dit.h"', "int main(void) {"]
     for cname, py in structs.items():
         lines.append(f'  printf("{cname} sizeof %zu\\n", sizeof({cname}));')
@@ -336,3 +341,34 @@ int main(void) {
     assert out[1:4] == ["0", "0", str(shp.n_video_tiles)]
     assert int(out[4]) == first[-1] and int(out[5]) == nrows[-1] == 13899 - 217 * 64
     assert " ".join(out[6:]) == "pointer not 16-byte aligned"
+
+
+def test_workspace_layout_regions(h3):
+    """Attention alone reserves only the status word and the router's regions; a block
+    reserves q..o, and with H3DIT_KEEP_INTERMEDIATES its MLP activations and x1 get
+    regions of their own; regions never overlap."""
+    shp = S.BLOCK_4K.shape
+    att = h3.workspace_layout(h3.attn_shape(shp))
+    assert att["total"] == h3.workspace_bytes(h3.attn_shape(shp))
+    for n in ("q", "k", "v", "g", "o", "u", "h", "x1"):
+        assert att[n] is None, n
+    H, d, Tv, k = shp.heads, shp.head_dim, shp.n_video_tiles, min(shp.topk, shp.n_video_tiles)
+    router = 3 * H * Tv * d * 4 + H * Tv * Tv * 4 + H * Tv * k * 4 + H * Tv * d * 4
+    assert att["total"] <= 256 + router + 4 * 256
+    assert att["total"] < 4 << 20  # fits the fixed scratch of the static entry point
+    blk = h3.workspace_layout(h3.make_shape(shp))
+    assert blk["u"] == blk["q"] and blk["x1"] is None  # u reuses the dead q..g region
+    keep = h3.workspace_layout(h3.make_shape(shp, h3.make_shape(shp).flags
+                                             | h3.H3DIT_KEEP_INTERMEDIATES))
+    assert keep["total"] == h3.workspace_bytes(h3.make_shape(
+        shp, h3.make_shape(shp).flags | h3.H3DIT_KEEP_INTERMEDIATES))
+    N, D, A, F = shp.n_rows, shp.hidden, shp.attn_width, shp.mlp_width
+    sizes = {"status": 4, "q": N * A * 2, "k": N * A * 2, "v": N * A * 2, "g": N * A * 2,
+             "o": N * A * 2, "u": N * F * 2, "h": N * D * 2, "x1": N * D * 2,
+             "means": 3 * H * Tv * d * 4, "scores": H * Tv * Tv * 4, "idx": H * Tv * k * 4,
+             "pooled": H * Tv * d * 4}
+    spans = sorted((keep[n], keep[n] + sz) for n, sz in sizes.items())
+    for (a0, a1), (b0, _) in zip(spans, spans[1:]):
+        assert a1 <= b0
+    assert spans[-1][1] <= keep["total"]
+    assert all(keep[n] % 256 == 0 for n in sizes)

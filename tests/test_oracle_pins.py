@@ -278,6 +278,32 @@ def test_attention_row_stochastic_and_zero_query():
             assert np.allclose(out[h, r0:r0 + nv], V[h, kr].mean(axis=0), atol=1e-13)
 
 
+def test_attention_layer_given_selections():
+    """Selections passed in replace the router's in the attention only: the router's own
+    set reproduces the plain call, and another set gives the attention of that set's key
+    rows (brute force) while the reported selections and scores stay the router's."""
+    H, P, Vn, d, k = 2, 64, 64 * 5, 8, 2
+    N = P + Vn
+    Q, K, V = (rng.standard_normal((H, N, d)) for _ in range(3))
+    G = rng.standard_normal((N, H * d))
+    base = O.attention_layer(Q, K, V, G, P, Vn, k)
+    same = O.attention_layer(Q, K, V, G, P, Vn, k, idx=base["idx"])
+    assert np.array_equal(same["o_f64"], base["o_f64"])
+    other = base["idx"].copy()
+    other[1, 3] = [0, 4] if list(base["idx"][1, 3]) != [0, 4] else [1, 2]
+    alt = O.attention_layer(Q, K, V, G, P, Vn, k, idx=other)
+    assert np.array_equal(alt["idx"], base["idx"]) and np.array_equal(alt["scores"],
+                                                                     base["scores"])
+    rows = range(P + 3 * 64, P + 4 * 64)
+    keys = list(range(P)) + [P + 64 * j + r for j in other[1, 3] for r in range(64)]
+    for r in list(rows)[:4]:
+        want = _brute_attention(Q[1, [r]], K[1, keys], V[1, keys], 1.0 / math.sqrt(d))[0]
+        got = alt["o_f64"][r, d:2 * d] - G[r, d:2 * d] * alt["pooled"][1, 3]
+        assert np.allclose(got, want, atol=1e-12)
+    untouched = [r for r in range(N) if not (P + 3 * 64 <= r < P + 4 * 64)]
+    assert np.array_equal(alt["o_f64"][untouched, d:2 * d], base["o_f64"][untouched, d:2 * d])
+
+
 def test_router_tile_permutation_equivariance():
     H, Vn, d, k = 2, 64 * 6, 16, 3
     Q, K, V = (rng.standard_normal((H, Vn, d)) for _ in range(3))
