@@ -24,9 +24,16 @@ final AdaLN and output heads with the Euler update fused.
 The loop workload (20 Euler steps, 45 of 50 blocks, reuse 2) also prints a
 top-k density sweep {4, 8, 16, 32, all 56 tiles} of one block.
 
---impl reference times the CPU oracle (float64, numpy) on a bounded sample of
-the same workload on this host's cores.  Multi-GPU runs are independent
-replicas (one per rank, no data-path collective).
+--workload routed_attention_1024 (or attn_tiny_1024) times h3dit_routed_attention
+alone on the 1,024-row, 4 x 64 case at top-k 4 and at top-k 16 (every tile: dense
+attention), beside the CPU oracle on the same inputs.
+
+The CPU baseline and --impl reference time the float32 C oracle (oracle/h3time.c,
+plain loops, OpenMP on all host cores): the whole block when it fits the time
+budget, else a uniform 1/s sample of it (every s-th 64-row chunk of rows through the
+row-local stages, every s-th query tile and prefix chunk through attention, the
+router over all tiles), reported as the rows processed per second.  Multi-GPU runs
+are independent replicas (one per rank, no data-path collective).
 """
 from __future__ import annotations
 
@@ -189,9 +196,6 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-_SAMPLE_INPUTS = {}
-
-
 def forward_config(wl, n_blocks, world):
     """The ``config`` object of a forward or sampler-step line (both arms print it)."""
     shape = wl.shape
@@ -228,92 +232,94 @@ def forward_config(wl, n_blocks, world):
                   f"{block_weight_bytes(shape) / 1e6:.0f} MB of weights)"}
 
 
-def oracle_block_sample(shape, rng_seed=0):
-    """Times the oracle on a bounded sample of one block of ``shape`` and scales it
-    to the whole block.  Returns (seconds per block, description)."""
+def _bf16_values(a):
+    """float32 array rounded to the nearest bf16 value (ties to even), as float32."""
+    import numpy as np
+    u = np.ascontiguousarray(a, np.float32).view(np.uint32)
+    u = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000)
+    return u.view(np.float32)
+
+
+def slice_shape(shape):
+    """The float32 baseline tiles video rows as 64-row slices: a cube layout is timed
+    at the same sizes with slice tiles (the same work up to the clipped cubes' fill)."""
+    if getattr(shape, "video_grid", None):
+        return shape.with_(video_grid=None, token_reduction=False)
+    return shape
+
+
+def cpu_block(shape, seed=0):
+    """The float32 C block with seeded inputs of the workload's distributions: weights
+    and biases bf16 N(0, 0.02) (input-major), modulation N(0, 0.1^2), q/k norm weights
+    1 + N(0, 0.02), x bf16 N(0, 1)."""
     import numpy as np
 
-    import oracle as O
-    s = shape
-    N, D, A, F, H, d = s.n_rows, s.hidden, s.attn_width, s.mlp_width, s.heads, s.head_dim
-    R = min(N, 2048)   # rows through the row-local stages
-    HS = min(H, 12)    # heads through the router and attention
-    key = (N, D, A, F, H, d, s.mlp, rng_seed)
-    if key not in _SAMPLE_INPUTS:  # drawn once per process; only the oracle's work is timed
-        rng = np.random.default_rng(rng_seed)
-        _SAMPLE_INPUTS[key] = (
-            {"w_qkvg": O.bf16(rng.standard_normal((4 * A, D)) * 0.02),
-             "b_qkvg": O.bf16(rng.standard_normal(4 * A) * 0.02),
-             "w_o": O.bf16(rng.standard_normal((D, A)) * 0.02), "b_o": np.zeros(D),
-             "w1": O.bf16(rng.standard_normal((2 * F if s.mlp == "swiglu" else F, D)) * 0.02),
-             "b1": np.zeros(2 * F if s.mlp == "swiglu" else F),
-             "w2": O.bf16(rng.standard_normal((D, F)) * 0.02), "b2": np.zeros(D),
-             "mod": rng.standard_normal((6, D)) * 0.1},
-            O.bf16(rng.standard_normal((R, D))),
-            [O.bf16(rng.standard_normal((HS, N, d))) for _ in range(3)])
-    w, x, (Q, K, V) = _SAMPLE_INPUTS[key]
-    # row-local stages on R rows
+    from oracle import ctime
+    s = slice_shape(shape)
+    rng = np.random.default_rng(seed)
+    D, A, F, d = s.hidden, s.attn_width, s.mlp_width, s.head_dim
+    F1 = fc1_width(s)
+
+    def rn(*sz, std=0.02, mean=0.0, round_bf16=True):
+        a = rng.standard_normal(sz, dtype=np.float32) * np.float32(std) + np.float32(mean)
+        return _bf16_values(a) if round_bf16 else a
+
+    w = {"w_qkvg": rn(D, 4 * A), "b_qkvg": rn(4 * A), "w_o": rn(A, D), "b_o": rn(D),
+         "w1": rn(D, F1), "b1": rn(F1), "w2": rn(F, D), "b2": rn(D),
+         "mod": rn(6, D, std=0.1, round_bf16=False), "qnorm_w": rn(d, mean=1.0),
+         "knorm_w": rn(d, mean=1.0)}
+    if getattr(s, "prefix_mod", False):
+        w["mod_prefix"] = rn(6, D, std=0.1, round_bf16=False)
+    blk = ctime.Block(s, w)
+    blk.scratch.fill(0.0)  # touch every page before anything is timed
+    x = rn(s.n_rows, D, std=1.0)
+    return blk, x, s
+
+
+def sampled_rows(n_rows, sample):
+    """Rows that a 1/sample call runs through the row-local stages (every sample-th
+    64-row chunk)."""
+    return sum(min(64, n_rows - c * 64) for c in range(0, -(-n_rows // 64), sample))
+
+
+def time_cpu_block(blk, x, sample):
     t0 = time.perf_counter()
-    h = O.rms_modulate(x, w["mod"][0], w["mod"][1])
-    qkvg = O.bf16(O.linear(h, w["w_qkvg"], w["b_qkvg"]))
-    O.qkv_heads(qkvg, H, d, np.ones(d), np.ones(d))
-    o = O.bf16(qkvg[:, :A])
-    x1 = O.bf16(x + w["mod"][2] * O.linear(o, w["w_o"], w["b_o"]))
-    h2 = O.rms_modulate(x1, w["mod"][3], w["mod"][4])
-    u = O.mlp_inner(h2, w, s.mlp)
-    O.bf16(x1 + w["mod"][5] * O.linear(u, w["w2"], w["b2"]))
-    t_rows = (time.perf_counter() - t0) * N / R
-    # router over all tiles, attention for a sample of query tiles of a few heads
-    hs = HS
-    t0 = time.perf_counter()
-    mq = O.tile_means(Q, s.n_prefix, s.n_video)
-    mk = O.tile_means(K, s.n_prefix, s.n_video)
-    mv = O.tile_means(V, s.n_prefix, s.n_video)
-    Sc = O.tile_scores(mq, mk)
-    idx = O.topk_select(Sc, s.topk)
-    O.pooled_branch(Sc, mv, d)
-    t_router = (time.perf_counter() - t0) * H / hs
-    tv = s.n_video_tiles
-    vt = [(h, i) for h in range(hs) for i in range(0, tv, max(1, tv // 12))][:12 * hs]
-    t0 = time.perf_counter()
-    O.routed_attention(Q, K, V, s.n_prefix, s.n_video, idx, tiles=vt)
-    t_vid = (time.perf_counter() - t0) * (H * tv) / len(vt)
-    t_pre = 0.0
-    n_chunks = 0
-    if s.n_prefix:
-        t0 = time.perf_counter()
-        n_chunks = min(2, (s.n_prefix + 63) // 64)
-        pre_rows = min(s.n_prefix, 64 * n_chunks)  # prefix query rows attended per head
-        for h in range(hs):
-            for c in range(n_chunks):
-                O.attend(Q[h, 64 * c:min(64 * c + 64, s.n_prefix)], K[h], V[h],
-                         1.0 / math.sqrt(d))
-        t_pre = (time.perf_counter() - t0) * (H * s.n_prefix) / (hs * pre_rows)
-    total = t_rows + t_router + t_vid + t_pre
-    pre = (f" and {hs * n_chunks} prefix chunks of up to 64 rows "
-           f"(x{H * s.n_prefix / (hs * pre_rows):.3g})" if n_chunks else "")
-    desc = (f"one block of the {N}-row shape, float64 oracle: row-local stages on {R} rows "
-            f"(x{N / R:.3g}), router on {hs} of {H} heads (x{H / hs:.3g}), attention on "
-            f"{len(vt)} video query tiles (x{H * tv / len(vt):.3g}){pre}; scaled to the whole "
-            f"block")
-    return total, desc
+    blk.run(x, sample=sample)
+    return time.perf_counter() - t0
 
 
-def blas_threads():
-    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
-        if os.environ.get(v, "").isdigit():
-            return int(os.environ[v])
-    return os.cpu_count() or 1
+def cpu_sample_plan(blk, x, n_rows, budget_s):
+    """Times a 1/16 calibration call and picks the smallest sample divisor s whose call
+    should take about budget_s (1 = the whole block)."""
+    t16 = time_cpu_block(blk, x, 16)
+    est_full = t16 * n_rows / max(sampled_rows(n_rows, 16), 1)
+    return max(1, math.ceil(est_full / budget_s)), est_full
 
 
-def cpu_baseline(shape, samples=1):
-    best = None
-    desc = ""
-    for _ in range(samples):
-        t, desc = oracle_block_sample(shape)
-        best = t if best is None else min(best, t)
-    return {"value": shape.n_rows / best, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": desc, "s_per_block": best}
+def sample_desc(s, sample, n_rows):
+    what = ("the whole block" if sample == 1 else
+            f"a 1/{sample} sample of the block: rows of every {sample}th 64-row chunk "
+            f"({sampled_rows(n_rows, sample)} of {n_rows}) through the norms, projections "
+            f"and MLP, every {sample}th video query tile and prefix chunk through attention, "
+            f"the router over all tiles")
+    return (f"float32 C oracle (plain loops, OpenMP) on {s.n_rows} rows, hidden {s.hidden}, "
+            f"{s.heads} x {s.head_dim}, top-k {s.topk}: {what}; value = rows processed / s")
+
+
+def cpu_baseline(shape, budget_s=30.0):
+    """Measured CPU baseline: the float32 C oracle on the whole block when that fits the
+    budget, else on the smallest uniform sample that does."""
+    from oracle import ctime
+    blk, x, s = cpu_block(shape)
+    sample, est = cpu_sample_plan(blk, x, s.n_rows, budget_s)
+    if sample > 1 and est <= 1.5 * budget_s:
+        sample = 1
+    t = time_cpu_block(blk, x, sample)
+    rows = sampled_rows(s.n_rows, sample)
+    measured = "measured full block" if sample == 1 else f"measured 1/{sample} sample"
+    return {"value": rows / t, "unit": UNIT, "cores": ctime.threads(),
+            "kind": f"oracle fp32, {measured}", "sample": sample_desc(s, sample, s.n_rows),
+            "s_per_block": t * s.n_rows / rows, "seconds_timed": t}
 
 
 # ----------------------------------------------------------------------------- ranks
@@ -374,9 +380,20 @@ def make_ends(torch, shape, cv, ca, seed, dev):
     return e
 
 
-def dominant_kernel(shape, shapes, stages, K, workload_name):
+FLOP_PER_CLK_SM = 8192  # dense bf16 tcgen05: one M=128 N=256 K=16 MMA per 128 cycles per SM
+
+
+def per_clock_peak(n_sms, sm_mhz):
+    """Dense bf16 tensor peak at the sampled SM clock, TFLOP/s (None without a clock)."""
+    if not n_sms or not sm_mhz:
+        return None
+    return FLOP_PER_CLK_SM * n_sms * sm_mhz * 1e6 / 1e12
+
+
+def dominant_kernel(shape, shapes, stages, K, workload_name, clk_peak=None):
     """Roofline of the kernel with the largest stage time, from the live stage records
-    (ms, launches); achieved = its algorithmic flops / its time.  Also per-kernel rates."""
+    (ms, launches); achieved = its algorithmic flops / its time.  Also per-kernel rates.
+    ``clk_peak``: the tensor peak at the sampled SM clock (frac_per_clock)."""
     pk, pk_kind = peaks()
     peak_tc = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     # per-launch flops of each stage, averaged over the block positions
@@ -396,12 +413,81 @@ def dominant_kernel(shape, shapes, stages, K, workload_name):
                 "traffic": recorded_traffic(kernel, dom, workload_name),
                 "launch_ms": g_ms[dom] / max(n_launch, 1), "launches": n_launch}
     roofline["frac"] = roofline["achieved"] / peak_tc
+    if clk_peak:
+        roofline["peak_per_clock"] = clk_peak
+        roofline["frac_per_clock"] = roofline["achieved"] / clk_peak
     kernels = {}
     for g, st in groups.items():
         fl = sum(sf[s_] * stages[s_][1] for s_ in st)
-        kernels[g] = {"ms_per_step": g_ms[g] / K,
-                      "tflops": fl / (g_ms[g] / 1e3) / 1e12 if g_ms[g] > 0 else None}
+        tf = fl / (g_ms[g] / 1e3) / 1e12 if g_ms[g] > 0 else None
+        kernels[g] = {"ms_per_step": g_ms[g] / K, "tflops": tf,
+                      "frac": tf / peak_tc if tf else None}
+        if clk_peak and tf:
+            kernels[g]["frac_per_clock"] = tf / clk_peak
     return roofline, kernels
+
+
+def near_tie_audit(scores, idx, k, rel_gap=1e-5):
+    """Near-ties of the router's top-k on the GPU's own fp32 tile scores [H, Tv, Tv]:
+    (head, query tile) pairs whose k-th and (k+1)-th largest scores differ by less than
+    rel_gap of the k-th (the pairs where two correct implementations may select
+    differently).  Also checks that every selection [H, Tv, k] is a top-k of its scores
+    under the (score desc, tile asc) order with NaN as -inf."""
+    import numpy as np
+    sc = np.where(np.isnan(scores), -np.inf, scores.astype(np.float64))
+    H, T, n_keys = sc.shape
+    order = np.argsort(-sc, axis=-1, kind="stable")  # ties: lower tile first
+    srt = np.take_along_axis(sc, order, axis=-1)
+    if k < n_keys:
+        kth, nxt = srt[..., k - 1], srt[..., k]
+        with np.errstate(invalid="ignore"):
+            gap = (kth - nxt) / np.maximum(np.abs(kth), 1e-30)
+        near = int(np.sum(gap < rel_gap))
+    else:
+        near = 0
+    want = np.sort(order[..., :k], axis=-1)
+    consistent = bool(np.array_equal(want, np.sort(idx, axis=-1)))
+    return {"pairs": int(H * T), "near_ties": near, "rel_gap": rel_gap,
+            "selections_are_topk_of_scores": consistent}
+
+
+def block_near_ties(h3, torch, shape, weights, x_rows, dev):
+    """Near-tie audit of one block at the bench's input: the block runs once with its
+    intermediates kept, and its own tile scores and selections are read back."""
+    cs = h3.make_shape(shape)
+    cs = h3.make_shape(shape, cs.flags | h3.H3DIT_KEEP_INTERMEDIATES)
+    ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device=dev)
+    x = x_rows.clone()
+    h3.block_forward(cs, weights, x, ws)
+    torch.cuda.synchronize()
+    lay = h3.workspace_layout(cs)
+    H, tv = shape.heads, shape.n_video_tiles
+    k = min(shape.topk, tv)
+    sc = ws[lay["scores"]:lay["scores"] + H * tv * tv * 4].view(torch.float32)
+    ix = ws[lay["idx"]:lay["idx"] + H * tv * k * 4].view(torch.int32)
+    out = near_tie_audit(sc.view(H, tv, tv).cpu().numpy(), ix.view(H, tv, k).cpu().numpy(), k)
+    out["where"] = "block 0 at the bench input (the GPU's fp32 tile scores)"
+    del ws
+    return out
+
+
+def timed_steps(torch, stream, step, K):
+    """K steps with a CUDA event between consecutive steps on the launching stream:
+    (total ms, per-step ms list)."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    ev[0].record(stream)
+    for i in range(K):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(K)]
+    return ev[0].elapsed_time(ev[K]), per
+
+
+def median(xs):
+    xs = sorted(xs)
+    n = len(xs)
+    return xs[n // 2] if n % 2 else 0.5 * (xs[n // 2 - 1] + xs[n // 2])
 
 
 def run_ours(args, rank, world, local_rank):
@@ -437,18 +523,21 @@ def run_ours(args, rank, world, local_rank):
 
         red = wl.extra.get("reduction")
 
-        def step():
+        def step_on(st):
             h3.sample_step(cs, ends, blocks, ids, zv, za, rv, ra, None, h3.H3DIT_PASS_FRESH,
                            (1.0, 0.0, 0.0, dt), (1.0, 0.0, 0.0, dt), 0, ws,
-                           stream=stream.cuda_stream, reduction=red)
+                           stream=st, reduction=red)
     else:
         z0 = torch.randn(N, D, generator=gz, device=dev, dtype=torch.float32)
         z = z0.clone()
         ring = torch.zeros(2, N, D, dtype=torch.float32, device=dev)
 
-        def step():
+        def step_on(st):
             h3.denoise_step(cs, blocks, ids, z, ring, True, (1.0, 0.0, 0.0, dt), 0, ws,
-                            stream=stream.cuda_stream)
+                            stream=st)
+
+    def step():
+        step_on(stream.cuda_stream)
 
     def barrier():
         if world > 1:
@@ -462,27 +551,18 @@ def run_ours(args, rank, world, local_rank):
         raise SystemExit("device status error after warm-up")
     barrier()
     torch.cuda.synchronize()
-    bus = None
-    try:
-        bus = torch.cuda.get_device_properties(dev).pci_bus_id
-    except AttributeError:
-        pass
+    props = torch.cuda.get_device_properties(dev)
+    bus = getattr(props, "pci_bus_id", None)
     sampler = ClockSampler(bus)
     sampler.start()
     time.sleep(0.3)
     h3.profile_begin(16 * n_blocks * args.steps + 64)
     l0 = h3.launch_count()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms, per_step = timed_steps(torch, stream, step, args.steps)
     stages = h3.profile_end()
     launches = h3.launch_count() - l0
     clocks = sampler.stop()
     barrier()
-    ms = e0.elapsed_time(e1)
     if h3.sync_status(ws) != 0:
         raise SystemExit("device status error in the timed region")
     ms_max = max_over_ranks(ms, world, dev)
@@ -503,6 +583,40 @@ def run_ours(args, rank, world, local_rank):
         e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world, dev)
         assert torch.isfinite(z_back).all().item()
 
+    # the same step captured once into a CUDA graph and replayed
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step_on(side.cuda_stream)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        c0 = h3.launch_count()
+        with torch.cuda.graph(g):
+            step_on(torch.cuda.current_stream().cuda_stream)
+        g_launches = h3.launch_count() - c0
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        barrier()
+        g_ms, g_per = timed_steps(torch, stream, g.replay, args.steps)
+        if h3.sync_status(ws) != 0:
+            raise SystemExit("device status error in the graph replays")
+        g_ms = max_over_ranks(g_ms, world, dev)
+        graph = {"value": job_rows_per_s(N * n_blocks * args.steps, world, g_ms),
+                 "ms_per_step": g_ms / args.steps, "ms_per_step_median": median(g_per),
+                 "launches_per_step": int(g_launches),
+                 "how": "one step captured into a CUDA graph, replayed per step"}
+        del g
+
+    ties = None
+    if not args.no_ties and rank == 0:
+        xr = z0.view(-1)[:N * D].view(N, D).to(torch.bfloat16) if not wl.extra.get("ends") \
+            else torch.randn(N, D, generator=gz, device=dev).to(torch.bfloat16)
+        ties = block_near_ties(h3, torch, shape, blocks[0], xr, dev)
+
     if rank != 0:
         return None
     K = args.steps
@@ -514,14 +628,17 @@ def run_ours(args, rank, world, local_rank):
     pk, pk_kind = peaks()
     peak_tc = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     achieved_total = step_flops * K / (ms_max / 1e3) / 1e12
-    roofline, kernels = dominant_kernel(shape, shapes, stages, K, wl.name)
+    clk_peak = per_clock_peak(props.multi_processor_count, (clocks or {}).get("sm_mhz"))
+    roofline, kernels = dominant_kernel(shape, shapes, stages, K, wl.name, clk_peak)
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms_max / K, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": ms_max / K,
+        "ms_per_step_median": median(per_step), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": forward_config(wl, n_blocks, world),
         "s_per_forward": ms_max / K / 1e3 * (50 / n_blocks),
         "tc_frac_of_peak": achieved_total / peak_tc,
+        "tc_frac_of_peak_per_clock": achieved_total / clk_peak if clk_peak else None,
         "achieved_tflops": achieved_total,
         "roofline": roofline,
         "stages_ms_per_step": {k: v[0] / K for k, v in stages.items()},
@@ -529,6 +646,10 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": int(launches),
         "clocks": clocks,
     }
+    if graph is not None:
+        out["graph"] = graph
+    if ties is not None:
+        out["near_ties"] = ties
     if e2e_ms is not None:
         out["e2e"] = {"value": rows_blocks / (e2e_ms / 1e3), "unit": UNIT,
                       "h2d_bytes_per_step": z.numel() * 4, "d2h_bytes_per_step": z.numel() * 4}
@@ -698,28 +819,228 @@ def run_loop(args, rank, world, local_rank):
     })
 
 
-def run_reference(args, rank, world):
+WORKLOAD_ALIASES = {"routed_attention_1024": "attn_tiny_1024"}
+
+
+def attention_flops(s):
+    """Algorithmic attention flops of one routed-attention call (4 d per query-key pair)."""
+    return block_flops(s)[1]
+
+
+def run_attention_only(args, rank, world, local_rank):
+    """h3dit_routed_attention alone on the 1,024-row case (4 heads x 64, 16 tiles of 64,
+    N(0,1) Q/K/V and gate from seed): top-k 4 with the pooled branch (the line's value)
+    and top-k 16 (every tile: dense attention).  Each timed call is bracketed by events
+    on its stream and preceded by an L2 flush (a 256 MB write) outside the brackets."""
+    import numpy as np
+    import torch
+
+    import audio_diffusion_transformer_gb300 as h3
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = S.ATTN_TINY
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    inp = S.attention_inputs(wl.shape, wl.seed + 1000 * rank)
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+
+    q, k, v, g = (to_dev(inp[n]) for n in ("q", "k", "v", "gate"))
+    props = torch.cuda.get_device_properties(dev)
+    sampler = ClockSampler(getattr(props, "pci_bus_id", None))
+    lines = {}
+    for topk in (wl.shape.topk, 16):
+        shp = wl.shape.with_(topk=topk)
+        cs = h3.attn_shape(shp)
+        ws = torch.zeros(h3.workspace_bytes(cs), dtype=torch.uint8, device=dev)
+        tv = shp.n_video_tiles
+        kk = min(topk, tv)
+        out = torch.empty(shp.n_rows, shp.attn_width, dtype=torch.bfloat16, device=dev)
+        idx = torch.empty(shp.heads, tv, kk, dtype=torch.int32, device=dev)
+        sc = torch.empty(shp.heads, tv, tv, dtype=torch.float32, device=dev)
+
+        def call():
+            h3.routed_attention(cs, q, k, v, g, out, ws, idx=idx, scores=sc,
+                                stream=stream.cuda_stream)
+
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize()
+        if topk == wl.shape.topk:
+            sampler.start()
+            time.sleep(0.2)
+        h3.profile_begin(4 * args.steps + 8)
+        l0 = h3.launch_count()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize()
+        stages = h3.profile_end()
+        launches = h3.launch_count() - l0
+        if h3.sync_status(ws) != 0:
+            raise SystemExit("device status error in the timed region")
+        per = [a.elapsed_time(b) for a, b in evs]
+        att_ms = stages["attention"][0] / max(stages["attention"][1], 1)
+        fl = attention_flops(shp)
+        lines[topk] = {"ms_per_call": sum(per) / len(per), "ms_per_call_median": median(per),
+                       "rows_per_s": shp.n_rows / (sum(per) / len(per) / 1e3),
+                       "attention_kernel_ms": att_ms,
+                       "router_ms": stages["router"][0] / max(stages["router"][1], 1),
+                       "attention_gflop": fl / 1e9,
+                       "attention_tflops": fl / (att_ms / 1e3) / 1e12 if att_ms else None,
+                       "gpu_launches": int(launches),
+                       "near_ties": near_tie_audit(sc.cpu().numpy(), idx.cpu().numpy(), kk)}
+        if topk == wl.shape.topk:
+            clocks = sampler.stop()
+            # end to end: H2D of q, k, v, gate from pinned memory, the call, D2H of out
+            hq, hk, hv, hg = (t.cpu().pin_memory() for t in (q, k, v, g))
+            ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+            dq, dk, dv, dg = (torch.empty_like(t) for t in (q, k, v, g))
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(args.steps):
+                for d_, h_ in ((dq, hq), (dk, hk), (dv, hv), (dg, hg)):
+                    d_.copy_(h_, non_blocking=True)
+                h3.routed_attention(cs, dq, dk, dv, dg, out, ws, stream=stream.cuda_stream)
+                ho.copy_(out, non_blocking=True)
+            torch.cuda.synchronize()
+            e2e_s = (time.perf_counter() - t0) / args.steps
+            lines[topk]["e2e"] = {"value": shp.n_rows / e2e_s, "unit": UNIT,
+                                  "h2d_bytes_per_step": sum(t.numel() * 2 for t in (q, k, v, g)),
+                                  "d2h_bytes_per_step": out.numel() * 2}
     if rank != 0:
         return None
-    wl, n_blocks = workload(args.workload)
-    shape = wl.shape
+    main = lines[wl.shape.topk]
+    pk, pk_kind = peaks()
+    peak_tc = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    value = main["rows_per_s"] * world
+    bytes_moved = (3 * wl.shape.heads * wl.shape.n_rows * wl.shape.head_dim * 2
+                   + 2 * wl.shape.n_rows * wl.shape.attn_width * 2)
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": main["ms_per_call"],
+           "ms_per_step_median": main["ms_per_call_median"], "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": wl.name, "n_rows": wl.shape.n_rows, "heads": wl.shape.heads,
+                      "head_dim": wl.shape.head_dim, "tiles": wl.shape.n_video_tiles,
+                      "topk": wl.shape.topk, "pooled": True, "parallelism": f"replicas x{world}",
+                      "l2": "L2 flushed (256 MB write) before every timed call",
+                      "step": "one h3dit_routed_attention call (router + attention)"},
+           "roofline": {"bound": "tensor", "kernel": "attention",
+                        "achieved": main["attention_tflops"], "peak": peak_tc,
+                        "peak_kind": f"bf16 sustained, {pk_kind}", "unit": "TFLOP/s",
+                        "frac": (main["attention_tflops"] or 0) / peak_tc, "traffic": None,
+                        "note": "latency-bound: 32 work units for 152 SMs; "
+                                f"{bytes_moved / 1e6:.1f} MB of q, k, v, gate and output"},
+           "topk_4": main, "dense_topk_16": lines[16],
+           "near_ties": main["near_ties"], "gpu_launches": main["gpu_launches"],
+           "clocks": clocks, "e2e": main["e2e"]}
+    if not args.no_cpu_baseline and world == 1:
+        from oracle import ctime
+        qf, kf, vf, gf = (S.bf16_bits_to_f64(inp[n]).astype(np.float32)
+                          for n in ("q", "k", "v", "gate"))
+        att = ctime.Attention(wl.shape, qf, kf, vf, gf)
+        att.run()
+        reps = 0
+        t0 = time.perf_counter()
+        while reps < 3 or time.perf_counter() - t0 < 2.0:
+            att.run()
+            reps += 1
+        t = (time.perf_counter() - t0) / reps
+        out["cpu_baseline"] = {"value": wl.shape.n_rows / t, "unit": UNIT,
+                               "cores": ctime.threads(), "kind": "oracle fp32, measured full call",
+                               "sample": f"the float32 C oracle's router + attention + pooled "
+                                         f"mix on the same inputs, {reps} calls averaged"}
+    return out
+
+
+def run_reference_attention(args, world):
+    """CPU oracle arm of the 1,024-row attention line: the float32 C oracle's router,
+    attention and pooled mix on the same inputs, every step timed."""
+    import numpy as np
+
+    from oracle import ctime
+    wl = S.ATTN_TINY
+    inp = S.attention_inputs(wl.shape, wl.seed)
+    qf, kf, vf, gf = (S.bf16_bits_to_f64(inp[n]).astype(np.float32)
+                      for n in ("q", "k", "v", "gate"))
+    att = ctime.Attention(wl.shape, qf, kf, vf, gf)
     for _ in range(args.warmup):
-        oracle_block_sample(shape)
-    tot = 0.0
-    desc = ""
+        att.run()
+    times = []
     for _ in range(args.steps):
-        t, desc = oracle_block_sample(shape)
-        tot += t
-    value = shape.n_rows * args.steps / tot
-    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": tot / args.steps * 1e3 * n_blocks, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": forward_config(wl, n_blocks, world),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(),
-                             "kind": "oracle", "sample": desc},
+        t0 = time.perf_counter()
+        att.run()
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = wl.shape.n_rows * args.steps / tot
+    desc = "float32 C oracle: router, attention and pooled mix of the 1,024-row call"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot / args.steps * 1e3,
+            "ms_per_step_median": median(times) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "n_rows": wl.shape.n_rows, "heads": wl.shape.heads,
+                       "head_dim": wl.shape.head_dim, "tiles": wl.shape.n_video_tiles,
+                       "topk": wl.shape.topk, "pooled": True,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "L2 flushed (256 MB write) before every timed call",
+                       "step": "one h3dit_routed_attention call (router + attention)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": ctime.threads(),
+                             "kind": "oracle fp32, measured full call", "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle arm: each step runs the float32 C oracle on the same workload shape,
+    on all host cores -- the whole block when a step fits about four seconds, else a
+    uniform 1/s sample chosen from a calibration call -- and every step is timed."""
+    if rank != 0:
+        return None
+    from oracle import ctime
+    if S.workload_by_name(args.workload) is S.ATTN_TINY:
+        return run_reference_attention(args, world)
+    wl, n_blocks = workload(args.workload)
+    blk, x, s = cpu_block(wl.shape)
+    sample, est_full = cpu_sample_plan(blk, x, s.n_rows, 4.0)
+    rows = sampled_rows(s.n_rows, sample)
+    for _ in range(args.warmup):
+        time_cpu_block(blk, x, sample)
+    times = [time_cpu_block(blk, x, sample) for _ in range(args.steps)]
+    tot = sum(times)
+    value = rows * args.steps / tot
+    s_block = tot / args.steps * s.n_rows / rows
+    desc = sample_desc(s, sample, s.n_rows)
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": tot / args.steps * 1e3,
+           "ms_per_step_median": sorted(times)[len(times) // 2] * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic", "config": forward_config(wl, n_blocks, world),
+           "step": desc,
+           "s_per_block": s_block,
+           "s_per_forward": s_block * 50,
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": ctime.threads(),
+                            "kind": "oracle fp32, measured " + ("full block" if sample == 1
+                                                                else f"1/{sample} sample"),
+                            "sample": desc},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    if sample > 1:
+        out["extrapolated_from"] = (f"1/{sample} sample per step: s_per_block and "
+                                    f"s_per_forward scale the measured step time by "
+                                    f"{s.n_rows}/{rows} rows (and x50 blocks)")
+    else:
+        out["extrapolated_from"] = "s_per_forward = 50 x the measured block"
+    if s is not wl.shape:
+        out["slice_tiles"] = "cube layout timed with 64-row slice tiles of the same sizes"
+    return out
 
 
 def main():
@@ -731,11 +1052,15 @@ def main():
     ap.add_argument("--workload", default="forward50_15435_d5120")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay arm of a forward line")
+    ap.add_argument("--no-ties", action="store_true", help="skip the near-tie audit")
     ap.add_argument("--graph", action="store_true",
                     help="loop workload: capture the loop into a CUDA graph and replay it")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    args.workload = WORKLOAD_ALIASES.get(args.workload, args.workload)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -748,6 +1073,8 @@ def main():
             torch.distributed.init_process_group("nccl")
         if S.workload_by_name(args.workload) is S.LOOP_4K:
             out = run_loop(args, rank, world, local_rank)
+        elif S.workload_by_name(args.workload) is S.ATTN_TINY:
+            out = run_attention_only(args, rank, world, local_rank)
         else:
             out = run_ours(args, rank, world, local_rank)
         if world > 1:

@@ -92,27 +92,41 @@ def same_fraction(got, ref) -> float:
     return float(np.mean(np.asarray(got) == np.asarray(ref)))
 
 
-def workspace_views(h3, cs, shp, ws) -> dict:
-    """Host float64 copies of a block's intermediates from a workspace laid out with
+def workspace_views(h3, cs, shp, ws, names=None) -> dict:
+    """Host copies of a block's intermediates from a workspace laid out with
     H3DIT_KEEP_INTERMEDIATES (library row order): q, k, v [H, N, d]; g, o [N, A];
-    x1, h2 [N, D]; u [N, F]; idx [H, Tv, k] (int32)."""
+    x1, h2 [N, D]; u [N, F] (float64 values of the bf16 data); idx [H, Tv, k] int32.
+    ``names`` restricts the copy (full-size shapes)."""
     import torch
     lay = h3.workspace_layout(cs)
     N, H, d, A, D, F = (shp.n_rows, shp.heads, shp.head_dim, shp.attn_width, shp.hidden,
                         shp.mlp_width)
     tv, ks = shp.n_video_tiles, min(shp.topk, shp.n_video_tiles)
-
-    def view(name, shape, dtype, size):
-        off = lay[name]
-        assert off is not None, name
-        n = int(np.prod(shape)) * size
-        return ws[off:off + n].view(dtype).view(*shape)
-
-    out = {n: host_f64(view(n, (H, N, d), torch.bfloat16, 2)) for n in ("q", "k", "v")}
-    out["g"] = host_f64(view("g", (N, A), torch.bfloat16, 2))
-    out["o"] = host_f64(view("o", (N, A), torch.bfloat16, 2))
-    out["x1"] = host_f64(view("x1", (N, D), torch.bfloat16, 2))
-    out["h2"] = host_f64(view("h", (N, D), torch.bfloat16, 2))
-    out["u"] = host_f64(view("u", (N, F), torch.bfloat16, 2))
-    out["idx"] = view("idx", (H, tv, ks), torch.int32, 4).cpu().numpy()
+    spec = {"q": ("q", (H, N, d)), "k": ("k", (H, N, d)), "v": ("v", (H, N, d)),
+            "g": ("g", (N, A)), "o": ("o", (N, A)), "x1": ("x1", (N, D)), "h2": ("h", (N, D)),
+            "u": ("u", (N, F))}
+    out = {}
+    for n in (names or list(spec) + ["idx"]):
+        if n == "idx":
+            off, size = lay["idx"], H * tv * ks * 4
+            out[n] = ws[off:off + size].view(torch.int32).view(H, tv, ks).cpu().numpy()
+            continue
+        region, shape = spec[n]
+        off = lay[region]
+        assert off is not None, region
+        size = int(np.prod(shape)) * 2
+        out[n] = host_f64(ws[off:off + size].view(torch.bfloat16).view(*shape))
     return out
+
+
+def router_on_gpu_inputs(q, k, shp, idx, sets=None):
+    """The router's selections against the oracle's on the GPU's own q and k (raster row
+    order, float64 values of the bf16 data): index sets must be equal except near-ties.
+    Returns the number of near-tied (head, tile) pairs that differ."""
+    import oracle
+    P, V = shp.n_prefix, shp.n_video
+    sets = oracle.shape_tiles(shp) if sets is None else sets
+    S = oracle.tile_scores(oracle.tile_means(q, P, V, shp.tile, sets),
+                           oracle.tile_means(k, P, V, shp.tile, sets))
+    ks = min(shp.topk, shp.n_video_tiles)
+    return compare_topk(idx, oracle.topk_select(S, ks), S, ks)

@@ -1,17 +1,20 @@
-"""bench.py's reference arm (the float64 oracle timed on host cores) keeps the JSON
-contract; runs on the CPU with the 1,024-row attention workload and a short-prefix shape."""
+"""bench.py's reference arm (the float32 C oracle timed on host cores) keeps the JSON
+contract; runs on the CPU with the 1,024-row attention workload and a small block shape.
+Also the host-side pieces of the GPU line: the near-tie audit and the flop accounting."""
 import importlib.util
 import json
 import os
 import subprocess
 import sys
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_reference_arm_json_line():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                          "--workload", "attn_tiny_1024", "--steps", "1", "--warmup", "0"],
+                          "--workload", "routed_attention_1024", "--steps", "2", "--warmup", "1"],
                          check=True, capture_output=True, text=True, cwd=ROOT).stdout
     lines = [ln for ln in out.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
@@ -22,21 +25,52 @@ def test_reference_arm_json_line():
         assert k in d, k
     assert d["config"]["workload"] == "attn_tiny_1024"
     cb = d["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert cb["kind"].startswith("oracle") and cb["value"] == d["value"] and cb["cores"] >= 1
     assert cb["unit"] == d["unit"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+    # the value is the rows of the measured steps over their measured time
+    assert abs(d["value"] - 1024 / (d["ms_per_step"] / 1e3)) < 1e-6 * d["value"]
 
 
-def test_oracle_sample_with_a_prefix_shorter_than_a_chunk():
-    sys.path.insert(0, ROOT)
+def test_reference_block_steps_are_measured_samples():
+    """A block step of the reference arm is a uniform sample of the block; its time is
+    measured, and the value is the rows the sample processed per second."""
+    bench = _bench()
     import synthetic as S
-    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
-    bench = importlib.util.module_from_spec(spec)
-    spec.loader.exec_module(bench)
-    s = S.BlockShape(36, 0, 256, hidden=256, heads=2, head_dim=64, mlp_width=512, topk=2)
-    t, desc = bench.oracle_block_sample(s)
-    assert t > 0 and "prefix chunks" in desc
+    s = S.BlockShape(36, 64, 7 * 64 + 5, hidden=256, heads=2, head_dim=64, mlp_width=512,
+                     topk=2)
+    blk, x, s2 = bench.cpu_block(s)
+    assert s2 is s
+    for sample in (1, 3):
+        t = bench.time_cpu_block(blk, x, sample)
+        assert t > 0
+    assert bench.sampled_rows(s.n_rows, 1) == s.n_rows
+    assert bench.sampled_rows(s.n_rows, 3) == 64 * len(range(0, -(-s.n_rows // 64), 3)) - (
+        64 - s.n_rows % 64 if (s.n_rows // 64) % 3 == 0 else 0)
+    cb = bench.cpu_baseline(s, budget_s=30.0)
+    assert cb["kind"] == "oracle fp32, measured full block" and cb["value"] > 0
+    assert cb["s_per_block"] == cb["seconds_timed"]
+
+
+def test_near_tie_audit_counts_gaps_and_checks_selections():
+    bench = _bench()
+    just_above_4 = np.nextafter(np.float32(4.0), np.float32(5.0))
+    sc = np.array([[[5.0, 4.0, just_above_4, 1.0], [1.0, 2.0, 3.0, np.nan]]], np.float32)
+    idx = np.array([[[0, 1], [1, 2]]], np.int32)
+    a = bench.near_tie_audit(sc, idx, 2)
+    assert a["pairs"] == 2 and a["near_ties"] == 1  # 4 vs 4 + 1 ulp is a near-tie; 2 vs 1 not
+    assert a["selections_are_topk_of_scores"] is False  # row 0: the top-2 is {0, 2}
+    idx = np.array([[[0, 2], [1, 2]]], np.int32)
+    assert bench.near_tie_audit(sc, idx, 2)["selections_are_topk_of_scores"] is True
+    # every tile selected: no (k+1)-th score, no near-tie
+    assert bench.near_tie_audit(sc, np.array([[[0, 1, 2, 3]] * 2], np.int32), 4)["near_ties"] == 0
+
+
+def test_per_clock_peak():
+    bench = _bench()
+    assert bench.per_clock_peak(152, 2070.0) == 8192 * 152 * 2070e6 / 1e12
+    assert bench.per_clock_peak(152, None) is None
 
 
 def _bench():

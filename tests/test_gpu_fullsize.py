@@ -10,7 +10,7 @@ import pytest
 import oracle
 import synthetic as S
 from helpers import assert_close, check_close, compare_topk, dev_bf16, dev_f32, host_f64, log, \
-    weights_to_device, weights_to_f64, workspace_views
+    router_on_gpu_inputs, weights_to_device, weights_to_f64, workspace_views
 
 pytestmark = pytest.mark.gpu
 
@@ -99,9 +99,13 @@ def test_routed_attention_fullsize(h3):
 
 def block_sampled(h3, shp, seed, name, rows, perm=None):
     """One block on the device with its intermediates kept, checked on sampled rows
-    against the oracle that rounds the softmax weights to bf16: x2, and the block's own
-    updates x1 - x and x2 - x at the required bar (rel L2 2e-2, cos 0.998).  ``perm``
-    (cube layouts) maps library rows to the oracle's raster rows."""
+    against the oracle that rounds the softmax weights to bf16: the router against the
+    oracle's on the GPU's own q and k (all heads and tiles; equal except near-ties);
+    then, with the oracle attending over the GPU's selections, x2 and the block's own
+    updates x1 - x and x2 - x at the required bar (rel L2 2e-2, cos 0.998), and the out
+    projection given the GPU's attention output.  ``perm`` (cube layouts) maps library
+    rows to the oracle's raster rows."""
+    import oracle.h3block as OB
     t0 = time.time()
     w = S.block_weights(shp, seed)
     xb = S.hidden_rows(shp, seed)
@@ -113,28 +117,39 @@ def block_sampled(h3, shp, seed, name, rows, perm=None):
     h3.block_forward(cs, weights_to_device(w), x, ws)
     torch.cuda.synchronize()
     assert h3.sync_status(ws) == 0
-    it = workspace_views(h3, cs, shp, ws)
+    lib = workspace_views(h3, cs, shp, ws, ["q", "k", "o", "x1", "idx"])
+    del ws
     got = host_f64(x)
-    x1 = it["x1"]
+    it = dict(lib)
     if perm is not None:
-        got, x1 = np.empty_like(got), np.empty_like(x1)
-        got[perm], x1[perm] = host_f64(x), it["x1"]
+        got = np.empty_like(got)
+        got[perm] = host_f64(x)
+        for n in ("q", "k"):
+            it[n] = np.empty_like(lib[n])
+            it[n][:, perm] = lib[n]
+        for n in ("o", "x1"):
+            it[n] = np.empty_like(lib[n])
+            it[n][perm] = lib[n]
     assert np.all(np.isfinite(got))
     t0 = time.time()
+    n_tie = router_on_gpu_inputs(it["q"], it["k"], shp, it["idx"])
     x64, wo = S.bf16_bits_to_f64(xb), weights_to_f64(w)
-    ref = oracle.block_forward_rows(x64, wo, shp, rows, p_bf16=True)
-    n_diff = compare_topk(it["idx"], ref["idx"], ref["scores"], min(shp.topk, shp.n_video_tiles))
-    if n_diff:
-        ref = oracle.block_forward_rows(x64, wo, shp, rows, p_bf16=True, idx=it["idx"])
-    _log(f"{name} sampled oracle {time.time() - t0:.1f}s; query tiles whose selections "
-         f"differ (near-ties): {n_diff} of {shp.heads * shp.n_video_tiles}")
+    ref = oracle.block_forward_rows(x64, wo, shp, rows, p_bf16=True, idx=it["idx"])
+    n_own = int(np.any(it["idx"] != ref["idx"], axis=-1).sum())
+    _log(f"{name} sampled oracle {time.time() - t0:.1f}s; of {shp.heads * shp.n_video_tiles} "
+         f"(head, tile) pairs: near-ties differing on the GPU's q/k {n_tie}, selections "
+         f"differing from the oracle's own q/k {n_own}")
     r = ref["rows"]
     x0 = x64[r]
     check_close(got[r], ref["x2"], f"{name} x2 (sampled rows)", rel=2e-3, cos=0.99999)
-    check_close(x1[r] - x0, ref["x1"] - x0, f"{name} x1 - x (sampled rows)", rel=2e-2,
+    check_close(it["x1"][r] - x0, ref["x1"] - x0, f"{name} x1 - x (sampled rows)", rel=2e-2,
                 cos=0.998)
     check_close(got[r] - x0, ref["x2"] - x0, f"{name} x2 - x (sampled rows)", rel=2e-2,
                 cos=0.998)
+    x1 = oracle.bf16(x0 + OB.gate_rows(wo["mod"], wo.get("mod_prefix"), shp.n_prefix, 2, r)
+                     * oracle.linear(it["o"][r], wo["w_o"], wo["b_o"]))
+    check_close(it["x1"][r] - x0, x1 - x0, f"{name} x1 - x given o (sampled rows)", rel=1e-3,
+                cos=0.999999)
 
 
 def test_block_forward_fullsize_sampled(h3):
