@@ -117,6 +117,7 @@ _SIGS = [
     ("h3dit_profile_begin", ctypes.c_int, [ctypes.c_int]),
     ("h3dit_profile_end", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]),
     ("h3dit_launch_count", ctypes.c_ulonglong, []),
+    ("h3dit_gemm_cta_pairs", ctypes.c_int, [ctypes.c_int]),
     ("h3dit_selftest_timeout", ctypes.c_int,
      [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]),
 ]
@@ -343,6 +344,12 @@ def selftest_timeout(workspace, limit_ms: int = 200, stream=None):
     _check("h3dit_selftest_timeout", lib().h3dit_selftest_timeout(
         _ptr(workspace), workspace.numel() * workspace.element_size(), int(limit_ms),
         _stream(stream)))
+
+
+def gemm_cta_pairs(enable: int = -1) -> int:
+    """1: projection GEMMs on SM pairs (cluster kernel) where possible; 0: one SM per
+    tile; -1: query.  Returns the previous setting."""
+    return int(lib().h3dit_gemm_cta_pairs(int(enable)))
 
 
 def launch_count() -> int:

@@ -924,6 +924,8 @@ h3dit_status h3dit_linear(const void* a, const void* w, const void* b_or_null, v
 
 unsigned long long h3dit_launch_count(void) { return g_launches.load(); }
 
+int h3dit_gemm_cta_pairs(int enable) { return gemm_cta_pairs(enable) ? 1 : 0; }
+
 h3dit_status h3dit_profile_begin(int max_records) {
   if (g_prof.on || max_records < 1 || max_records > (1 << 20)) return H3DIT_ERR_ARG;
   g_prof.ev.assign(2 * (size_t)max_records, nullptr);

@@ -521,7 +521,261 @@ cudaError_t launch_one(const GemmArgs& g, const CUtensorMap& tb, Params p, cudaS
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ CTA-pair kernel
+// 256 x 256 output tiles on a cluster of two CTAs (two SMs) with cta_group::2 MMAs: each
+// CTA loads its own 128 rows of A and its own 128 rows of the W tile (no multicast), and
+// rank 0's MMA thread issues M = 256, N = 256, K = 16 MMAs that read both CTAs' shared
+// memory and write 128 x 256 fp32 accumulators into each CTA's TMEM.  Per SM and K step
+// that is 32 KB of operands written and read through shared memory for 1,024 MMA cycles
+// of tensor work, against 48 KB per 512 cycles for the one-SM 128 x 256 tile, and each
+// CTA keeps two 256-column accumulators, so the epilogue of one tile overlaps the K loop
+// of the next.
+//   warp 0      TMA producer (both CTAs): A rows and W rows of this CTA's half into a
+//               6-stage ring; the bytes of both halves are counted on rank 0's barrier
+//   warp 1      rank 0: the MMA issuer; both ranks: TMEM allocation for the pair
+//   warps 2..5  epilogue (both CTAs): this CTA's 128 rows; accumulator release counted
+//               on rank 0's barrier (eight warps)
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = BM * BK * 2;           // 16 KB: this CTA's 128 rows of A
+constexpr int P_B_BYTES = (BN_WIDE / 2) * BK * 2;  // 16 KB: this CTA's 128 rows of W
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 + 256;
+constexpr int P_THREADS = 192;
+constexpr uint32_t P_TMEM_COLS = 512;  // two 256-column accumulators per CTA
+
+template <int EPI, int HD>
+__global__ void __launch_bounds__(P_THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + P_STAGES * P_A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+  uint64_t* full = bars;                  // [P_STAGES] rank 0: both halves landed
+  uint64_t* empty = bars + P_STAGES;      // [P_STAGES] the stage's MMAs completed
+  uint64_t* acc_full = bars + 2 * P_STAGES;  // [2] accumulator ready (both CTAs)
+  uint64_t* acc_empty = acc_full + 2;     // [2] rank 0: both CTAs' epilogues read it
+  uint64_t* drain = acc_empty + 2;        // rank 0: every MMA completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int cluster = blockIdx.x >> 1;
+  const int n_clusters = gridDim.x >> 1;
+  const int num_m = (p.M + 2 * BM - 1) / (2 * BM);  // 256-row tiles
+  const int num_n = p.N / BN_WIDE;
+  const int num_tiles = num_m * num_n;
+  const int num_k = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  // both CTAs are running and their barriers initialised before any remote access
+  cluster_sync();
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, P_TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the pair's TMEM is allocated in both CTAs before rank 0 issues MMAs
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // completion of both CTAs' loads is counted on rank 0's full barriers
+      const uint32_t full0 = rank == 0 ? smem_u32(full) : mapa_shared(smem_u32(full), 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = cluster; ok && tile < num_tiles; tile += n_clusters) {
+        int m_blk, n_blk;
+        tile_coords(tile, num_m, num_n, p.group, m_blk, n_blk);
+        const int arow = m_blk * 2 * BM + (int)rank * BM;
+        const int brow = n_blk * BN_WIDE + (int)rank * (BN_WIDE / 2);
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
+          const uint32_t fb = full0 + stage * 8;
+          tma_load_2d_pair(sA + stage * P_A_BYTES, &tmA, fb, kb * BK, arow);
+          tma_load_2d_pair(sB + stage * P_B_BYTES, &tmB, fb, kb * BK, brow);
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16(2 * BM, BN_WIDE, false, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = cluster; ok && tile < num_tiles; tile += n_clusters) {
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * 256;
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * P_A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * P_B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            umma_bf16_pair(d_tmem, sdesc_sw128(a0 + k * 32, 16, 1024),
+                           sdesc_sw128(b0 + k * 32, 16, 1024), idesc, (kb | k) != 0 ? 1u : 0u);
+          umma_commit_pair(&empty[stage], 0x3);
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(&acc_full[acc], 0x3);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // every MMA this thread issued has completed before either CTA releases TMEM
+      umma_commit_pair(drain, 0x1);
+      mbar_drain(drain, 0);
+    }
+  } else {
+    const int quad = warp & 3;
+    const uint32_t rel0 = smem_u32(acc_empty);
+    const uint32_t rel0_remote = rank == 0 ? 0u : mapa_shared(rel0, 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = cluster; tile < num_tiles; tile += n_clusters) {
+      int m_blk, n_blk;
+      tile_coords(tile, num_m, num_n, p.group, m_blk, n_blk);
+      if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const int row = m_blk * 2 * BM + (int)rank * BM + quad * 32 + lane;
+      const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16) + acc * 256;
+      if (EPI == kEpiQkvg)
+        epilogue_qkvg<HD, BN_WIDE>(p, t_row, row, n_blk * BN_WIDE);
+      else if (EPI == kEpiSwiglu)
+        epilogue_swiglu(p, t_row, row, n_blk * BN_WIDE);
+      else
+        epilogue_rows<EPI, BN_WIDE>(p, t_row, row, n_blk * BN_WIDE);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(&acc_empty[acc]);
+        else
+          mbar_arrive_cluster(rel0_remote + acc * 8);
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // rank 0's MMAs have drained and both epilogues are done with TMEM
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, P_TMEM_COLS);
+  }
+}
+
+// Clusters of two that can be resident at once for this kernel (0: none / unsupported).
+template <int EPI, int HD>
+int pair_capacity() {
+  static int cap = -1;
+  if (cap >= 0) return cap;
+  auto kern = gemm_pair_kernel<EPI, HD>;
+  cap = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES) !=
+      cudaSuccess)
+    return cap;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+  cfg.blockDim = dim3(P_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = P_SMEM_BYTES;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) cap = n;
+  cudaGetLastError();  // a refused query leaves no sticky error behind
+  return cap;
+}
+
+// Launches the pair kernel; cudaErrorNotSupported when clusters of two cannot run here.
+template <int EPI, int HD>
+cudaError_t launch_pair(const GemmArgs& g, Params p, cudaStream_t stream) {
+  const int cap = pair_capacity<EPI, HD>();
+  if (cap < 1) return cudaErrorNotSupported;
+  CUtensorMap ta, tb;
+  if (!make_tmap_2d(&ta, g.a, g.M, g.K, BM) || !make_tmap_2d(&tb, g.w, g.N, g.K, BN_WIDE / 2))
+    return cudaErrorInvalidValue;
+  // raster groups of 256-row tiles: 8 when N or K is long, else 4
+  p.group = (g.N >= 16384 || g.K >= 16384) ? 8 : 4;
+  p.pairs = 0;
+  const int tiles = ((g.M + 2 * BM - 1) / (2 * BM)) * (g.N / BN_WIDE);
+  const int clusters = tiles < cap ? tiles : cap;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(P_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = P_SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI, HD>, ta, tb, p);
+}
+
+bool g_use_pairs = true;  // h3dit_gemm_cta_pairs
+
 }  // namespace
+
+bool gemm_cta_pairs(int enable) {
+  const bool prev = g_use_pairs;
+  if (enable >= 0) g_use_pairs = enable != 0;
+  return prev;
+}
 
 cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   // the output heads use one tile of exactly N columns; everything else 256-wide tiles
@@ -559,6 +813,22 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   p.z = g.z;
   p.dt = g.dt;
   p.status = g.status;
+  if (g_use_pairs && epi != kEpiHeadEuler && !(epi == kEpiSwiglu && !g.bias) &&
+      (epi != kEpiQkvg || g.head_dim == 64 || g.head_dim == 128)) {
+    cudaError_t e = cudaErrorNotSupported;
+    switch (epi) {
+      case kEpiStore: e = launch_pair<kEpiStore, 128>(g, p, stream); break;
+      case kEpiGelu: e = launch_pair<kEpiGelu, 128>(g, p, stream); break;
+      case kEpiResid: e = launch_pair<kEpiResid, 128>(g, p, stream); break;
+      case kEpiSwiglu: e = launch_pair<kEpiSwiglu, 128>(g, p, stream); break;
+      case kEpiQkvg:
+        e = g.head_dim == 128 ? launch_pair<kEpiQkvg, 128>(g, p, stream)
+                              : launch_pair<kEpiQkvg, 64>(g, p, stream);
+        break;
+      default: break;
+    }
+    if (e != cudaErrorNotSupported) return e;  // launched (or failed for another reason)
+  }
   switch (epi) {
     // plain stores: pair tiles; the rest 128 x 256
     case kEpiStore:

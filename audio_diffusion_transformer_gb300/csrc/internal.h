@@ -45,6 +45,9 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(int epi, const GemmArgs& args, cudaStream_t stream);
+// 1: the 256-wide projection GEMMs run on CTA pairs (clusters of two SMs, cta_group::2)
+// where the device can host them; 0: one SM per tile; -1: query.  Returns the previous.
+bool gemm_cta_pairs(int enable);
 
 // ---------------------------------------------------------------- attention
 struct AttnArgs {

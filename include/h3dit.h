@@ -130,6 +130,14 @@ size_t h3dit_workspace_bytes(const h3dit_shape* shape);
 /* Checks a shape without touching the GPU. */
 h3dit_status h3dit_check_shape(const h3dit_shape* shape);
 
+/* Host-only switch of the projection GEMMs (no counterpart on the pages: a choice of
+ * kernel).  1 (the default): the 256-wide projections run each 256 x 256 output tile
+ * on a pair of SMs (a cluster of two CTAs issuing cta_group::2 tensor-core MMAs) when
+ * the device can host such clusters, else on one SM; 0: one SM per 128 x 256 tile;
+ * -1: query only.  Both kernels sum in the same order and give the same bytes.
+ * Returns the previous setting (1 or 0).  Set it while no call is being made. */
+int h3dit_gemm_cta_pairs(int enable);
+
 /*
  * Byte offsets, from the start of the workspace, of the regions a call with this
  * shape uses (host only; no counterpart on the pages: a debugging aid).  A region

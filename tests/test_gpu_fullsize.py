@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import synthetic as S
-from helpers import assert_close, check_close, compare_topk, dev_bf16, dev_f32, host_f64, log, \
+from helpers import assert_close, check_bf16_stage, check_close, compare_topk, dev_bf16, dev_f32, host_f64, log, \
     router_on_gpu_inputs, weights_to_device, weights_to_f64, workspace_views
 
 pytestmark = pytest.mark.gpu
@@ -148,8 +148,7 @@ def block_sampled(h3, shp, seed, name, rows, perm=None):
                 cos=0.998)
     x1 = oracle.bf16(x0 + OB.gate_rows(wo["mod"], wo.get("mod_prefix"), shp.n_prefix, 2, r)
                      * oracle.linear(it["o"][r], wo["w_o"], wo["b_o"]))
-    check_close(it["x1"][r] - x0, x1 - x0, f"{name} x1 - x given o (sampled rows)", rel=1e-3,
-                cos=0.999999)
+    check_bf16_stage(it["x1"][r], x1, f"{name} x1 given o (sampled rows)")
 
 
 def test_block_forward_fullsize_sampled(h3):
