@@ -133,13 +133,16 @@ def router_on_gpu_inputs(q, k, shp, idx, sets=None):
 
 
 def check_bf16_stage(got, ref, what, min_same=0.995):
-    """A stage's bf16 output against the oracle's rounding of the SAME inputs: every
-    element within one bf16 spacing (only fp32-vs-float64 sums separate the two, which
-    can move a rounding by one step) and nearly all identical."""
+    """A stage's bf16 output against the oracle's rounding of the SAME inputs: only
+    fp32-vs-float64 sums separate the two.  Nearly every value identical, and every
+    value within one bf16 spacing plus 2^-12 of the tensor's RMS (a sum that cancels to
+    near zero carries the fp32 error of its much larger terms, which one spacing of the
+    small result does not cover)."""
     got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
     same = same_fraction(got, ref)
-    spacing = np.maximum(np.abs(got), np.abs(ref)) * 2.0 ** -7 + 1e-30
-    worst = float(np.max(np.abs(got - ref) / spacing)) if got.size else 0.0
-    log(f"{what}: identical {same:.6f} (bar {min_same}), largest difference "
-        f"{worst:.3f} bf16 spacings (bar 1)")
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    tol = np.maximum(np.abs(got), np.abs(ref)) * 2.0 ** -7 + 2.0 ** -12 * rms + 1e-30
+    worst = float(np.max(np.abs(got - ref) / tol)) if got.size else 0.0
+    log(f"{what}: identical {same:.6f} (bar {min_same}), largest difference {worst:.3f} of "
+        f"(1 bf16 spacing + 2^-12 RMS) (bar 1)")
     assert worst <= 1.0 and same >= min_same, f"{what}: identical {same}, worst {worst}"
