@@ -161,7 +161,8 @@ __device__ __forceinline__ void pair_tile(const Params& p, int tile, int num_n, 
 // cancellation for negative x.  About 2.5% faster per fc1 launch than erff.
 __device__ __forceinline__ float gelu_erf(float x) {
   const float z = fabsf(x) * 0.70710678118654752f;
-  const float t = __frcp_rn(fmaf(0.3275911f, z, 1.0f));
+  float t;  // 1 / (1 + p z), approximate reciprocal (relative error ~2^-23)
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, z, 1.0f)));
   float q = fmaf(t, 1.061405429f, -1.453152027f);
   q = fmaf(t, q, 1.421413741f);
   q = fmaf(t, q, -0.284496736f);
@@ -243,11 +244,13 @@ __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
 
 // Epilogue of the SwiGLU fc1: tile columns 0..127 are gate, 128..255 up, for the 128
 // activated outputs 128 * (n0 / 256) ..; y has N / 2 columns.
-__device__ __forceinline__ void epilogue_swiglu(const Params& p, uint32_t t_row, int row, int n0) {
+// Chunks [c0, c1) of the tile's four 32-output chunks.
+__device__ __forceinline__ void epilogue_swiglu(const Params& p, uint32_t t_row, int row, int n0,
+                                                int c0 = 0, int c1 = 4) {
   const int F = p.N / 2;
   const int out0 = n0 / 2;
 #pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
+  for (int c = c0; c < c1; ++c) {
     float g[32], u[32];
     tmem_ld32(t_row + c * 32, g);
     tmem_ld32(t_row + 128 + c * 32, u);
@@ -558,11 +561,15 @@ constexpr int P_A_BYTES = BM * BK * 2;           // 16 KB: this CTA's 128 rows o
 constexpr int P_B_BYTES = (BN_WIDE / 2) * BK * 2;  // 16 KB: this CTA's 128 rows of W
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 + 256;
-constexpr int P_THREADS = 192;
+// Epilogue warps EW: 4 (one per SM sub-partition) or 8 (two, each taking half of the
+// tile's columns).  Eight pay where the K loop is short (K <= 4,096: the 4,096-row block's
+// fc1 took 16% less time with them) and cost 2-3% where it is long (K = 5,120 and 20,480 at
+// 15,435 rows); the q/k/v/gate epilogue's per-head registers allow only four.
+__host__ __device__ constexpr int pair_threads(int ew) { return 64 + 32 * ew; }
 constexpr uint32_t P_TMEM_COLS = 512;  // two 256-column accumulators per CTA
 
-template <int EPI, int HD>
-__global__ void __launch_bounds__(P_THREADS, 1)
+template <int EPI, int HD, int EW>
+__global__ void __launch_bounds__(pair_threads(EW), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -596,7 +603,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 8);
+      mbar_init(&acc_empty[b], 2 * EW);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -689,6 +696,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     }
   } else {
     const int quad = warp & 3;
+    const int half = EW == 8 ? (warp - 2) >> 2 : 0;  // eight warps: the tile's column half
     const uint32_t rel0 = smem_u32(acc_empty);
     const uint32_t rel0_remote = rank == 0 ? 0u : mapa_shared(rel0, 0);
     int acc = 0;
@@ -702,8 +710,13 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       const uint32_t t_row = tmem + ((uint32_t)(quad * 32) << 16) + acc * 256;
       if (EPI == kEpiQkvg)
         epilogue_qkvg<HD, BN_WIDE>(p, t_row, row, n_blk * BN_WIDE);
+      else if (EPI == kEpiSwiglu && EW == 8)
+        epilogue_swiglu(p, t_row, row, n_blk * BN_WIDE, 2 * half, 2 * half + 2);
       else if (EPI == kEpiSwiglu)
         epilogue_swiglu(p, t_row, row, n_blk * BN_WIDE);
+      else if (EW == 8)
+        epilogue_rows<EPI, BN_WIDE / 2>(p, t_row + half * (BN_WIDE / 2), row,
+                                        n_blk * BN_WIDE + half * (BN_WIDE / 2));
       else
         epilogue_rows<EPI, BN_WIDE>(p, t_row, row, n_blk * BN_WIDE);
       tc_fence_before();
@@ -731,11 +744,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 }
 
 // Clusters of two that can be resident at once for this kernel (0: none / unsupported).
-template <int EPI, int HD>
+template <int EPI, int HD, int EW>
 int pair_capacity() {
   static int cap = -1;
   if (cap >= 0) return cap;
-  auto kern = gemm_pair_kernel<EPI, HD>;
+  auto kern = gemm_pair_kernel<EPI, HD, EW>;
   cap = 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES) !=
       cudaSuccess)
@@ -747,7 +760,7 @@ int pair_capacity() {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
-  cfg.blockDim = dim3(P_THREADS, 1, 1);
+  cfg.blockDim = dim3(pair_threads(EW), 1, 1);
   cfg.dynamicSmemBytes = P_SMEM_BYTES;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -758,9 +771,9 @@ int pair_capacity() {
 }
 
 // Launches the pair kernel; cudaErrorNotSupported when clusters of two cannot run here.
-template <int EPI, int HD>
+template <int EPI, int HD, int EW>
 cudaError_t launch_pair(const GemmArgs& g, Params p, cudaStream_t stream) {
-  const int cap = pair_capacity<EPI, HD>();
+  const int cap = pair_capacity<EPI, HD, EW>();
   if (cap < 1) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
   if (!make_tmap_2d(&ta, g.a, g.M, g.K, BM) || !make_tmap_2d(&tb, g.w, g.N, g.K, BN_WIDE / 2))
@@ -777,12 +790,12 @@ cudaError_t launch_pair(const GemmArgs& g, Params p, cudaStream_t stream) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  cfg.blockDim = dim3(P_THREADS, 1, 1);
+  cfg.blockDim = dim3(pair_threads(EW), 1, 1);
   cfg.dynamicSmemBytes = P_SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI, HD>, ta, tb, p);
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI, HD, EW>, ta, tb, p);
 }
 
 bool g_use_pairs = true;  // h3dit_gemm_cta_pairs
@@ -834,14 +847,27 @@ cudaError_t launch_gemm(int epi, const GemmArgs& g, cudaStream_t stream) {
   if (g_use_pairs && epi != kEpiHeadEuler && !(epi == kEpiSwiglu && !g.bias) &&
       (epi != kEpiQkvg || g.head_dim == 64 || g.head_dim == 128)) {
     cudaError_t e = cudaErrorNotSupported;
+    const bool short_k = g.K <= 4096;  // eight epilogue warps
     switch (epi) {
-      case kEpiStore: e = launch_pair<kEpiStore, 128>(g, p, stream); break;
-      case kEpiGelu: e = launch_pair<kEpiGelu, 128>(g, p, stream); break;
-      case kEpiResid: e = launch_pair<kEpiResid, 128>(g, p, stream); break;
-      case kEpiSwiglu: e = launch_pair<kEpiSwiglu, 128>(g, p, stream); break;
+      case kEpiStore:
+        e = short_k ? launch_pair<kEpiStore, 128, 8>(g, p, stream)
+                    : launch_pair<kEpiStore, 128, 4>(g, p, stream);
+        break;
+      case kEpiGelu:
+        e = short_k ? launch_pair<kEpiGelu, 128, 8>(g, p, stream)
+                    : launch_pair<kEpiGelu, 128, 4>(g, p, stream);
+        break;
+      case kEpiResid:
+        e = short_k ? launch_pair<kEpiResid, 128, 8>(g, p, stream)
+                    : launch_pair<kEpiResid, 128, 4>(g, p, stream);
+        break;
+      case kEpiSwiglu:
+        e = short_k ? launch_pair<kEpiSwiglu, 128, 8>(g, p, stream)
+                    : launch_pair<kEpiSwiglu, 128, 4>(g, p, stream);
+        break;
       case kEpiQkvg:
-        e = g.head_dim == 128 ? launch_pair<kEpiQkvg, 128>(g, p, stream)
-                              : launch_pair<kEpiQkvg, 64>(g, p, stream);
+        e = g.head_dim == 128 ? launch_pair<kEpiQkvg, 128, 4>(g, p, stream)
+                              : launch_pair<kEpiQkvg, 64, 4>(g, p, stream);
         break;
       default: break;
     }

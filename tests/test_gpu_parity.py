@@ -80,10 +80,13 @@ def test_linear_random_close(h3):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 256, 64), (255, 512, 192), (15435, 768, 320),
-                                   (4097, 1024, 1280)])
+                                   (4097, 1024, 1280), (515, 512, 5120),
+                                   # 1,220 tiles: a short last round on 76 SM pairs
+                                   (15435, 5120, 512), (15435, 5120, 4608)])
 def test_linear_cta_pairs_equal_one_sm_kernel(h3, M, N, K):
-    """The cluster-pair GEMM (256 x 256 tiles over two SMs) and the one-SM kernel sum in
-    the same order: byte-identical outputs on random inputs, ragged rows included."""
+    """The cluster-pair GEMM (256 x 256 tiles over two SMs; eight epilogue warps for
+    K <= 4,096, four above) and the one-SM kernel sum in the same order: byte-identical
+    outputs on random inputs, ragged rows included."""
     a = S.normal_bf16(M + K, "a", (M, K))
     w = S.normal_bf16(M + K, "w", (N, K), std=0.02)
     b = S.normal_bf16(M + K, "b", (N,), std=0.02)
@@ -309,13 +312,14 @@ def test_block_forward_4096_rows(h3):
     check_block(h3, wl.shape, wl.seed, "block 4096")
 
 
-@pytest.mark.parametrize("case", ["gelu_d128", "norope_d64", "swiglu_prefix_table"])
+@pytest.mark.parametrize("case", ["gelu_d128", "norope_d64", "swiglu_prefix_table", "block_4096"])
 def test_block_cta_pairs_equal_one_sm_kernel(h3, case):
     """Every epilogue of the block (q/k norm + rotary + head layout for d 64 and 128,
     GELU, SwiGLU, gated residual with a prefix table) gives the same bytes on the
-    cluster-pair GEMM as on the one-SM kernel."""
+    cluster-pair GEMM as on the one-SM kernel, from tiny shapes to the 4,096-row block."""
     shp = {"gelu_d128": BLOCK_CASES[0][1], "norope_d64": BLOCK_CASES[1][1],
-           "swiglu_prefix_table": SWIGLU_CASES[0][1].with_(prefix_mod=True)}[case]
+           "swiglu_prefix_table": SWIGLU_CASES[0][1].with_(prefix_mod=True),
+           "block_4096": S.BLOCK_4K.shape}[case]
     w = S.block_weights(shp, 91)
     outs = []
     prev = h3.gemm_cta_pairs(-1)
