@@ -523,18 +523,27 @@ def run_ours(args, rank, world, local_rank):
 
         red = wl.extra.get("reduction")
 
-        def step_on(st):
-            h3.sample_step(cs, ends, blocks, ids, zv, za, rv, ra, None, h3.H3DIT_PASS_FRESH,
-                           (1.0, 0.0, 0.0, dt), (1.0, 0.0, 0.0, dt), 0, ws,
-                           stream=st, reduction=red)
+        def step_for(zb):
+            zvb = zb[:shape.n_video * cv].view(shape.n_video, cv)
+            zab = zb[shape.n_video * cv:].view(shape.n_audio, ca)
+
+            def run(st):
+                h3.sample_step(cs, ends, blocks, ids, zvb, zab, rv, ra, None,
+                               h3.H3DIT_PASS_FRESH, (1.0, 0.0, 0.0, dt), (1.0, 0.0, 0.0, dt), 0,
+                               ws, stream=st, reduction=red)
+            return run
     else:
         z0 = torch.randn(N, D, generator=gz, device=dev, dtype=torch.float32)
         z = z0.clone()
         ring = torch.zeros(2, N, D, dtype=torch.float32, device=dev)
 
-        def step_on(st):
-            h3.denoise_step(cs, blocks, ids, z, ring, True, (1.0, 0.0, 0.0, dt), 0, ws,
-                            stream=st)
+        def step_for(zb):
+            def run(st):
+                h3.denoise_step(cs, blocks, ids, zb, ring, True, (1.0, 0.0, 0.0, dt), 0, ws,
+                                stream=st)
+            return run
+
+    step_on = step_for(z)
 
     def step():
         step_on(stream.cuda_stream)
@@ -567,10 +576,14 @@ def run_ours(args, rank, world, local_rank):
         raise SystemExit("device status error in the timed region")
     ms_max = max_over_ranks(ms, world, dev)
 
-    # end to end through the C ABI with host buffers: H2D z, the step, D2H z
+    # end to end through the C ABI with host buffers: every step copies its latents in
+    # from pinned host memory, runs, and copies its result back.  Serial: H2D, step, D2H
+    # in one stream.  Pipelined (the headline e2e): the steps are independent requests, so
+    # two device latent buffers alternate and the copies run on a second stream, each
+    # step's H2D and the previous step's D2H overlapping the compute stream.
     z_host = z0.cpu().pin_memory()
-    z_back = torch.empty_like(z_host).pin_memory()
-    e2e_ms = None
+    z_back = [torch.empty_like(z_host).pin_memory() for _ in range(2)]
+    e2e_ms = e2e_serial_ms = None
     if not args.no_e2e:
         barrier()
         torch.cuda.synchronize()
@@ -578,10 +591,35 @@ def run_ours(args, rank, world, local_rank):
         for _ in range(args.steps):
             z.copy_(z_host, non_blocking=True)
             step()
-            z_back.copy_(z, non_blocking=True)
+            z_back[0].copy_(z, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_serial_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world, dev)
+        assert torch.isfinite(z_back[0]).all().item()
+        zb = [z, torch.empty_like(z)]
+        runs = [step_for(zb[0]), step_for(zb[1])]
+        copy = torch.cuda.Stream()
+        ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(copy):
+            zb[0].copy_(z_host, non_blocking=True)
+            ev_in[0].record(copy)
+        for i in range(args.steps):
+            b = i % 2
+            stream.wait_event(ev_in[b])
+            runs[b](stream.cuda_stream)
+            ev_done[b].record(stream)
+            with torch.cuda.stream(copy):
+                if i + 1 < args.steps:  # buffer b ^ 1: its previous D2H is earlier in this stream
+                    zb[b ^ 1].copy_(z_host, non_blocking=True)
+                    ev_in[b ^ 1].record(copy)
+                copy.wait_event(ev_done[b])
+                z_back[b].copy_(zb[b], non_blocking=True)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world, dev)
-        assert torch.isfinite(z_back).all().item()
+        assert all(torch.isfinite(t).all().item() for t in z_back)
 
     # the same step captured once into a CUDA graph and replayed
     graph = None
@@ -652,7 +690,11 @@ def run_ours(args, rank, world, local_rank):
         out["near_ties"] = ties
     if e2e_ms is not None:
         out["e2e"] = {"value": rows_blocks / (e2e_ms / 1e3), "unit": UNIT,
-                      "h2d_bytes_per_step": z.numel() * 4, "d2h_bytes_per_step": z.numel() * 4}
+                      "h2d_bytes_per_step": z.numel() * 4, "d2h_bytes_per_step": z.numel() * 4,
+                      "mode": "pipelined: independent steps, two latent buffers, copies on a "
+                              "second stream overlapping the neighbouring steps' compute",
+                      "serial": {"value": rows_blocks / (e2e_serial_ms / 1e3),
+                                 "mode": "H2D, step, D2H in one stream"}}
     if not args.no_cpu_baseline and world == 1:
         out["cpu_baseline"] = cpu_baseline(shape)
         out["cpu_baseline"].pop("s_per_block")
