@@ -338,6 +338,9 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
                        cudaStream_t st) {
   const int N = m.N, D = m.D, A = m.A, F = m.F;
   int* status = at<int>(ws, w.status);
+  // the projection GEMMs' tile counters share the status block (a separate 64-byte
+  // sector from the status word and the attention unit counter); the norms zero them
+  int* tiles = status + 48;
   __nv_bfloat16* h = at<__nv_bfloat16>(ws, w.h);
   __nv_bfloat16* q = at<__nv_bfloat16>(ws, w.q);
   __nv_bfloat16* k = at<__nv_bfloat16>(ws, w.k);
@@ -360,7 +363,7 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
     StageScope sc(H3DIT_STAGE_NORM1, st);
     H3_TRY(cu(counted(launch_rms_modulate(x, mod + 0 * D, mod + 1 * D, modp ? modp + 0 * D : nullptr,
                                           modp ? modp + 1 * D : nullptr, P, h, N, D, s->rms_eps,
-                                          st), 1)));
+                                          st, tiles), 1)));
   }
   // a2 + a3: q/k/v/gate projection with q/k norm, rotary and head-major layout
   GemmArgs ga;
@@ -385,6 +388,7 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   ga.rope_cs = use_rope ? rope : nullptr;
   ga.eps = s->rms_eps;
   ga.status = status;
+  ga.tile_counter = tiles;
   {
     StageScope sc(H3DIT_STAGE_QKVG, st);
     H3_TRY(cu(counted(launch_gemm(kEpiQkvg, ga, st), 1)));
@@ -405,6 +409,7 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   gb.gate_prefix = modp ? modp + 2 * D : nullptr;
   gb.n_prefix = P;
   gb.status = status;
+  gb.tile_counter = tiles;
   {
     StageScope sc(H3DIT_STAGE_OUT, st);
     H3_TRY(cu(counted(launch_gemm(kEpiResid, gb, st), 1)));
@@ -418,7 +423,7 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
     StageScope sc(H3DIT_STAGE_NORM2, st);
     H3_TRY(cu(counted(launch_rms_modulate(x, mod + 3 * D, mod + 4 * D, modp ? modp + 3 * D : nullptr,
                                           modp ? modp + 4 * D : nullptr, P, h, N, D, s->rms_eps,
-                                          st), 1)));
+                                          st, tiles), 1)));
   }
   // a12: fc1 + GELU, or the gate/up projection + SwiGLU
   const bool swiglu = (s->flags & H3DIT_SWIGLU) != 0;
@@ -432,6 +437,7 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   gc.bias = static_cast<const __nv_bfloat16*>(wt->b1);
   gc.y = u;
   gc.status = status;
+  gc.tile_counter = tiles;
   {
     StageScope sc(H3DIT_STAGE_FC1, st);
     H3_TRY(cu(counted(launch_gemm(swiglu ? kEpiSwiglu : kEpiGelu, gc, st), 1)));
@@ -450,6 +456,7 @@ h3dit_status run_block(const h3dit_shape* s, const Dims& m, const Ws& w, void* w
   gd.gate_prefix = modp ? modp + 5 * D : nullptr;
   gd.n_prefix = P;
   gd.status = status;
+  gd.tile_counter = tiles;
   StageScope sc(H3DIT_STAGE_FC2, st);
   return cu(counted(launch_gemm(kEpiResid, gd, st), 1));
 }

@@ -42,6 +42,10 @@ struct GemmArgs {
   float* z;      // fp32 [M, N]
   float dt;
   int* status;
+  // two ints, zero at launch: the CTA-pair kernel fetches tiles from the first and
+  // counts finished clusters in the second (the last resets both); null: tiles are
+  // dealt round-robin
+  int* tile_counter;
 };
 
 cudaError_t launch_gemm(int epi, const GemmArgs& args, cudaStream_t stream);
@@ -79,10 +83,12 @@ struct RouterArgs {
 cudaError_t launch_router(const RouterArgs& args, cudaStream_t stream);
 
 // ---------------------------------------------------------------- row kernels
-// rows < n_prefix use (shift_p, scale_p) when shift_p is not null
+// rows < n_prefix use (shift_p, scale_p) when shift_p is not null; zero2 (if set): two
+// ints set to zero before any row is written (the GEMM tile counters)
 cudaError_t launch_rms_modulate(const __nv_bfloat16* x, const float* shift, const float* scale,
                                 const float* shift_p, const float* scale_p, int n_prefix,
-                                __nv_bfloat16* h, int rows, int D, float eps, cudaStream_t s);
+                                __nv_bfloat16* h, int rows, int D, float eps, cudaStream_t s,
+                                int* zero2 = nullptr);
 // (cos, sin) per row and rotary pair: 1-D over the packed index, or 3-D (t, h, w) when
 // the geometry has a video grid
 cudaError_t launch_rope_table(float2* cs, int rows, int d, float theta, const TileGeom& g,

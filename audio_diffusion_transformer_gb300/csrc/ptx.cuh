@@ -46,30 +46,43 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// kCluster: acquire at cluster scope, for phases completed by arrivals from the other
+// CTA of the cluster whose prior shared-memory writes the waiter then reads
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(addr), "r"(parity)
-      : "memory");
+  if (kCluster)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 
 // Waits until the phase with the given parity has completed.  Returns false
 // if the CTA is aborting (flag already set, or this wait ran out of time).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* status,
                                           unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t addr = smem_u32(bar);
-  if (mbar_try_wait(addr, parity)) return true;
+  if (mbar_try_wait<kCluster>(addr, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
     // poll 256 times between clock and abort checks (try_wait itself suspends briefly)
     for (int i = 0; i < 256; ++i)
-      if (mbar_try_wait(addr, parity)) return true;
+      if (mbar_try_wait<kCluster>(addr, parity)) return true;
     if (*abort_flag) return false;
     if (global_ns() - t0 > limit_ns) {
       *abort_flag = 1;
@@ -284,6 +297,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 // non-.aligned form: a warp need not be converged when it reaches it)
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// 32-bit store into the shared memory of a CTA of the cluster (shared::cluster address)
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // arrive on an mbarrier of another CTA of the cluster (shared::cluster address)

@@ -37,9 +37,11 @@ __global__ void __launch_bounds__(ROW_THREADS)
     rms_modulate_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ shift_v,
                         const float* __restrict__ scale_v, const float* __restrict__ shift_p,
                         const float* __restrict__ scale_p, int n_prefix,
-                        __nv_bfloat16* __restrict__ h, int D, float eps) {
+                        __nv_bfloat16* __restrict__ h, int D, float eps, int* zero2) {
   __shared__ float wsum[ROW_THREADS / 32];
   const int row = blockIdx.x;
+  // the tile counters of the projection GEMMs that follow start from zero
+  if (zero2 != nullptr && row == 0 && threadIdx.x < 2) zero2[threadIdx.x] = 0;
   const bool pre = shift_p != nullptr && row < n_prefix;
   const float* shift = pre ? shift_p : shift_v;
   const float* scale = pre ? scale_p : scale_v;
@@ -317,10 +319,11 @@ int grid_for(size_t n, int threads) {
 
 cudaError_t launch_rms_modulate(const __nv_bfloat16* x, const float* shift, const float* scale,
                                 const float* shift_p, const float* scale_p, int n_prefix,
-                                __nv_bfloat16* h, int rows, int D, float eps, cudaStream_t s) {
+                                __nv_bfloat16* h, int rows, int D, float eps, cudaStream_t s,
+                                int* zero2) {
   if (rows <= 0 || D % 8 != 0 || D > 8 * MAXV * ROW_THREADS) return cudaErrorInvalidValue;
   rms_modulate_kernel<<<rows, ROW_THREADS, 0, s>>>(x, shift, scale, shift_p, scale_p, n_prefix, h,
-                                                   D, eps);
+                                                   D, eps, zero2);
   return cudaGetLastError();
 }
 

@@ -142,7 +142,8 @@ int h3dit_gemm_cta_pairs(int enable);
  * Byte offsets, from the start of the workspace, of the regions a call with this
  * shape uses (host only; no counterpart on the pages: a debugging aid).  A region
  * the shape does not reserve reads H3DIT_WS_ABSENT.
- *   status   int32 device status word (h3dit_sync_status)
+ *   status   256 bytes: the int32 device status word (h3dit_sync_status) and the
+ *            kernels' work counters (reset by the kernels themselves)
  *   q, k, v  bf16 [H, N, d] after q/k norm and rotary        (block shapes only)
  *   g        bf16 [N, A] routing gate                          (block shapes only)
  *   o        bf16 [N, A] attention output after the gate mix (block shapes only)
