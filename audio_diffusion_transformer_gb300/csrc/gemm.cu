@@ -859,8 +859,10 @@ cudaError_t launch_pair(const GemmArgs& g, Params p, cudaStream_t stream) {
   CUtensorMap ta, tb;
   if (!make_tmap_2d(&ta, g.a, g.M, g.K, BM) || !make_tmap_2d(&tb, g.w, g.N, g.K, BN_WIDE / 2))
     return cudaErrorInvalidValue;
-  // raster groups of 256-row tiles: 8 when N or K is long, else 4
-  p.group = (g.N >= 16384 || g.K >= 16384) ? 8 : 4;
+  // raster groups of 256-row tiles (tiles taken in order from the counter): 16 for the
+  // 20,480- and 28,672-wide projections, 8 otherwise (measured at 15,435 rows: 0.5-1.5%
+  // over 8 and 4 respectively; 16 made the 20,480-deep fc2 slower)
+  p.group = g.N >= 16384 ? 16 : 8;
   p.pairs = 0;
   const int tiles = ((g.M + 2 * BM - 1) / (2 * BM)) * (g.N / BN_WIDE);
   const int clusters = tiles < cap ? tiles : cap;
