@@ -45,8 +45,9 @@
 //                in whole octaves (rounded up to an integer in the log2 domain), so a
 //                weight's bf16 rounding does not depend on which max the row had met
 //                (a power-of-two scale commutes with it); O is rescaled in TMEM, by an
-//                exact power of two, only when the row max grows by more than 2^8, and
-//                only then does a step wait for the previous PV
+//                exact power of two, only when the row max grows by more than 2^32
+//                (weights up to 2^32 keep l and O finite for |v| < 2^80 over 65,536
+//                keys), and only then does a step wait for the previous PV
 //   warp 6       TMA: the V ring
 //   warps 7..10  per unit: O / l, + gate * pooled for video rows, bf16 store; then Q of
 //                the unit two ahead into tensor memory; warp 7 also fetches units and
@@ -63,7 +64,7 @@ namespace {
 constexpr int THREADS = 384;     // 12 warps
 constexpr int MAX_STEPS = 512;   // steps per unit (a prefix unit walks N / 128 steps)
 constexpr int NST = 3;           // stages of the K ring and of the V ring
-constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleLog2 = 32.0f;
 
 template <int HD>
 struct Layout {
@@ -491,19 +492,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const int2 e = list[t];
         const uint32_t s_addr = t_lane + L::S_COL + sb * 128;
-        float sv[64];
+        float sv[128];
         uint32_t pk[32];
         float mx, lsum, alpha;
         bool need;
         if (e.x & 1) {
-          // dense: every row uses X (columns 0-63) and Y (64-127)
+          // dense: every row uses X (columns 0-63) and Y (64-127), read in one load
           const int cx = (e.x >> 2) & 127, cy = (e.y >> 2) & 127;
           float my = -INFINITY;
           if (cy > 0) {
-            tmem_ld64(s_addr + 64, sv);
-            my = masked_max64(sv, cy);
+            tmem_ld128(s_addr, sv);
+            my = masked_max64(sv + 64, cy);
+          } else {
+            tmem_ld64(s_addr, sv);
           }
-          tmem_ld64(s_addr, sv);
           mx = fmaxf(masked_max64(sv, cx), my) * sl2;
           need = mx > m_run + kRescaleLog2;
           const float m_new = need ? ceilf(mx) : m_run;
@@ -514,9 +516,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (cy == 0) tmem_zero32(s_addr + 32);  // no Y keys
           tmem_st32_u(s_addr, pk);  // P_X over S columns 0-31 (already read)
           if (cy > 0) {
-            tmem_ld64(s_addr + 64, sv);
-            masked_max64(sv, cy);  // re-apply the mask
-            lsum += exp_pack64(sv, sl2, m_use, pk);
+            lsum += exp_pack64(sv + 64, sl2, m_use, pk);  // masked scores are -inf
             tmem_st32_u(s_addr + 32, pk);  // P_Y over S columns 32-63 (already read)
           }
         } else {
