@@ -390,10 +390,16 @@ def per_clock_peak(n_sms, sm_mhz):
     return FLOP_PER_CLK_SM * n_sms * sm_mhz * 1e6 / 1e12
 
 
-def dominant_kernel(shape, shapes, stages, K, workload_name, clk_peak=None):
+def dominant_kernel(shape, shapes, stages, K, workload_name, clk_peak=None, calls=None):
     """Roofline of the kernel with the largest stage time, from the live stage records
-    (ms, launches); achieved = its algorithmic flops / its time.  Also per-kernel rates.
-    ``clk_peak``: the tensor peak at the sampled SM clock (frac_per_clock)."""
+    (ms, kernel launches); achieved = its algorithmic flops / its time.  Also per-kernel
+    rates.  ``calls``: how many times each block stage ran in the records (default: one
+    per block position per step; a projection whose last round of tiles is split runs
+    two kernels per call, its GEMM and the reduction of the split tiles, both timed in
+    the stage).  ``clk_peak``: the tensor peak at the sampled SM clock
+    (frac_per_clock)."""
+    if calls is None:
+        calls = len(shapes) * K
     pk, pk_kind = peaks()
     peak_tc = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     # per-launch flops of each stage, averaged over the block positions
@@ -404,21 +410,23 @@ def dominant_kernel(shape, shapes, stages, K, workload_name, clk_peak=None):
               "attention": ["attention"]}
     g_ms = {g: sum(stages[s_][0] for s_ in st) for g, st in groups.items()}
     dom = max(g_ms, key=g_ms.get)
-    n_launch = sum(stages[s_][1] for s_ in groups[dom])
-    flops = sum(sf[s_] * stages[s_][1] for s_ in groups[dom])
+    n_launch = calls * len(groups[dom])
+    n_kernels = sum(stages[s_][1] for s_ in groups[dom])
+    flops = sum(sf[s_] * calls for s_ in groups[dom])
     kernel = "attention" if dom == "attention" else "gemm"
     roofline = {"bound": "tensor", "kernel": dom,
                 "achieved": flops / (g_ms[dom] / 1e3) / 1e12, "peak": peak_tc,
                 "peak_kind": f"bf16 sustained, {pk_kind}", "unit": "TFLOP/s",
                 "traffic": recorded_traffic(kernel, dom, workload_name),
-                "launch_ms": g_ms[dom] / max(n_launch, 1), "launches": n_launch}
+                "launch_ms": g_ms[dom] / max(n_launch, 1), "launches": n_launch,
+                "kernel_launches": n_kernels}
     roofline["frac"] = roofline["achieved"] / peak_tc
     if clk_peak:
         roofline["peak_per_clock"] = clk_peak
         roofline["frac_per_clock"] = roofline["achieved"] / clk_peak
     kernels = {}
     for g, st in groups.items():
-        fl = sum(sf[s_] * stages[s_][1] for s_ in st)
+        fl = sum(sf[s_] * calls for s_ in st)
         tf = fl / (g_ms[g] / 1e3) / 1e12 if g_ms[g] > 0 else None
         kernels[g] = {"ms_per_step": g_ms[g] / K, "tflops": tf,
                       "frac": tf / peak_tc if tf else None}
@@ -835,7 +843,7 @@ def run_loop(args, rank, world, local_rank):
     pk, pk_kind = peaks()
     gf, af = block_flops(shape)
     achieved = block_evals * (gf + af) * args.steps / (ms / 1e3) / 1e12
-    roofline, kernels = dominant_kernel(shape, [shape], stages, 1, wl.name)
+    roofline, kernels = dominant_kernel(shape, [shape], stages, 1, wl.name, calls=block_evals)
     roofline["measured"] = "one profiled pass after the timed region"
     extra = {"roofline": roofline, "kernels": kernels,
              "stages_ms_per_step": {k: v[0] for k, v in stages.items()}}

@@ -339,6 +339,37 @@ def test_block_forward_deterministic(h3):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+def test_block_work_counters_need_no_zeroed_workspace(h3):
+    """The kernels' work counters in the workspace's status block (the attention unit
+    counter and the projection GEMMs' tile counters) are zeroed by the block's own
+    kernels and reset by the last CTA pair of every GEMM launch: a workspace whose
+    status block holds garbage (status word aside) gives the same bytes as a zeroed one,
+    and repeated calls on one workspace give the same bytes each time.  The 4,096-row
+    block's projections have 192-768 tiles on at most 76 SM pairs, so the counter hands
+    out most of them."""
+    shp = S.BLOCK_4K.shape
+    seed = 9
+    w = weights_to_device(S.block_weights(shp, seed))
+    xb = S.hidden_rows(shp, seed)
+    cs = h3.make_shape(shp)
+    nbytes = h3.workspace_bytes(cs)
+    status_at = h3.workspace_layout(cs)["status"]
+
+    def run(ws):
+        x = dev_bf16(xb)
+        h3.block_forward(cs, w, x, ws)
+        torch.cuda.synchronize()
+        assert h3.sync_status(ws) == 0
+        return x.view(torch.int16).clone()
+
+    ref = run(torch.zeros(nbytes, dtype=torch.uint8, device="cuda"))
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    words = ws[status_at:status_at + 256].view(torch.int32)
+    words[1:] = torch.tensor(0x3FFFFFFF, dtype=torch.int32)  # every counter word
+    for _ in range(3):
+        assert torch.equal(run(ws), ref)
+
+
 # ----------------------------------------------------------------------------- denoiser
 def test_denoise_fresh_and_extrapolated_steps(h3):
     shp = BLOCK_CASES[0][1]
