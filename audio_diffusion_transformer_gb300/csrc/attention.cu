@@ -29,13 +29,17 @@
 // which runs first), so that the long prefix units spread evenly; units are numbered
 // prefix units first (head-major), then video units head-major, so the CTAs in flight
 // share one or two heads' K/V in L2.  The pipelines run across unit boundaries.
-// Tensor memory (512 columns): two 128-column score buffers, the O accumulator, and
-// two Q buffers -- Q is the score MMA's A operand straight from tensor memory, which
-// leaves shared memory to three-stage K and V rings (192 KB).  The kernel's time is set
-// by the latency of each step's S -> softmax -> PV chain, not by memory bandwidth.
-//   warp 0       TMA: the K ring (a stage = X + Y, 128 keys)
+// Tensor memory (512 columns): three 128-column score buffers and the O accumulator.
+// The kernel's time is set by the latency of each step's S -> softmax -> PV chain, not
+// by memory bandwidth: step g + 3's score MMAs wait for step g's PV to free their
+// buffer, so a third buffer gives the chain a step more of slack than two (measured:
+// attention 5% faster on the default block, 9% on the receipt block).  Q therefore
+// lives in shared memory (one buffer, the score MMA reading both operands there), beside
+// a three-stage K ring and a two-stage V ring (32 KB stages; 192 KB in all).
+//   warp 0       TMA: the K ring (a stage = X + Y, 128 keys), and the unit's Q (rows
+//                0-63 and 64-127 as X and Y) once the previous unit's score MMAs are done
 //   warp 1       S issuer: S = Q [K_X; K_Y]^T (M = 128, N = 128, fp32) into the step's
-//                score buffer once the PV two steps back has read it
+//                score buffer once the PV three steps back has read it
 //   warp 11      PV issuer: O += P [V_X; V_Y] (K = 128, P from tensor memory, V
 //                MN-major).  Two issuing threads keep the tensor pipe fed: the S
 //                MMAs of later steps queue while the PV issuer waits for a softmax.
@@ -49,9 +53,8 @@
 //                (weights up to 2^32 keep l and O finite for |v| < 2^80 over 65,536
 //                keys), and only then does a step wait for the previous PV
 //   warp 6       TMA: the V ring
-//   warps 7..10  per unit: O / l, + gate * pooled for video rows, bf16 store; then Q of
-//                the unit two ahead into tensor memory; warp 7 also fetches units and
-//                writes their step lists
+//   warps 7..10  per unit: O / l, + gate * pooled for video rows, bf16 store; warp 7
+//                also fetches units and writes their step lists
 #include <math.h>
 
 #include "internal.h"
@@ -63,7 +66,9 @@ namespace {
 
 constexpr int THREADS = 384;     // 12 warps
 constexpr int MAX_STEPS = 512;   // steps per unit (a prefix unit walks N / 128 steps)
-constexpr int NST = 3;           // stages of the K ring and of the V ring
+constexpr int NSK = 3;           // stages of the K ring
+constexpr int NSV = 2;           // stages of the V ring
+constexpr int NSB = 3;           // score buffers in tensor memory
 constexpr float kRescaleLog2 = 32.0f;
 
 template <int HD>
@@ -74,17 +79,19 @@ struct Layout {
   // 2c * KCHUNK, chunk c of Y right after it, so each chunk is one 128-row operand.
   static constexpr int STAGE = 2 * BLK;
   static constexpr int K_OFF = 0;
-  static constexpr int V_OFF = K_OFF + NST * STAGE;
-  static constexpr int LIST_OFF = V_OFF + NST * STAGE;          // two step lists (int2)
+  static constexpr int V_OFF = K_OFF + NSK * STAGE;
+  // Q of the unit: rows 0-63 and 64-127 as X and Y of a stage (one 128-row operand per
+  // 64-dim chunk), the score MMA's A operand
+  static constexpr int Q_OFF = V_OFF + NSV * STAGE;
+  static constexpr int LIST_OFF = Q_OFF + STAGE;                 // two step lists (int2)
   static constexpr int LBUF_OFF = LIST_OFF + 2 * MAX_STEPS * 8;  // 128 row sums
   static constexpr int UNIT_OFF = LBUF_OFF + 128 * 4;            // unit numbers, step counts
   static constexpr int MASK_OFF = UNIT_OFF + 16;                 // list builder's tile masks
   static constexpr int BAR_OFF = MASK_OFF + 2 * 32 * 4;
   static constexpr int USED = BAR_OFF + 256;
   static constexpr int SMEM = USED + 1024;                       // + alignment slack
-  static constexpr uint32_t S_COL = 0;    // two 128-column score buffers
-  static constexpr uint32_t O_COL = 256;  // the accumulator, HD columns
-  static constexpr uint32_t Q_COL = 384;  // two Q buffers, HD / 2 columns each (bf16 pairs)
+  static constexpr uint32_t S_COL = 0;    // three 128-column score buffers
+  static constexpr uint32_t O_COL = 384;  // the accumulator, HD columns
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -277,7 +284,8 @@ __device__ __forceinline__ float exp_pack64(const float* sv, float sl2, float m_
 template <int HD>
 __global__ void __launch_bounds__(THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const Params p) {
+                     const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmQ, const Params p) {
   using L = Layout<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -287,43 +295,49 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* unit_w = reinterpret_cast<volatile int*>(smem + L::UNIT_OFF);
   volatile int* unit_n = unit_w + 2;  // step counts of the units on list buffers 0 and 1
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-  uint64_t* k_full = bars + 0;      // [NST] K stage landed
-  uint64_t* k_free = bars + 3;      // [NST] the stage's S MMAs completed
-  uint64_t* v_full = bars + 6;      // [NST] V stage landed
-  uint64_t* v_free = bars + 9;      // [NST] the stage's PV MMAs completed (O stable)
-  uint64_t* s_done = bars + 12;     // [2] S of the step is in its buffer (step parity)
-  uint64_t* p_full = bars + 14;     // [2] P of the step written (four softmax warps)
-  uint64_t* q_full = bars + 16;     // [2] Q of the unit on this buffer written (four warps)
-  uint64_t* list_full = bars + 18;  // [2] unit number and step list written
-  uint64_t* o_full = bars + 20;     // the unit's last PV completed
-  uint64_t* o_free = bars + 21;     // O and the row sums read (four epilogue warps)
-  uint64_t* l_ready = bars + 22;    // the row sums are in lbuf (four softmax warps)
-  uint64_t* s_free = bars + 23;     // [2] the step's PV completed: its score buffer is free
-  uint64_t* drain = bars + 25;      // [2] per issuing thread
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 27);
+  uint64_t* k_full = bars + 0;      // [NSK] K stage landed
+  uint64_t* k_free = bars + 3;      // [NSK] the stage's S MMAs completed
+  uint64_t* v_full = bars + 6;      // [NSV] V stage landed
+  uint64_t* v_free = bars + 8;      // [NSV] the stage's PV MMAs completed (O stable)
+  uint64_t* s_done = bars + 10;     // [NSB] S of the step is in its buffer
+  uint64_t* p_full = bars + 13;     // [NSB] P of the step written (four softmax warps)
+  uint64_t* s_free = bars + 16;     // [NSB] the step's PV completed: its score buffer is free
+  uint64_t* list_full = bars + 19;  // [2] unit number and step list written
+  uint64_t* o_full = bars + 21;     // the unit's last PV completed
+  uint64_t* o_free = bars + 22;     // O and the row sums read (four epilogue warps)
+  uint64_t* l_ready = bars + 23;    // the row sums are in lbuf (four softmax warps)
+  uint64_t* q_full = bars + 24;     // the unit's Q landed in shared memory
+  uint64_t* q_free = bars + 25;     // the unit's S MMAs completed: Q may be overwritten
+  uint64_t* drain = bars + 26;      // [2] per issuing thread
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 28);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < NST; ++b) {
+    for (int b = 0; b < NSK; ++b) {
       mbar_init(&k_full[b], 1);
       mbar_init(&k_free[b], 1);
+    }
+    for (int b = 0; b < NSV; ++b) {
       mbar_init(&v_full[b], 1);
       mbar_init(&v_free[b], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_free[b], 1);
-      mbar_init(&drain[b], 1);
+    for (int b = 0; b < NSB; ++b) {
       mbar_init(&s_done[b], 1);
       mbar_init(&p_full[b], 4);
-      mbar_init(&q_full[b], 4);
+      mbar_init(&s_free[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&drain[b], 1);
       mbar_init(&list_full[b], 1);
     }
     mbar_init(o_full, 1);
     mbar_init(o_free, 4);
     mbar_init(l_ready, 4);
+    mbar_init(q_full, 1);
+    mbar_init(q_free, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -342,13 +356,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool is_k = warp == 0;
       const CUtensorMap* tm = is_k ? &tmK : &tmV;
       prefetch_tmap(tm);
+      if (is_k) prefetch_tmap(&tmQ);
       uint64_t* full = is_k ? k_full : v_full;
       uint64_t* freed = is_k ? k_free : v_free;
       uint8_t* ring = smem + (is_k ? L::K_OFF : L::V_OFF);
+      const int nst = is_k ? NSK : NSV;
       int st = 0;        // ring stage and phase of the next load
       uint32_t ph = 0;
       int issued = 0;
-      for (int lj = 0;; ++lj) {
+      int q_loads = 0;   // (K producer) Q loads issued
+      bool ok = true;
+      for (int lj = 0; ok; ++lj) {
         const int lb = lj & 1;
         if (!mbar_wait(&list_full[lb], (lj >> 1) & 1, abort_flag, p.status)) break;
         const int w = unit_w[lb];
@@ -356,12 +374,59 @@ __global__ void __launch_bounds__(THREADS, 1)
         const Unit u = unit_of(p, w);
         const int2* list = lists + lb * MAX_STEPS;
         const int n = unit_n[lb];
-        bool ok = true;
-        for (int t = 0; t < n; ++t) {
-          if (!mbar_wait(&freed[st], ph ^ 1, abort_flag, p.status)) {
-            ok = false;
-            break;
+        // (K producer) the unit's Q goes into the one Q buffer once the previous unit's
+        // score MMAs have completed; until then the unit's K loads go ahead, and every
+        // wait below polls for that moment
+        bool q_pending = is_k;
+        auto try_q = [&]() {
+          if (!q_pending) return;
+          if (lj > 0 && !mbar_try_wait(smem_u32(q_free), (uint32_t)(lj - 1) & 1u)) return;
+          int rx, ry;  // first rows of the unit's two 64-row query blocks
+          if (u.prefix) {
+            rx = u.unit * 128;
+            ry = rx + 64;
+          } else {
+            int c;
+            tile_span(p.geom, u.ta, &rx, &c);
+            // an odd tile count leaves the last unit's second half without a tile: it
+            // repeats a
+            if (u.tb < p.Tv)
+              tile_span(p.geom, u.tb, &ry, &c);
+            else
+              ry = rx;
           }
+          uint8_t* qs = smem + L::Q_OFF;
+          mbar_arrive_expect_tx(q_full, L::STAGE);
+#pragma unroll
+          for (int ch = 0; ch < HD / 64; ++ch) {
+            tma_load_3d(qs + 2 * ch * L::KCHUNK, &tmQ, q_full, 64 * ch, rx, u.h);
+            tma_load_3d(qs + (2 * ch + 1) * L::KCHUNK, &tmQ, q_full, 64 * ch, ry, u.h);
+          }
+          ++q_loads;
+          q_pending = false;
+        };
+        for (int t = 0; t < n; ++t) {
+          // wait for the stage to be free (bounded), polling for the Q buffer meanwhile
+          const uint32_t fa = smem_u32(&freed[st]);
+          if (!mbar_try_wait(fa, ph ^ 1)) {
+            const unsigned long long t0 = global_ns();
+            while (true) {
+              try_q();
+              bool done = false;
+              for (int i = 0; i < 64 && !done; ++i) done = mbar_try_wait(fa, ph ^ 1);
+              if (done) break;
+              if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
+                if (!*abort_flag) {
+                  *abort_flag = 1;
+                  if (p.status) atomicExch(p.status, kStatusTimeout);
+                }
+                ok = false;
+                break;
+              }
+            }
+            if (!ok) break;
+          }
+          try_q();
           const int2 e = list[t];
           uint8_t* s = ring + st * L::STAGE;
           mbar_arrive_expect_tx(&full[st], L::STAGE);
@@ -371,23 +436,32 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_3d(s + (2 * ch + 1) * L::KCHUNK, tm, &full[st], 64 * ch, e.y >> 9, u.h);
           }
           ++issued;
-          if (++st == NST) {
+          if (++st == nst) {
             st = 0;
             ph ^= 1;
           }
         }
         if (!ok) break;
+        // a unit whose K loads all went ahead still needs its Q
+        if (q_pending) {
+          if (lj > 0 && !mbar_wait(q_free, (uint32_t)(lj - 1) & 1u, abort_flag, p.status)) break;
+          try_q();
+        }
       }
-      // wait (bounded) for the last load into each stage before the CTA exits (already
-      // complete unless the CTA is aborting)
-      for (int i = issued > NST ? issued - NST : 0; i < issued; ++i)
-        mbar_drain(&full[i % NST], (i / NST) & 1);
+      // wait (bounded) for the last load into each stage, and the last Q load, before the
+      // CTA exits (already complete unless the CTA is aborting)
+      for (int i = issued > nst ? issued - nst : 0; i < issued; ++i)
+        mbar_drain(&full[i % nst], (i / nst) & 1);
+      if (q_loads > 0) mbar_drain(q_full, (uint32_t)(q_loads - 1) & 1u);
     }
   } else if (warp == 1 || warp == 11) {
     // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       const bool is_s = warp == 1;
+      const int nst = is_s ? NSK : NSV;
       uint32_t g = 0;  // steps issued, across units
+      int sb = 0;      // score buffer of step g (g mod NSB) and its use count parity
+      uint32_t sph = 0;
       int st = 0;      // K (S issuer) or V (PV issuer) ring stage and phase
       uint32_t ph = 0;
       bool ok = true;
@@ -398,16 +472,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (w >= p.total) break;
         const int n = unit_n[lb];
         for (int t = 0; t < n; ++t, ++g) {
-          const int sb = g & 1;
           if (is_s) {
             // S of step g: Q of the unit, K of the step, and a score buffer the PV of step
-            // g - 2 has finished reading
-            if (t == 0 && !mbar_wait(&q_full[lb], (lj >> 1) & 1, abort_flag, p.status)) {
+            // g - 3 has finished reading
+            if (t == 0 && !mbar_wait(q_full, (uint32_t)lj & 1u, abort_flag, p.status)) {
               ok = false;
               break;
             }
             if (!mbar_wait(&k_full[st], ph, abort_flag, p.status) ||
-                !mbar_wait(&s_free[sb], ((g >> 1) & 1) ^ 1, abort_flag, p.status)) {
+                !mbar_wait(&s_free[sb], sph ^ 1, abort_flag, p.status)) {
               ok = false;
               break;
             }
@@ -415,22 +488,24 @@ __global__ void __launch_bounds__(THREADS, 1)
             constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
             const uint64_t kd =
                 sdesc_sw128(smem_u32(smem + L::K_OFF + st * L::STAGE), 16, 1024);
+            const uint64_t qd = sdesc_sw128(smem_u32(smem + L::Q_OFF), 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < HD / 16; ++ks) {
-              // Q: dims 16ks..16ks+15 are columns 8ks..8ks+7 of the unit's Q buffer
+              // dims 16ks..16ks+15: 32-byte step within a 64-dim chunk of Q and of K
               const uint32_t koff = (ks >> 2) * 2 * L::KCHUNK + (ks & 3) * 32;
-              umma_bf16_ts(tmem + L::S_COL + sb * 128, tmem + L::Q_COL + lb * 64 + ks * 8,
-                           kd + (koff >> 4), idesc_s, ks > 0 ? 1u : 0u);
+              umma_bf16(tmem + L::S_COL + sb * 128, qd + (koff >> 4), kd + (koff >> 4), idesc_s,
+                        ks > 0 ? 1u : 0u);
             }
             umma_commit(&s_done[sb]);
             umma_commit(&k_free[st]);
+            if (t == n - 1) umma_commit(q_free);  // the unit's last read of Q
           } else {
             // PV of step g: O read out of the previous unit, P of the step, V of the step
             if (t == 0 && !mbar_wait(o_free, (lj & 1) ^ 1, abort_flag, p.status)) {
               ok = false;
               break;
             }
-            if (!mbar_wait(&p_full[sb], (g >> 1) & 1, abort_flag, p.status) ||
+            if (!mbar_wait(&p_full[sb], sph, abort_flag, p.status) ||
                 !mbar_wait(&v_full[st], ph, abort_flag, p.status)) {
               ok = false;
               break;
@@ -451,9 +526,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             umma_commit(&v_free[st]);
             if (t == n - 1) umma_commit(o_full);
           }
-          if (++st == NST) {
+          if (++st == nst) {
             st = 0;
             ph ^= 1;
+          }
+          if (++sb == NSB) {
+            sb = 0;
+            sph ^= 1;
           }
         }
       }
@@ -469,6 +548,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t o_addr = t_lane + L::O_COL;
     const float sl2 = p.scale_log2;
     uint32_t g = 0;
+    int sb = 0;    // score buffer of step g (g mod NSB) and its use count parity
+    uint32_t sph = 0;
     int v_st = 0;  // V stage and phase of step g (the rescale waits on step g - 1's PV)
     uint32_t v_ph = 0;
     int pv_st = 0;
@@ -484,8 +565,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       float m_run = -INFINITY;
       float l_run = 0.f;
       for (int t = 0; t < n; ++t, ++g) {
-        const int sb = g & 1;
-        if (!mbar_wait(&s_done[sb], (g >> 1) & 1, abort_flag, p.status)) {
+        if (!mbar_wait(&s_done[sb], sph, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -548,9 +628,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) mbar_arrive(&p_full[sb]);
         pv_st = v_st;
         pv_ph = v_ph;
-        if (++v_st == NST) {
+        if (++v_st == NSV) {
           v_st = 0;
           v_ph ^= 1;
+        }
+        if (++sb == NSB) {
+          sb = 0;
+          sph ^= 1;
         }
       }
       if (!ok) break;
@@ -561,7 +645,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(l_ready);
     }
   } else if (warp >= 7 && warp <= 10) {
-    // ------------------------------------------------------------ epilogue, Q, scheduler
+    // ------------------------------------------------------------ epilogue, scheduler
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const int half = row >> 6;
@@ -579,37 +663,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&list_full[buf]);
       if (w >= p.total) ended = true;
-    };
-    // Q rows of unit u (this thread's row) into tensor-memory Q buffer buf
-    auto load_q = [&](int buf, const Unit& u) {
-      int grow;
-      if (u.prefix) {
-        grow = u.unit * 128 + row;
-      } else {
-        // an odd tile count leaves the last unit's second half without a tile: it repeats a
-        const int tile = (half && u.tb < p.Tv) ? u.tb : u.ta;
-        int f, c;
-        tile_span(p.geom, tile, &f, &c);
-        grow = f + (row & 63);
-      }
-      const bool valid = grow < p.N;
-      const uint4* src = reinterpret_cast<const uint4*>(
-          p.q + ((size_t)u.h * p.N + (valid ? grow : 0)) * HD);
-      uint32_t wq[HD / 2];
-#pragma unroll
-      for (int i = 0; i < HD / 8; ++i) {
-        const uint4 v = valid ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
-        wq[4 * i + 0] = v.x;
-        wq[4 * i + 1] = v.y;
-        wq[4 * i + 2] = v.z;
-        wq[4 * i + 3] = v.w;
-      }
-#pragma unroll
-      for (int c = 0; c < HD / 64; ++c)
-        tmem_st32_u(t_lane + L::Q_COL + buf * 64 + c * 32, wq + 32 * c);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q_full[buf]);
     };
     int end_at = 1 << 30;  // first unit index known to be past the end
     int wc0 = 0, wc1 = 0;  // units on list buffers 0 and 1
@@ -629,7 +682,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         end_at = b;
         break;
       }
-      load_q(b, unit_of(p, w));
     }
     const int A = p.H * HD;
     for (int lj = 0; ok && lj < end_at; ++lj) {
@@ -696,8 +748,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      // unit lj + 2 takes this list and Q buffer once all four warps are done with unit lj
-      // (its S MMAs completed before o_full)
+      // unit lj + 2 takes this list buffer once all four warps are done with unit lj
+      // (every reader of its list finished before o_full)
       if (sched && !ended) {
         if (!mbar_wait(o_free, lj & 1, abort_flag, p.status)) break;
         int w2 = 0;
@@ -708,10 +760,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(&list_full[ob], ((lj + 2) >> 1) & 1, abort_flag, p.status)) break;
         const int w2 = unit_w[ob];
         if (ob) wc1 = w2; else wc0 = w2;
-        if (w2 >= p.total)
-          end_at = lj + 2;
-        else
-          load_q(ob, unit_of(p, w2));
+        if (w2 >= p.total) end_at = lj + 2;
       }
     }
   }
@@ -727,8 +776,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 template <int HD>
 cudaError_t launch_hd(const AttnArgs& a, cudaStream_t stream) {
   using L = Layout<HD>;
-  CUtensorMap tk, tv;
-  if (!make_tmap_3d(&tk, a.k, a.H, a.N, HD) || !make_tmap_3d(&tv, a.v, a.H, a.N, HD))
+  CUtensorMap tk, tv, tq;
+  if (!make_tmap_3d(&tk, a.k, a.H, a.N, HD) || !make_tmap_3d(&tv, a.v, a.H, a.N, HD) ||
+      !make_tmap_3d(&tq, a.q, a.H, a.N, HD))
     return cudaErrorInvalidValue;
   Params p;
   p.N = a.N;
@@ -756,7 +806,7 @@ cudaError_t launch_hd(const AttnArgs& a, cudaStream_t stream) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   const int grid = p.total < num_sms() ? p.total : num_sms();
-  kern<<<grid, THREADS, L::SMEM, stream>>>(tk, tv, p);
+  kern<<<grid, THREADS, L::SMEM, stream>>>(tk, tv, tq, p);
   return cudaGetLastError();
 }
 
