@@ -188,6 +188,38 @@ def test_attention_constant_v_and_row_stochastic(h3):
     assert np.all(np.abs(got["o"] - want) <= 2.0 ** -8 * np.abs(want) + 1e-6)
 
 
+def test_attention_running_max_past_2_32(h3):
+    # Hand-built scores, in octaves (s / ln 2): every video query tile sees the prefix keys
+    # at 0 first.  Query tiles 0 and 2 (direction A) select key tiles 0 and 1, met at ~20
+    # and then ~60 octaves: the running maximum must move, O rescaled by 2^-61 between the
+    # steps.  Query tiles 1 and 3 (direction B) select key tiles 2 and 3, at ~28 and ~31
+    # octaves: the sums of their 64 weights pass 2^32 although no single weight does, and
+    # the maximum stays.  Neighbouring tiles select disjoint pairs, so both are routed steps.
+    d = 64
+    shp = S.BlockShape(64, 0, 256, hidden=256, heads=1, head_dim=d, mlp_width=1024, topk=2)
+    N, P = shp.n_rows, shp.n_prefix
+    q, k = np.zeros((1, N, d)), np.zeros((1, N, d))
+    e_a, e_b = np.zeros(d), np.zeros(d)
+    e_a[:16], e_b[16:32] = 1.0, 1.0
+    amp = 4.0
+    per_unit = amp * 16 / np.sqrt(d) / np.log(2)  # octaves per unit of key amplitude
+    for t, e in enumerate((e_a, e_b, e_a, e_b)):
+        q[0, P + 64 * t:P + 64 * (t + 1)] = amp * e
+    for t, (e, z) in enumerate(((e_a, 20.0), (e_a, 60.0), (e_b, 28.0), (e_b, 31.0))):
+        k[0, P + 64 * t:P + 64 * (t + 1)] = (z / per_unit) * e
+    v = S.normal(5, "v", (1, N, d))
+    inp = {"q": S.to_bf16_bits(q), "k": S.to_bf16_bits(k), "v": S.to_bf16_bits(v)}
+    got = run_attention(h3, shp, inp, with_gate=False)
+    ref = oracle_attention(shp, inp, with_gate=False, pooled=False)
+    assert np.array_equal(got["idx"][0], [[0, 1], [2, 3], [0, 1], [2, 3]])
+    assert np.array_equal(ref["idx"], got["idx"])
+    assert np.all(np.isfinite(got["o"]))
+    check_close(got["o"], ref["o_f64"], "running max past 2^32")
+    refp = oracle_attention(shp, inp, with_gate=False, pooled=False, p_bf16=True)
+    check_close(got["o"], refp["o_f64"], "running max past 2^32 (bf16 P)", rel=2e-3,
+                cos=0.999998)
+
+
 def test_topk_nan_and_tie_rule(h3):
     # identical K tiles 1 and 2 give equal scores for every query: the lower tile must win
     shp = S.BlockShape(0, 0, 64 * 6, hidden=256, heads=1, head_dim=64, mlp_width=1024, topk=2)
