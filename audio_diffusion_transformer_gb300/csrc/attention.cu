@@ -30,10 +30,10 @@
 // prefix units first (head-major), then video units head-major, so the CTAs in flight
 // share one or two heads' K/V in L2.  The pipelines run across unit boundaries.
 // Tensor memory (512 columns): three 128-column score buffers and the O accumulator.
-// The kernel's time is set by the latency of each step's S -> softmax -> PV chain, not
-// by memory bandwidth: step g + 3's score MMAs wait for step g's PV to free their
-// buffer, so a third buffer gives the chain a step more of slack than two (measured:
-// attention 5% faster on the default block, 9% on the receipt block).  Q therefore
+// The kernel's time is set by each step's S -> softmax -> PV chain (mostly the softmax's
+// work on its TMEM lane quarter), not by memory bandwidth: step g + 3's score MMAs wait
+// for step g's PV to free their buffer, so a third buffer gives the chain a step more of
+// slack than two (attention 5% faster on the default block, 9% on the receipt).  Q therefore
 // lives in shared memory (one buffer, the score MMA reading both operands there), beside
 // a three-stage K ring and a two-stage V ring (32 KB stages; 192 KB in all).
 //   warp 0       TMA: the K ring (a stage = X + Y, 128 keys), and the unit's Q (rows
