@@ -31,6 +31,8 @@ PIN TABLE (function: pin tests, without their "test_" prefix)
   bf16: bf16_against_torch_conversion, bf16_hand_values
   f32: output_head_constant_rows, token_pool_brute_force_pairs
   rms_modulate: rms_modulate_closed_forms
+  modulate_rows: modulate_rows_picks_each_rows_table, block_prefix_table_norm_applies_to_its_rows
+  gate_rows: gate_rows_picks_each_rows_table, block_prefix_table_zero_gates_split_by_modality
   linear: linear_small_integers_exact
   gelu_erf: gelu_closed_forms
   silu: silu_closed_forms
@@ -102,6 +104,7 @@ __all__ = [
     "fresh_steps", "sigma_schedule", "denoise_forward", "denoise_loop", "thin_layers",
     "patch_in", "output_head", "sample_x0", "sample_heads", "sample_step", "sample_loop",
     "rope_coords_pooled", "reduced_shape", "token_pool", "token_restore", "run_blocks",
+    "modulate_rows", "gate_rows",
 ]
 
 

@@ -66,6 +66,34 @@ def test_rms_modulate_closed_forms():
     assert np.all(h == 0.25)
 
 
+def test_modulate_rows_picks_each_rows_table():
+    # scale = -1 on both tables makes every modulated row equal to its own table's shift
+    # exactly (the closed form above), so each row shows which table it took: packed
+    # indices below n_prefix the prefix table, the rest the main one, also for a row subset
+    D, P, eps = 64, 3, 1e-6
+    x = rng.standard_normal((7, D))
+    mod = np.zeros((6, D))
+    modp = np.zeros((6, D))
+    mod[1], modp[1] = -1.0, -1.0
+    mod[0], modp[0] = 0.5, -0.25
+    h = O.modulate_rows(x, mod, modp, P, 0, 1, eps)
+    assert np.all(h[:P] == -0.25) and np.all(h[P:] == 0.5)
+    rows = np.array([5, 0, 2, 3])
+    h = O.modulate_rows(x[:4], mod, modp, P, 0, 1, eps, rows=rows)
+    assert np.all(h[[1, 2]] == -0.25) and np.all(h[[0, 3]] == 0.5)
+    # without a prefix table every row takes the main table
+    assert np.all(O.modulate_rows(x, mod, None, P, 0, 1, eps) == 0.5)
+
+
+def test_gate_rows_picks_each_rows_table():
+    D, P = 8, 2
+    mod = np.arange(6 * D, dtype=np.float64).reshape(6, D)
+    modp = -mod - 1.0
+    g = O.gate_rows(mod, modp, P, 2, np.array([0, 1, 2, 5]))
+    assert np.array_equal(g, np.stack([modp[2], modp[2], mod[2], mod[2]]))
+    assert np.array_equal(O.gate_rows(mod, None, P, 5, np.array([0, 3])), mod[5])
+
+
 def test_linear_small_integers_exact():
     a = rng.integers(-8, 9, (37, 96))
     w = rng.integers(-8, 9, (53, 96))
